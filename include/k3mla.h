@@ -1,0 +1,194 @@
+/*
+ * k3mla.h -- C ABI of libk3mla.so: paged absorbed multi-head latent attention
+ * (MLA) decode for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one pegainfer PR #869, "K3: paged latent MLA KV +
+ * absorbed decode", describes:
+ *   - M1 commit: a page-first latent slab [page][mla_layer][64 tokens][576]
+ *     bf16 (512-wide kv latent c_t, then the 64-wide shared rope key), a per-slot
+ *     int32 block table in which -1 reads as an all-zero latent, a free-list
+ *     page allocator (claim on a 64-token boundary, release-all on slot reset),
+ *     and the new token's row written into the mapped page with a size_t
+ *     element index;
+ *   - M2 commit: one absorbed kernel per MLA layer,
+ *       score(t) = (W_UK[h]^T q_nope)^T c_t + q_rope^T k_rope_t,
+ *       o[h]     = W_UV[h] (sum_t softmax(scale * score)_t c_t),
+ *     with W_UK and W_UV read in place from w_kv_b (no expansion GEMM, no
+ *     per-head K/V), and a runtime-length block-table walk.
+ *
+ * Geometry is fixed: 96 heads, q_nope 128, q_rope 64, v_head 128, kv_lora 512,
+ * page 64 tokens, cache row 576 bf16.  w_kv_b is one layer's [96*256][512]
+ * bf16 matrix; rows h*256 .. h*256+127 are W_UK[h] ([d][j]) and rows
+ * h*256+128 .. h*256+255 are W_UV[h] ([v][j]).
+ *
+ * Conventions for every call below:
+ *   - bf16 values travel as uint16_t bit patterns; every array is dense,
+ *     row-major, in the layout its comment gives.
+ *   - "device" pointers are CUDA device memory owned by the caller; the library
+ *     never allocates, frees or synchronises device memory, so every device
+ *     call can be captured into a CUDA graph.  `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream).
+ *   - Return value: K3MLA_OK (0) or a negative K3MLA_E_* code.  Argument errors
+ *     are detected on the host before anything is launched.  A launch failure
+ *     returns K3MLA_E_CUDA (the CUDA error text is in k3mla_last_error()).
+ *   - Problems only the device can see (a table id outside [-1, n_pages), an
+ *     unmapped append position, a context longer than the table or max_ctx) never
+ *     fault or trap: the kernel ORs a K3MLA_DEV_* bit into *dev_err (when the
+ *     pointer is non-NULL), treats the entry as an all-zero latent or skips the
+ *     write, and carries on.  Bounded device waits that run out set
+ *     K3MLA_DEV_TIMEOUT and return.
+ */
+#ifndef K3MLA_H_
+#define K3MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MLA_HEADS 96
+#define K3MLA_QK_NOPE 128
+#define K3MLA_QK_ROPE 64
+#define K3MLA_V_HEAD 128
+#define K3MLA_KV_LORA 512
+#define K3MLA_PAGE 64
+#define K3MLA_ROW 576
+#define K3MLA_TILE 128 /* tokens per decode tile; split_tokens must be a multiple */
+
+#define K3MLA_OK 0
+#define K3MLA_E_INVALID (-1)   /* bad pointer, size or alignment */
+#define K3MLA_E_NO_PAGES (-2)  /* pool exhausted */
+#define K3MLA_E_SLOT (-3)      /* slot index out of range */
+#define K3MLA_E_CTX (-4)       /* context beyond the pool's max_ctx */
+#define K3MLA_E_CUDA (-5)      /* a CUDA call failed */
+#define K3MLA_E_WORKSPACE (-6) /* workspace too small */
+#define K3MLA_E_DEVICE (-7)    /* the current device is not sm_103 */
+
+#define K3MLA_DEV_BAD_PAGE 1u   /* table id outside [-1, n_pages): read as zero */
+#define K3MLA_DEV_UNMAPPED 2u   /* append position unmapped or past the table: skipped */
+#define K3MLA_DEV_CTX 4u        /* ctx_len > max_ctx or > table capacity: clamped */
+#define K3MLA_DEV_TIMEOUT 8u    /* a bounded device wait ran out; outputs invalid */
+
+/* Text of the last host-side error in this thread (never NULL). */
+const char* k3mla_last_error(void);
+
+/* ---- q absorption (PR #869, M2 commit: "q absorption lands bf16") ----------
+ * q_abs[b][h][0:512]   = bf16( W_UK[h]^T q[b][h][0:128] )  (f32 accumulation)
+ * q_abs[b][h][512:576] = q[b][h][128:192]                   (q_rope, copied)
+ * q      device [B][96][192] bf16 (q_nope | q_rope)
+ * w_kv_b device [24576][512] bf16, one layer
+ * q_abs  device [B][96][576] bf16, written
+ * B >= 0 (B == 0 launches nothing).  Pointers 16-byte aligned. */
+int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B,
+                   void* stream);
+
+/* ---- append: the new token's latent row into its mapped page ---------------
+ * (PR #869, M1 commit: "two indexed writes through the per-layer row shift";
+ *  the element index is size_t because the slab passes 2^31 elements.)
+ * For every b with pos[b] >= 0:
+ *   page = block_table[b][pos[b] / 64]
+ *   row  = ((size_t)page * n_layers + layer) * 64 + pos[b] % 64
+ *   slab[row][0:512] = c_kv[b][0:512];  slab[row][512:576] = k_rope[b][0:64]
+ * slab        device [n_pages][n_layers][64][576] bf16 (written in place)
+ * block_table device [B][max_pages_per_slot] int32
+ * pos         device [B] int32 write position (< 0: no write for that slot)
+ * c_kv        device bf16, row b at c_kv + b * c_stride (elements)
+ * k_rope      device bf16, row b at k_rope + b * r_stride (elements)
+ * dev_err     device int32 or NULL: K3MLA_DEV_UNMAPPED for a -1 / out-of-range
+ *             page or a position past the table (that row is skipped).
+ * All bf16 pointers and strides 4-byte aligned (strides even). */
+int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
+                        const int32_t* block_table, int max_pages_per_slot,
+                        const int32_t* pos, const uint16_t* c_kv, int64_t c_stride,
+                        const uint16_t* k_rope, int64_t r_stride, int B,
+                        int32_t* dev_err, void* stream);
+
+/* ---- paged absorbed decode ---------------------------------------------------
+ * For each slot b < B and head h, with n = ctx_len[b] tokens (logical token t
+ * lives in page block_table[b][t / 64], row t % 64; a -1 entry is an all-zero
+ * row that still takes part in the softmax):
+ *   s_t   = bf16( bf16( q_abs[b][h] . row_t ) * scale )       (576-wide dot)
+ *   p_t   = softmax_t(s)
+ *   o_lat = bf16( sum_t p_t row_t[0:512] )
+ *   out[b][h] = bf16( W_UV[h] o_lat )
+ * (PR #869, M2 commit.)  Rows at positions >= n are never used, whatever they
+ * hold.  n == 0 gives out = 0 and argmax -1.
+ *
+ * The context of each slot is cut into splits of split_tokens logical tokens
+ * (a positive multiple of K3MLA_TILE); each split is reduced on its own and the
+ * splits are merged in ascending order.  Split boundaries depend only on the
+ * logical position and ctx_len, never on B, the page ids or the GPU, so for a
+ * fixed split_tokens the result of a slot is bitwise independent of the other
+ * slots in the batch, of padding slots and of which physical pages hold it.
+ *
+ * q_abs       device [B][96][576] bf16 (from k3mla_absorb_q)
+ * slab        device [n_pages][n_layers][64][576] bf16; n_pages*n_layers*64 < 2^31
+ * block_table device [B][max_pages_per_slot] int32
+ * ctx_len     device [B] int32 (clamped to min(max_ctx, 64*max_pages_per_slot),
+ *             setting K3MLA_DEV_CTX when it had to be)
+ * w_kv_b      device [24576][512] bf16, the layer's weights
+ * scale_bf16  the softmax scale as a bf16 bit pattern (bf16(1/sqrt(192)) = 0x3D94)
+ * out         device [B][96][128] bf16, written
+ * argmax_t    device [B][96] int32 or NULL: per head, the lowest logical t with
+ *             the largest bf16 score (-1 for an empty context)
+ * workspace   device, >= k3mla_decode_workspace_bytes(B, max_ctx, split_tokens)
+ *             bytes, 256-byte aligned; scratch, contents need no initialisation
+ * max_ctx     upper bound of ctx_len, sets the grid (1 <= max_ctx)
+ * dev_err     device int32 or NULL (K3MLA_DEV_* bits are ORed in)
+ * Runs as two kernels on `stream`: the split decode, then the merge + W_UV
+ * expansion. */
+size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens);
+int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
+                       int layer, const int32_t* block_table, int max_pages_per_slot,
+                       const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
+                       uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes,
+                       int B, int max_ctx, int split_tokens, int32_t* dev_err, void* stream);
+
+/* A split length for a batch of B slots with contexts up to max_ctx on the
+ * current device: the smallest multiple of K3MLA_TILE that keeps the number of
+ * splits within one wave of SM pairs.  Results are bitwise invariant only for a
+ * FIXED split length, so a caller that wants padding invariance computes this
+ * once per configuration and reuses it. */
+int k3mla_default_split_tokens(int B, int max_ctx);
+
+/* ---- host page pool: free-list allocator (PR #869, M1 commit) ---------------
+ * n_pages == 0 sizes the pool for full coverage: n_slots * ceil(max_ctx / 64)
+ * pages, so every slot can reach max_ctx.  The free list holds page ids
+ * 0 .. n_pages-1; shuffle_seed != 0 shuffles it (splitmix64-driven
+ * Fisher-Yates) so that slots claim scattered ids.  The pool owns a host block
+ * table [n_slots][max_pages] (max_pages = ceil(max_ctx / 64)), -1 = unmapped;
+ * the caller copies it to the device.  Nothing here touches a GPU. */
+typedef struct k3mla_pool k3mla_pool;
+int k3mla_pool_create(int n_pages, int n_slots, int max_ctx, uint64_t shuffle_seed,
+                      k3mla_pool** out);
+/* Claims pages (one per 64-token boundary crossed) so that tokens
+ * [0, new_len) of `slot` are mapped.  All-or-nothing: on K3MLA_E_NO_PAGES no
+ * page is claimed.  new_len > max_ctx gives K3MLA_E_CTX. */
+int k3mla_pool_ensure(k3mla_pool* pool, int slot, int new_len);
+/* Returns every page of `slot` to the free list and unmaps its table row. */
+int k3mla_pool_release_slot(k3mla_pool* pool, int slot);
+const int32_t* k3mla_pool_host_table(const k3mla_pool* pool);
+int k3mla_pool_max_pages(const k3mla_pool* pool);
+int k3mla_pool_n_pages(const k3mla_pool* pool);
+/* Pool capacity and pages in use (PR #869 review: expose total / allocated). */
+int k3mla_pool_stats(const k3mla_pool* pool, int* total, int* used);
+void k3mla_pool_destroy(k3mla_pool* pool);
+
+/* ---- diagnostic --------------------------------------------------------------
+ * Runs one tile of the decode kernel's two tensor-core contractions in
+ * isolation so that their operand layouts can be checked against a plain
+ * matrix product.  Not part of the decode path.
+ *   mode 0: S[128][128] f32 = Q[128][576] (rows >= 96 zero) x T[128][576]^T,
+ *           Q from `a` (device [96][576] bf16), T from tokens 0..127 of a
+ *           2-page tile of `b` (device [2][64][576] bf16) -> d (device [128][128]).
+ *   mode 1: O[512][96] f32 = T[128][0:512]^T x P[96][128]^T with T from `b` as
+ *           above and P from `a` (device [96][128] bf16) -> d (device [512][96]).
+ */
+int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, float* d, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3MLA_H_ */

@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libk3mla.so (declared in include/k3mla.h).
+
+Argument marshalling only: every function checks shapes / dtypes / devices,
+passes raw pointers and the current CUDA stream to the C ABI, and raises on a
+non-zero status.  All arithmetic runs in the library's CUDA kernels; if the
+library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+H, NOPE, ROPE, V, LORA, PAGE, ROW, TILE = 96, 128, 64, 128, 512, 64, 576, 128
+
+DEV_BAD_PAGE, DEV_UNMAPPED, DEV_CTX, DEV_TIMEOUT = 1, 2, 4, 8
+
+# Every symbol include/k3mla.h declares.
+EXPORTS = (
+    "k3mla_last_error", "k3mla_absorb_q", "k3mla_append_latent", "k3mla_decode_workspace_bytes",
+    "k3mla_paged_decode", "k3mla_default_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
+    "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
+    "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class K3mlaError(RuntimeError):
+    pass
+
+
+def load(build_if_needed: bool = True):
+    """Load libk3mla.so (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_needed else _build.LIB
+        lib = ctypes.CDLL(path)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "k3mla_last_error": ([], ctypes.c_char_p),
+            "k3mla_absorb_q": ([P, P, P, I, P], I),
+            "k3mla_append_latent": ([P, I, I, I, P, I, P, P, I64, P, I64, I, P, P], I),
+            "k3mla_decode_workspace_bytes": ([I, I, I], SZ),
+            "k3mla_paged_decode": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, P, P],
+                                   I),
+            "k3mla_default_split_tokens": ([I, I], I),
+            "k3mla_pool_create": ([I, I, I, ctypes.c_uint64, ctypes.POINTER(P)], I),
+            "k3mla_pool_ensure": ([P, I, I], I),
+            "k3mla_pool_release_slot": ([P, I], I),
+            "k3mla_pool_host_table": ([P], ctypes.POINTER(ctypes.c_int32)),
+            "k3mla_pool_max_pages": ([P], I),
+            "k3mla_pool_n_pages": ([P], I),
+            "k3mla_pool_stats": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "k3mla_pool_destroy": ([P], None),
+            "k3mla_diag_umma": ([I, P, P, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = load().k3mla_last_error().decode(errors="replace")
+        raise K3mlaError(f"{what} failed with status {rc}: {msg}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, shape=None, name="tensor"):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise K3mlaError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise K3mlaError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise K3mlaError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise K3mlaError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _opt(t, dtype, shape, name):
+    return None if t is None else _dev(t, dtype, shape, name)
+
+
+def absorb_q(q: torch.Tensor, w_kv_b: torch.Tensor, q_abs: torch.Tensor, stream=None) -> None:
+    """q [B,96,192] bf16, w_kv_b [24576,512] bf16 -> q_abs [B,96,576] bf16 (written)."""
+    B = q.shape[0]
+    lib = load()
+    _check(lib.k3mla_absorb_q(_dev(q, torch.bfloat16, (B, H, NOPE + ROPE), "q"),
+                              _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"),
+                              _dev(q_abs, torch.bfloat16, (B, H, ROW), "q_abs"), B, _stream(stream)),
+           "k3mla_absorb_q")
+
+
+def append_latent(slab: torch.Tensor, layer: int, block_table: torch.Tensor, pos: torch.Tensor,
+                  c_kv: torch.Tensor, k_rope: torch.Tensor, dev_err: torch.Tensor | None = None,
+                  stream=None) -> None:
+    """slab [n_pages,L,64,576] bf16 (in place); block_table [B,max_pages] int32; pos [B]
+    int32; c_kv [B,>=512] bf16 and k_rope [B,>=64] bf16 with unit inner stride."""
+    n_pages, L = slab.shape[0], slab.shape[1]
+    B = pos.shape[0]
+    for t, name in ((c_kv, "c_kv"), (k_rope, "k_rope")):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1 or t.shape[0] != B:
+            raise K3mlaError(f"{name} must be a CUDA bf16 [B, n] tensor with unit inner stride")
+    lib = load()
+    _check(lib.k3mla_append_latent(
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(pos, torch.int32, (B,), "pos"), ctypes.c_void_p(c_kv.data_ptr()), c_kv.stride(0),
+        ctypes.c_void_p(k_rope.data_ptr()), k_rope.stride(0), B,
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_append_latent")
+
+
+def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:
+    return int(load().k3mla_decode_workspace_bytes(B, max_ctx, split_tokens))
+
+
+def default_split_tokens(B: int, max_ctx: int) -> int:
+    return int(load().k3mla_default_split_tokens(B, max_ctx))
+
+
+def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
+                 ctx_len: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor,
+                 workspace: torch.Tensor, max_ctx: int, split_tokens: int,
+                 argmax: torch.Tensor | None = None, dev_err: torch.Tensor | None = None,
+                 stream=None) -> None:
+    """Paged absorbed decode of one layer for B slots; see include/k3mla.h."""
+    B = q_abs.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise K3mlaError("workspace must be a CUDA uint8 tensor")
+    lib = load()
+    _check(lib.k3mla_paged_decode(
+        _dev(q_abs, torch.bfloat16, (B, H, ROW), "q_abs"),
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"),
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"), int(scale_bf16),
+        _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), B, int(max_ctx), int(split_tokens),
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_paged_decode")
+
+
+def diag_umma(mode: int, a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, stream=None) -> None:
+    lib = load()
+    _check(lib.k3mla_diag_umma(int(mode), _dev(a, torch.bfloat16, None, "a"),
+                               _dev(b, torch.bfloat16, (2, PAGE, ROW), "b"),
+                               _dev(d, torch.float32, None, "d"), _stream(stream)), "k3mla_diag_umma")
+
+
+class Pool:
+    """Host free-list page allocator (k3mla_pool_*)."""
+
+    def __init__(self, n_slots: int, max_ctx: int, n_pages: int = 0, shuffle_seed: int = 0):
+        lib = load(build_if_needed=True)
+        h = ctypes.c_void_p()
+        _check(lib.k3mla_pool_create(n_pages, n_slots, max_ctx, shuffle_seed, ctypes.byref(h)),
+               "k3mla_pool_create")
+        self._h = h
+        self.n_slots = n_slots
+        self.max_ctx = max_ctx
+        self.max_pages = lib.k3mla_pool_max_pages(h)
+        self.n_pages = lib.k3mla_pool_n_pages(h)
+
+    def ensure(self, slot: int, new_len: int) -> int:
+        """Returns the status code (0 ok, negative K3MLA_E_*)."""
+        return int(load().k3mla_pool_ensure(self._h, slot, new_len))
+
+    def release(self, slot: int) -> int:
+        return int(load().k3mla_pool_release_slot(self._h, slot))
+
+    def table(self) -> np.ndarray:
+        ptr = load().k3mla_pool_host_table(self._h)
+        return np.ctypeslib.as_array(ptr, shape=(self.n_slots, self.max_pages)).copy()
+
+    def stats(self) -> tuple[int, int]:
+        t, u = ctypes.c_int(), ctypes.c_int()
+        _check(load().k3mla_pool_stats(self._h, ctypes.byref(t), ctypes.byref(u)), "k3mla_pool_stats")
+        return t.value, u.value
+
+    def close(self):
+        if self._h:
+            load().k3mla_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,54 @@
+"""The decode kernel's two tcgen05 contractions, one tile each, against a plain
+float64 matrix product (operand layouts, descriptors and TMEM lane mapping).
+
+Score form: S[128 x 128] = Q[128 x 576] . T^T with Q in TMEM (rows >= 96 zero)
+and the 2-page token tile T staged by TMA.  PV form: O[512 x 96] = T[:, :512]^T .
+P^T with the latent tile as an MN-major operand and P^T written by threads in the
+128-byte-swizzled K-major layout.  Products of bf16 values are exact, so the only
+difference from float64 is f32 accumulation."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_common import dump
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(d, ref, absref, name):
+    d = d.double().cpu().numpy()
+    ref = ref.cpu().numpy()
+    bound = 64 * 2.0**-24 * absref.cpu().numpy() + 1e-30
+    ok = np.all(np.abs(d - ref) <= bound)
+    if not ok:
+        dump(name, d=d, ref=ref)
+    assert ok, f"{name}: max |diff| / bound = {np.max(np.abs(d - ref) / bound):.3g}"
+
+
+def test_score_contraction_tile(gpu_lib):
+    g = torch.Generator(device="cuda").manual_seed(1)
+    a = torch.randn(96, 576, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(2, 64, 576, generator=g, device="cuda").to(torch.bfloat16)
+    d = torch.full((128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    gpu_lib.diag_umma(0, a, b, d)
+    torch.cuda.synchronize()
+    t = b.reshape(128, 576).double()
+    ref = a.double() @ t.T
+    absref = a.double().abs() @ t.abs().T
+    _check(d[:96], ref, absref, "diag_score")
+    assert torch.all(d[96:] == 0)
+
+
+def test_pv_contraction_tile(gpu_lib):
+    g = torch.Generator(device="cuda").manual_seed(2)
+    p = torch.rand(96, 128, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(2, 64, 576, generator=g, device="cuda").to(torch.bfloat16)
+    d = torch.full((512, 96), float("nan"), dtype=torch.float32, device="cuda")
+    gpu_lib.diag_umma(1, p, b, d)
+    torch.cuda.synchronize()
+    t = b.reshape(128, 576)[:, :512].double()
+    ref = t.T @ p.double().T
+    absref = t.abs().T @ p.double().abs().T
+    _check(d, ref, absref, "diag_pv")

@@ -1,0 +1,95 @@
+"""Paged absorbed decode on the GPU against the oracle, element by element.
+
+Bar: every output element within 4 bf16 ULP of its (slot, head) row's largest
+oracle magnitude, and the argmax of the attention probabilities identical up to
+the <= 1-ULP coin flips (a differing token must have an oracle score within one
+bf16 ULP of the oracle maximum, or a tied oracle probability).
+
+Cases span several 128-token tiles, ragged tails, multi-split merges, -1 holes,
+padding slots and empty contexts at sizes the oracle finishes in seconds; the
+full-size workloads are checked on sampled slots in the launch configuration the
+benchmark times."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from paged_latent_attention_k3mla_gb300 import k3mla, synth
+from tests.gpu_common import compare, gpu_layer, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity(wl, layer, slots=None, split=None, max_ctx=None, name="case"):
+    g = gpu_layer(wl, layer, split=split, max_ctx=max_ctx)
+    o = oracle_layer(wl, layer, slots=slots, probs_stride=int(max(1, wl.ctx_len.max())))
+    ok, stats = compare(g, o, wl.ctx_len, name=name)
+    print(f"{name}: split={g['split']} {stats}")
+    assert g["dev_err"] == 0, g["dev_err"]
+    assert ok, stats
+    return stats
+
+
+def test_tiny(gpu_lib):
+    wl = synth.make_workload("tiny", device="cuda")
+    _parity(wl, 0, name="tiny")
+
+
+@pytest.mark.parametrize("split", [128, 256, 1024])
+def test_ragged_tails_and_split_merges(gpu_lib, split):
+    ctx = [1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 640, 1000]
+    wl = synth.make_custom(ctx, seed=300, device="cuda")
+    _parity(wl, 0, split=split, max_ctx=1024, name=f"ragged_split{split}")
+
+
+def test_heavy_tailed_rows_force_rescales(gpu_lib):
+    # a late token with a much larger score than the early ones moves the
+    # reference max by more than the rescale threshold
+    wl = synth.make_custom([700, 1500], seed=301, device="cuda", row_scale=(0.25, 4.0))
+    wl.slab[wl.block_table[0, 9], 0, 5, :] *= 6
+    wl.slab[wl.block_table[1, 20], 0, 17, :] *= 8
+    _parity(wl, 0, split=1024, max_ctx=1536, name="rescale")
+
+
+def test_padding_bucket(gpu_lib):
+    wl = synth.make_workload("padding128", device="cuda")
+    assert (wl.ctx_len == 0).sum() == 1 and (wl.block_table < 0).all(axis=1).sum() > 30
+    _parity(wl, 0, name="padding128")
+
+
+def test_ragged16_two_layers(gpu_lib):
+    wl = synth.make_workload("ragged16", device="cuda", n_layers=24)
+    for layer in (0, 23):
+        _parity(wl, layer, name=f"ragged16_l{layer}")
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_steady64_sampled_full_size(gpu_lib):
+    wl = synth.make_workload("steady64", device="cuda")
+    split = k3mla.default_split_tokens(64, 4096)
+    _parity(wl, 7, slots=[0, 31, 63], split=split, max_ctx=4096, name="steady64")
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_long8_sampled_full_size(gpu_lib):
+    wl = synth.make_workload("long8", device="cuda")
+    split = k3mla.default_split_tokens(8, 32768)
+    _parity(wl, 11, slots=[3], split=split, max_ctx=32768, name="long8")
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_a_flipped_latent_bit_fails_parity(gpu_lib):
+    """Negative control: the comparison must catch a one-bit change in one row."""
+    wl = synth.make_workload("tiny", device="cuda")
+    o = oracle_layer(wl, 0, probs_stride=130)
+    g0 = gpu_layer(wl, 0)
+    assert compare(g0, o, wl.ctx_len, name="negctl_clean")[0]
+    row = wl.slab[wl.block_table[0, 1], 0, 10]
+    bits = row.view(torch.int16)
+    bits[3] ^= 0x4000                         # exponent bit of one latent value
+    g1 = gpu_layer(wl, 0)
+    assert not compare(g1, o, wl.ctx_len, name="negctl_flipped")[0]

@@ -1,0 +1,102 @@
+"""Host-side tests of libk3mla.so that need no GPU: the library builds and loads,
+exports every symbol include/k3mla.h declares, the page pool behaves as the
+free-list allocator of pegainfer PR #869 ("K3: paged latent MLA KV + absorbed
+decode", M1 commit: claim on a 64-token boundary, release-all on reset, 0 =
+full coverage; review comment: expose total / allocated pages), and argument
+errors come back as status codes before anything is launched."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_latent_attention_k3mla_gb300 import k3mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_header_declarations_are_all_exported():
+    hdr = open(os.path.join(ROOT, "include", "k3mla.h")).read()
+    declared = set(re.findall(r"\b(k3mla_[a-z_]+)\s*\(", hdr))
+    assert declared == set(k3mla.EXPORTS), declared ^ set(k3mla.EXPORTS)
+    lib = k3mla.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    nm = os.popen(f"nm -D --defined-only {k3mla._build.LIB}").read()
+    for name in declared:
+        assert re.search(rf"\bT {name}\b", nm), f"{name} not exported"
+
+
+def test_pool_claims_on_page_boundaries_and_releases():
+    pool = k3mla.Pool(n_slots=3, max_ctx=256)
+    assert (pool.n_pages, pool.max_pages) == (12, 4)          # full coverage: 3 slots x 4 pages
+    assert pool.stats() == (12, 0)
+    assert pool.ensure(0, 1) == 0
+    assert pool.stats() == (12, 1)
+    assert pool.ensure(0, 64) == 0 and pool.stats()[1] == 1  # still inside page 0
+    assert pool.ensure(0, 65) == 0 and pool.stats()[1] == 2  # crossed a 64-token boundary
+    t = pool.table()
+    assert list(t[0, :2]) == [0, 1] and list(t[0, 2:]) == [-1, -1]
+    assert pool.ensure(1, 256) == 0
+    assert pool.stats() == (12, 6)
+    before = pool.table()[1].copy()
+    assert pool.release(1) == 0
+    assert pool.stats() == (12, 2)
+    assert np.all(pool.table()[1] == -1)
+    assert pool.ensure(1, 256) == 0                            # the same ids come back
+    assert np.array_equal(pool.table()[1], before)
+    pool.close()
+
+
+def test_pool_errors_are_all_or_nothing():
+    pool = k3mla.Pool(n_slots=2, max_ctx=256, n_pages=5)
+    assert pool.ensure(0, 256) == 0                            # 4 pages
+    assert pool.ensure(1, 129) == -2                           # needs 3, 1 left: K3MLA_E_NO_PAGES
+    assert pool.stats() == (5, 4) and np.all(pool.table()[1] == -1)
+    assert pool.ensure(1, 64) == 0
+    assert pool.ensure(1, 257) == -4                           # beyond max_ctx: K3MLA_E_CTX
+    assert pool.ensure(2, 1) == -3                             # no such slot: K3MLA_E_SLOT
+    assert pool.release(7) == -3
+    pool.close()
+
+
+def test_pool_shuffle_is_seeded_and_a_permutation():
+    a = k3mla.Pool(n_slots=4, max_ctx=1024, shuffle_seed=99)
+    b = k3mla.Pool(n_slots=4, max_ctx=1024, shuffle_seed=99)
+    c = k3mla.Pool(n_slots=4, max_ctx=1024, shuffle_seed=100)
+    for p in (a, b, c):
+        for s in range(4):
+            assert p.ensure(s, 1024) == 0
+    ta, tb, tc = a.table(), b.table(), c.table()
+    assert np.array_equal(ta, tb) and not np.array_equal(ta, tc)
+    assert sorted(ta.ravel().tolist()) == list(range(64))      # every page exactly once
+    assert not np.array_equal(ta.ravel(), np.arange(64))       # actually scattered
+
+
+def test_invalid_arguments_return_status_without_launching():
+    lib = k3mla.load()
+    null = None
+    # negative batch, bad layer, split not a multiple of the 128-token tile
+    assert lib.k3mla_absorb_q(null, null, null, -1, null) == -1
+    assert lib.k3mla_append_latent(null, 4, 2, 2, null, 1, null, null, 512, null, 64, 1, null, null) == -1
+    assert lib.k3mla_append_latent(null, 4, 2, 0, null, 1, null, null, 511, null, 64, 1, null, null) == -1
+    args = [null, null, 4, 1, 0, null, 4, null, null, 0x3D94, null, null, null, 0, 1, 256, 100, null, null]
+    assert lib.k3mla_paged_decode(*args) == -1
+    args[16] = 128
+    assert lib.k3mla_paged_decode(*args) == -1                 # null pointers
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    assert lib.k3mla_absorb_q(null, null, null, 0, null) == 0   # B == 0: nothing to do
+    assert lib.k3mla_diag_umma(5, null, null, null, null) == -1
+
+
+def test_workspace_formula():
+    # [B][nsplit][96][512] f32 partial O (rounded up to 256 B) + [B][nsplit][96][4] f32
+    for B, max_ctx, split in ((1, 130, 128), (64, 4096, 4096), (8, 32768, 3712), (128, 256, 256)):
+        ns = -(-max_ctx // split)
+        o = B * ns * 96 * 512 * 4
+        o = (o + 255) // 256 * 256
+        assert k3mla.decode_workspace_bytes(B, max_ctx, split) == o + B * ns * 96 * 4 * 4
+    assert k3mla.decode_workspace_bytes(0, 4096, 128) == 0
