@@ -1,0 +1,376 @@
+"""Benchmark: paged absorbed-MLA decode, microseconds per layer-call, on one GB300.
+
+Workload (default): 64 slots x 24 MLA layers, every slot at 4096 tokens (64
+pages), 96 heads, kv_lora 512 + rope 64, seed 2 -- synthetic, device-resident
+(7.25 GB slab, 302 MB of latent per layer, so every layer's inputs exceed the
+129 MB L2; no flush is needed between steps).
+
+A step is one pass of the whole hot path over the batch, for every layer: the
+new token's latent row appended into its mapped page, q absorbed, and the paged
+decode (split decode + merge / W_UV expansion).  The host page claim (pool
+ensure + table) runs once per step in the end-to-end leg.
+
+JSON line fields beyond the usual ones:
+  value            us per layer-call (24-layer step replayed as a CUDA graph / 24)
+  latent_gbs       latent bytes read per layer-call / time
+  roofline         the paged-decode call (split decode + merge/expand kernels):
+                   algorithmic bytes / its event-timed duration vs measured HBM
+  layer_roofline   the same for the whole layer-call (append + absorb + decode)
+  e2e              the same metric through the C ABI with host buffers: pinned
+                   H2D of the step's q / new rows / tables and D2H of the outputs
+                   inside the timed region, eager launches
+  cpu_baseline     the CPU oracle on a bounded sample of the workload
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_latent_attention_k3mla_gb300 import synth  # noqa: E402
+
+METRIC = "absorbed-MLA decode µs/layer and latent GB/s vs HBM/tensor roofline"
+H, NOPE, ROPE, V, LORA, ROW = 96, 128, 64, 128, 512, 576
+WORKLOAD_DESC = {
+    "steady64": "64 slots x 24 MLA layers x 4096 tokens (seed 2)",
+    "ragged16": "16 slots x 24 MLA layers, ctx U[1,4096] (seed 1)",
+    "long8": "8 slots x 24 MLA layers x 32768 tokens, heavy-tailed rows (seed 3)",
+    "padding128": "128 rows, 40% padding, ctx U[1,256] (seed 4)",
+    "tiny": "1 slot x 1 layer x 130 tokens (seed 0)",
+}
+MAX_CTX = {"steady64": 4096, "ragged16": 4096, "long8": 32768, "padding128": 256, "tiny": 256}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev=0):
+        self.dev = dev
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def alg_bytes(wl):
+    lat = wl.latent_bytes()
+    q = wl.B * H * (NOPE + ROPE) * 2
+    out = wl.B * H * V * 2
+    w = H * (NOPE + V) * LORA * 2
+    return dict(latent=lat, layer=lat + q + out + w + wl.B * ROW * 2,
+                decode=lat + wl.B * H * ROW * 2 + H * V * LORA * 2 + out)
+
+
+def alg_flops(wl):
+    n = int(wl.ctx_len.astype(np.int64).clip(min=0).sum())
+    return n * H * 2 * (ROW + LORA) + 2 * 2 * wl.B * H * 128 * LORA
+
+
+def cpu_baseline(wl, layer=0, n_slots=None):
+    """The oracle (as it stands) on a bounded sample: n_slots slots of one layer."""
+    import oracle
+    B = wl.B
+    if n_slots is None:
+        n_slots = min(B, 16 if int(wl.ctx_len.max()) <= 4096 else 2)
+    slots = list(range(n_slots))
+    ncores = os.cpu_count() or 1
+    tbl = wl.block_table[slots]
+    used = sorted(set(int(x) for x in tbl.ravel() if x >= 0))
+    remap = {p: i for i, p in enumerate(used)}
+    idx = torch.tensor(used if used else [0], dtype=torch.long, device=wl.slab.device)
+    slab = synth.bf16_bits(wl.slab.index_select(0, idx)[:, layer:layer + 1])
+    t2 = np.vectorize(lambda x: remap.get(int(x), -1))(tbl).astype(np.int32)
+    q = synth.bf16_bits(wl.q[layer][slots])
+    w = synth.bf16_bits(wl.w_kv_b[layer])
+    t0 = time.perf_counter()
+    qa = oracle.absorb(q, w)
+    oracle.decode(qa, slab, 0, t2, wl.ctx_len[slots].astype(np.int32), w, wl.scale_bits, nthreads=ncores)
+    dt = time.perf_counter() - t0
+    us_per_layer = dt * 1e6 * (B / n_slots)
+    return {"value": us_per_layer, "unit": "us/layer-call", "cores": ncores, "kind": "oracle",
+            "sample": f"{n_slots} of {B} slots of one layer-call (absorb + decode chain), "
+                      f"{dt:.2f} s wall on {ncores} threads, scaled by {B}/{n_slots}"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.make_workload(args.workload, device="cuda" if torch.cuda.is_available() else "cpu")
+    n_slots = min(wl.B, 4 if int(wl.ctx_len.max()) <= 4096 else 1)
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; kept for the contract's shape
+    vals = []
+    cb = None
+    for _ in range(args.steps):
+        cb = cpu_baseline(wl, 0, n_slots)
+        vals.append(cb["value"])
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/layer-call",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v * wl.n_layers / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC[args.workload], "slots": wl.B, "layers": wl.n_layers},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": v,
+                             "unit": "us/layer-call"},
+            "e2e": {"value": v, "unit": "us/layer-call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="steady64", choices=list(WORKLOAD_DESC))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling aid: fewer layers of the same per-layer workload")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != 1 or world != 1:
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"metric": METRIC, "unavailable": "single-GPU build: the decode needs no "
+                              "collective and runs as independent replicas only; no multi-GPU path is built"}))
+        return
+
+    from paged_latent_attention_k3mla_gb300 import k3mla
+    torch.cuda.set_device(0)
+    k3mla.load()
+    dev = "cuda"
+    wl = synth.make_workload(args.workload, device=dev, n_layers=args.layers)
+    B, L = wl.B, wl.n_layers
+    max_ctx = MAX_CTX[args.workload]
+    # a1: page claims from the host free-list pool (shuffled), table to the device
+    pool = k3mla.Pool(n_slots=B, max_ctx=max_ctx, n_pages=wl.n_pages, shuffle_seed=wl.seed + 1)
+    for b in range(B):
+        rc = pool.ensure(b, int(wl.ctx_len[b]))
+        assert rc == 0, rc
+    host_table = pool.table()
+    table = torch.from_numpy(host_table).to(dev)
+    ctx = torch.from_numpy(wl.ctx_len).to(dev)
+    pos = torch.from_numpy(wl.pos).to(dev)
+    split = k3mla.default_split_tokens(B, max_ctx)
+    q_abs = torch.empty(B, H, ROW, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(L, B, H, V, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(k3mla.decode_workspace_bytes(B, max_ctx, split), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    q_all, c_all, r_all = wl.q, wl.new_c, wl.new_rope
+    stream = torch.cuda.Stream()
+
+    def layer_call(layer, dec_events=None):
+        k3mla.append_latent(wl.slab, layer, table, pos, c_all[layer], r_all[layer], dev_err=err, stream=stream)
+        k3mla.absorb_q(q_all[layer], wl.w_kv_b[layer], q_abs, stream=stream)
+        if dec_events is not None:
+            dec_events[0].record(stream)
+        k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer], ws,
+                           max_ctx, split, dev_err=err, stream=stream)
+        if dec_events is not None:
+            dec_events[1].record(stream)
+
+    def step():
+        for layer in range(L):
+            layer_call(layer)
+
+    # ---- device-timed: the 24-layer step as one CUDA graph ----
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks() as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_per_step = ms_total / args.steps
+    us_per_layer = ms_per_step * 1e3 / L
+    assert err.item() == 0, f"device error bits {err.item()}"
+
+    # ---- the dominant call alone: paged decode (split decode + merge/expand) ----
+    pairs = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer_call(0)
+        for i in range(args.steps):
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            layer_call(i % L, e)
+            pairs.append(e)
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+    # ---- end to end through the C ABI with host buffers ----
+    q_h = q_all.cpu().pin_memory()
+    c_h = c_all.cpu().pin_memory()
+    r_h = r_all.cpu().pin_memory()
+    pos_h = torch.from_numpy(wl.pos).pin_memory()
+    ctx_h = torch.from_numpy(wl.ctx_len).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, c_d, r_d = torch.empty_like(q_all), torch.empty_like(c_all), torch.empty_like(r_all)
+    h2d = (q_h.numel() + c_h.numel() + r_h.numel()) * 2 + (pos_h.numel() + ctx_h.numel()) * 4 + host_table.nbytes
+    d2h = out_h.numel() * 2
+
+    tbl_pin = torch.from_numpy(host_table.copy()).pin_memory()
+
+    def e2e_step():
+        for b in range(B):                      # a1: claims on 64-token boundaries (none in steady state)
+            pool.ensure(b, int(wl.ctx_len[b]))
+        t_now = pool.table()
+        if not np.array_equal(t_now, tbl_pin.numpy()):
+            torch.cuda.current_stream().synchronize()
+            tbl_pin.numpy()[:] = t_now
+        with torch.cuda.stream(stream):
+            table.copy_(tbl_pin, non_blocking=True)
+            pos.copy_(pos_h, non_blocking=True)
+            ctx.copy_(ctx_h, non_blocking=True)
+            q_d.copy_(q_h, non_blocking=True)
+            c_d.copy_(c_h, non_blocking=True)
+            r_d.copy_(r_h, non_blocking=True)
+            for layer in range(L):
+                k3mla.append_latent(wl.slab, layer, table, pos, c_d[layer], r_d[layer], dev_err=err,
+                                    stream=stream)
+                k3mla.absorb_q(q_d[layer], wl.w_kv_b[layer], q_abs, stream=stream)
+                k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
+                                   ws, max_ctx, split, dev_err=err, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / args.steps
+    digest = hashlib.sha256(out_h.view(torch.int16).numpy().tobytes()).hexdigest()[:16]
+
+    hbm, tflops, src = peaks()
+    ab = alg_bytes(wl)
+    dec_gbs = ab["decode"] / (dec_ms * 1e-3) / 1e9
+    layer_gbs = ab["layer"] / (us_per_layer * 1e-6) / 1e9
+    flops = alg_flops(wl)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(prof):
+        try:
+            d = json.load(open(prof))
+            if d.get("workload") == args.workload and d.get("kernel_rev") == kernel_rev():
+                traffic = d.get("bytes_per_call")
+        except (ValueError, OSError):
+            traffic = None
+    cpu = None if args.no_cpu else cpu_baseline(wl, 0)
+    line = {
+        "metric": METRIC, "value": round(us_per_layer, 3), "unit": "us/layer-call", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload] if args.layers is None else
+                   f"{WORKLOAD_DESC[args.workload]}, first {L} layer(s) only", "slots": B, "layers": L,
+                   "context_tokens": int(wl.ctx_len.max()), "split_tokens": split,
+                   "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)",
+                   "timing": "24-layer step as one CUDA graph, CUDA events on the launch stream"},
+        "latent_gbs": round(ab["latent"] / (us_per_layer * 1e-6) / 1e9, 1),
+        "roofline": {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
+                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
+                     "traffic": traffic, "alg_bytes_per_call": ab["decode"], "avg_call_us": round(dec_ms * 1e3, 3),
+                     "peak_source": f"{src} hbm_gbs"},
+        "layer_roofline": {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": hbm, "unit": "GB/s",
+                           "frac": round(layer_gbs / hbm, 4), "alg_bytes_per_layer_call": ab["layer"],
+                           "tensor_frac": round(flops / (us_per_layer * 1e-6) / 1e12 / tflops, 4),
+                           "tensor_peak_tflops": tflops},
+        "e2e": {"value": round(e2e_ms * 1e3 / L, 3), "unit": "us/layer-call", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * L * 4,
+        "clocks": clk.summary(),
+        "out_sha256_16": digest,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def kernel_rev() -> str:
+    """Hash of the CUDA sources, so stored ncu traffic is only used for the kernel it measured."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_latent_attention_k3mla_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+if __name__ == "__main__":
+    main()
