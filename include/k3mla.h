@@ -177,14 +177,13 @@ int k3mla_pool_stats(const k3mla_pool* pool, int* total, int* used);
 void k3mla_pool_destroy(k3mla_pool* pool);
 
 /* ---- diagnostic --------------------------------------------------------------
- * Runs one tile of the decode kernel's two tensor-core contractions in
- * isolation so that their operand layouts can be checked against a plain
- * matrix product.  Not part of the decode path.
- *   mode 0: S[128][128] f32 = Q[128][576] (rows >= 96 zero) x T[128][576]^T,
- *           Q from `a` (device [96][576] bf16), T from tokens 0..127 of a
- *           2-page tile of `b` (device [2][64][576] bf16) -> d (device [128][128]).
- *   mode 1: O[512][96] f32 = T[128][0:512]^T x P[96][128]^T with T from `b` as
- *           above and P from `a` (device [96][128] bf16) -> d (device [512][96]).
+ * Runs the decode kernel's two tensor-core contractions on one 64-token page in
+ * isolation so that their operand layouts can be checked against a plain matrix
+ * product.  Not part of the decode path.  `b` is one page, device [64][576] bf16.
+ *   mode 0: S[128][64] f32 = Q[128][576] x T^T, Q from `a` (device [96][576]
+ *           bf16, rows >= 96 zero), T the page -> d (device [128][64] f32).
+ *   mode 1: O[512][96] f32 = T[:, 0:512]^T x P^T, P from `a` (device [96][64]
+ *           bf16) -> d (device [512][96] f32).
  */
 int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, float* d, void* stream);
 

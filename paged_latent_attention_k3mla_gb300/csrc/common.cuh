@@ -35,6 +35,26 @@ bool device_ok();
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows);
 
+// 3-D bf16 tensor map over the latent slab viewed as (64 elements, rows, chunks):
+// dim0 = 64 contiguous elements (128 bytes), dim1 = slab rows (pitch row_bytes),
+// dim2 = 64-element chunks of a row (pitch 128 bytes).  A box of
+// (64, box_rows, box_chunks) lands in shared memory as [chunk][row][128 B] with
+// 128-byte swizzle -- the K-major / MN-major operand layout of the tensor cores.
+int make_tmap_slab_3d(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems, uint32_t n_chunks,
+                      uint32_t box_rows, uint32_t box_chunks);
+
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Split partials -> o_lat -> W_UV expansion (merge_expand.cu).
+struct MergeParams {
+    const float* ws_o;     // [B][nsplit][96][512] f32 partial O
+    const float* ws_ml;    // [B][nsplit][96][4]: m_ref, l, best score, best t (int bits)
+    const int32_t* ctx_len;
+    const uint16_t* w_kv_b;
+    uint16_t* out;         // [B][96][128] bf16
+    int32_t* argmax;       // [B][96] or null
+    int B, max_ctx, max_pages, split, nsplit;
+};
+int launch_merge_expand(const MergeParams& mp, cudaStream_t st);
 
 }  // namespace k3

@@ -1,4 +1,4 @@
-// decode.cu -- paged absorbed-MLA decode for sm_103a.
+// decode.cu -- paged absorbed-MLA decode for sm_103a: the split kernel.
 //
 // Math (pegainfer PR #869, "K3: paged latent MLA KV + absorbed decode", M2
 // commit): for slot b, head h and logical token t with cache row r_t (a -1 block
@@ -7,34 +7,37 @@
 //     p     = softmax(s)
 //     o_lat = bf16( sum_t p_t r_t[0:512] )
 //     out   = bf16( W_UV[h] o_lat )
-// q_abs comes from k3mla_absorb_q; W_UV is read in place from w_kv_b.
+// q_abs comes from k3mla_absorb_q; the merge of splits and the W_UV expansion
+// are in merge_expand.cu.
 //
-// Structure (GB300-first; the page's own 3-sweep kernel is prior art only):
-//   * The context of a slot is cut into fixed splits of `split` logical tokens
-//     (a multiple of the 128-token tile).  Each split is one unit of work for a
-//     CLUSTER OF TWO CTAs, and each 64-token page is read once for all 96 heads:
-//       - CTA rank 0 ("score CTA") holds q_abs for the slot in TMEM (lanes =
-//         heads, 96 of 128 used) and streams 128-token tiles through a TMA ring
-//         of 16 KB chunks [128 tokens x 64 dims].  One tcgen05 MMA chain per
-//         tile computes S^T[heads x 128 tokens] = Q . C^T (K = 576, A from TMEM,
-//         B from shared memory) into TMEM.  Its four softmax warps (thread =
-//         head) land the scores to bf16 exactly as the chain does, keep a lazily
-//         rescaled running max per head, and write bf16 p_t straight into the
-//         partner CTA's shared memory (distributed shared memory) as the K-major
-//         B operand of the second contraction.
-//       - CTA rank 1 ("PV CTA") streams the same tiles (dims 0..511, 32 KB
-//         pair-slots [2 x 64 dims][128 tokens]) and accumulates
-//         O^T[512 dims x 96 heads] += C^T . P^T in TMEM (four M = 128 blocks,
-//         N = 96, K = 128 tokens per tile; A is the MN-major latent tile).  Its
-//         four epilogue warps rescale O when the score CTA moves a head's
-//         reference max, zero rows past the context in the final tile (stale
-//         rows must not meet p = 0 as 0 * NaN), and write the split's f32
-//         partial.
-//     TMEM holds Q (288 columns) + S (128) in rank 0 and O (384) in rank 1,
-//     which is why the two contractions live in different CTAs.
-//   * A second kernel merges the splits of each (slot, head) in ascending split
-//     order, lands o_lat in bf16 and expands it with W_UV[h] on tensor cores
-//     (mma.sync; W_UV is read once per head).
+// Structure (GB300-first; the page's own 3-sweep kernel is prior art only).
+// The context of a slot is cut into fixed splits of `split` logical tokens;
+// each split is one unit of work for a CLUSTER OF TWO CTAs, and the unit of the
+// pipeline is one 64-token page:
+//   * rank 0, the score CTA, holds q_abs of the slot in TMEM (lane = head, 96 of
+//     128 lanes used; 288 columns) and streams each page as two half-page TMA
+//     boxes of [9 chunks][32 rows][128 B] (one 36 KB 3-D box each: a TMA
+//     instruction costs about the same issue time whatever its size, so pages
+//     travel in big boxes) through a 5-slot ring filled by two producer threads.
+//     tcgen05 MMAs with A = Q from TMEM compute S^T[heads x 64 tokens] (K = 576,
+//     N = 32 per half page) into a double-buffered TMEM region.  Its softmax
+//     warps (thread = head) land the scores to bf16 exactly as the chain does --
+//     bf16(dot), then bf16(. * scale) with packed bf16x2 instructions -- keep a
+//     lazily moved reference max per head, and write bf16 p into a staging
+//     buffer laid out as the K-major B operand of the second contraction; one
+//     bulk copy per page moves it into the partner CTA's shared memory
+//     (distributed shared memory).
+//   * rank 1, the PV CTA, streams the same pages (chunks 0..7, one 64 KB 3-D box
+//     per page, 3-slot ring, two producers; these reads mostly hit L2 right after
+//     the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T in
+//     TMEM (four M = 128 blocks, N = 96, K = 64 tokens per page; A is the
+//     MN-major latent page).  Its epilogue warps rescale O when the score CTA
+//     moved a head's reference max, zero rows past the context in the final page
+//     (stale rows must never meet p = 0 as 0 * NaN), and write the split's f32
+//     partial.
+// TMEM holds Q (288 columns) + S (2 x 64) in rank 0 and O (384) in rank 1, which
+// is why the two contractions live in different CTAs.
+//
 // Split boundaries depend only on the logical position and ctx_len, and no
 // physical page id enters the arithmetic, so a slot's result is bitwise
 // independent of the batch, of padding and of page placement.
@@ -42,9 +45,12 @@
 // Departures from the chain, all inside the stated tolerance: the tensor cores
 // add the 576 products of a score and the tokens of o_lat in their own order;
 // probabilities are landed in bf16 before normalisation (p~_t = bf16(exp(s_t -
-// m_ref)), normalised by sum p~ at the end); the reference max m_ref of a head
-// moves only when the tile max exceeds it by more than TAU (else exp(s - m_ref)
-// <= e^TAU, far inside f32 / bf16 range); exp is the hardware ex2.
+// m_ref)), normalised by the f32 sum of exp at the end); the reference max m_ref
+// of a head moves only when a page max exceeds it by more than TAU (else
+// exp(s - m_ref) <= e^TAU, far inside f32 / bf16 range); exp is the hardware ex2.
+//
+// Every wait is bounded: after WAIT_NS a wait sets K3MLA_DEV_TIMEOUT in the
+// device error word, lets in-flight copies land and returns (no trap, no hang).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -56,42 +62,50 @@
 
 namespace k3 {
 
-constexpr int NS0 = 13;                // score-CTA ring slots
-constexpr int NS1 = 5;                 // PV-CTA ring pair-slots
-constexpr int SLOT0 = 16384;           // [128 tokens][64 dims] bf16, two 8 KB TMA boxes
-constexpr int SLOT1 = 32768;           // [2][128 tokens][64 dims] bf16, four boxes
-constexpr int PT_ATOM = H * 128;       // 96 rows x 128 B = one K-atom of P^T
-constexpr int PT_BYTES = 2 * PT_ATOM;  // P^T for a 128-token tile
+constexpr int HALF = 32;                       // tokens per score-CTA TMA box
+constexpr int NS0 = 5;                         // score CTA: half-page slots
+constexpr int SLOT0 = 9 * HALF * 128;          // 36864 B: [9 chunks][32 rows][128 B]
+constexpr int CHUNK0 = HALF * 128;             // 4096 B per chunk in a half-page slot
+constexpr int NS1 = 3;                         // PV CTA: page slots
+constexpr int SLOT1 = 8 * PAGE * 128;          // 65536 B: [8 chunks][64 rows][128 B]
+constexpr int CHUNK1 = PAGE * 128;             // 8192 B per chunk in a page slot
+constexpr int PT_BYTES = H * 128;              // 12288 B: P^T [96 heads][64 tokens] bf16, K-major SW128
+constexpr int META_ALPHA = PT_BYTES;           // f32 alpha[96]
+constexpr int META_FLAGS = PT_BYTES + 4 * H;   // u32 flags[4]: "some head of warp w rescaled"
+constexpr int PCOPY = PT_BYTES + 4 * H + 16;   // bytes moved per page (12688, a multiple of 16)
+constexpr int PBUF = 13 * 1024;                // buffer pitch, keeps every P^T 1024-byte aligned
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;          // score CTA: S^T [128 lanes x 128 cols f32]
-constexpr uint32_t Q_COL = 128;        // score CTA: Q   [128 lanes x 288 cols (576 bf16)]
-constexpr float TAU = 8.0f;            // max growth (natural log) before a rescale
-constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
-constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);   // S^T = Q . C^T
-constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T = C^T . P^T (A MN-major)
-constexpr int THREADS = 192;
+constexpr uint32_t S_COL = 0;                  // score CTA: S^T double buffer, 2 x 64 columns
+constexpr uint32_t Q_COL = 128;                // score CTA: Q, 288 columns (576 bf16)
+constexpr float TAU = 8.0f;                    // max growth (natural log) before a rescale
+constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
+constexpr uint32_t IDESC_S = make_idesc_bf16(128, HALF, 0, 0);  // S^T half page = Q . C^T
+constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
+constexpr int THREADS = 224;                   // warps 0-3 softmax / epilogue, 4 and 6 producers, 5 MMA
+constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the three softmax warps
 
 struct __align__(1024) Smem {
     union {
-        uint8_t ring0[NS0][SLOT0];
         struct {
-            uint8_t ring1[NS1][SLOT1];
-            uint8_t pt[2][PT_BYTES];
+            uint8_t ring[NS0][SLOT0];
+            uint8_t stage[2][PBUF];
+        } c0;
+        struct {
+            uint8_t ring[NS1][SLOT1];
+            uint8_t recv[2][PBUF];
         } c1;
     } u;
-    float alpha[2][H];        // PV CTA: per-head rescale factors (written by the score CTA)
-    uint32_t rflag[2][4];     // PV CTA: per-warp "some head rescaled" flags
-    uint64_t full[16];
-    uint64_t empty[16];
-    uint64_t s_full, s_empty, q_ready;
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t s_full[2], s_empty[2], q_ready;
     uint64_t p_full[2], p_empty[2];
     uint64_t o_done, epi_req, epi_done;
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot, epi_stage, epi_vrows;
     int32_t abort_flag;
 };
-static_assert(sizeof(Smem::u) == NS0 * SLOT0, "ring layouts");
-static_assert(NS1 * SLOT1 + 2 * PT_BYTES == NS0 * SLOT0, "ring layouts");
+static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
+static_assert(PCOPY % 16 == 0 && PCOPY <= PBUF, "bulk copy size");
 
 struct DecodeParams {
     const uint16_t* q_abs;
@@ -102,7 +116,7 @@ struct DecodeParams {
     int32_t* dev_err;
     int max_pages, n_pages, n_layers, layer;
     int B, max_ctx, split, nsplit;
-    float scale;
+    uint32_t scale2;  // the bf16 scale in both halves
 };
 
 __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int max_ctx, int max_pages,
@@ -117,6 +131,11 @@ __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int 
     return n < 0 ? 0 : n;
 }
 
+__device__ __forceinline__ bool aborted(const Smem& sm)
+{
+    return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
+}
+
 // Bounded mbarrier wait: gives up after WAIT_NS or when this CTA aborted.
 __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
                                       bool cluster_scope = false)
@@ -127,7 +146,7 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, 
     for (uint32_t n = 1;; ++n) {
         if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
         if ((n & 127u) == 0) {
-            if (*reinterpret_cast<volatile int32_t*>(&sm.abort_flag)) return false;
+            if (aborted(sm)) return false;
             if (globaltimer() - t0 > WAIT_NS) {
                 *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
                 if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
@@ -144,7 +163,9 @@ __device__ __noinline__ void drain_inflight()
     while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
 }
 
-// TMA row coordinate of logical page lp of slot b, or an out-of-range row (zero fill).
+// First slab row of logical page lp of slot b at this layer, or a row past the
+// end of the slab (the TMA box then reads zeros) for -1, for pages past the
+// context, and for ids outside [-1, n_pages) (flagged).
 __device__ __forceinline__ int32_t page_row(const DecodeParams& p, int b, int lp, int n_lp, int32_t oob_row)
 {
     if (lp >= n_lp) return oob_row;
@@ -157,10 +178,10 @@ __device__ __forceinline__ int32_t page_row(const DecodeParams& p, int b, int lp
     return (id * p.n_layers + p.layer) * PAGE;
 }
 
-// ---- shared building blocks (also used by the diagnostic kernel) ---------------
+// ---- building blocks shared with the diagnostic kernel -----------------------------
 
-// Score CTA: rows 0..95 of Q (one row per thread h = 0..127, rows >= 96 zero)
-// into TMEM columns [Q_COL, Q_COL+288) of lane h.  Called by warps 0..3.
+// Score CTA: row h of Q (thread h = 0..127; rows >= 96 zero) into TMEM columns
+// [Q_COL, Q_COL + 288) of lane h, two bf16 per column.  Called by warps 0..3.
 __device__ __forceinline__ void load_q_tmem(uint32_t tbase, const uint16_t* qrow_or_null)
 {
     const uint32_t w = threadIdx.x >> 5;
@@ -187,40 +208,43 @@ __device__ __forceinline__ void load_q_tmem(uint32_t tbase, const uint16_t* qrow
     tmem_wait_st();
 }
 
-// Score CTA: the MMAs of one 576-wide chunk c (4 K-steps of 16) of a tile.
-__device__ __forceinline__ void issue_score_chunk(uint32_t tbase, uint32_t slot_addr, int c)
+// Score CTA: S^T[:, 32 tokens] = Q . C^T for one half-page slot (36 MMAs, K = 576).
+__device__ __forceinline__ void issue_score_half(uint32_t tbase, uint32_t d_col, uint32_t slot_addr)
 {
+#pragma unroll 1
+    for (int c = 0; c < 9; ++c) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t a = tbase + Q_COL + (uint32_t)(4 * c + ks) * 8u;
-        const uint64_t bd = make_sdesc(slot_addr + ks * 32, 16, 1024);
-        umma_ts(tbase + S_COL, a, bd, IDESC_S, (c | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t a = tbase + Q_COL + (uint32_t)(4 * c + ks) * 8u;
+            const uint64_t bd = make_sdesc(slot_addr + c * CHUNK0 + ks * 32, 16, 1024);
+            umma_ts(tbase + d_col, a, bd, IDESC_S, (c | ks) != 0);
+        }
     }
 }
 
-// PV CTA: O^T block j (dims 128j..128j+127) += C^T . P^T over one 128-token tile.
-__device__ __forceinline__ void issue_pv_block(uint32_t tbase, uint32_t pair_addr, uint32_t pt_addr, int j,
-                                               bool accumulate_first)
+// PV CTA: O^T (+)= C^T . P^T over one 64-token page: 4 blocks of 128 dims x 4 K-steps.
+__device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t page_addr, uint32_t pt_addr,
+                                              bool accumulate_first)
 {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = make_sdesc(pair_addr + ks * 2048, SLOT1 / 2, 1024);
-        const uint64_t bd = make_sdesc(pt_addr + (ks >> 2) * PT_ATOM + (ks & 3) * 32, 16, 1024);
-        umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || ks > 0) ? 1u : 0u);
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = make_sdesc(page_addr + 2 * j * CHUNK1 + ks * 2048, CHUNK1, 1024);
+            const uint64_t bd = make_sdesc(pt_addr + ks * 32, 16, 1024);
+            umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || ks > 0) ? 1u : 0u);
+        }
     }
 }
 
-// Byte offset, inside a P^T buffer, of the 16-byte chunk holding tokens
-// 64a + 8j .. 64a + 8j + 7 of head h (K-major, 128-byte swizzle).
-__device__ __forceinline__ uint32_t pt_chunk_off(int h, int a, int j)
-{
-    return (uint32_t)(a * PT_ATOM + h * 128 + ((j ^ (h & 7)) << 4));
-}
+// Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
+__device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_t)(h * 128 + ((j ^ (h & 7)) << 4)); }
 
-// ---- the split decode kernel ---------------------------------------------------
+// ---- the split decode kernel ---------------------------------------------------------
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p)
+    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_half,
+                              const __grid_constant__ CUtensorMap tmap_page, const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -236,33 +260,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int start = s * p.split;
     if (start >= ctx) return;  // empty split: both CTAs leave, nothing was shared
     const int ntok = min(ctx, start + p.split) - start;
-    const int ntiles = (ntok + TILE - 1) / TILE;
+    const int npg = (ntok + PAGE - 1) / PAGE;
     const int n_lp = (ctx + PAGE - 1) / PAGE;
+    const int lp0 = start / PAGE;
     const int32_t oob_row = p.n_pages * p.n_layers * PAGE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
         }
-        mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_empty, 3);
-        mbar_init(&sm.q_ready, 4);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.p_full[i], H);
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], 3);
+            mbar_init(&sm.p_full[i], 1);
             mbar_init(&sm.p_empty[i], 1);
         }
+        mbar_init(&sm.q_ready, 4);
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.epi_req, 1);
         mbar_init(&sm.epi_done, 4);
         sm.abort_flag = 0;
+        if (rank == 1) {  // the P buffers of pages 0 and 1 are expected before anything is sent
+            mbar_arrive_expect_tx(&sm.p_full[0], PCOPY);
+            mbar_arrive_expect_tx(&sm.p_full[1], PCOPY);
+        }
         fence_mbarrier_init_cluster();
     }
     if (warp == 5) {
         tmem_alloc(&sm.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) tma_prefetch_desc(&tmap);
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmap_half);
+        tma_prefetch_desc(&tmap_page);
+    }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
@@ -270,29 +302,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     if (rank == 0) {
         // =========================== score CTA ===========================
-        if (warp == 4) {
-            if (lane == 0) {
-                const uint64_t pol = policy_evict_first();
-                int slot = 0;
-                uint32_t ph = 0;
+        if (warp == 4 || warp == 6) {
+            if (lane == 0) {  // producer hh streams half hh of every page
+                const int hh = warp == 4 ? 0 : 1;
                 bool ok = true;
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    const int lp0 = start / PAGE + 2 * i;
-                    const int32_t ya = page_row(p, b, lp0, n_lp, oob_row);
-                    const int32_t yb = page_row(p, b, lp0 + 1, n_lp, oob_row);
-                    for (int c = 0; c < 9; ++c) {
-                        if (!wait_bar(&sm.empty[slot], ph ^ 1u, sm, p.dev_err)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&sm.full[slot], SLOT0);
-                        tma_load_2d(sm.u.ring0[slot], &tmap, 64 * c, ya, &sm.full[slot], pol);
-                        tma_load_2d(sm.u.ring0[slot] + SLOT0 / 2, &tmap, 64 * c, yb, &sm.full[slot], pol);
-                        if (++slot == NS0) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
+                for (int i = 0; i < npg && ok; ++i) {
+                    const int u = 2 * i + hh, slot = u % NS0, k = u / NS0;
+                    const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
+                    if (!wait_bar(&sm.empty[slot], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                        ok = false;
+                        break;
                     }
+                    mbar_arrive_expect_tx(&sm.full[slot], SLOT0);
+                    tma_load_3d(sm.u.c0.ring[slot], &tmap_half, 0, y + HALF * hh, 0, &sm.full[slot]);
                 }
                 if (!ok) drain_inflight();
             }
@@ -300,33 +322,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (lane == 0) {
                 bool ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
                 tc_fence_after();
-                int slot = 0;
-                uint32_t ph = 0;
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    if (!wait_bar(&sm.s_empty, (uint32_t)(i & 1) ^ 1u, sm, p.dev_err)) {
+                for (int i = 0; i < npg && ok; ++i) {
+                    const int sb = i & 1;
+                    if (!wait_bar(&sm.s_empty[sb], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int c = 0; c < 9; ++c) {
-                        if (!wait_bar(&sm.full[slot], ph, sm, p.dev_err)) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int u = 2 * i + hh, slot = u % NS0, k = u / NS0;
+                        if (!wait_bar(&sm.full[slot], (uint32_t)(k & 1), sm, p.dev_err)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_score_chunk(tbase, smem_u32(sm.u.ring0[slot]), c);
+                        issue_score_half(tbase, S_COL + 64u * sb + HALF * hh, smem_u32(sm.u.c0.ring[slot]));
                         umma_commit(&sm.empty[slot]);
-                        if (++slot == NS0) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
                     }
-                    if (ok) umma_commit(&sm.s_full);
+                    if (ok) umma_commit(&sm.s_full[sb]);
                 }
                 if (!ok) drain_inflight();
             }
-        } else {
-            // softmax warps 0..3: thread h owns head h (h < 96)
+        } else if (warp < 4) {
+            // softmax warps 0..2 (thread h = head); warp 3 only loads its Q lanes
             const int h = (int)threadIdx.x;
             load_q_tmem(tbase, h < H ? p.q_abs + ((size_t)b * H + h) * ROW : nullptr);
             tc_fence_before();
@@ -334,55 +352,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (lane == 0) mbar_arrive(&sm.q_ready);
             if (warp < 3) {
                 const uint32_t t_lane = tbase + ((32u * warp) << 16);
-                const float scale = p.scale;
                 const float LOG2E = 1.4426950408889634f;
                 float m_ref = -INFINITY, l = 0.f, best_s = -INFINITY;
                 int best_t = -1;
-                bool ok = true;
-                const uint32_t pt_remote0 = mapa(smem_u32(sm.u.c1.pt[0]), 1);
-                const uint32_t pt_remote1 = mapa(smem_u32(sm.u.c1.pt[1]), 1);
-                for (int i = 0; i < ntiles; ++i) {
-                    const bool got = wait_bar(&sm.s_full, (uint32_t)(i & 1), sm, p.dev_err);
+                const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
+                const uint32_t recv1 = mapa(smem_u32(sm.u.c1.recv[1]), 1);
+                const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
+                const uint32_t pfull1 = mapa(smem_u32(&sm.p_full[1]), 1);
+                for (int i = 0; i < npg; ++i) {
+                    const int sb = i & 1;
+                    const bool got = wait_bar(&sm.s_full[sb], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
+                    if (named_bar_any(SOFTMAX_BAR, 96, !got || aborted(sm))) break;  // uniform decision
                     __syncwarp();
-                    if (!__all_sync(0xFFFFFFFFu, got)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
-                    const int nvalid = min(TILE, ntok - TILE * i);
-                    uint32_t sp[64];  // bf16 scores, two per word (token 2k low, 2k+1 high)
-                    float tmax = -INFINITY;
+                    const int nvalid = min(PAGE, ntok - PAGE * i);
+                    uint32_t sp[32];  // bf16 scores: token 2k in the low half, 2k+1 in the high half
 #pragma unroll
-                    for (int piece = 0; piece < 4; ++piece) {
+                    for (int piece = 0; piece < 2; ++piece) {
                         uint32_t r[32];
-                        tmem_ld32(t_lane + S_COL + 32 * piece, r);
+                        tmem_ld32(t_lane + S_COL + 64u * sb + 32u * piece, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
-                            const int t = 32 * piece + k;
-                            // land the dot in bf16, multiply by the bf16 scale, land again
-                            const uint32_t d2 = pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]));
-                            float s0 = bf16lo_to_f32(d2) * scale;
-                            float s1 = bf16hi_to_f32(d2) * scale;
-                            uint32_t s2 = pack_bf16x2(s0, s1);
-                            if (t >= nvalid) s2 = (s2 & 0xFFFF0000u) | 0xFF80u;            // -inf
-                            if (t + 1 >= nvalid) s2 = (s2 & 0x0000FFFFu) | 0xFF800000u;
-                            sp[t >> 1] = s2;
-                            tmax = fmaxf(tmax, fmaxf(bf16lo_to_f32(s2), bf16hi_to_f32(s2)));
-                        }
+                        for (int k = 0; k < 16; ++k)  // bf16(dot), then bf16(bf16(dot) * scale)
+                            sp[16 * piece + k] =
+                                mul_bf16x2(pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
+                                           p.scale2);
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.s_empty);
-
+                    if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
+                    if (nvalid < PAGE) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            if (2 * k >= nvalid) sp[k] = (sp[k] & 0xFFFF0000u) | 0xFF80u;  // -inf
+                            if (2 * k + 1 >= nvalid) sp[k] = (sp[k] & 0x0000FFFFu) | 0xFF800000u;
+                        }
+                    }
+                    uint32_t m2 = sp[0];
+#pragma unroll
+                    for (int k = 1; k < 32; ++k) m2 = max_bf16x2(m2, sp[k]);
+                    const float tmax = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
                     if (tmax > best_s) {  // lowest logical t attaining the best score
                         best_s = tmax;
                         int first = 0;
-                        for (int k = 63; k >= 0; --k) {
+                        for (int k = 31; k >= 0; --k) {
                             if (bf16hi_to_f32(sp[k]) == tmax) first = 2 * k + 1;
                             if (bf16lo_to_f32(sp[k]) == tmax) first = 2 * k;
                         }
-                        best_t = start + TILE * i + first;
+                        best_t = start + PAGE * i + first;
                     }
                     float alpha = 1.f;
                     bool resc = false;
@@ -395,112 +412,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         resc = true;
                     }
                     const float mb = m_ref * LOG2E;
-                    uint32_t pp[64];
+                    uint32_t pp[32];
 #pragma unroll
-                    for (int k = 0; k < 64; ++k) {
+                    for (int k = 0; k < 32; ++k) {
                         const float e0 = ex2_approx(fmaf(bf16lo_to_f32(sp[k]), LOG2E, -mb));
                         const float e1 = ex2_approx(fmaf(bf16hi_to_f32(sp[k]), LOG2E, -mb));
-                        const uint32_t q2 = pack_bf16x2(e0, e1);
-                        l += bf16lo_to_f32(q2);
-                        l += bf16hi_to_f32(q2);
-                        pp[k] = q2;
+                        l += e0;
+                        l += e1;
+                        pp[k] = pack_bf16x2(e0, e1);
                     }
-                    const int stage = i & 1;
-                    const bool freed = wait_bar(&sm.p_empty[stage], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err);
-                    if (!__all_sync(0xFFFFFFFFu, freed)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dst = stage ? pt_remote1 : pt_remote0;
+                    const int st = i & 1;
+                    uint8_t* stage = sm.u.c0.stage[st];
+                    if (h == 0) bulk_wait_read<1>();  // the copy of page i-2 has read this buffer
+                    named_bar(SOFTMAX_BAR, 96);
 #pragma unroll
-                    for (int a = 0; a < 2; ++a)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int k = 32 * a + 4 * j;
-                            st_cluster_v4(dst + pt_chunk_off(h, a, j), make_uint4(pp[k], pp[k + 1], pp[k + 2], pp[k + 3]));
-                        }
-                    st_cluster_u32(mapa(smem_u32(&sm.alpha[stage][h]), 1), __float_as_uint(alpha));
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(stage + pt_chunk_off(h, j)) =
+                            make_uint4(pp[4 * j], pp[4 * j + 1], pp[4 * j + 2], pp[4 * j + 3]);
+                    reinterpret_cast<float*>(stage + META_ALPHA)[h] = alpha;
                     const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc);
-                    if (lane == 0) st_cluster_u32(mapa(smem_u32(&sm.rflag[stage][warp]), 1), any ? 1u : 0u);
-                    fence_proxy_async_cluster();
-                    mbar_arrive_remote(mapa(smem_u32(&sm.p_full[stage]), 1));
+                    if (lane == 0) reinterpret_cast<uint32_t*>(stage + META_FLAGS)[warp] = any ? 1u : 0u;
+                    fence_proxy_async_cta();
+                    named_bar(SOFTMAX_BAR, 96);
+                    if (h == 0) {
+                        // the PV CTA has finished with its buffer from page i-2
+                        if (wait_bar(&sm.p_empty[st], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err)) {
+                            bulk_copy_to_cluster(st ? recv1 : recv0, stage, PCOPY, st ? pfull1 : pfull0);
+                            bulk_commit();
+                        }
+                    }
                 }
-                if (ok) {
+                if (!aborted(sm)) {
                     float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
                     ml[0] = m_ref;
                     ml[1] = l;
                     ml[2] = best_s;
                     ml[3] = __int_as_float(best_t);
-                    // the PV CTA's last releases of the P buffers land here before exit
-                    for (int i = max(0, ntiles - 2); i < ntiles && ok; ++i)
-                        ok = wait_bar(&sm.p_empty[i & 1], (uint32_t)(((i >> 1) & 1)), sm, p.dev_err);
+                }
+                if (h == 0) {
+                    bulk_wait<0>();  // every P copy has landed in the PV CTA
+                    // the PV CTA's last releases of its P buffers land here before exit
+                    for (int i = max(0, npg - 2); i < npg && !aborted(sm); ++i)
+                        wait_bar(&sm.p_empty[i & 1], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
                 }
             }
         }
     } else {
         // ============================ PV CTA ============================
-        if (warp == 4) {
-            if (lane == 0) {
-                const uint64_t pol = policy_evict_first();
-                int slot = 0;
-                uint32_t ph = 0;
+        if (warp == 4 || warp == 6) {
+            if (lane == 0) {  // producer q streams the pages i with i % 2 == q
+                const uint64_t pol = policy_evict_first();  // last reader of the latent
+                const int q = warp == 4 ? 0 : 1;
                 bool ok = true;
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    const int lp0 = start / PAGE + 2 * i;
-                    const int32_t ya = page_row(p, b, lp0, n_lp, oob_row);
-                    const int32_t yb = page_row(p, b, lp0 + 1, n_lp, oob_row);
-                    for (int j = 0; j < 4; ++j) {
-                        if (!wait_bar(&sm.empty[slot], ph ^ 1u, sm, p.dev_err)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t* dst = sm.u.c1.ring1[slot];
-                        mbar_arrive_expect_tx(&sm.full[slot], SLOT1);
-                        tma_load_2d(dst, &tmap, 128 * j, ya, &sm.full[slot], pol);
-                        tma_load_2d(dst + 8192, &tmap, 128 * j, yb, &sm.full[slot], pol);
-                        tma_load_2d(dst + 16384, &tmap, 128 * j + 64, ya, &sm.full[slot], pol);
-                        tma_load_2d(dst + 24576, &tmap, 128 * j + 64, yb, &sm.full[slot], pol);
-                        if (++slot == NS1) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
+                for (int i = q; i < npg && ok; i += 2) {
+                    const int slot = i % NS1, k = i / NS1;
+                    const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
+                    if (!wait_bar(&sm.empty[slot], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                        ok = false;
+                        break;
                     }
+                    mbar_arrive_expect_tx(&sm.full[slot], SLOT1);
+                    tma_load_3d_hint(sm.u.c1.ring[slot], &tmap_page, 0, y, 0, &sm.full[slot], pol);
                 }
                 if (!ok) drain_inflight();
             }
         } else if (warp == 5) {
             if (lane == 0) {
-                int slot = 0;
-                uint32_t ph = 0;
                 uint32_t epi_k = 0;
                 bool ok = true;
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    const int stage = i & 1;
-                    if (!wait_bar(&sm.p_full[stage], (uint32_t)((i >> 1) & 1), sm, p.dev_err, true)) {
+                for (int i = 0; i < npg && ok; ++i) {
+                    const int st = i & 1;
+                    if (!wait_bar(&sm.p_full[st], (uint32_t)((i >> 1) & 1), sm, p.dev_err, true)) {
                         ok = false;
                         break;
                     }
-                    const volatile uint32_t* rf = sm.rflag[stage];
+                    const volatile uint32_t* rf =
+                        reinterpret_cast<const volatile uint32_t*>(sm.u.c1.recv[st] + META_FLAGS);
                     const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2]) != 0u);
-                    const int nvalid = min(TILE, ntok - TILE * i);
-                    const bool tail = nvalid < TILE;
-                    if (tail) {  // the epilogue zeroes stale rows once the tile has landed
-                        int sl = slot;
-                        uint32_t pf = ph;
-                        for (int j = 0; j < 4 && ok; ++j) {
-                            ok = wait_bar(&sm.full[sl], pf, sm, p.dev_err);
-                            if (++sl == NS1) {
-                                sl = 0;
-                                pf ^= 1u;
-                            }
-                        }
-                        if (!ok) break;
+                    const int nvalid = min(PAGE, ntok - PAGE * i);
+                    const bool tail = nvalid < PAGE;
+                    const int slot = i % NS1, k = i / NS1;
+                    if (!wait_bar(&sm.full[slot], (uint32_t)(k & 1), sm, p.dev_err)) {
+                        ok = false;
+                        break;
                     }
                     if (resc || tail) {
                         if (resc) umma_commit(&sm.o_done);
                         sm.epi_cmd = (resc ? 1u : 0u) | (tail ? 2u : 0u);
                         sm.epi_slot = (uint32_t)slot;
-                        sm.epi_stage = (uint32_t)stage;
+                        sm.epi_stage = (uint32_t)st;
                         sm.epi_vrows = (uint32_t)nvalid;
                         mbar_arrive(&sm.epi_req);
                         if (!wait_bar(&sm.epi_done, epi_k & 1u, sm, p.dev_err)) {
@@ -509,21 +509,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         }
                         ++epi_k;
                     }
-                    const uint32_t pt = smem_u32(sm.u.c1.pt[stage]);
-                    for (int j = 0; j < 4; ++j) {
-                        if (!tail && !wait_bar(&sm.full[slot], ph, sm, p.dev_err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_pv_block(tbase, smem_u32(sm.u.c1.ring1[slot]), pt, j, i > 0);
-                        umma_commit(&sm.empty[slot]);
-                        if (++slot == NS1) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (ok) umma_commit_mc(&sm.p_empty[stage], (uint16_t)0x1);
+                    tc_fence_after();
+                    issue_pv_page(tbase, smem_u32(sm.u.c1.ring[slot]), smem_u32(sm.u.c1.recv[st]), i > 0);
+                    umma_commit(&sm.empty[slot]);
+                    umma_commit_mc(&sm.p_empty[st], (uint16_t)0x1);
+                    if (i + 2 < npg) mbar_arrive_expect_tx(&sm.p_full[st], PCOPY);
                 }
                 if (ok) {
                     umma_commit(&sm.o_done);
@@ -534,8 +524,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
                 }
             }
-        } else {
-            // epilogue warps 0..3: thread owns TMEM lane 32*warp + lane (a latent dim per block)
+        } else if (warp < 4) {
+            // epilogue warps 0..3: thread owns TMEM lane 32*warp + lane (one latent dim per block)
             const uint32_t t_lane = tbase + ((32u * warp) << 16);
             uint32_t k = 0, od = 0;
             for (;;) {
@@ -544,11 +534,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 ++k;
                 const uint32_t cmd = *reinterpret_cast<volatile uint32_t*>(&sm.epi_cmd);
                 if (cmd & 1u) {  // rescale O^T columns by alpha[head]
-                    const bool got = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
-                    if (!__all_sync(0xFFFFFFFFu, got)) break;
+                    const bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
+                    if (!__all_sync(0xFFFFFFFFu, got2)) break;
                     ++od;
                     tc_fence_after();
-                    const float* al = sm.alpha[sm.epi_stage];
+                    const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + META_ALPHA);
                     for (int j = 0; j < 4; ++j)
                         for (int piece = 0; piece < 3; ++piece) {
                             uint32_t r[32];
@@ -563,27 +553,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     tmem_wait_st();
                     tc_fence_before();
                 }
-                if (cmd & 2u) {  // zero rows >= vrows of the tile's four pair-slots
+                if (cmd & 2u) {  // zero rows >= vrows of chunks 0..7 of the final page
                     const int vr = (int)sm.epi_vrows;
-                    const int rows = TILE - vr;
-                    const int per_half = rows * 8;  // 16-byte chunks
-                    const int total = 4 * 2 * per_half;
-                    for (int q = (int)threadIdx.x; q < total; q += 128) {
-                        const int sl_off = q / (2 * per_half);
-                        const int rem = q % (2 * per_half);
-                        const int half = rem / per_half;
-                        const int c16 = rem % per_half;
-                        const int row = vr + c16 / 8;
-                        const int sl = ((int)sm.epi_slot + sl_off) % NS1;
-                        uint4* d = reinterpret_cast<uint4*>(sm.u.c1.ring1[sl] + half * (SLOT1 / 2) + row * 128 +
-                                                            (c16 % 8) * 16);
-                        *d = make_uint4(0u, 0u, 0u, 0u);
+                    const int per_chunk = (PAGE - vr) * 8;  // 16-byte pieces
+                    uint8_t* page = sm.u.c1.ring[sm.epi_slot];
+                    for (int q = (int)threadIdx.x; q < 8 * per_chunk; q += 128) {
+                        const int c = q / per_chunk, rem = q % per_chunk;
+                        *reinterpret_cast<uint4*>(page + c * CHUNK1 + (vr + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_cta();
                 }
                 if (cmd & 4u) {  // final: write the split's f32 partial O
-                    const bool got = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
-                    if (!__all_sync(0xFFFFFFFFu, got)) break;
+                    const bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
+                    if (!__all_sync(0xFFFFFFFFu, got2)) break;
                     ++od;
                     tc_fence_after();
                     float* o = p.ws_o + (((size_t)b * p.nsplit + s) * H) * LORA;
@@ -614,135 +597,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 5) tmem_dealloc(tbase, TMEM_COLS);
 }
 
-// ---- merge of the splits + W_UV expansion ------------------------------------------
-
-constexpr int MX_THREADS = 256;
-constexpr int W_PITCH = LORA + 8;   // bf16 elements per smem row (16-byte pad)
-
-struct MergeParams {
-    const float* ws_o;
-    const float* ws_ml;
-    const int32_t* ctx_len;
-    const uint16_t* w_kv_b;
-    uint16_t* out;
-    int32_t* argmax;
-    int B, max_ctx, max_pages, split, nsplit;
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// grid (2 halves of v, 96 heads); each CTA keeps W_UV[h][64 v][512] in shared memory.
-__global__ void __launch_bounds__(MX_THREADS) k3mla_merge_expand_kernel(const MergeParams p)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint16_t* sw = reinterpret_cast<uint16_t*>(smem_raw);   // [64][W_PITCH]
-    uint16_t* so = sw + 64 * W_PITCH;                         // [16][W_PITCH]
-    const int vh = blockIdx.x;
-    const int h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-
-    // W_UV[h] rows vh*64 .. vh*64+63 (w_kv_b rows h*256 + 128 + v)
-    const uint16_t* wsrc = p.w_kv_b + ((size_t)h * WROWS_PER_HEAD + NOPE + vh * 64) * LORA;
-    for (int q = tid; q < 64 * (LORA / 8); q += MX_THREADS) {
-        const int r = q / (LORA / 8), c8 = q % (LORA / 8);
-        *reinterpret_cast<uint4*>(sw + r * W_PITCH + c8 * 8) =
-            __ldg(reinterpret_cast<const uint4*>(wsrc + (size_t)r * LORA) + c8);
-    }
-
-    for (int m0 = 0; m0 < p.B; m0 += 16) {
-        __syncthreads();
-        {   // merge: thread -> (row r, dims 32*jc .. 32*jc+31)
-            const int r = tid >> 4, jc = tid & 15;
-            const int b = m0 + r;
-            float o[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = 0.f;
-            float l = 1.f;
-            if (b < p.B) {
-                const int ctx = ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages, nullptr, false);
-                const int ns = (ctx + p.split - 1) / p.split;
-                if (ns > 0) {
-                    const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-                    float m = -INFINITY;
-                    for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-                    l = 0.f;
-                    float best = -INFINITY;
-                    int best_t = -1;
-                    for (int i = 0; i < ns; ++i) {
-                        const float* mi = ml + (size_t)i * H * 4;
-                        const float wgt = expf(mi[0] - m);
-                        l += wgt * mi[1];
-                        const float* oi = p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA + 32 * jc;
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 v = *reinterpret_cast<const float4*>(oi + k);
-                            o[k + 0] += wgt * v.x;
-                            o[k + 1] += wgt * v.y;
-                            o[k + 2] += wgt * v.z;
-                            o[k + 3] += wgt * v.w;
-                        }
-                        if (mi[2] > best) {
-                            best = mi[2];
-                            best_t = __float_as_int(mi[3]);
-                        }
-                    }
-                    if (p.argmax && vh == 0 && jc == 0) p.argmax[(size_t)b * H + h] = best_t;
-                } else if (p.argmax && vh == 0 && jc == 0) {
-                    p.argmax[(size_t)b * H + h] = -1;
-                }
-            }
-            const float inv_l_div = l;  // divide each element by l (IEEE quotient)
-            uint32_t* dst = reinterpret_cast<uint32_t*>(so + r * W_PITCH + 32 * jc);
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) dst[k >> 1] = pack_bf16x2(o[k] / inv_l_div, o[k + 1] / inv_l_div);
-        }
-        __syncthreads();
-        // out[16 x 64] = o_lat[16 x 512] . W_UV^T ; warp w -> v columns 8w .. 8w+7
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t a_base = smem_u32(so) + ((lane & 15) * W_PITCH + (lane >> 4) * 8) * 2;
-        const uint32_t b_base = smem_u32(sw) + ((8 * warp + (lane & 7)) * W_PITCH + ((lane >> 3) & 1) * 8) * 2;
-#pragma unroll 4
-        for (int ks = 0; ks < LORA / 16; ++ks) {
-            uint32_t a0, a1, a2, a3, b0, b1;
-            ldsm_x4(a_base + ks * 32, a0, a1, a2, a3);
-            ldsm_x2(b_base + ks * 32, b0, b1);
-            mma_bf16_16816(acc, a0, a1, a2, a3, b0, b1);
-        }
-        const int g = lane >> 2, t4 = lane & 3;
-        const int v = vh * 64 + 8 * warp + 2 * t4;
-        if (m0 + g < p.B)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(m0 + g) * H + h) * VH + v) = pack_bf16x2(acc[0], acc[1]);
-        if (m0 + g + 8 < p.B)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(m0 + g + 8) * H + h) * VH + v) =
-                pack_bf16x2(acc[2], acc[3]);
-    }
-}
-
-// ---- diagnostic: one tile of each contraction ----------------------------------------
+// ---- diagnostic: one page of each contraction --------------------------------------
 
 __global__ void __launch_bounds__(128, 1)
-    k3mla_diag_kernel(const __grid_constant__ CUtensorMap tmap, int mode, const uint16_t* a, float* d)
+    k3mla_diag_kernel(const __grid_constant__ CUtensorMap tmap_half, const __grid_constant__ CUtensorMap tmap_page,
+                      int mode, const uint16_t* a, float* d)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -763,16 +622,13 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t tbase = sm.tmem_base;
     const uint32_t t_lane = tbase + ((32u * warp) << 16);
     const int h = (int)threadIdx.x;
-    const uint64_t pol = policy_evict_first();
     bool ok = true;
     if (mode == 0) {
         load_q_tmem(tbase, h < H ? a + (size_t)h * ROW : nullptr);
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&sm.full[0], 9 * SLOT0);
-            for (int c = 0; c < 9; ++c) {
-                tma_load_2d(sm.u.ring0[c], &tmap, 64 * c, 0, &sm.full[0], pol);
-                tma_load_2d(sm.u.ring0[c] + SLOT0 / 2, &tmap, 64 * c, 64, &sm.full[0], pol);
-            }
+            mbar_arrive_expect_tx(&sm.full[0], 2 * SLOT0);
+            tma_load_3d(sm.u.c0.ring[0], &tmap_half, 0, 0, 0, &sm.full[0]);
+            tma_load_3d(sm.u.c0.ring[1], &tmap_half, 0, HALF, 0, &sm.full[0]);
         }
         tc_fence_before();
         __syncthreads();
@@ -780,7 +636,8 @@ __global__ void __launch_bounds__(128, 1)
             ok = wait_bar(&sm.full[0], 0, sm, nullptr);
             tc_fence_after();
             if (ok) {
-                for (int c = 0; c < 9; ++c) issue_score_chunk(tbase, smem_u32(sm.u.ring0[c]), c);
+                issue_score_half(tbase, S_COL, smem_u32(sm.u.c0.ring[0]));
+                issue_score_half(tbase, S_COL + HALF, smem_u32(sm.u.c0.ring[1]));
                 umma_commit(&sm.o_done);
             }
         }
@@ -788,30 +645,21 @@ __global__ void __launch_bounds__(128, 1)
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.o_done, 0, sm, nullptr));
         tc_fence_after();
         if (ok)
-            for (int piece = 0; piece < 4; ++piece) {
+            for (int piece = 0; piece < 2; ++piece) {
                 uint32_t r[32];
                 tmem_ld32(t_lane + S_COL + 32 * piece, r);
                 tmem_wait_ld();
-                for (int c = 0; c < 32; ++c) d[(size_t)h * 128 + 32 * piece + c] = __uint_as_float(r[c]);
+                for (int c = 0; c < 32; ++c) d[(size_t)h * 64 + 32 * piece + c] = __uint_as_float(r[c]);
             }
     } else {
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&sm.full[0], 4 * SLOT1);
-            for (int j = 0; j < 4; ++j) {
-                uint8_t* dst = sm.u.c1.ring1[j];
-                tma_load_2d(dst, &tmap, 128 * j, 0, &sm.full[0], pol);
-                tma_load_2d(dst + 8192, &tmap, 128 * j, 64, &sm.full[0], pol);
-                tma_load_2d(dst + 16384, &tmap, 128 * j + 64, 0, &sm.full[0], pol);
-                tma_load_2d(dst + 24576, &tmap, 128 * j + 64, 64, &sm.full[0], pol);
-            }
+            mbar_arrive_expect_tx(&sm.full[0], SLOT1);
+            tma_load_3d(sm.u.c1.ring[0], &tmap_page, 0, 0, 0, &sm.full[0]);
         }
-        if (h < H) {  // P^T row h from a[h][0..127]
-            for (int aa = 0; aa < 2; ++aa)
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(a + (size_t)h * 128 + 64 * aa + 8 * j);
-                    *reinterpret_cast<uint4*>(sm.u.c1.pt[0] + pt_chunk_off(h, aa, j)) = v;
-                }
-        }
+        if (h < H)  // P^T row h from a[h][0..63]
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(sm.u.c1.recv[0] + pt_chunk_off(h, j)) =
+                    *reinterpret_cast<const uint4*>(a + (size_t)h * 64 + 8 * j);
         fence_proxy_async_cta();
         tc_fence_before();
         __syncthreads();
@@ -819,8 +667,7 @@ __global__ void __launch_bounds__(128, 1)
             ok = wait_bar(&sm.full[0], 0, sm, nullptr);
             tc_fence_after();
             if (ok) {
-                for (int j = 0; j < 4; ++j)
-                    issue_pv_block(tbase, smem_u32(sm.u.c1.ring1[j]), smem_u32(sm.u.c1.pt[0]), j, false);
+                issue_pv_page(tbase, smem_u32(sm.u.c1.ring[0]), smem_u32(sm.u.c1.recv[0]), false);
                 umma_commit(&sm.o_done);
             }
         }
@@ -849,6 +696,23 @@ static size_t smem_bytes() { return sizeof(Smem) + 1024; }
 
 static int num_splits(int max_ctx, int split) { return (max_ctx + split - 1) / split; }
 
+static int make_maps(const void* slab, uint64_t rows, CUtensorMap* half, CUtensorMap* page)
+{
+    int rc = make_tmap_slab_3d(half, slab, rows, ROW, 9, HALF, 9);
+    if (rc) return rc;
+    return make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 8);
+}
+
+static void set_smem_attr(const void* fn, size_t bytes, bool* done)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+}
+
 }  // namespace k3
 
 using namespace k3;
@@ -865,11 +729,10 @@ extern "C" size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tok
 extern "C" int k3mla_default_split_tokens(int B, int max_ctx)
 {
     if (B <= 0 || max_ctx <= 0) return TILE;
-    int clusters = 0;
     int sms = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    clusters = sms / 2;
+    const int clusters = sms / 2;
     int per_slot = clusters / B;
     if (per_slot < 1) per_slot = 1;
     int split = (max_ctx + per_slot - 1) / per_slot;
@@ -910,20 +773,13 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
         set_error("k3mla_paged_decode: grid too large");
         return K3MLA_E_INVALID;
     }
-    CUtensorMap tmap;
-    int rc = make_tmap_bf16_2d(&tmap, slab, ROW, (uint64_t)n_pages * n_layers * PAGE, 64, 64);
+    CUtensorMap tm_half, tm_page;
+    int rc = make_maps(slab, (uint64_t)n_pages * n_layers * PAGE, &tm_half, &tm_page);
     if (rc) return rc;
-
-    static bool attr_set[64] = {};
+    static bool attr_done[64] = {};
     const size_t smem = smem_bytes();
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaFuncSetAttribute(k3mla_decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k3mla_merge_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((64 + 16) * W_PITCH * 2));
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+    set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel), smem, attr_done);
+
     DecodeParams dp;
     dp.q_abs = q_abs;
     dp.table = block_table;
@@ -942,14 +798,9 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     dp.max_ctx = max_ctx;
     dp.split = split_tokens;
     dp.nsplit = ns;
-    {
-        uint32_t u = (uint32_t)scale_bf16 << 16;
-        float f;
-        memcpy(&f, &u, 4);
-        dp.scale = f;
-    }
+    dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    k3mla_decode_split_kernel<<<dim3(2 * B * ns), dim3(THREADS), smem, st>>>(tmap, dp);
+    k3mla_decode_split_kernel<<<dim3(2 * B * ns), dim3(THREADS), smem, st>>>(tm_half, tm_page, dp);
     rc = check_launch("k3mla_decode_split_kernel");
     if (rc) return rc;
 
@@ -965,8 +816,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.max_pages = max_pages_per_slot;
     mp.split = split_tokens;
     mp.nsplit = ns;
-    k3mla_merge_expand_kernel<<<dim3(2, H), dim3(MX_THREADS), (64 + 16) * W_PITCH * 2, st>>>(mp);
-    return check_launch("k3mla_merge_expand_kernel");
+    return launch_merge_expand(mp, st);
 }
 
 extern "C" int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, float* d, void* stream)
@@ -976,11 +826,12 @@ extern "C" int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, f
         return K3MLA_E_INVALID;
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
-    CUtensorMap tmap;
-    int rc = make_tmap_bf16_2d(&tmap, b, ROW, 128, 64, 64);
+    CUtensorMap tm_half, tm_page;
+    int rc = make_maps(b, PAGE, &tm_half, &tm_page);
     if (rc) return rc;
+    static bool attr_done[64] = {};
     const size_t smem = smem_bytes();
-    cudaFuncSetAttribute(k3mla_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k3mla_diag_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmap, mode, a, d);
+    set_smem_attr(reinterpret_cast<const void*>(k3mla_diag_kernel), smem, attr_done);
+    k3mla_diag_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tm_half, tm_page, mode, a, d);
     return check_launch("k3mla_diag_kernel");
 }

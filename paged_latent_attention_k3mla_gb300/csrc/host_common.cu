@@ -90,6 +90,28 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_
     return K3MLA_OK;
 }
 
+int make_tmap_slab_3d(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems, uint32_t n_chunks,
+                      uint32_t box_rows, uint32_t box_chunks)
+{
+    auto fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled unavailable");
+        return K3MLA_E_CUDA;
+    }
+    cuuint64_t dims[3] = {64, rows, n_chunks};
+    cuuint64_t strides[2] = {(cuuint64_t)row_elems * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (3-D slab view) failed (%d)", (int)r);
+        return K3MLA_E_CUDA;
+    }
+    return K3MLA_OK;
+}
+
 }  // namespace k3
 
 extern "C" const char* k3mla_last_error(void) { return k3::g_err; }

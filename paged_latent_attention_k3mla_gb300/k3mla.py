@@ -160,7 +160,7 @@ def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_tabl
 def diag_umma(mode: int, a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, stream=None) -> None:
     lib = load()
     _check(lib.k3mla_diag_umma(int(mode), _dev(a, torch.bfloat16, None, "a"),
-                               _dev(b, torch.bfloat16, (2, PAGE, ROW), "b"),
+                               _dev(b, torch.bfloat16, (PAGE, ROW), "b"),
                                _dev(d, torch.float32, None, "d"), _stream(stream)), "k3mla_diag_umma")
 
 

@@ -1,10 +1,11 @@
 """The decode kernel's two tcgen05 contractions, one tile each, against a plain
 float64 matrix product (operand layouts, descriptors and TMEM lane mapping).
 
-Score form: S[128 x 128] = Q[128 x 576] . T^T with Q in TMEM (rows >= 96 zero)
-and the 2-page token tile T staged by TMA.  PV form: O[512 x 96] = T[:, :512]^T .
-P^T with the latent tile as an MN-major operand and P^T written by threads in the
-128-byte-swizzled K-major layout.  Products of bf16 values are exact, so the only
+Score form: S[128 x 64] = Q[128 x 576] . T^T with Q in TMEM (rows >= 96 zero)
+and the 64-token page T staged by two half-page 3-D TMA boxes.  PV form:
+O[512 x 96] = T[:, :512]^T . P^T with the page (one 3-D box of chunks 0..7) as an
+MN-major operand and P^T written by threads in the 128-byte-swizzled K-major
+layout.  Products of bf16 values are exact, so the only
 difference from float64 is f32 accumulation."""
 from __future__ import annotations
 
@@ -30,11 +31,11 @@ def _check(d, ref, absref, name):
 def test_score_contraction_tile(gpu_lib):
     g = torch.Generator(device="cuda").manual_seed(1)
     a = torch.randn(96, 576, generator=g, device="cuda").to(torch.bfloat16)
-    b = torch.randn(2, 64, 576, generator=g, device="cuda").to(torch.bfloat16)
-    d = torch.full((128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    b = torch.randn(64, 576, generator=g, device="cuda").to(torch.bfloat16)
+    d = torch.full((128, 64), float("nan"), dtype=torch.float32, device="cuda")
     gpu_lib.diag_umma(0, a, b, d)
     torch.cuda.synchronize()
-    t = b.reshape(128, 576).double()
+    t = b.double()
     ref = a.double() @ t.T
     absref = a.double().abs() @ t.abs().T
     _check(d[:96], ref, absref, "diag_score")
@@ -43,12 +44,12 @@ def test_score_contraction_tile(gpu_lib):
 
 def test_pv_contraction_tile(gpu_lib):
     g = torch.Generator(device="cuda").manual_seed(2)
-    p = torch.rand(96, 128, generator=g, device="cuda").to(torch.bfloat16)
-    b = torch.randn(2, 64, 576, generator=g, device="cuda").to(torch.bfloat16)
+    p = torch.rand(96, 64, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(64, 576, generator=g, device="cuda").to(torch.bfloat16)
     d = torch.full((512, 96), float("nan"), dtype=torch.float32, device="cuda")
     gpu_lib.diag_umma(1, p, b, d)
     torch.cuda.synchronize()
-    t = b.reshape(128, 576)[:, :512].double()
+    t = b[:, :512].double()
     ref = t.T @ p.double().T
     absref = t.abs().T @ p.double().abs().T
     _check(d, ref, absref, "diag_pv")
