@@ -13,29 +13,30 @@
 // Structure (GB300-first; the page's own 3-sweep kernel is prior art only).
 // The context of a slot is cut into fixed splits of `split` logical tokens;
 // each split is one unit of work for a CLUSTER OF TWO CTAs, and the unit of the
-// pipeline is one 64-token page:
-//   * rank 0, the score CTA, holds q_abs of the slot in TMEM (lane = head, 96 of
-//     128 lanes used; 288 columns) and streams each page as two half-page TMA
-//     boxes of [9 chunks][32 rows][128 B] (one 36 KB 3-D box each: a TMA
-//     instruction costs about the same issue time whatever its size, so pages
-//     travel in big boxes) through a 5-slot ring filled by two producer threads.
-//     tcgen05 MMAs with A = Q from TMEM compute S^T[heads x 64 tokens] (K = 576,
-//     N = 32 per half page) into a double-buffered TMEM region.  Its softmax
-//     warps (thread = head) land the scores to bf16 exactly as the chain does --
-//     bf16(dot), then bf16(. * scale) with packed bf16x2 instructions -- keep a
-//     lazily moved reference max per head, and write bf16 p into a staging
-//     buffer laid out as the K-major B operand of the second contraction; one
-//     bulk copy per page moves it into the partner CTA's shared memory
-//     (distributed shared memory).
-//   * rank 1, the PV CTA, streams the same pages (chunks 0..7, one 64 KB 3-D box
-//     per page, 3-slot ring, two producers; these reads mostly hit L2 right after
-//     the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T in
-//     TMEM (four M = 128 blocks, N = 96, K = 64 tokens per page; A is the
+// pipeline is one 64-token page, held whole in shared memory.
+//   * rank 0, the score CTA, holds q_abs of the slot in TMEM (24 heads in each
+//     32-lane quarter so that all four SM sub-partitions run softmax; 288
+//     columns).  Three page slots of [9 chunks][64 rows][128 B] (one 72 KB 3-D TMA
+//     box per page) rotate; slot r has its own producer thread and its own MMA
+//     issuer thread, so every barrier has one producer and one consumer, and the
+//     three issuers keep the tensor core busy (one thread alone cannot issue
+//     M=128 x N=64 MMAs as fast as the tensor core retires them).  The MMAs
+//     (A = Q from TMEM, B = the page, K-major, 128-byte swizzle) write S^T[heads x
+//     64 tokens] into one of three TMEM buffers.  Four softmax warps (thread =
+//     head) land the scores to bf16 exactly as the chain does -- bf16(dot), then
+//     bf16(. * scale) with packed bf16x2 instructions -- keep a lazily moved
+//     reference max per head, and store bf16 p straight into the partner CTA's
+//     shared memory with st.async (completion counted in bytes on the partner's
+//     mbarrier), laid out as the K-major B operand of the second contraction.
+//   * rank 1, the PV CTA, streams the same pages (chunks 0..7, one 64 KB box per
+//     page, three slots with one producer each; these reads mostly hit L2 right
+//     after the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T
+//     in TMEM (four M = 128 blocks, N = 96, K = 64 tokens per page; A is the
 //     MN-major latent page).  Its epilogue warps rescale O when the score CTA
 //     moved a head's reference max, zero rows past the context in the final page
 //     (stale rows must never meet p = 0 as 0 * NaN), and write the split's f32
 //     partial.
-// TMEM holds Q (288 columns) + S (2 x 64) in rank 0 and O (384) in rank 1, which
+// TMEM holds Q (288 columns) + S (3 x 64) in rank 0 and O (384) in rank 1, which
 // is why the two contractions live in different CTAs.
 //
 // Split boundaries depend only on the logical position and ctx_len, and no
@@ -62,42 +63,41 @@
 
 namespace k3 {
 
-constexpr int HALF = 32;                       // tokens per score-CTA TMA box
-constexpr int NS0 = 5;                         // score CTA: half-page slots
-constexpr int SLOT0 = 9 * HALF * 128;          // 36864 B: [9 chunks][32 rows][128 B]
-constexpr int CHUNK0 = HALF * 128;             // 4096 B per chunk in a half-page slot
-constexpr int NS1 = 3;                         // PV CTA: page slots
-constexpr int SLOT1 = 8 * PAGE * 128;          // 65536 B: [8 chunks][64 rows][128 B]
-constexpr int CHUNK1 = PAGE * 128;             // 8192 B per chunk in a page slot
+constexpr int NSLOT = 3;                       // page slots per CTA (one producer + one consumer each)
+constexpr int SLOT0 = 9 * PAGE * 128;          // 73728 B: [9 chunks][64 rows][128 B]
+constexpr int SLOT1 = 8 * PAGE * 128;          // 65536 B: chunks 0..7 only
+constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk
+constexpr int QBYTES = H * ROW * 2;            // 110592 B: q_abs of one slot, [9 chunks][96 rows][128 B]
+constexpr int QCHUNK = H * 128;                // 12288 B per chunk of Q
+constexpr int HPW = 24;                        // heads per softmax warp (lanes 0..23 of each quarter)
 constexpr int PT_BYTES = H * 128;              // 12288 B: P^T [96 heads][64 tokens] bf16, K-major SW128
 constexpr int META_ALPHA = PT_BYTES;           // f32 alpha[96]
 constexpr int META_FLAGS = PT_BYTES + 4 * H;   // u32 flags[4]: "some head of warp w rescaled"
-constexpr int PCOPY = PT_BYTES + 4 * H + 16;   // bytes moved per page (12688, a multiple of 16)
+constexpr int PCOPY = PT_BYTES + 4 * H + 16;   // bytes stored per page (12688)
 constexpr int PBUF = 13 * 1024;                // buffer pitch, keeps every P^T 1024-byte aligned
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;                  // score CTA: S^T double buffer, 2 x 64 columns
-constexpr uint32_t Q_COL = 128;                // score CTA: Q, 288 columns (576 bf16)
+constexpr uint32_t S_COL = 0;                  // score CTA: S^T buffers r = 0..2 at 64 r
+constexpr uint32_t Q_COL = 192;                // score CTA: Q, 288 columns (576 bf16)
 constexpr float TAU = 8.0f;                    // max growth (natural log) before a rescale
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
-constexpr uint32_t IDESC_S = make_idesc_bf16(128, HALF, 0, 0);  // S^T half page = Q . C^T
+constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
-constexpr int THREADS = 224;                   // warps 0-3 softmax / epilogue, 4 and 6 producers, 5 MMA
-constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the three softmax warps
+constexpr int THREADS = 320;  // warps 0-3 softmax/epilogue, 4-6 producers, 7-9 MMA issuers (rank 1: warp 7)
+constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the four softmax warps
 
 struct __align__(1024) Smem {
     union {
         struct {
-            uint8_t ring[NS0][SLOT0];
-            uint8_t stage[2][PBUF];
+            uint8_t ring[NSLOT][SLOT0];
         } c0;
         struct {
-            uint8_t ring[NS1][SLOT1];
+            uint8_t ring[NSLOT][SLOT1];
             uint8_t recv[2][PBUF];
         } c1;
     } u;
-    uint64_t full[8];
-    uint64_t empty[8];
-    uint64_t s_full[2], s_empty[2], q_ready;
+    uint64_t full[NSLOT], empty[NSLOT];
+    uint64_t s_full[NSLOT], s_empty[NSLOT];
+    uint64_t q_land, q_ready;
     uint64_t p_full[2], p_empty[2];
     uint64_t o_done, epi_req, epi_done;
     uint32_t tmem_base;
@@ -105,10 +105,10 @@ struct __align__(1024) Smem {
     int32_t abort_flag;
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
-static_assert(PCOPY % 16 == 0 && PCOPY <= PBUF, "bulk copy size");
+static_assert(QBYTES <= (NSLOT - 1) * SLOT0, "q_abs staging fits in slots 1..2");
+static_assert(PCOPY <= PBUF, "P buffer");
 
 struct DecodeParams {
-    const uint16_t* q_abs;
     const int32_t* table;
     const int32_t* ctx_len;
     float* ws_o;    // [B][nsplit][96][512]
@@ -180,43 +180,44 @@ __device__ __forceinline__ int32_t page_row(const DecodeParams& p, int b, int lp
 
 // ---- building blocks shared with the diagnostic kernel -----------------------------
 
-// Score CTA: row h of Q (thread h = 0..127; rows >= 96 zero) into TMEM columns
-// [Q_COL, Q_COL + 288) of lane h, two bf16 per column.  Called by warps 0..3.
-__device__ __forceinline__ void load_q_tmem(uint32_t tbase, const uint16_t* qrow_or_null)
+// TMEM lane of head h: 24 heads per 32-lane quarter.
+__device__ __forceinline__ int head_lane(int h) { return 32 * (h / HPW) + (h % HPW); }
+
+// Score CTA, warps 0..3: copy Q (smem, [9 chunks][96 rows][128 B], 128-byte
+// swizzle, as a 3-D TMA box lands it) into TMEM columns [Q_COL, Q_COL + 288):
+// lane 32w + l <- head 24w + l (l < 24), other lanes zero.
+__device__ __forceinline__ void q_smem_to_tmem(uint32_t tbase, const uint8_t* qs)
 {
-    const uint32_t w = threadIdx.x >> 5;
+    const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31);
+    const int h = HPW * w + l;
     const uint32_t taddr = tbase + ((32u * w) << 16) + Q_COL;
 #pragma unroll 1
     for (int c = 0; c < 9; ++c) {
         uint32_t r[32];
-        if (qrow_or_null) {
-            const uint4* src = reinterpret_cast<const uint4*>(qrow_or_null + c * 64);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint4 v = __ldg(src + k);
-                r[4 * k + 0] = v.x;
-                r[4 * k + 1] = v.y;
-                r[4 * k + 2] = v.z;
-                r[4 * k + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = 0u;
+        for (int j = 0; j < 8; ++j) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (l < HPW) v = *reinterpret_cast<const uint4*>(qs + c * QCHUNK + h * 128 + ((j ^ (h & 7)) << 4));
+            r[4 * j + 0] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
         }
         tmem_st32(taddr + c * 32, r);
     }
     tmem_wait_st();
 }
 
-// Score CTA: S^T[:, 32 tokens] = Q . C^T for one half-page slot (36 MMAs, K = 576).
-__device__ __forceinline__ void issue_score_half(uint32_t tbase, uint32_t d_col, uint32_t slot_addr)
+// Score CTA: S^T[:, 64 tokens] = Q . C^T for one page slot (36 MMAs, K = 576).
+__device__ __forceinline__ void issue_score_page(uint32_t tbase, uint32_t d_col, uint32_t slot_addr)
 {
-#pragma unroll 1
+    const uint64_t b0 = make_sdesc(slot_addr, 16, 1024);
+#pragma unroll
     for (int c = 0; c < 9; ++c) {
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             const uint32_t a = tbase + Q_COL + (uint32_t)(4 * c + ks) * 8u;
-            const uint64_t bd = make_sdesc(slot_addr + c * CHUNK0 + ks * 32, 16, 1024);
+            const uint64_t bd = b0 + (uint64_t)((uint32_t)(c * CHUNK + ks * 32) >> 4);
             umma_ts(tbase + d_col, a, bd, IDESC_S, (c | ks) != 0);
         }
     }
@@ -226,12 +227,14 @@ __device__ __forceinline__ void issue_score_half(uint32_t tbase, uint32_t d_col,
 __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t page_addr, uint32_t pt_addr,
                                               bool accumulate_first)
 {
+    const uint64_t a0 = make_sdesc(page_addr, CHUNK, 1024);
+    const uint64_t b0 = make_sdesc(pt_addr, 16, 1024);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = make_sdesc(page_addr + 2 * j * CHUNK1 + ks * 2048, CHUNK1, 1024);
-            const uint64_t bd = make_sdesc(pt_addr + ks * 32, 16, 1024);
+            const uint64_t ad = a0 + (uint64_t)((uint32_t)(2 * j * CHUNK + ks * 2048) >> 4);
+            const uint64_t bd = b0 + (uint64_t)((uint32_t)(ks * 32) >> 4);
             umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || ks > 0) ? 1u : 0u);
         }
     }
@@ -242,9 +245,10 @@ __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_
 
 // ---- the split decode kernel ---------------------------------------------------------
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_half,
-                              const __grid_constant__ CUtensorMap tmap_page, const DecodeParams p)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
+    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
+                              const __grid_constant__ CUtensorMap tmap_page8,
+                              const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,16 +270,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int32_t oob_row = p.n_pages * p.n_layers * PAGE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 3);
             mbar_init(&sm.p_full[i], 1);
             mbar_init(&sm.p_empty[i], 1);
         }
+        mbar_init(&sm.q_land, 1);
         mbar_init(&sm.q_ready, 4);
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.epi_req, 1);
@@ -286,14 +291,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_arrive_expect_tx(&sm.p_full[1], PCOPY);
         }
         fence_mbarrier_init_cluster();
+        if (rank == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
+            tma_prefetch_desc(&tmap_q);
+            mbar_arrive_expect_tx(&sm.q_land, QBYTES);
+            tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, b * H, 0, &sm.q_land);
+        }
     }
-    if (warp == 5) {
+    if (warp == 7) {
         tmem_alloc(&sm.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
     if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tmap_half);
         tma_prefetch_desc(&tmap_page);
+        tma_prefetch_desc(&tmap_page8);
     }
     tc_fence_before();
     cluster_sync();
@@ -302,181 +312,170 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     if (rank == 0) {
         // =========================== score CTA ===========================
-        if (warp == 4 || warp == 6) {
-            if (lane == 0) {  // producer hh streams half hh of every page
-                const int hh = warp == 4 ? 0 : 1;
+        if (warp >= 4 && warp <= 6) {
+            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r
+                const int r = (int)warp - 4;
                 bool ok = true;
-                for (int i = 0; i < npg && ok; ++i) {
-                    const int u = 2 * i + hh, slot = u % NS0, k = u / NS0;
+                if (r > 0) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // slots 1..2 hold q_abs until then
+                for (int i = r; i < npg && ok; i += NSLOT) {
+                    const int k = i / NSLOT;
                     const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
-                    if (!wait_bar(&sm.empty[slot], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                    if (!wait_bar(&sm.empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.full[slot], SLOT0);
-                    tma_load_3d(sm.u.c0.ring[slot], &tmap_half, 0, y + HALF * hh, 0, &sm.full[slot]);
+                    mbar_arrive_expect_tx(&sm.full[r], SLOT0);
+                    tma_load_3d(sm.u.c0.ring[r], &tmap_page, 0, y, 0, &sm.full[r]);
                 }
                 if (!ok) drain_inflight();
             }
-        } else if (warp == 5) {
-            if (lane == 0) {
+        } else if (warp >= 7) {
+            if (lane == 0) {  // MMA issuer r: scores of the pages i = r (mod 3) into S buffer r
+                const int r = (int)warp - 7;
                 bool ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
                 tc_fence_after();
-                for (int i = 0; i < npg && ok; ++i) {
-                    const int sb = i & 1;
-                    if (!wait_bar(&sm.s_empty[sb], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err)) {
+                const uint32_t slot = smem_u32(sm.u.c0.ring[r]);
+                for (int i = r; i < npg && ok; i += NSLOT) {
+                    const int k = i / NSLOT;
+                    if (!wait_bar(&sm.s_empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err) ||
+                        !wait_bar(&sm.full[r], (uint32_t)(k & 1), sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int u = 2 * i + hh, slot = u % NS0, k = u / NS0;
-                        if (!wait_bar(&sm.full[slot], (uint32_t)(k & 1), sm, p.dev_err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_score_half(tbase, S_COL + 64u * sb + HALF * hh, smem_u32(sm.u.c0.ring[slot]));
-                        umma_commit(&sm.empty[slot]);
-                    }
-                    if (ok) umma_commit(&sm.s_full[sb]);
+                    issue_score_page(tbase, S_COL + 64u * r, slot);
+                    umma_commit(&sm.empty[r]);
+                    umma_commit(&sm.s_full[r]);
                 }
                 if (!ok) drain_inflight();
             }
-        } else if (warp < 4) {
-            // softmax warps 0..2 (thread h = head); warp 3 only loads its Q lanes
-            const int h = (int)threadIdx.x;
-            load_q_tmem(tbase, h < H ? p.q_abs + ((size_t)b * H + h) * ROW : nullptr);
+        } else {
+            // softmax warps 0..3: thread l < 24 of warp w owns head 24w + l
+            const int w = (int)warp, l = (int)lane;
+            const int h = HPW * w + l;
+            const bool has_head = l < HPW;
+            const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
+            if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.q_ready);
-            if (warp < 3) {
-                const uint32_t t_lane = tbase + ((32u * warp) << 16);
-                const float LOG2E = 1.4426950408889634f;
-                float m_ref = -INFINITY, l = 0.f, best_s = -INFINITY;
-                int best_t = -1;
-                const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
-                const uint32_t recv1 = mapa(smem_u32(sm.u.c1.recv[1]), 1);
-                const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
-                const uint32_t pfull1 = mapa(smem_u32(&sm.p_full[1]), 1);
-                for (int i = 0; i < npg; ++i) {
-                    const int sb = i & 1;
-                    const bool got = wait_bar(&sm.s_full[sb], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
-                    if (named_bar_any(SOFTMAX_BAR, 96, !got || aborted(sm))) break;  // uniform decision
-                    __syncwarp();
-                    tc_fence_after();
-                    const int nvalid = min(PAGE, ntok - PAGE * i);
-                    uint32_t sp[32];  // bf16 scores: token 2k in the low half, 2k+1 in the high half
+            const uint32_t t_lane = tbase + ((32u * warp) << 16);
+            const float LOG2E = 1.4426950408889634f;
+            float m_ref = -INFINITY, lsum = 0.f, best_s = -INFINITY;
+            int best_t = -1;
+            const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
+            const uint32_t recv1 = mapa(smem_u32(sm.u.c1.recv[1]), 1);
+            const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
+            const uint32_t pfull1 = mapa(smem_u32(&sm.p_full[1]), 1);
+            for (int i = 0; i < npg; ++i) {
+                const int r = i % NSLOT, k = i / NSLOT;
+                const bool got = wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err);
+                if (named_bar_any(SOFTMAX_BAR, 128, !got || aborted(sm))) break;  // uniform decision
+                __syncwarp();
+                tc_fence_after();
+                const int nvalid = min(PAGE, ntok - PAGE * i);
+                uint32_t sp[32];  // bf16 scores: token 2k in the low half, 2k+1 in the high half
 #pragma unroll
-                    for (int piece = 0; piece < 2; ++piece) {
-                        uint32_t r[32];
-                        tmem_ld32(t_lane + S_COL + 64u * sb + 32u * piece, r);
-                        tmem_wait_ld();
+                for (int piece = 0; piece < 2; ++piece) {
+                    uint32_t rr[32];
+                    tmem_ld32(t_lane + S_COL + 64u * r + 32u * piece, rr);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 16; ++k)  // bf16(dot), then bf16(bf16(dot) * scale)
-                            sp[16 * piece + k] =
-                                mul_bf16x2(pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
-                                           p.scale2);
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
-                    if (nvalid < PAGE) {
+                    for (int q = 0; q < 16; ++q)  // bf16(dot), then bf16(bf16(dot) * scale)
+                        sp[16 * piece + q] =
+                            mul_bf16x2(pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])),
+                                       p.scale2);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.s_empty[r]);
+                if (nvalid < PAGE) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            if (2 * k >= nvalid) sp[k] = (sp[k] & 0xFFFF0000u) | 0xFF80u;  // -inf
-                            if (2 * k + 1 >= nvalid) sp[k] = (sp[k] & 0x0000FFFFu) | 0xFF800000u;
-                        }
+                    for (int q = 0; q < 32; ++q) {
+                        if (2 * q >= nvalid) sp[q] = (sp[q] & 0xFFFF0000u) | 0xFF80u;  // -inf
+                        if (2 * q + 1 >= nvalid) sp[q] = (sp[q] & 0x0000FFFFu) | 0xFF800000u;
                     }
-                    uint32_t m2 = sp[0];
+                }
+                uint32_t m2 = sp[0];
 #pragma unroll
-                    for (int k = 1; k < 32; ++k) m2 = max_bf16x2(m2, sp[k]);
-                    const float tmax = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
-                    if (tmax > best_s) {  // lowest logical t attaining the best score
-                        best_s = tmax;
-                        int first = 0;
-                        for (int k = 31; k >= 0; --k) {
-                            if (bf16hi_to_f32(sp[k]) == tmax) first = 2 * k + 1;
-                            if (bf16lo_to_f32(sp[k]) == tmax) first = 2 * k;
-                        }
-                        best_t = start + PAGE * i + first;
+                for (int q = 1; q < 32; ++q) m2 = max_bf16x2(m2, sp[q]);
+                const float tmax = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
+                if (tmax > best_s) {  // lowest logical t attaining the best score
+                    best_s = tmax;
+                    int first = 0;
+                    for (int q = 31; q >= 0; --q) {
+                        if (bf16hi_to_f32(sp[q]) == tmax) first = 2 * q + 1;
+                        if (bf16lo_to_f32(sp[q]) == tmax) first = 2 * q;
                     }
-                    float alpha = 1.f;
-                    bool resc = false;
-                    if (i == 0) {
-                        m_ref = tmax;
-                    } else if (tmax > m_ref + TAU) {
-                        alpha = ex2_approx((m_ref - tmax) * LOG2E);
-                        l *= alpha;
-                        m_ref = tmax;
-                        resc = true;
-                    }
-                    const float mb = m_ref * LOG2E;
-                    uint32_t pp[32];
+                    best_t = start + PAGE * i + first;
+                }
+                float alpha = 1.f;
+                bool resc = false;
+                if (i == 0) {
+                    m_ref = tmax;
+                } else if (tmax > m_ref + TAU) {
+                    alpha = ex2_approx((m_ref - tmax) * LOG2E);
+                    lsum *= alpha;
+                    m_ref = tmax;
+                    resc = true;
+                }
+                const float mb = m_ref * LOG2E;
+                uint32_t pp[32];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float e0 = ex2_approx(fmaf(bf16lo_to_f32(sp[k]), LOG2E, -mb));
-                        const float e1 = ex2_approx(fmaf(bf16hi_to_f32(sp[k]), LOG2E, -mb));
-                        l += e0;
-                        l += e1;
-                        pp[k] = pack_bf16x2(e0, e1);
-                    }
-                    const int st = i & 1;
-                    uint8_t* stage = sm.u.c0.stage[st];
-                    if (h == 0) bulk_wait_read<1>();  // the copy of page i-2 has read this buffer
-                    named_bar(SOFTMAX_BAR, 96);
+                for (int q = 0; q < 32; ++q) {
+                    const float e0 = ex2_approx(fmaf(bf16lo_to_f32(sp[q]), LOG2E, -mb));
+                    const float e1 = ex2_approx(fmaf(bf16hi_to_f32(sp[q]), LOG2E, -mb));
+                    lsum += e0;
+                    lsum += e1;
+                    pp[q] = pack_bf16x2(e0, e1);
+                }
+                const int st = i & 1;
+                // the PV CTA has finished with its buffer from page i-2
+                const bool freed = wait_bar(&sm.p_empty[st], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err);
+                const uint32_t dst = st ? recv1 : recv0;
+                const uint32_t bar = st ? pfull1 : pfull0;
+                if (freed && has_head) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(stage + pt_chunk_off(h, j)) =
-                            make_uint4(pp[4 * j], pp[4 * j + 1], pp[4 * j + 2], pp[4 * j + 3]);
-                    reinterpret_cast<float*>(stage + META_ALPHA)[h] = alpha;
-                    const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc);
-                    if (lane == 0) reinterpret_cast<uint32_t*>(stage + META_FLAGS)[warp] = any ? 1u : 0u;
-                    fence_proxy_async_cta();
-                    named_bar(SOFTMAX_BAR, 96);
-                    if (h == 0) {
-                        // the PV CTA has finished with its buffer from page i-2
-                        if (wait_bar(&sm.p_empty[st], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err)) {
-                            bulk_copy_to_cluster(st ? recv1 : recv0, stage, PCOPY, st ? pfull1 : pfull0);
-                            bulk_commit();
-                        }
-                    }
+                        st_async_v4(dst + pt_chunk_off(h, j),
+                                    make_uint4(pp[4 * j], pp[4 * j + 1], pp[4 * j + 2], pp[4 * j + 3]), bar);
+                    st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 }
-                if (!aborted(sm)) {
-                    float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
-                    ml[0] = m_ref;
-                    ml[1] = l;
-                    ml[2] = best_s;
-                    ml[3] = __int_as_float(best_t);
-                }
-                if (h == 0) {
-                    bulk_wait<0>();  // every P copy has landed in the PV CTA
-                    // the PV CTA's last releases of its P buffers land here before exit
-                    for (int i = max(0, npg - 2); i < npg && !aborted(sm); ++i)
-                        wait_bar(&sm.p_empty[i & 1], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
-                }
+                const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
+                if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * w, any ? 1u : 0u, bar);
             }
+            if (has_head && !aborted(sm)) {
+                float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
+                ml[0] = m_ref;
+                ml[1] = lsum;
+                ml[2] = best_s;
+                ml[3] = __int_as_float(best_t);
+            }
+            // the PV CTA's last releases of its P buffers land here before exit
+            if (lane == 0)
+                for (int i = max(0, npg - 2); i < npg && !aborted(sm); ++i)
+                    wait_bar(&sm.p_empty[i & 1], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
         }
     } else {
         // ============================ PV CTA ============================
-        if (warp == 4 || warp == 6) {
-            if (lane == 0) {  // producer q streams the pages i with i % 2 == q
+        if (warp >= 4 && warp <= 6) {
+            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r
                 const uint64_t pol = policy_evict_first();  // last reader of the latent
-                const int q = warp == 4 ? 0 : 1;
+                const int r = (int)warp - 4;
                 bool ok = true;
-                for (int i = q; i < npg && ok; i += 2) {
-                    const int slot = i % NS1, k = i / NS1;
+                for (int i = r; i < npg && ok; i += NSLOT) {
+                    const int k = i / NSLOT;
                     const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
-                    if (!wait_bar(&sm.empty[slot], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                    if (!wait_bar(&sm.empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.full[slot], SLOT1);
-                    tma_load_3d_hint(sm.u.c1.ring[slot], &tmap_page, 0, y, 0, &sm.full[slot], pol);
+                    mbar_arrive_expect_tx(&sm.full[r], SLOT1);
+                    tma_load_3d_hint(sm.u.c1.ring[r], &tmap_page8, 0, y, 0, &sm.full[r], pol);
                 }
                 if (!ok) drain_inflight();
             }
-        } else if (warp == 5) {
+        } else if (warp == 7) {
             if (lane == 0) {
                 uint32_t epi_k = 0;
                 bool ok = true;
@@ -486,12 +485,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
+                    fence_proxy_async_cta();  // the P tile arrived through st.async; the MMA reads it
                     const volatile uint32_t* rf =
                         reinterpret_cast<const volatile uint32_t*>(sm.u.c1.recv[st] + META_FLAGS);
-                    const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2]) != 0u);
+                    const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2] | rf[3]) != 0u);
                     const int nvalid = min(PAGE, ntok - PAGE * i);
                     const bool tail = nvalid < PAGE;
-                    const int slot = i % NS1, k = i / NS1;
+                    const int slot = i % NSLOT, k = i / NSLOT;
                     if (!wait_bar(&sm.full[slot], (uint32_t)(k & 1), sm, p.dev_err)) {
                         ok = false;
                         break;
@@ -541,14 +541,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + META_ALPHA);
                     for (int j = 0; j < 4; ++j)
                         for (int piece = 0; piece < 3; ++piece) {
-                            uint32_t r[32];
+                            uint32_t rr[32];
                             const uint32_t ta = t_lane + 96u * j + 32u * piece;
-                            tmem_ld32(ta, r);
+                            tmem_ld32(ta, rr);
                             tmem_wait_ld();
 #pragma unroll
                             for (int c = 0; c < 32; ++c)
-                                r[c] = __float_as_uint(__uint_as_float(r[c]) * al[32 * piece + c]);
-                            tmem_st32(ta, r);
+                                rr[c] = __float_as_uint(__uint_as_float(rr[c]) * al[32 * piece + c]);
+                            tmem_st32(ta, rr);
                         }
                     tmem_wait_st();
                     tc_fence_before();
@@ -559,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     uint8_t* page = sm.u.c1.ring[sm.epi_slot];
                     for (int q = (int)threadIdx.x; q < 8 * per_chunk; q += 128) {
                         const int c = q / per_chunk, rem = q % per_chunk;
-                        *reinterpret_cast<uint4*>(page + c * CHUNK1 + (vr + rem / 8) * 128 + (rem % 8) * 16) =
+                        *reinterpret_cast<uint4*>(page + c * CHUNK + (vr + rem / 8) * 128 + (rem % 8) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_cta();
@@ -573,12 +573,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     for (int j = 0; j < 4; ++j) {
                         const int d = 128 * j + 32 * (int)warp + (int)lane;
                         for (int piece = 0; piece < 3; ++piece) {
-                            uint32_t r[32];
-                            tmem_ld32(t_lane + 96u * j + 32u * piece, r);
+                            uint32_t rr[32];
+                            tmem_ld32(t_lane + 96u * j + 32u * piece, rr);
                             tmem_wait_ld();
 #pragma unroll
                             for (int c = 0; c < 32; ++c)
-                                o[(size_t)(32 * piece + c) * LORA + d] = __uint_as_float(r[c]);
+                                o[(size_t)(32 * piece + c) * LORA + d] = __uint_as_float(rr[c]);
                         }
                     }
                     break;
@@ -594,20 +594,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tbase, TMEM_COLS);
+    if (warp == 7) tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // ---- diagnostic: one page of each contraction --------------------------------------
 
 __global__ void __launch_bounds__(128, 1)
-    k3mla_diag_kernel(const __grid_constant__ CUtensorMap tmap_half, const __grid_constant__ CUtensorMap tmap_page,
-                      int mode, const uint16_t* a, float* d)
+    k3mla_diag_kernel(const __grid_constant__ CUtensorMap tmap_page, const __grid_constant__ CUtensorMap tmap_page8,
+                      const __grid_constant__ CUtensorMap tmap_q, int mode, const uint16_t* a, float* d)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     if (threadIdx.x == 0) {
         mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.q_land, 1);
         mbar_init(&sm.o_done, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init_cluster();
@@ -621,23 +622,23 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t t_lane = tbase + ((32u * warp) << 16);
-    const int h = (int)threadIdx.x;
     bool ok = true;
     if (mode == 0) {
-        load_q_tmem(tbase, h < H ? a + (size_t)h * ROW : nullptr);
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&sm.full[0], 2 * SLOT0);
-            tma_load_3d(sm.u.c0.ring[0], &tmap_half, 0, 0, 0, &sm.full[0]);
-            tma_load_3d(sm.u.c0.ring[1], &tmap_half, 0, HALF, 0, &sm.full[0]);
+            mbar_arrive_expect_tx(&sm.q_land, QBYTES);
+            tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, 0, 0, &sm.q_land);
+            mbar_arrive_expect_tx(&sm.full[0], SLOT0);
+            tma_load_3d(sm.u.c0.ring[0], &tmap_page, 0, 0, 0, &sm.full[0]);
         }
+        ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.q_land, 0, sm, nullptr));
+        if (ok) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
         tc_fence_before();
         __syncthreads();
         if (threadIdx.x == 0) {
             ok = wait_bar(&sm.full[0], 0, sm, nullptr);
             tc_fence_after();
             if (ok) {
-                issue_score_half(tbase, S_COL, smem_u32(sm.u.c0.ring[0]));
-                issue_score_half(tbase, S_COL + HALF, smem_u32(sm.u.c0.ring[1]));
+                issue_score_page(tbase, S_COL, smem_u32(sm.u.c0.ring[0]));
                 umma_commit(&sm.o_done);
             }
         }
@@ -645,17 +646,20 @@ __global__ void __launch_bounds__(128, 1)
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.o_done, 0, sm, nullptr));
         tc_fence_after();
         if (ok)
-            for (int piece = 0; piece < 2; ++piece) {
+            for (int piece = 0; piece < 2; ++piece) {  // row = head, through the lane map
                 uint32_t r[32];
                 tmem_ld32(t_lane + S_COL + 32 * piece, r);
                 tmem_wait_ld();
-                for (int c = 0; c < 32; ++c) d[(size_t)h * 64 + 32 * piece + c] = __uint_as_float(r[c]);
+                if (lane < HPW)
+                    for (int c = 0; c < 32; ++c)
+                        d[(size_t)(HPW * warp + lane) * 64 + 32 * piece + c] = __uint_as_float(r[c]);
             }
     } else {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&sm.full[0], SLOT1);
-            tma_load_3d(sm.u.c1.ring[0], &tmap_page, 0, 0, 0, &sm.full[0]);
+            tma_load_3d(sm.u.c1.ring[0], &tmap_page8, 0, 0, 0, &sm.full[0]);
         }
+        const int h = (int)threadIdx.x;
         if (h < H)  // P^T row h from a[h][0..63]
             for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<uint4*>(sm.u.c1.recv[0] + pt_chunk_off(h, j)) =
@@ -696,11 +700,14 @@ static size_t smem_bytes() { return sizeof(Smem) + 1024; }
 
 static int num_splits(int max_ctx, int split) { return (max_ctx + split - 1) / split; }
 
-static int make_maps(const void* slab, uint64_t rows, CUtensorMap* half, CUtensorMap* page)
+static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_rows, CUtensorMap* page,
+                     CUtensorMap* page8, CUtensorMap* qmap)
 {
-    int rc = make_tmap_slab_3d(half, slab, rows, ROW, 9, HALF, 9);
+    int rc = make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 9);
     if (rc) return rc;
-    return make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 8);
+    rc = make_tmap_slab_3d(page8, slab, rows, ROW, 9, PAGE, 8);
+    if (rc) return rc;
+    return make_tmap_slab_3d(qmap, q, q_rows, ROW, 9, H, 9);
 }
 
 static void set_smem_attr(const void* fn, size_t bytes, bool* done)
@@ -752,7 +759,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
         return K3MLA_E_INVALID;
     }
     if (B == 0) return K3MLA_OK;
-    if ((long long)n_pages * n_layers * PAGE + PAGE > 0x7FFFFFFFll) {
+    if ((long long)n_pages * n_layers * PAGE + PAGE > 0x7FFFFFFFll || (long long)B * H > 0x7FFFFFFFll) {
         set_error("k3mla_paged_decode: slab rows exceed the 2^31 TMA row range");
         return K3MLA_E_INVALID;
     }
@@ -773,15 +780,14 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
         set_error("k3mla_paged_decode: grid too large");
         return K3MLA_E_INVALID;
     }
-    CUtensorMap tm_half, tm_page;
-    int rc = make_maps(slab, (uint64_t)n_pages * n_layers * PAGE, &tm_half, &tm_page);
+    CUtensorMap tm_page, tm_page8, tm_q;
+    int rc = make_maps(slab, (uint64_t)n_pages * n_layers * PAGE, q_abs, (uint64_t)B * H, &tm_page, &tm_page8, &tm_q);
     if (rc) return rc;
     static bool attr_done[64] = {};
     const size_t smem = smem_bytes();
     set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel), smem, attr_done);
 
     DecodeParams dp;
-    dp.q_abs = q_abs;
     dp.table = block_table;
     dp.ctx_len = ctx_len;
     float* ws_o = reinterpret_cast<float*>(workspace);
@@ -800,7 +806,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     dp.nsplit = ns;
     dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    k3mla_decode_split_kernel<<<dim3(2 * B * ns), dim3(THREADS), smem, st>>>(tm_half, tm_page, dp);
+    k3mla_decode_split_kernel<<<dim3(2 * B * ns), dim3(THREADS), smem, st>>>(tm_page, tm_page8, tm_q, dp);
     rc = check_launch("k3mla_decode_split_kernel");
     if (rc) return rc;
 
@@ -826,12 +832,12 @@ extern "C" int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, f
         return K3MLA_E_INVALID;
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
-    CUtensorMap tm_half, tm_page;
-    int rc = make_maps(b, PAGE, &tm_half, &tm_page);
+    CUtensorMap tm_page, tm_page8, tm_q;
+    int rc = make_maps(b, PAGE, a, H, &tm_page, &tm_page8, &tm_q);
     if (rc) return rc;
     static bool attr_done[64] = {};
     const size_t smem = smem_bytes();
     set_smem_attr(reinterpret_cast<const void*>(k3mla_diag_kernel), smem, attr_done);
-    k3mla_diag_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tm_half, tm_page, mode, a, d);
+    k3mla_diag_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tm_page, tm_page8, tm_q, mode, a, d);
     return check_launch("k3mla_diag_kernel");
 }

@@ -1,8 +1,9 @@
 """The decode kernel's two tcgen05 contractions, one tile each, against a plain
 float64 matrix product (operand layouts, descriptors and TMEM lane mapping).
 
-Score form: S[128 x 64] = Q[128 x 576] . T^T with Q in TMEM (rows >= 96 zero)
-and the 64-token page T staged by two half-page 3-D TMA boxes.  PV form:
+Score form: S[96 x 64] = Q[96 x 576] . T^T with Q staged by one 3-D TMA box and
+copied into TMEM (24 heads per 32-lane quarter) and the 64-token page T staged by
+one 3-D TMA box.  PV form:
 O[512 x 96] = T[:, :512]^T . P^T with the page (one 3-D box of chunks 0..7) as an
 MN-major operand and P^T written by threads in the 128-byte-swizzled K-major
 layout.  Products of bf16 values are exact, so the only
@@ -39,7 +40,6 @@ def test_score_contraction_tile(gpu_lib):
     ref = a.double() @ t.T
     absref = a.double().abs() @ t.abs().T
     _check(d[:96], ref, absref, "diag_score")
-    assert torch.all(d[96:] == 0)
 
 
 def test_pv_contraction_tile(gpu_lib):
