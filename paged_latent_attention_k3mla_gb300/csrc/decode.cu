@@ -83,6 +83,7 @@ constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
 constexpr int THREADS = 320;  // warps 0-3 softmax/epilogue, 4-6 producers, 7-9 MMA issuers (rank 1: warp 7)
+// 10 warps put three on some SM sub-partitions (16K registers each): at most 168 registers per thread.
 constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the four softmax warps
 
 struct __align__(1024) Smem {
@@ -209,17 +210,19 @@ __device__ __forceinline__ void q_smem_to_tmem(uint32_t tbase, const uint8_t* qs
 }
 
 // Score CTA: S^T[:, 64 tokens] = Q . C^T for one page slot (36 MMAs, K = 576).
+// Descriptors advance by additions only, so the issuing thread spends its time
+// issuing (chunk c is 8192 B = 512 descriptor units; a K step is 32 B = 2 units).
 __device__ __forceinline__ void issue_score_page(uint32_t tbase, uint32_t d_col, uint32_t slot_addr)
 {
-    const uint64_t b0 = make_sdesc(slot_addr, 16, 1024);
-#pragma unroll
+    uint64_t bd = make_sdesc(slot_addr, 16, 1024);
+    uint32_t a = tbase + Q_COL;
+    const uint32_t d = tbase + d_col;
+#pragma unroll 1
     for (int c = 0; c < 9; ++c) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t a = tbase + Q_COL + (uint32_t)(4 * c + ks) * 8u;
-            const uint64_t bd = b0 + (uint64_t)((uint32_t)(c * CHUNK + ks * 32) >> 4);
-            umma_ts(tbase + d_col, a, bd, IDESC_S, (c | ks) != 0);
-        }
+        for (int ks = 0; ks < 4; ++ks) umma_ts(d, a + 8u * ks, bd + 2u * ks, IDESC_S, (c | ks) != 0);
+        a += 32u;
+        bd += (uint64_t)(CHUNK >> 4);
     }
 }
 
@@ -245,7 +248,7 @@ __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_
 
 // ---- the split decode kernel ---------------------------------------------------------
 
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
                               const __grid_constant__ CUtensorMap tmap_page8,
                               const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
@@ -403,6 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
                 if (tmax > best_s) {  // lowest logical t attaining the best score
                     best_s = tmax;
                     int first = 0;
+#pragma unroll
                     for (int q = 31; q >= 0; --q) {
                         if (bf16hi_to_f32(sp[q]) == tmax) first = 2 * q + 1;
                         if (bf16lo_to_f32(sp[q]) == tmax) first = 2 * q;
@@ -420,27 +424,27 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
                     resc = true;
                 }
                 const float mb = m_ref * LOG2E;
-                uint32_t pp[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float e0 = ex2_approx(fmaf(bf16lo_to_f32(sp[q]), LOG2E, -mb));
-                    const float e1 = ex2_approx(fmaf(bf16hi_to_f32(sp[q]), LOG2E, -mb));
-                    lsum += e0;
-                    lsum += e1;
-                    pp[q] = pack_bf16x2(e0, e1);
-                }
                 const int st = i & 1;
                 // the PV CTA has finished with its buffer from page i-2
                 const bool freed = wait_bar(&sm.p_empty[st], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err);
                 const uint32_t dst = st ? recv1 : recv0;
                 const uint32_t bar = st ? pfull1 : pfull0;
-                if (freed && has_head) {
+                const bool send = freed && has_head;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_async_v4(dst + pt_chunk_off(h, j),
-                                    make_uint4(pp[4 * j], pp[4 * j + 1], pp[4 * j + 2], pp[4 * j + 3]), bar);
-                    st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
+                for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), stored as they come
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t s2 = sp[4 * j + q];
+                        const float e0 = ex2_approx(fmaf(bf16lo_to_f32(s2), LOG2E, -mb));
+                        const float e1 = ex2_approx(fmaf(bf16hi_to_f32(s2), LOG2E, -mb));
+                        lsum += e0;
+                        lsum += e1;
+                        w4[q] = pack_bf16x2(e0, e1);
+                    }
+                    if (send) st_async_v4(dst + pt_chunk_off(h, j), make_uint4(w4[0], w4[1], w4[2], w4[3]), bar);
                 }
+                if (send) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
                 if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * w, any ? 1u : 0u, bar);
             }
@@ -539,17 +543,22 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
                     ++od;
                     tc_fence_after();
                     const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + META_ALPHA);
-                    for (int j = 0; j < 4; ++j)
-                        for (int piece = 0; piece < 3; ++piece) {
+#pragma unroll 1
+                    for (int piece = 0; piece < 3; ++piece) {  // heads 32 piece .. 32 piece + 31
+                        float a32[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) a32[c] = al[32 * piece + c];
+#pragma unroll 1
+                        for (int j = 0; j < 4; ++j) {
                             uint32_t rr[32];
                             const uint32_t ta = t_lane + 96u * j + 32u * piece;
                             tmem_ld32(ta, rr);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                rr[c] = __float_as_uint(__uint_as_float(rr[c]) * al[32 * piece + c]);
+                            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * a32[c]);
                             tmem_st32(ta, rr);
                         }
+                    }
                     tmem_wait_st();
                     tc_fence_before();
                 }
