@@ -63,10 +63,14 @@
 
 namespace k3 {
 
-constexpr int NSLOT = 3;                       // page slots per CTA (one producer + one consumer each)
+constexpr int NSLOT = 3;                       // score CTA: page slots (one producer + one issuer each)
 constexpr int SLOT0 = 9 * PAGE * 128;          // 73728 B: [9 chunks][64 rows][128 B]
-constexpr int SLOT1 = 8 * PAGE * 128;          // 65536 B: chunks 0..7 only
-constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk
+constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk of a page slot
+constexpr int HALF = 32;                       // PV CTA: tokens per half-page box
+constexpr int NHSLOT = 5;                      // PV CTA: half-page slots (one producer each)
+constexpr int SLOT1 = 8 * HALF * 128;          // 32768 B: [8 chunks][32 rows][128 B], chunks 0..7 only
+constexpr int HCHUNK = HALF * 128;             // 4096 B per chunk of a half-page slot
+constexpr int NPBUF = 4;                       // P buffers in the PV CTA
 constexpr int QBYTES = H * ROW * 2;            // 110592 B: q_abs of one slot, [9 chunks][96 rows][128 B]
 constexpr int QCHUNK = H * 128;                // 12288 B per chunk of Q
 constexpr int HPW = 24;                        // heads per softmax warp (lanes 0..23 of each quarter)
@@ -82,7 +86,9 @@ constexpr float TAU = 8.0f;                    // max growth (natural log) befor
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
-constexpr int THREADS = 320;  // warps 0-3 softmax/epilogue, 4-6 producers, 7-9 MMA issuers (rank 1: warp 7)
+// rank 0: warps 0-3 softmax, 4-6 producers, 7-9 MMA issuers; rank 1: warps 0-3 epilogue,
+// 4-8 producers, 9 MMA issuer.
+constexpr int THREADS = 320;
 // 10 warps put three on some SM sub-partitions (16K registers each): at most 168 registers per thread.
 constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the four softmax warps
 
@@ -92,20 +98,21 @@ struct __align__(1024) Smem {
             uint8_t ring[NSLOT][SLOT0];
         } c0;
         struct {
-            uint8_t ring[NSLOT][SLOT1];
-            uint8_t recv[2][PBUF];
+            uint8_t ring[NHSLOT][SLOT1];
+            uint8_t recv[NPBUF][PBUF];
         } c1;
     } u;
-    uint64_t full[NSLOT], empty[NSLOT];
+    uint64_t full[8], empty[8];
     uint64_t s_full[NSLOT], s_empty[NSLOT];
     uint64_t q_land, q_ready;
-    uint64_t p_full[2], p_empty[2];
+    uint64_t p_full[NPBUF], p_empty[NPBUF];
     uint64_t o_done, epi_req, epi_done;
     uint32_t tmem_base;
-    uint32_t epi_cmd, epi_slot, epi_stage, epi_vrows;
+    uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
+static_assert(NHSLOT <= 8, "barrier arrays");
 static_assert(QBYTES <= (NSLOT - 1) * SLOT0, "q_abs staging fits in slots 1..2");
 static_assert(PCOPY <= PBUF, "P buffer");
 
@@ -226,19 +233,23 @@ __device__ __forceinline__ void issue_score_page(uint32_t tbase, uint32_t d_col,
     }
 }
 
-// PV CTA: O^T (+)= C^T . P^T over one 64-token page: 4 blocks of 128 dims x 4 K-steps.
-__device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t page_addr, uint32_t pt_addr,
-                                              bool accumulate_first)
+// PV CTA: O^T (+)= C^T . P^T over one 64-token page held as two half-page slots
+// ([8 chunks][32 rows][128 B] each): 4 blocks of 128 dims x 4 K-steps of 16 tokens.
+__device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_addr, uint32_t half1_addr,
+                                              uint32_t pt_addr, bool accumulate_first)
 {
-    const uint64_t a0 = make_sdesc(page_addr, CHUNK, 1024);
     const uint64_t b0 = make_sdesc(pt_addr, 16, 1024);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint64_t a0 = make_sdesc(hh ? half1_addr : half0_addr, HCHUNK, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = a0 + (uint64_t)((uint32_t)(2 * j * CHUNK + ks * 2048) >> 4);
-            const uint64_t bd = b0 + (uint64_t)((uint32_t)(ks * 32) >> 4);
-            umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || ks > 0) ? 1u : 0u);
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t ad = a0 + (uint64_t)((uint32_t)(2 * j * HCHUNK + ks * 2048) >> 4);
+                const uint64_t bd = b0 + (uint64_t)((uint32_t)((2 * hh + ks) * 32) >> 4);
+                umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || hh > 0 || ks > 0) ? 1u : 0u);
+            }
         }
     }
 }
@@ -273,13 +284,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     const int32_t oob_row = p.n_pages * p.n_layers * PAGE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSLOT; ++i) {
+        for (int i = 0; i < 8; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_empty[i], 4);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NPBUF; ++i) {
             mbar_init(&sm.p_full[i], 1);
             mbar_init(&sm.p_empty[i], 1);
         }
@@ -289,10 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
         mbar_init(&sm.epi_req, 1);
         mbar_init(&sm.epi_done, 4);
         sm.abort_flag = 0;
-        if (rank == 1) {  // the P buffers of pages 0 and 1 are expected before anything is sent
-            mbar_arrive_expect_tx(&sm.p_full[0], PCOPY);
-            mbar_arrive_expect_tx(&sm.p_full[1], PCOPY);
-        }
+        if (rank == 1)  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
+            for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
         fence_mbarrier_init_cluster();
         if (rank == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
             tma_prefetch_desc(&tmap_q);
@@ -367,9 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             float m_ref = -INFINITY, lsum = 0.f, best_s = -INFINITY;
             int best_t = -1;
             const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
-            const uint32_t recv1 = mapa(smem_u32(sm.u.c1.recv[1]), 1);
             const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
-            const uint32_t pfull1 = mapa(smem_u32(&sm.p_full[1]), 1);
             for (int i = 0; i < npg; ++i) {
                 const int r = i % NSLOT, k = i / NSLOT;
                 const bool got = wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err);
@@ -399,10 +408,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                         if (2 * q + 1 >= nvalid) sp[q] = (sp[q] & 0x0000FFFFu) | 0xFF800000u;
                     }
                 }
-                uint32_t m2 = sp[0];
+                uint32_t mx[16];  // tree max over the 64 packed scores
 #pragma unroll
-                for (int q = 1; q < 32; ++q) m2 = max_bf16x2(m2, sp[q]);
-                const float tmax = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
+                for (int q = 0; q < 16; ++q) mx[q] = max_bf16x2(sp[q], sp[q + 16]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx[q] = max_bf16x2(mx[q], mx[q + 8]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mx[q] = max_bf16x2(mx[q], mx[q + 4]);
+                mx[0] = max_bf16x2(max_bf16x2(mx[0], mx[2]), max_bf16x2(mx[1], mx[3]));
+                const float tmax = fmaxf(bf16lo_to_f32(mx[0]), bf16hi_to_f32(mx[0]));
                 if (tmax > best_s) {  // lowest logical t attaining the best score
                     best_s = tmax;
                     int first = 0;
@@ -424,26 +438,30 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     resc = true;
                 }
                 const float mb = m_ref * LOG2E;
-                const int st = i & 1;
-                // the PV CTA has finished with its buffer from page i-2
-                const bool freed = wait_bar(&sm.p_empty[st], (uint32_t)((i >> 1) & 1) ^ 1u, sm, p.dev_err);
-                const uint32_t dst = st ? recv1 : recv0;
-                const uint32_t bar = st ? pfull1 : pfull0;
+                const int st = i % NPBUF;
+                // the PV CTA has finished with its buffer from page i - NPBUF
+                const bool freed =
+                    wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
+                const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
+                const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
                 const bool send = freed && has_head;
+                float part[8];  // independent partial sums, combined in a fixed order below
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), stored as they come
                     uint32_t w4[4];
+                    float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t s2 = sp[4 * j + q];
                         const float e0 = ex2_approx(fmaf(bf16lo_to_f32(s2), LOG2E, -mb));
                         const float e1 = ex2_approx(fmaf(bf16hi_to_f32(s2), LOG2E, -mb));
-                        lsum += e0;
-                        lsum += e1;
+                        acc += e0 + e1;
                         w4[q] = pack_bf16x2(e0, e1);
                     }
+                    part[j] = acc;
                     if (send) st_async_v4(dst + pt_chunk_off(h, j), make_uint4(w4[0], w4[1], w4[2], w4[3]), bar);
                 }
+                lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
                 if (send) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
                 if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * w, any ? 1u : 0u, bar);
@@ -457,35 +475,35 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             }
             // the PV CTA's last releases of its P buffers land here before exit
             if (lane == 0)
-                for (int i = max(0, npg - 2); i < npg && !aborted(sm); ++i)
-                    wait_bar(&sm.p_empty[i & 1], (uint32_t)((i >> 1) & 1), sm, p.dev_err);
+                for (int i = max(0, npg - NPBUF); i < npg && !aborted(sm); ++i)
+                    wait_bar(&sm.p_empty[i % NPBUF], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err);
         }
     } else {
         // ============================ PV CTA ============================
-        if (warp >= 4 && warp <= 6) {
-            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r
+        if (warp >= 4 && warp <= 8) {
+            if (lane == 0) {  // producer q streams the half pages u = q (mod 5) into half-slot q
                 const uint64_t pol = policy_evict_first();  // last reader of the latent
-                const int r = (int)warp - 4;
+                const int q = (int)warp - 4;
                 bool ok = true;
-                for (int i = r; i < npg && ok; i += NSLOT) {
-                    const int k = i / NSLOT;
-                    const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
-                    if (!wait_bar(&sm.empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                for (int u = q; u < 2 * npg && ok; u += NHSLOT) {
+                    const int k = u / NHSLOT;
+                    const int32_t y = page_row(p, b, lp0 + u / 2, n_lp, oob_row) + HALF * (u & 1);
+                    if (!wait_bar(&sm.empty[q], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.full[r], SLOT1);
-                    tma_load_3d_hint(sm.u.c1.ring[r], &tmap_page8, 0, y, 0, &sm.full[r], pol);
+                    mbar_arrive_expect_tx(&sm.full[q], SLOT1);
+                    tma_load_3d_hint(sm.u.c1.ring[q], &tmap_page8, 0, y, 0, &sm.full[q], pol);
                 }
                 if (!ok) drain_inflight();
             }
-        } else if (warp == 7) {
+        } else if (warp == 9) {
             if (lane == 0) {
                 uint32_t epi_k = 0;
                 bool ok = true;
                 for (int i = 0; i < npg && ok; ++i) {
-                    const int st = i & 1;
-                    if (!wait_bar(&sm.p_full[st], (uint32_t)((i >> 1) & 1), sm, p.dev_err, true)) {
+                    const int st = i % NPBUF;
+                    if (!wait_bar(&sm.p_full[st], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err, true)) {
                         ok = false;
                         break;
                     }
@@ -495,15 +513,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2] | rf[3]) != 0u);
                     const int nvalid = min(PAGE, ntok - PAGE * i);
                     const bool tail = nvalid < PAGE;
-                    const int slot = i % NSLOT, k = i / NSLOT;
-                    if (!wait_bar(&sm.full[slot], (uint32_t)(k & 1), sm, p.dev_err)) {
+                    const int u0 = 2 * i, q0 = u0 % NHSLOT, q1 = (u0 + 1) % NHSLOT;
+                    if (!wait_bar(&sm.full[q0], (uint32_t)((u0 / NHSLOT) & 1), sm, p.dev_err) ||
+                        !wait_bar(&sm.full[q1], (uint32_t)(((u0 + 1) / NHSLOT) & 1), sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
                     if (resc || tail) {
                         if (resc) umma_commit(&sm.o_done);
                         sm.epi_cmd = (resc ? 1u : 0u) | (tail ? 2u : 0u);
-                        sm.epi_slot = (uint32_t)slot;
+                        sm.epi_slot0 = (uint32_t)q0;
+                        sm.epi_slot1 = (uint32_t)q1;
                         sm.epi_stage = (uint32_t)st;
                         sm.epi_vrows = (uint32_t)nvalid;
                         mbar_arrive(&sm.epi_req);
@@ -514,10 +534,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                         ++epi_k;
                     }
                     tc_fence_after();
-                    issue_pv_page(tbase, smem_u32(sm.u.c1.ring[slot]), smem_u32(sm.u.c1.recv[st]), i > 0);
-                    umma_commit(&sm.empty[slot]);
+                    issue_pv_page(tbase, smem_u32(sm.u.c1.ring[q0]), smem_u32(sm.u.c1.ring[q1]),
+                                  smem_u32(sm.u.c1.recv[st]), i > 0);
+                    umma_commit(&sm.empty[q0]);
+                    umma_commit(&sm.empty[q1]);
                     umma_commit_mc(&sm.p_empty[st], (uint16_t)0x1);
-                    if (i + 2 < npg) mbar_arrive_expect_tx(&sm.p_full[st], PCOPY);
+                    if (i + NPBUF < npg) mbar_arrive_expect_tx(&sm.p_full[st], PCOPY);
                 }
                 if (ok) {
                     umma_commit(&sm.o_done);
@@ -562,13 +584,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     tmem_wait_st();
                     tc_fence_before();
                 }
-                if (cmd & 2u) {  // zero rows >= vrows of chunks 0..7 of the final page
+                if (cmd & 2u) {  // zero rows >= vrows of chunks 0..7 of the final page (two half slots)
                     const int vr = (int)sm.epi_vrows;
                     const int per_chunk = (PAGE - vr) * 8;  // 16-byte pieces
-                    uint8_t* page = sm.u.c1.ring[sm.epi_slot];
                     for (int q = (int)threadIdx.x; q < 8 * per_chunk; q += 128) {
                         const int c = q / per_chunk, rem = q % per_chunk;
-                        *reinterpret_cast<uint4*>(page + c * CHUNK + (vr + rem / 8) * 128 + (rem % 8) * 16) =
+                        const int row = vr + rem / 8;  // page row
+                        uint8_t* half = sm.u.c1.ring[row < HALF ? sm.epi_slot0 : sm.epi_slot1];
+                        *reinterpret_cast<uint4*>(half + c * HCHUNK + (row % HALF) * 128 + (rem % 8) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_cta();
@@ -665,8 +688,9 @@ __global__ void __launch_bounds__(128, 1)
             }
     } else {
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&sm.full[0], SLOT1);
+            mbar_arrive_expect_tx(&sm.full[0], 2 * SLOT1);
             tma_load_3d(sm.u.c1.ring[0], &tmap_page8, 0, 0, 0, &sm.full[0]);
+            tma_load_3d(sm.u.c1.ring[1], &tmap_page8, 0, HALF, 0, &sm.full[0]);
         }
         const int h = (int)threadIdx.x;
         if (h < H)  // P^T row h from a[h][0..63]
@@ -680,7 +704,8 @@ __global__ void __launch_bounds__(128, 1)
             ok = wait_bar(&sm.full[0], 0, sm, nullptr);
             tc_fence_after();
             if (ok) {
-                issue_pv_page(tbase, smem_u32(sm.u.c1.ring[0]), smem_u32(sm.u.c1.recv[0]), false);
+                issue_pv_page(tbase, smem_u32(sm.u.c1.ring[0]), smem_u32(sm.u.c1.ring[1]), smem_u32(sm.u.c1.recv[0]),
+                              false);
                 umma_commit(&sm.o_done);
             }
         }
@@ -714,7 +739,7 @@ static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_
 {
     int rc = make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 9);
     if (rc) return rc;
-    rc = make_tmap_slab_3d(page8, slab, rows, ROW, 9, PAGE, 8);
+    rc = make_tmap_slab_3d(page8, slab, rows, ROW, 9, HALF, 8);
     if (rc) return rc;
     return make_tmap_slab_3d(qmap, q, q_rows, ROW, 9, H, 9);
 }
