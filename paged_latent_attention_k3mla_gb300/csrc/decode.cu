@@ -90,7 +90,6 @@ constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C
 // 4-8 producers, 9 MMA issuer.
 constexpr int THREADS = 320;
 // 10 warps put three on some SM sub-partitions (16K registers each): at most 168 registers per thread.
-constexpr uint32_t SOFTMAX_BAR = 1;            // named barrier of the four softmax warps
 
 struct __align__(1024) Smem {
     union {
@@ -144,9 +143,9 @@ __device__ __forceinline__ bool aborted(const Smem& sm)
     return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
 }
 
-// Bounded mbarrier wait: gives up after WAIT_NS or when this CTA aborted.
-__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
-                                      bool cluster_scope = false)
+// Bounded mbarrier wait, slow path: gives up after WAIT_NS or when this CTA aborted.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
+                                           bool cluster_scope)
 {
     const uint32_t a = smem_u32(bar);
     if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
@@ -162,6 +161,16 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, 
             }
         }
     }
+}
+
+// Bounded mbarrier wait: an inline non-blocking test first (most waits are already
+// satisfied when they are reached), then the suspending slow path.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
+                                         bool cluster_scope = false)
+{
+    const uint32_t a = smem_u32(bar);
+    if (cluster_scope ? mbar_test_wait_cluster(a, parity) : mbar_test_wait(a, parity)) return true;
+    return wait_bar_slow(bar, parity, sm, dev_err, cluster_scope);
 }
 
 // After an abort: let this thread's in-flight TMA copies / MMAs land (bounded, ~2 ms).
@@ -382,8 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             for (int i = 0; i < npg; ++i) {
                 const int r = i % NSLOT, k = i / NSLOT;
                 const bool got = wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err);
-                if (named_bar_any(SOFTMAX_BAR, 128, !got || aborted(sm))) break;  // uniform decision
-                __syncwarp();
+                if (!__all_sync(0xFFFFFFFFu, got)) break;  // warps run independently; a wait gave up
                 tc_fence_after();
                 const int nvalid = min(PAGE, ntok - PAGE * i);
                 uint32_t sp[32];  // bf16 scores: token 2k in the low half, 2k+1 in the high half
@@ -419,12 +427,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                 const float tmax = fmaxf(bf16lo_to_f32(mx[0]), bf16hi_to_f32(mx[0]));
                 if (tmax > best_s) {  // lowest logical t attaining the best score
                     best_s = tmax;
-                    int first = 0;
+                    uint32_t lo = 0u, hi = 0u;  // bit t set where score t equals the page max
 #pragma unroll
-                    for (int q = 31; q >= 0; --q) {
-                        if (bf16hi_to_f32(sp[q]) == tmax) first = 2 * q + 1;
-                        if (bf16lo_to_f32(sp[q]) == tmax) first = 2 * q;
+                    for (int q = 0; q < 16; ++q) {
+                        lo |= (bf16lo_to_f32(sp[q]) == tmax ? 1u : 0u) << (2 * q);
+                        lo |= (bf16hi_to_f32(sp[q]) == tmax ? 1u : 0u) << (2 * q + 1);
+                        hi |= (bf16lo_to_f32(sp[q + 16]) == tmax ? 1u : 0u) << (2 * q);
+                        hi |= (bf16hi_to_f32(sp[q + 16]) == tmax ? 1u : 0u) << (2 * q + 1);
                     }
+                    const int first = lo ? __ffs(lo) - 1 : 32 + __ffs(hi) - 1;
                     best_t = start + PAGE * i + first;
                 }
                 float alpha = 1.f;
@@ -447,8 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                 const bool send = freed && has_head;
                 float part[8];  // independent partial sums, combined in a fixed order below
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), stored as they come
-                    uint32_t w4[4];
+                for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), in place of s
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -456,10 +466,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                         const float e0 = ex2_approx(fmaf(bf16lo_to_f32(s2), LOG2E, -mb));
                         const float e1 = ex2_approx(fmaf(bf16hi_to_f32(s2), LOG2E, -mb));
                         acc += e0 + e1;
-                        w4[q] = pack_bf16x2(e0, e1);
+                        sp[4 * j + q] = pack_bf16x2(e0, e1);
                     }
                     part[j] = acc;
-                    if (send) st_async_v4(dst + pt_chunk_off(h, j), make_uint4(w4[0], w4[1], w4[2], w4[3]), bar);
+                }
+                if (send) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_async_v4(dst + pt_chunk_off(h, j), make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]),
+                                    bar);
                 }
                 lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
                 if (send) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);

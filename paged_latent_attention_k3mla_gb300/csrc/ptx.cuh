@@ -74,6 +74,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of a phase (no suspension): the fast path of every wait.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity)
 {
     uint32_t ok;
@@ -180,17 +207,17 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const
 // complete on the mbarrier (same CTA as the destination, cluster addresses).
 __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint4 v, uint32_t mbar_cluster)
 {
+    // no "memory" clobber: the destination is another CTA's buffer that this thread never reads, and
+    // volatile asm keeps the order against the barrier waits, so arithmetic may be scheduled around it
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      dst_cluster),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar_cluster)
-                 : "memory");
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar_cluster));
 }
 
 __device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t mbar_cluster)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
-                 "r"(v), "r"(mbar_cluster)
-                 : "memory");
+                 "r"(v), "r"(mbar_cluster));
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
