@@ -86,10 +86,11 @@ constexpr float TAU = 8.0f;                    // max growth (natural log) befor
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
-// rank 0: warps 0-3 softmax, 4-6 producers, 7-9 MMA issuers; rank 1: warps 0-3 epilogue,
-// 4-8 producers, 9 MMA issuer.
-constexpr int THREADS = 320;
-// 10 warps put three on some SM sub-partitions (16K registers each): at most 168 registers per thread.
+// rank 0: warps 0-7 softmax, 8-10 producers, 11-13 MMA issuers; rank 1: warps 0-3
+// epilogue, 4-8 producers, 9 MMA issuer, 10-13 idle.  Warp 8 allocates TMEM in both.
+constexpr int THREADS = 448;
+constexpr int W_PROD0 = 8, W_MMA0 = 11, W_ALLOC = 8;
+// 14 warps put four on some SM sub-partitions (16K registers each): at most 128 registers per thread.
 
 struct __align__(1024) Smem {
     union {
@@ -106,6 +107,9 @@ struct __align__(1024) Smem {
     uint64_t q_land, q_ready;
     uint64_t p_full[NPBUF], p_empty[NPBUF];
     uint64_t o_done, epi_req, epi_done;
+    float xmax[2][4][32];    // score CTA: per-half page max of each head, exchanged inside a warp pair
+    int32_t xidx[2][4][32];  // ... and the first token of the half attaining it
+    float xsum[4][32];       // ... and, at the end, the second half's sum of exp
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
@@ -268,7 +272,7 @@ __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_
 
 // ---- the split decode kernel ---------------------------------------------------------
 
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
                               const __grid_constant__ CUtensorMap tmap_page8,
                               const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
@@ -299,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
         }
         for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 4);
+            mbar_init(&sm.s_empty[i], 8);
         }
         for (int i = 0; i < NPBUF; ++i) {
             mbar_init(&sm.p_full[i], 1);
@@ -320,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, b * H, 0, &sm.q_land);
         }
     }
-    if (warp == 7) {
+    if (warp == W_ALLOC) {
         tmem_alloc(&sm.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
@@ -335,9 +339,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
 
     if (rank == 0) {
         // =========================== score CTA ===========================
-        if (warp >= 4 && warp <= 6) {
+        if (warp >= W_PROD0 && warp < W_PROD0 + NSLOT) {
             if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r
-                const int r = (int)warp - 4;
+                const int r = (int)warp - W_PROD0;
                 bool ok = true;
                 if (r > 0) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // slots 1..2 hold q_abs until then
                 for (int i = r; i < npg && ok; i += NSLOT) {
@@ -352,9 +356,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                 }
                 if (!ok) drain_inflight();
             }
-        } else if (warp >= 7) {
+        } else if (warp >= W_MMA0 && warp < W_MMA0 + NSLOT) {
             if (lane == 0) {  // MMA issuer r: scores of the pages i = r (mod 3) into S buffer r
-                const int r = (int)warp - 7;
+                const int r = (int)warp - W_MMA0;
                 bool ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
                 tc_fence_after();
                 const uint32_t slot = smem_u32(sm.u.c0.ring[r]);
@@ -372,71 +376,86 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                 }
                 if (!ok) drain_inflight();
             }
-        } else {
-            // softmax warps 0..3: thread l < 24 of warp w owns head 24w + l
-            const int w = (int)warp, l = (int)lane;
-            const int h = HPW * w + l;
+        } else if (warp < 8) {
+            // softmax warps 0..7: warp (qd = warp % 4, hf = warp / 4); thread l < 24 owns head 24 qd + l
+            // for tokens 32 hf .. 32 hf + 31 of every page.  The two warps of a quarter exchange their
+            // half-page max (and its first token) through shared memory and then take identical
+            // decisions, so the reference max, the rescale factor and the argmax agree.
+            const int qd = (int)(warp & 3u), hf = (int)(warp >> 2), l = (int)lane;
+            const int h = HPW * qd + l;
             const bool has_head = l < HPW;
-            const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
-            if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.q_ready);
-            const uint32_t t_lane = tbase + ((32u * warp) << 16);
+            const uint32_t pair_bar = 1u + (uint32_t)qd;  // named barrier of warps qd and qd + 4
+            if (hf == 0) {
+                const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
+                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.q_ready);
+            }
+            const uint32_t t_lane = tbase + ((32u * qd) << 16) + S_COL + 32u * hf;
             const float LOG2E = 1.4426950408889634f;
             float m_ref = -INFINITY, lsum = 0.f, best_s = -INFINITY;
             int best_t = -1;
             const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
             const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
+            bool stopped = false;
             for (int i = 0; i < npg; ++i) {
                 const int r = i % NSLOT, k = i / NSLOT;
                 const bool got = wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err);
-                if (!__all_sync(0xFFFFFFFFu, got)) break;  // warps run independently; a wait gave up
+                if (named_bar_any(pair_bar, 64, !got)) {  // the pair stops together
+                    stopped = true;
+                    break;
+                }
+                __syncwarp();
                 tc_fence_after();
-                const int nvalid = min(PAGE, ntok - PAGE * i);
-                uint32_t sp[32];  // bf16 scores: token 2k in the low half, 2k+1 in the high half
-#pragma unroll
-                for (int piece = 0; piece < 2; ++piece) {
+                const int nvalid = min(PAGE, ntok - PAGE * i) - 32 * hf;  // valid tokens of this half
+                uint32_t sp[16];  // bf16 scores: token 2q in the low half, 2q+1 in the high half
+                {
                     uint32_t rr[32];
-                    tmem_ld32(t_lane + S_COL + 64u * r + 32u * piece, rr);
+                    tmem_ld32(t_lane + 64u * r, rr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q)  // bf16(dot), then bf16(bf16(dot) * scale)
-                        sp[16 * piece + q] =
-                            mul_bf16x2(pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])),
-                                       p.scale2);
+                        sp[q] = mul_bf16x2(pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])),
+                                           p.scale2);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.s_empty[r]);
-                if (nvalid < PAGE) {
+                if (nvalid < 32) {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
+                    for (int q = 0; q < 16; ++q) {
                         if (2 * q >= nvalid) sp[q] = (sp[q] & 0xFFFF0000u) | 0xFF80u;  // -inf
                         if (2 * q + 1 >= nvalid) sp[q] = (sp[q] & 0x0000FFFFu) | 0xFF800000u;
                     }
                 }
-                uint32_t mx[16];  // tree max over the 64 packed scores
+                uint32_t mx[8];  // tree max over the 32 scores of this half
 #pragma unroll
-                for (int q = 0; q < 16; ++q) mx[q] = max_bf16x2(sp[q], sp[q + 16]);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mx[q] = max_bf16x2(mx[q], mx[q + 8]);
+                for (int q = 0; q < 8; ++q) mx[q] = max_bf16x2(sp[q], sp[q + 8]);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) mx[q] = max_bf16x2(mx[q], mx[q + 4]);
                 mx[0] = max_bf16x2(max_bf16x2(mx[0], mx[2]), max_bf16x2(mx[1], mx[3]));
-                const float tmax = fmaxf(bf16lo_to_f32(mx[0]), bf16hi_to_f32(mx[0]));
-                if (tmax > best_s) {  // lowest logical t attaining the best score
-                    best_s = tmax;
-                    uint32_t lo = 0u, hi = 0u;  // bit t set where score t equals the page max
+                const float lm = fmaxf(bf16lo_to_f32(mx[0]), bf16hi_to_f32(mx[0]));
+                int li = 0;  // first token of this half with score lm (needed only for a new best)
+                if (lm > best_s) {
+                    uint32_t bits = 0u;
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        lo |= (bf16lo_to_f32(sp[q]) == tmax ? 1u : 0u) << (2 * q);
-                        lo |= (bf16hi_to_f32(sp[q]) == tmax ? 1u : 0u) << (2 * q + 1);
-                        hi |= (bf16lo_to_f32(sp[q + 16]) == tmax ? 1u : 0u) << (2 * q);
-                        hi |= (bf16hi_to_f32(sp[q + 16]) == tmax ? 1u : 0u) << (2 * q + 1);
+                        bits |= (bf16lo_to_f32(sp[q]) == lm ? 1u : 0u) << (2 * q);
+                        bits |= (bf16hi_to_f32(sp[q]) == lm ? 1u : 0u) << (2 * q + 1);
                     }
-                    const int first = lo ? __ffs(lo) - 1 : 32 + __ffs(hi) - 1;
-                    best_t = start + PAGE * i + first;
+                    li = __ffs(bits) - 1;
+                }
+                sm.xmax[hf][qd][l] = lm;
+                sm.xidx[hf][qd][l] = li;
+                named_bar(pair_bar, 64);
+                const float pm = sm.xmax[hf ^ 1][qd][l];
+                const int pi = sm.xidx[hf ^ 1][qd][l];
+                const float m0 = hf ? pm : lm, m1 = hf ? lm : pm;
+                const float tmax = fmaxf(m0, m1);
+                if (tmax > best_s) {  // lowest logical t attaining the best score
+                    best_s = tmax;
+                    best_t = start + PAGE * i + (m0 == tmax ? (hf ? pi : li) : 32 + (hf ? li : pi));
                 }
                 float alpha = 1.f;
                 bool resc = false;
@@ -449,16 +468,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     resc = true;
                 }
                 const float mb = m_ref * LOG2E;
-                const int st = i % NPBUF;
-                // the PV CTA has finished with its buffer from page i - NPBUF
-                const bool freed =
-                    wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
-                const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
-                const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
-                const bool send = freed && has_head;
-                float part[8];  // independent partial sums, combined in a fixed order below
+                float part[4];  // independent partial sums, combined in a fixed order below
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), in place of s
+                for (int j = 0; j < 4; ++j) {  // tokens 8j .. 8j+7 of the half: p~ = bf16(exp(s - m_ref))
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -470,23 +482,33 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     }
                     part[j] = acc;
                 }
-                if (send) {
+                lsum += (part[0] + part[1]) + (part[2] + part[3]);
+                const int st = i % NPBUF;
+                // the PV CTA has finished with its buffer from page i - NPBUF
+                const bool freed =
+                    wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
+                const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
+                const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
+                if (freed && has_head) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_async_v4(dst + pt_chunk_off(h, j), make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]),
-                                    bar);
+                    for (int j = 0; j < 4; ++j)
+                        st_async_v4(dst + pt_chunk_off(h, 4 * hf + j),
+                                    make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]), bar);
+                    if (hf == 0) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 }
-                lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                if (send) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
-                if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * w, any ? 1u : 0u, bar);
+                if (freed && hf == 0 && lane == 0) st_async_b32(dst + META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
             }
-            if (has_head && !aborted(sm)) {
-                float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
-                ml[0] = m_ref;
-                ml[1] = lsum;
-                ml[2] = best_s;
-                ml[3] = __int_as_float(best_t);
+            if (!stopped) {  // l = (sum over half 0) + (sum over half 1)
+                if (hf == 1) sm.xsum[qd][l] = lsum;
+                named_bar(pair_bar, 64);
+                if (hf == 0 && has_head && !aborted(sm)) {
+                    float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
+                    ml[0] = m_ref;
+                    ml[1] = lsum + sm.xsum[qd][l];
+                    ml[2] = best_s;
+                    ml[3] = __int_as_float(best_t);
+                }
             }
             // the PV CTA's last releases of its P buffers land here before exit
             if (lane == 0)
@@ -641,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
-    if (warp == 7) tmem_dealloc(tbase, TMEM_COLS);
+    if (warp == W_ALLOC) tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // ---- diagnostic: one page of each contraction --------------------------------------
