@@ -26,7 +26,8 @@
  *     row-major, in the layout its comment gives.
  *   - "device" pointers are CUDA device memory owned by the caller; the library
  *     never allocates, frees or synchronises device memory, so every device
- *     call can be captured into a CUDA graph.  `stream` is a cudaStream_t
+ *     call other than k3mla_paged_decode_noalloc can be captured into a CUDA
+ *     graph.  `stream` is a cudaStream_t
  *     (NULL = the legacy default stream).
  *   - Return value: K3MLA_OK (0) or a negative K3MLA_E_* code.  Argument errors
  *     are detected on the host before anything is launched.  A launch failure
@@ -175,6 +176,36 @@ int k3mla_pool_n_pages(const k3mla_pool* pool);
 /* Pool capacity and pages in use (PR #869 review: expose total / allocated). */
 int k3mla_pool_stats(const k3mla_pool* pool, int* total, int* used);
 void k3mla_pool_destroy(k3mla_pool* pool);
+
+/* ---- paged decode with built-in scratch ---------------------------------------
+ * The paper has no counterpart to this call.  It is k3mla_paged_decode without the
+ * `workspace` / `ws_bytes` pair, for callers that cannot allocate device memory at
+ * the point where they decode: a serving process that reserves all device memory
+ * for its own pool at start-up and forbids allocation while it serves, or a plugin
+ * that its host framework hands only the pointers of its inputs and outputs.  The
+ * scratch is a fixed array of K3MLA_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the
+ * library; every GPU that loads the library holds it until the process exits.  The
+ * call itself allocates and frees nothing.  Arguments, results and error behaviour
+ * are those of k3mla_paged_decode, and:
+ *   - Limit: k3mla_decode_workspace_bytes(B, max_ctx, split_tokens) must not exceed
+ *     K3MLA_NOALLOC_SCRATCH_BYTES, i.e. B * ceil(max_ctx / split_tokens) <= 84
+ *     (enough for k3mla_default_split_tokens with up to 84 slots).  A larger request
+ *     returns K3MLA_E_WORKSPACE before anything is launched; k3mla_last_error() gives
+ *     the sizes.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current).  Make that first call before any stream
+ *     capture begins.
+ *   - All calls on a device share the one array.  Calls whose kernels overlap on
+ *     the GPU (different streams, or threads with no ordering between their calls)
+ *     race on it and corrupt each other's results: order them, e.g. on one stream.
+ *   - Nothing in the array needs to start at zero: a call writes every scratch value
+ *     it reads, so what the previous call left there does not matter. */
+#define K3MLA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int k3mla_paged_decode_noalloc(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
+                               int layer, const int32_t* block_table, int max_pages_per_slot,
+                               const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
+                               uint16_t* out, int32_t* argmax_t, int B, int max_ctx, int split_tokens,
+                               int32_t* dev_err, void* stream);
 
 /* ---- diagnostic --------------------------------------------------------------
  * Runs the decode kernel's two tensor-core contractions on one 64-token page in

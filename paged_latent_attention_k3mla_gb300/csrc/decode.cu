@@ -57,6 +57,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -894,6 +895,65 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.split = split_tokens;
     mp.nsplit = ns;
     return launch_merge_expand(mp, st);
+}
+
+// ---- decode with built-in scratch ----------------------------------------------------
+// For callers that cannot allocate device memory when they decode (a server that reserves
+// all device memory for its own pool at start-up, a plugin that is handed only input and
+// output pointers): the split results live in this fixed array instead of a caller's
+// workspace.  Every device that loads the library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[K3MLA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device
+// with that device current (in host code the array's name is only a host-side handle).
+static int noalloc_scratch(void** out)
+{
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error("k3mla_paged_decode_noalloc: no usable current device (%s)", cudaGetErrorString(e));
+        return K3MLA_E_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+        if (e != cudaSuccess || !a) {
+            set_error("k3mla_paged_decode_noalloc: cudaGetSymbolAddress failed on device %d: %s", dev,
+                      cudaGetErrorString(e));
+            return K3MLA_E_CUDA;
+        }
+        addr[dev] = a;
+    }
+    *out = addr[dev];
+    return K3MLA_OK;
+}
+
+extern "C" int k3mla_paged_decode_noalloc(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
+                                          int layer, const int32_t* block_table, int max_pages_per_slot,
+                                          const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
+                                          uint16_t* out, int32_t* argmax_t, int B, int max_ctx, int split_tokens,
+                                          int32_t* dev_err, void* stream)
+{
+    if (B > 0 && max_ctx > 0 && split_tokens > 0) {
+        const size_t need = k3mla_decode_workspace_bytes(B, max_ctx, split_tokens);
+        if (need > (size_t)K3MLA_NOALLOC_SCRATCH_BYTES) {
+            set_error("k3mla_paged_decode_noalloc: B=%d, max_ctx=%d, split_tokens=%d need %zu bytes of scratch; "
+                      "the built-in scratch holds %zu (B * ceil(max_ctx / split_tokens) <= %zu)",
+                      B, max_ctx, split_tokens, need, (size_t)K3MLA_NOALLOC_SCRATCH_BYTES,
+                      (size_t)K3MLA_NOALLOC_SCRATCH_BYTES / k3mla_decode_workspace_bytes(1, 1, TILE));
+            return K3MLA_E_WORKSPACE;
+        }
+    }
+    if (!device_ok()) return K3MLA_E_DEVICE;
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return k3mla_paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len,
+                              w_kv_b, scale_bf16, out, argmax_t, scratch, (size_t)K3MLA_NOALLOC_SCRATCH_BYTES, B,
+                              max_ctx, split_tokens, dev_err, stream);
 }
 
 extern "C" int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, float* d, void* stream)

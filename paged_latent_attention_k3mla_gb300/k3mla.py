@@ -24,8 +24,11 @@ EXPORTS = (
     "k3mla_last_error", "k3mla_absorb_q", "k3mla_append_latent", "k3mla_decode_workspace_bytes",
     "k3mla_paged_decode", "k3mla_default_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
-    "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma",
+    "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
 )
+
+# Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -61,6 +64,7 @@ def load(build_if_needed: bool = True):
             "k3mla_pool_stats": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "k3mla_pool_destroy": ([P], None),
             "k3mla_diag_umma": ([I, P, P, P, P], I),
+            "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -155,6 +159,28 @@ def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_tabl
         _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), B, int(max_ctx), int(split_tokens),
         _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_paged_decode")
+
+
+def paged_decode_noalloc(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
+                         ctx_len: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor,
+                         max_ctx: int, split_tokens: int, argmax: torch.Tensor | None = None,
+                         dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """paged_decode without a workspace argument, for callers that cannot allocate
+    device memory where they decode: the split results go to the library's built-in
+    16 MiB scratch (B * ceil(max_ctx / split_tokens) <= 84).  Calls that overlap on
+    the GPU share that scratch and race; see include/k3mla.h."""
+    B = q_abs.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    lib = load()
+    _check(lib.k3mla_paged_decode_noalloc(
+        _dev(q_abs, torch.bfloat16, (B, H, ROW), "q_abs"),
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"),
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"), int(scale_bf16),
+        _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
+        B, int(max_ctx), int(split_tokens), _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)),
+        "k3mla_paged_decode_noalloc")
 
 
 def diag_umma(mode: int, a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, stream=None) -> None:
