@@ -53,6 +53,7 @@ struct MergeParams {
     const uint16_t* w_kv_b;
     uint16_t* out;         // [B][96][128] bf16
     int32_t* argmax;       // [B][96] or null
+    int32_t* dev_err;      // K3MLA_DEV_* bits or null
     int B, max_ctx, max_pages, split, nsplit;
 };
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st);

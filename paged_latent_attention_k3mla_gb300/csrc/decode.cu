@@ -889,6 +889,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.w_kv_b = w_kv_b;
     mp.out = out;
     mp.argmax = argmax_t;
+    mp.dev_err = dev_err;
     mp.B = B;
     mp.max_ctx = max_ctx;
     mp.max_pages = max_pages_per_slot;

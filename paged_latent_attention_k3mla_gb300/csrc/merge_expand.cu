@@ -6,21 +6,38 @@
 // PR #869, "K3: paged latent MLA KV + absorbed decode", M2 commit: "f32 latent
 // accumulation over ascending t landing bf16"), and out[b][h] = bf16(W_UV[h]
 // o_lat) with W_UV read in place from w_kv_b ("f32 W_UV expansion landing bf16").
-// Per head the expansion is a [B x 512] x [512 x 128] product: one CTA per
-// (half of v, head) keeps its 64 KB of W_UV in shared memory and runs it on
-// tensor cores with mma.sync, so W_UV is read from HBM once per layer.
+//
+// Per head the expansion is a dense product across slots,
+//     OUT_h^T [128 v x B] = W_UV[h] [128 v x 512] . O_lat_h^T [512 x B],
+// run on the 5th-generation tensor cores.  One CTA per (head, tile of 64 slots):
+//   * one elected thread stages W_UV[h] whole (128 KB) with a single 3-D TMA box,
+//     landing as the K-major A operand ([8 chunks][128 rows][128 B], 128-byte
+//     swizzle), while
+//   * eight warps merge the split partials of the tile's 64 slots (f32, ascending
+//     splits) and write bf16 o_lat straight into shared memory as the K-major B
+//     operand ([8 chunks][64 rows][128 B], same swizzle);
+//   * the elected thread then issues 32 MMAs (M = 128 v, N = 64 slots, K = 16)
+//     into a 128 x 64 f32 TMEM accumulator, and the eight warps read it back
+//     (lane = v, column = slot) and store bf16 out.
+// W_UV is read from HBM once per layer per 64 slots; the f32 partials are read
+// once, from L2 where the split kernel just wrote them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace k3 {
 
-__device__ __forceinline__ uint32_t mx_smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+constexpr int MX_SLOTS = 64;                   // slots per CTA (the MMA's N)
+constexpr int MX_MERGE_WARPS = 8;              // merge + epilogue warps
+constexpr int MX_THREADS = 32 * (MX_MERGE_WARPS + 1);  // + one TMA / MMA warp
+constexpr int MX_A_BYTES = 8 * VH * 128;       // W_UV[h]: 8 chunks x 128 rows x 128 B
+constexpr int MX_B_BYTES = 8 * MX_SLOTS * 128; // o_lat tile: 8 chunks x 64 rows x 128 B
+constexpr uint32_t MX_IDESC = make_idesc_bf16(128, MX_SLOTS, 0, 0);
+constexpr uint64_t MX_WAIT_NS = 1000000000ull;  // bounded waits: 1 s
 
 __device__ __forceinline__ uint32_t mx_pack_bf16x2(float lo, float hi)
 {
@@ -37,133 +54,170 @@ __device__ __forceinline__ int mx_ctx_effective(const int32_t* ctx_len, int b, i
     return n < 0 ? 0 : n;
 }
 
-
-constexpr int MX_THREADS = 256;
-constexpr int W_PITCH = LORA + 8;   // bf16 elements per smem row (16-byte pad)
-
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+// Bounded mbarrier wait: false (and K3MLA_DEV_TIMEOUT) after 1 s.
+__device__ __noinline__ bool mx_wait(uint64_t* bar, uint32_t parity, int32_t* dev_err)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+    const uint32_t a = smem_u32(bar);
+    if (mbar_test_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer() - t0 > MX_WAIT_NS) {
+            if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
 }
 
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// grid (2 halves of v, 96 heads); each CTA keeps W_UV[h][64 v][512] in shared memory.
-__global__ void __launch_bounds__(MX_THREADS) k3mla_merge_expand_kernel(const MergeParams p)
+// grid (96 heads, ceil(B / 64) slot tiles); block MX_THREADS.
+__global__ void __launch_bounds__(MX_THREADS, 1)
+    k3mla_merge_expand_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint16_t* sw = reinterpret_cast<uint16_t*>(smem_raw);   // [64][W_PITCH]
-    uint16_t* so = sw + 64 * W_PITCH;                         // [16][W_PITCH]
-    const int vh = blockIdx.x;
-    const int h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
+    uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sb = sa + MX_A_BYTES;
+    __shared__ uint64_t w_full, b_ready, d_full;
+    __shared__ uint32_t tmem_slot;
+    const int h = blockIdx.x;
+    const int b0 = blockIdx.y * MX_SLOTS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // W_UV[h] rows vh*64 .. vh*64+63 (w_kv_b rows h*256 + 128 + v)
-    const uint16_t* wsrc = p.w_kv_b + ((size_t)h * WROWS_PER_HEAD + NOPE + vh * 64) * LORA;
-    for (int q = tid; q < 64 * (LORA / 8); q += MX_THREADS) {
-        const int r = q / (LORA / 8), c8 = q % (LORA / 8);
-        *reinterpret_cast<uint4*>(sw + r * W_PITCH + c8 * 8) =
-            __ldg(reinterpret_cast<const uint4*>(wsrc + (size_t)r * LORA) + c8);
+    if (threadIdx.x == 0) {
+        mbar_init(&w_full, 1);
+        mbar_init(&b_ready, 32 * MX_MERGE_WARPS);
+        mbar_init(&d_full, 1);
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tmap_w);
     }
+    if (warp == MX_MERGE_WARPS) {
+        tmem_alloc(&tmem_slot, MX_SLOTS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
 
-    for (int m0 = 0; m0 < p.B; m0 += 16) {
-        __syncthreads();
-        {   // merge: thread -> (row r, dims 32*jc .. 32*jc+31)
-            const int r = tid >> 4, jc = tid & 15;
-            const int b = m0 + r;
-            float o[32];
+    if (warp == MX_MERGE_WARPS) {
+        if (lane == 0) {
+            // W_UV[h] = w_kv_b rows h*256 + 128 .. h*256 + 255, all 512 columns
+            mbar_arrive_expect_tx(&w_full, MX_A_BYTES);
+            tma_load_3d(sa, &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, 0, &w_full);
+            const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&b_ready, 0, p.dev_err);
+            if (ok) {
+                tc_fence_after();
+                const uint64_t ad = make_sdesc(smem_u32(sa), 16, 1024);
+                const uint64_t bd = make_sdesc(smem_u32(sb), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = 0.f;
-            float l = 1.f;
-            if (b < p.B) {
-                const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
-                const int ns = (ctx + p.split - 1) / p.split;
-                if (ns > 0) {
-                    const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-                    float m = -INFINITY;
-                    for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-                    l = 0.f;
-                    float best = -INFINITY;
-                    int best_t = -1;
-                    for (int i = 0; i < ns; ++i) {
-                        const float* mi = ml + (size_t)i * H * 4;
-                        const float wgt = expf(mi[0] - m);
-                        l += wgt * mi[1];
-                        const float* oi = p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA + 32 * jc;
+                for (int ks = 0; ks < LORA / 16; ++ks) {
+                    const int c = ks >> 2, kk = ks & 3;
+                    umma_ss(tbase, ad + (uint64_t)((c * (VH * 128) + kk * 32) >> 4),
+                            bd + (uint64_t)((c * (MX_SLOTS * 128) + kk * 32) >> 4), MX_IDESC, ks > 0 ? 1u : 0u);
+                }
+            } else {
+                // a wait gave up: let an in-flight TMA land before the CTA can exit
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+            }
+            umma_commit(&d_full);  // arrives once every MMA above is complete (at once if none)
+        }
+    } else {
+        // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are
+        // 128 float4, float4 f belongs to segment f % 4 (4 threads read 64 contiguous bytes).
+        const int r = threadIdx.x >> 2, seg = threadIdx.x & 3;
+        const int b = b0 + r;
+        int ns = 0;
+        if (b < p.B) {
+            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
+            ns = (ctx + p.split - 1) / p.split;
+        }
+        const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
+        float m = -INFINITY, l = 0.f, best = -INFINITY;
+        int best_t = -1;
+        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
+        for (int i = 0; i < ns; ++i) {
+            const float* mi = ml + (size_t)i * H * 4;
+            l += expf(mi[0] - m) * mi[1];
+            if (mi[2] > best) {  // ascending splits: the lowest t wins ties
+                best = mi[2];
+                best_t = __float_as_int(mi[3]);
+            }
+        }
+        if (ns == 0) l = 1.f;  // empty context: o_lat = 0
+        if (p.argmax && b < p.B && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {  // dims 256 pass .. 256 pass + 255
+            float acc[64];
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 v = *reinterpret_cast<const float4*>(oi + k);
-                            o[k + 0] += wgt * v.x;
-                            o[k + 1] += wgt * v.y;
-                            o[k + 2] += wgt * v.z;
-                            o[k + 3] += wgt * v.w;
-                        }
-                        if (mi[2] > best) {
-                            best = mi[2];
-                            best_t = __float_as_int(mi[3]);
-                        }
-                    }
-                    if (p.argmax && vh == 0 && jc == 0) p.argmax[(size_t)b * H + h] = best_t;
-                } else if (p.argmax && vh == 0 && jc == 0) {
-                    p.argmax[(size_t)b * H + h] = -1;
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
+            for (int i = 0; i < ns; ++i) {
+                const float wgt = expf(ml[(size_t)i * H * 4] - m);
+                const float4* oi = reinterpret_cast<const float4*>(
+                    p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA + 256 * pass);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 v = oi[seg + 4 * k];
+                    acc[4 * k + 0] += wgt * v.x;
+                    acc[4 * k + 1] += wgt * v.y;
+                    acc[4 * k + 2] += wgt * v.z;
+                    acc[4 * k + 3] += wgt * v.w;
                 }
             }
-            const float inv_l_div = l;  // divide each element by l (IEEE quotient)
-            uint32_t* dst = reinterpret_cast<uint32_t*>(so + r * W_PITCH + 32 * jc);
+            // dims d = 256 pass + 16 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) dst[k >> 1] = mx_pack_bf16x2(o[k] / inv_l_div, o[k + 1] / inv_l_div);
+            for (int k = 0; k < 16; ++k) {
+                const int c = 4 * pass + (k >> 2);
+                const int u = 2 * (k & 3) + (seg >> 1);
+                const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] / l, acc[4 * k + 1] / l),
+                                           mx_pack_bf16x2(acc[4 * k + 2] / l, acc[4 * k + 3] / l));
+                *reinterpret_cast<uint2*>(sb + c * (MX_SLOTS * 128) + r * 128 + ((u ^ (r & 7)) << 4) +
+                                          8 * (seg & 1)) = v;
+            }
         }
-        __syncthreads();
-        // out[16 x 64] = o_lat[16 x 512] . W_UV^T ; warp w -> v columns 8w .. 8w+7
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t a_base = mx_smem_u32(so) + ((lane & 15) * W_PITCH + (lane >> 4) * 8) * 2;
-        const uint32_t b_base = mx_smem_u32(sw) + ((8 * warp + (lane & 7)) * W_PITCH + ((lane >> 3) & 1) * 8) * 2;
-#pragma unroll 4
-        for (int ks = 0; ks < LORA / 16; ++ks) {
-            uint32_t a0, a1, a2, a3, b0, b1;
-            ldsm_x4(a_base + ks * 32, a0, a1, a2, a3);
-            ldsm_x2(b_base + ks * 32, b0, b1);
-            mma_bf16_16816(acc, a0, a1, a2, a3, b0, b1);
+        fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
+        mbar_arrive(&b_ready);
+
+        // ---- epilogue: warp (quarter q, half hf) reads v rows 32q .. 32q+31, slots 32hf .. 32hf+31
+        const int q = warp & 3, hf = warp >> 2;
+        const bool got = mx_wait(&d_full, 0, p.dev_err);
+        if (__all_sync(0xFFFFFFFFu, got)) {
+            tc_fence_after();
+            uint32_t acc32[32];
+            tmem_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * hf), acc32);
+            tmem_wait_ld();
+            const int v = 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int bb = b0 + 32 * hf + j;
+                if (bb < p.B)
+                    p.out[((size_t)bb * H + h) * VH + v] =
+                        (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc32[j]), 0.f) & 0xFFFFu);
+            }
         }
-        const int g = lane >> 2, t4 = lane & 3;
-        const int v = vh * 64 + 8 * warp + 2 * t4;
-        if (m0 + g < p.B)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(m0 + g) * H + h) * VH + v) = mx_pack_bf16x2(acc[0], acc[1]);
-        if (m0 + g + 8 < p.B)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(m0 + g + 8) * H + h) * VH + v) =
-                mx_pack_bf16x2(acc[2], acc[3]);
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MX_MERGE_WARPS) tmem_dealloc(tbase, MX_SLOTS);
 }
 
 
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
 {
     static bool attr_set[64] = {};
-    const int smem = (64 + 16) * W_PITCH * 2;
+    const int smem = MX_A_BYTES + MX_B_BYTES + 1024;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         cudaFuncSetAttribute(k3mla_merge_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    k3mla_merge_expand_kernel<<<dim3(2, H), dim3(MX_THREADS), smem, st>>>(mp);
+    // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = W_UV[h]
+    CUtensorMap tmap_w;
+    const int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 8);
+    if (rc) return rc;
+    const dim3 grid(H, (mp.B + MX_SLOTS - 1) / MX_SLOTS);
+    k3mla_merge_expand_kernel<<<grid, dim3(MX_THREADS), smem, st>>>(tmap_w, mp);
     return check_launch("k3mla_merge_expand_kernel");
 }
 
