@@ -91,6 +91,9 @@ constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C
 // epilogue, 4-8 producers, 9 MMA issuer, 10-13 idle.  Warp 8 allocates TMEM in both.
 constexpr int THREADS = 448;
 constexpr int W_PROD0 = 8, W_MMA0 = 11, W_ALLOC = 8;
+// named barriers of the score CTA (0 is __syncthreads): the decision hand-off between the two
+// softmax warps of a quarter (2 per quarter) and their final combine
+constexpr uint32_t HAND_BAR0 = 1, FIN_BAR0 = 9;
 // 14 warps put four on some SM sub-partitions (16K registers each): at most 128 registers per thread.
 
 struct __align__(1024) Smem {
@@ -108,9 +111,11 @@ struct __align__(1024) Smem {
     uint64_t q_land, q_ready;
     uint64_t p_full[NPBUF], p_empty[NPBUF];
     uint64_t o_done, epi_req, epi_done;
-    float xmax[2][4][32];    // score CTA: per-half page max of each head, exchanged inside a warp pair
-    int32_t xidx[2][4][32];  // ... and the first token of the half attaining it
-    float xsum[4][32];       // ... and, at the end, the second half's sum of exp
+    float xm[2][4][32];      // score CTA: reference max after a page, by page parity / quarter / lane
+    float xa[2][4][32];      // ... and that page's rescale factor (1 when it kept the reference)
+    float fin_l[4][32];      // ... the odd-page warp's sum of exp, best score and its token
+    float fin_s[4][32];
+    int32_t fin_t[4][32];
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
@@ -304,7 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
         }
         for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 8);
+            mbar_init(&sm.s_empty[i], 4);
         }
         for (int i = 0; i < NPBUF; ++i) {
             mbar_init(&sm.p_full[i], 1);
@@ -378,100 +383,118 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 if (!ok) drain_inflight();
             }
         } else if (warp < 8) {
-            // softmax warps 0..7: warp (qd = warp % 4, hf = warp / 4); thread l < 24 owns head 24 qd + l
-            // for tokens 32 hf .. 32 hf + 31 of every page.  The two warps of a quarter exchange their
-            // half-page max (and its first token) through shared memory and then take identical
-            // decisions, so the reference max, the rescale factor and the argmax agree.
-            const int qd = (int)(warp & 3u), hf = (int)(warp >> 2), l = (int)lane;
+            // softmax warps 0..7: warp (qd = warp % 4, par = warp / 4) owns heads 24 qd .. 24 qd + 23
+            // (thread l < 24 -> head 24 qd + l) for all 64 tokens of the pages of parity par.  The
+            // reference max is a chain through the pages: each warp hands its page's decision (new
+            // reference max, rescale factor) to the other warp of its quarter through shared memory
+            // and a named barrier, and takes the previous page's decision from it; everything else
+            // (scores, max, argmax, exp, the P store) of the two pages runs in parallel.
+            const int qd = (int)(warp & 3u), par = (int)(warp >> 2), l = (int)lane;
             const int h = HPW * qd + l;
             const bool has_head = l < HPW;
-            const uint32_t pair_bar = 1u + (uint32_t)qd;  // named barrier of warps qd and qd + 4
-            if (hf == 0) {
+            const uint32_t bar_in = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)(par ^ 1);
+            const uint32_t bar_out = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)par;
+            if (par == 0) {
                 const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
                 if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.q_ready);
             }
-            const uint32_t t_lane = tbase + ((32u * qd) << 16) + S_COL + 32u * hf;
+            const uint32_t t_lane = tbase + ((32u * qd) << 16) + S_COL;
             const float LOG2E = 1.4426950408889634f;
             float m_ref = -INFINITY, lsum = 0.f, best_s = -INFINITY;
             int best_t = -1;
             const uint32_t recv0 = mapa(smem_u32(sm.u.c1.recv[0]), 1);
             const uint32_t pfull0 = mapa(smem_u32(&sm.p_full[0]), 1);
-            bool stopped = false;
-            for (int i = 0; i < npg; ++i) {
+            bool ok = true;
+            for (int i = par; i < npg; i += 2) {
                 const int r = i % NSLOT, k = i / NSLOT;
-                const bool got = wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err);
-                if (named_bar_any(pair_bar, 64, !got)) {  // the pair stops together
-                    stopped = true;
-                    break;
-                }
-                __syncwarp();
-                tc_fence_after();
-                const int nvalid = min(PAGE, ntok - PAGE * i) - 32 * hf;  // valid tokens of this half
-                uint32_t sp[16];  // bf16 scores: token 2q in the low half, 2q+1 in the high half
-                {
-                    uint32_t rr[32];
-                    tmem_ld32(t_lane + 64u * r, rr);
-                    tmem_wait_ld();
+                if (ok) ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err));
+                const int nvalid = min(PAGE, ntok - PAGE * i);
+                uint32_t sp[32];  // bf16 scores: token 2q in the low half, 2q+1 in the high half
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)  // bf16(dot), then bf16(bf16(dot) * scale)
-                        sp[q] = mul_bf16x2(pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])),
-                                           p.scale2);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.s_empty[r]);
-                if (nvalid < 32) {
+                    for (int piece = 0; piece < 2; ++piece) {
+                        uint32_t rr[32];
+                        tmem_ld32(t_lane + 64u * r + 32u * piece, rr);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                        for (int q = 0; q < 16; ++q)  // bf16(dot), then bf16(bf16(dot) * scale)
+                            sp[16 * piece + q] = mul_bf16x2(
+                                pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])), p.scale2);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.s_empty[r]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) sp[q] = 0xFF80FF80u;
+                }
+                if (nvalid < PAGE) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
                         if (2 * q >= nvalid) sp[q] = (sp[q] & 0xFFFF0000u) | 0xFF80u;  // -inf
                         if (2 * q + 1 >= nvalid) sp[q] = (sp[q] & 0x0000FFFFu) | 0xFF800000u;
                     }
                 }
-                uint32_t mx[8];  // tree max over the 32 scores of this half
+                uint32_t g[8];  // max of each group of 8 tokens (packed: even tokens low, odd high)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) mx[q] = max_bf16x2(sp[q], sp[q + 8]);
+                for (int j = 0; j < 8; ++j)
+                    g[j] = max_bf16x2(max_bf16x2(sp[4 * j], sp[4 * j + 1]), max_bf16x2(sp[4 * j + 2], sp[4 * j + 3]));
+                const uint32_t g4 = max_bf16x2(max_bf16x2(max_bf16x2(g[0], g[1]), max_bf16x2(g[2], g[3])),
+                                               max_bf16x2(max_bf16x2(g[4], g[5]), max_bf16x2(g[6], g[7])));
+                const float pmax = fmaxf(bf16lo_to_f32(g4), bf16hi_to_f32(g4));
+                if (pmax > best_s) {  // lowest logical t attaining the best score
+                    best_s = pmax;
+                    int jg = 7;  // first group holding the max ...
 #pragma unroll
-                for (int q = 0; q < 4; ++q) mx[q] = max_bf16x2(mx[q], mx[q + 4]);
-                mx[0] = max_bf16x2(max_bf16x2(mx[0], mx[2]), max_bf16x2(mx[1], mx[3]));
-                const float lm = fmaxf(bf16lo_to_f32(mx[0]), bf16hi_to_f32(mx[0]));
-                int li = 0;  // first token of this half with score lm (needed only for a new best)
-                if (lm > best_s) {
-                    uint32_t bits = 0u;
+                    for (int j = 6; j >= 0; --j)
+                        if (fmaxf(bf16lo_to_f32(g[j]), bf16hi_to_f32(g[j])) == pmax) jg = j;
+                    uint32_t w[4] = {sp[0], sp[1], sp[2], sp[3]};
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        bits |= (bf16lo_to_f32(sp[q]) == lm ? 1u : 0u) << (2 * q);
-                        bits |= (bf16hi_to_f32(sp[q]) == lm ? 1u : 0u) << (2 * q + 1);
+                    for (int j = 1; j < 8; ++j)
+                        if (jg == j) {
+                            w[0] = sp[4 * j];
+                            w[1] = sp[4 * j + 1];
+                            w[2] = sp[4 * j + 2];
+                            w[3] = sp[4 * j + 3];
+                        }
+                    int tq = 7;  // ... and the first token in it
+#pragma unroll
+                    for (int q = 3; q >= 0; --q) {
+                        if (bf16hi_to_f32(w[q]) == pmax) tq = 2 * q + 1;
+                        if (bf16lo_to_f32(w[q]) == pmax) tq = 2 * q;
                     }
-                    li = __ffs(bits) - 1;
+                    best_t = start + PAGE * i + 8 * jg + tq;
                 }
-                sm.xmax[hf][qd][l] = lm;
-                sm.xidx[hf][qd][l] = li;
-                named_bar(pair_bar, 64);
-                const float pm = sm.xmax[hf ^ 1][qd][l];
-                const int pi = sm.xidx[hf ^ 1][qd][l];
-                const float m0 = hf ? pm : lm, m1 = hf ? lm : pm;
-                const float tmax = fmaxf(m0, m1);
-                if (tmax > best_s) {  // lowest logical t attaining the best score
-                    best_s = tmax;
-                    best_t = start + PAGE * i + (m0 == tmax ? (hf ? pi : li) : 32 + (hf ? li : pi));
+                // the decision of page i - 1, from the other warp
+                float m_prev = -INFINITY;
+                if (i > 0) {
+                    named_bar(bar_in, 64);
+                    m_prev = sm.xm[(i - 1) & 1][qd][l];
+                    lsum *= sm.xa[(i - 1) & 1][qd][l];
                 }
                 float alpha = 1.f;
                 bool resc = false;
                 if (i == 0) {
-                    m_ref = tmax;
-                } else if (tmax > m_ref + TAU) {
-                    alpha = ex2_approx((m_ref - tmax) * LOG2E);
+                    m_ref = pmax;
+                } else if (pmax > m_prev + TAU) {
+                    alpha = ex2_approx((m_prev - pmax) * LOG2E);
                     lsum *= alpha;
-                    m_ref = tmax;
+                    m_ref = pmax;
                     resc = true;
+                } else {
+                    m_ref = m_prev;
                 }
+                sm.xm[i & 1][qd][l] = m_ref;  // hand this page's decision on
+                sm.xa[i & 1][qd][l] = alpha;
+                named_bar_arrive(bar_out, 64);
                 const float mb = m_ref * LOG2E;
-                float part[4];  // independent partial sums, combined in a fixed order below
+                float part[8];  // independent partial sums, combined in a fixed order below
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {  // tokens 8j .. 8j+7 of the half: p~ = bf16(exp(s - m_ref))
+                for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), in place of s
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -483,33 +506,49 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                     }
                     part[j] = acc;
                 }
-                lsum += (part[0] + part[1]) + (part[2] + part[3]);
+                lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
                 const int st = i % NPBUF;
                 // the PV CTA has finished with its buffer from page i - NPBUF
-                const bool freed =
-                    wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
+                bool freed = false;
+                if (ok) freed = wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
                 const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
                 const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
                 if (freed && has_head) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        st_async_v4(dst + pt_chunk_off(h, 4 * hf + j),
+                    for (int j = 0; j < 8; ++j)
+                        st_async_v4(dst + pt_chunk_off(h, j),
                                     make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]), bar);
-                    if (hf == 0) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
+                    st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 }
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
-                if (freed && hf == 0 && lane == 0) st_async_b32(dst + META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
+                if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
             }
-            if (!stopped) {  // l = (sum over half 0) + (sum over half 1)
-                if (hf == 1) sm.xsum[qd][l] = lsum;
-                named_bar(pair_bar, 64);
-                if (hf == 0 && has_head && !aborted(sm)) {
-                    float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
-                    ml[0] = m_ref;
-                    ml[1] = lsum + sm.xsum[qd][l];
-                    ml[2] = best_s;
-                    ml[3] = __int_as_float(best_t);
+            // the other warp's decision on the last page, when that page was not this warp's
+            const int last = npg - 1;
+            if ((last & 1) != par) {
+                named_bar(bar_in, 64);
+                m_ref = sm.xm[last & 1][qd][l];
+                lsum *= sm.xa[last & 1][qd][l];
+            }
+            // l = (sum over even pages) + (sum over odd pages); best = the larger score, the lower t on ties
+            if (par == 1) {
+                sm.fin_l[qd][l] = lsum;
+                sm.fin_s[qd][l] = best_s;
+                sm.fin_t[qd][l] = best_t;
+            }
+            named_bar(FIN_BAR0 + (uint32_t)qd, 64);
+            if (par == 0 && has_head && ok && !aborted(sm)) {
+                const float s1 = sm.fin_s[qd][l];
+                const int t1 = sm.fin_t[qd][l];
+                if (s1 > best_s || (s1 == best_s && t1 < best_t && t1 >= 0)) {
+                    best_s = s1;
+                    best_t = t1;
                 }
+                float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
+                ml[0] = m_ref;
+                ml[1] = lsum + sm.fin_l[qd][l];
+                ml[2] = best_s;
+                ml[3] = __int_as_float(best_t);
             }
             // the PV CTA's last releases of its P buffers land here before exit
             if (lane == 0)

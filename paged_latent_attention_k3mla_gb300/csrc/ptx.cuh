@@ -257,6 +257,12 @@ __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive on a named barrier without waiting (the other `count - 32 * warps` threads bar.sync on it).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
