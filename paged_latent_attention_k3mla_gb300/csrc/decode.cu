@@ -68,6 +68,7 @@ constexpr int NSLOT = 3;                       // score CTA: page slots (one pro
 constexpr int SLOT0 = 9 * PAGE * 128;          // 73728 B: [9 chunks][64 rows][128 B]
 constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk of a page slot
 constexpr int HALF = 32;                       // PV CTA: tokens per half-page box
+constexpr int THIRD = 3 * 8192;  // score CTA: a third of a page slot (3 chunks), one TMA box
 constexpr int NHSLOT = 5;                      // PV CTA: half-page slots (one producer each)
 constexpr int SLOT1 = 8 * HALF * 128;          // 32768 B: [8 chunks][32 rows][128 B], chunks 0..7 only
 constexpr int HCHUNK = HALF * 128;             // 4096 B per chunk of a half-page slot
@@ -106,7 +107,7 @@ struct __align__(1024) Smem {
             uint8_t recv[NPBUF][PBUF];
         } c1;
     } u;
-    uint64_t full[8], empty[8];
+    uint64_t full[9], empty[9];  // score CTA: one pair per third of a page slot; PV CTA: per half-slot
     uint64_t s_full[NSLOT], s_empty[NSLOT];
     uint64_t q_land, q_ready;
     uint64_t p_full[NPBUF], p_empty[NPBUF];
@@ -121,7 +122,7 @@ struct __align__(1024) Smem {
     int32_t abort_flag;
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
-static_assert(NHSLOT <= 8, "barrier arrays");
+static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
 static_assert(QBYTES <= (NSLOT - 1) * SLOT0, "q_abs staging fits in slots 1..2");
 static_assert(PCOPY <= PBUF, "P buffer");
 
@@ -252,6 +253,21 @@ __device__ __forceinline__ void issue_score_page(uint32_t tbase, uint32_t d_col,
     }
 }
 
+// Score CTA: the 12 K steps of third t (chunks 3t .. 3t+2, at third_addr) of the same product.
+__device__ __forceinline__ void issue_score_third(uint32_t tbase, uint32_t d_col, uint32_t third_addr, int t)
+{
+    uint64_t bd = make_sdesc(third_addr, 16, 1024);
+    uint32_t a = tbase + Q_COL + 96u * (uint32_t)t;
+    const uint32_t d = tbase + d_col;
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_ts(d, a + 8u * ks, bd + 2u * ks, IDESC_S, (t | c | ks) != 0);
+        a += 32u;
+        bd += (uint64_t)(CHUNK >> 4);
+    }
+}
+
 // PV CTA: O^T (+)= C^T . P^T over one 64-token page held as two half-page slots
 // ([8 chunks][32 rows][128 B] each): 4 blocks of 128 dims x 4 K-steps of 16 tokens.
 __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_addr, uint32_t half1_addr,
@@ -303,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     const int32_t oob_row = p.n_pages * p.n_layers * PAGE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 9; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
         }
@@ -346,19 +362,21 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     if (rank == 0) {
         // =========================== score CTA ===========================
         if (warp >= W_PROD0 && warp < W_PROD0 + NSLOT) {
-            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r
+            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r, a third at a time
                 const int r = (int)warp - W_PROD0;
                 bool ok = true;
                 if (r > 0) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // slots 1..2 hold q_abs until then
                 for (int i = r; i < npg && ok; i += NSLOT) {
                     const int k = i / NSLOT;
                     const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
-                    if (!wait_bar(&sm.empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
-                        ok = false;
-                        break;
+                    for (int t = 0; t < 3; ++t) {  // third t = chunks 3t .. 3t+2, freed as soon as its MMAs end
+                        if (!wait_bar(&sm.empty[3 * r + t], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&sm.full[3 * r + t], THIRD);
+                        tma_load_3d(sm.u.c0.ring[r] + t * THIRD, &tmap_page, 0, y, 3 * t, &sm.full[3 * r + t]);
                     }
-                    mbar_arrive_expect_tx(&sm.full[r], SLOT0);
-                    tma_load_3d(sm.u.c0.ring[r], &tmap_page, 0, y, 0, &sm.full[r]);
                 }
                 if (!ok) drain_inflight();
             }
@@ -370,15 +388,20 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 const uint32_t slot = smem_u32(sm.u.c0.ring[r]);
                 for (int i = r; i < npg && ok; i += NSLOT) {
                     const int k = i / NSLOT;
-                    if (!wait_bar(&sm.s_empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err) ||
-                        !wait_bar(&sm.full[r], (uint32_t)(k & 1), sm, p.dev_err)) {
+                    if (!wait_bar(&sm.s_empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    issue_score_page(tbase, S_COL + 64u * r, slot);
-                    umma_commit(&sm.empty[r]);
-                    umma_commit(&sm.s_full[r]);
+                    for (int t = 0; t < 3 && ok; ++t) {
+                        if (!wait_bar(&sm.full[3 * r + t], (uint32_t)(k & 1), sm, p.dev_err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_score_third(tbase, S_COL + 64u * r, slot + (uint32_t)(t * THIRD), t);
+                        umma_commit(&sm.empty[3 * r + t]);
+                    }
+                    if (ok) umma_commit(&sm.s_full[r]);
                 }
                 if (!ok) drain_inflight();
             }
@@ -737,7 +760,7 @@ __global__ void __launch_bounds__(128, 1)
             mbar_arrive_expect_tx(&sm.q_land, QBYTES);
             tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, 0, 0, &sm.q_land);
             mbar_arrive_expect_tx(&sm.full[0], SLOT0);
-            tma_load_3d(sm.u.c0.ring[0], &tmap_page, 0, 0, 0, &sm.full[0]);
+            for (int t = 0; t < 3; ++t) tma_load_3d(sm.u.c0.ring[0] + t * THIRD, &tmap_page, 0, 0, 3 * t, &sm.full[0]);
         }
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.q_land, 0, sm, nullptr));
         if (ok) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
@@ -814,7 +837,7 @@ static int num_splits(int max_ctx, int split) { return (max_ctx + split - 1) / s
 static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_rows, CUtensorMap* page,
                      CUtensorMap* page8, CUtensorMap* qmap)
 {
-    int rc = make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 9);
+    int rc = make_tmap_slab_3d(page, slab, rows, ROW, 9, PAGE, 3);  // a third of a page
     if (rc) return rc;
     rc = make_tmap_slab_3d(page8, slab, rows, ROW, 9, HALF, 8);
     if (rc) return rc;
