@@ -10,14 +10,16 @@
 // Per head the expansion is a dense product across slots,
 //     OUT_h^T [128 v x B] = W_UV[h] [128 v x 512] . O_lat_h^T [512 x B],
 // run on the 5th-generation tensor cores.  One CTA per (head, tile of 64 slots):
-//   * one elected thread stages W_UV[h] whole (128 KB) with a single 3-D TMA box,
+//   * one elected thread stages W_UV[h] (128 KB) with eight 3-D TMA boxes, one per
+//     64-column chunk (several boxes in flight load faster than one large box),
 //     landing as the K-major A operand ([8 chunks][128 rows][128 B], 128-byte
 //     swizzle), while
-//   * eight warps merge the split partials of the tile's 64 slots (f32, ascending
-//     splits) and write bf16 o_lat straight into shared memory as the K-major B
-//     operand ([8 chunks][64 rows][128 B], same swizzle);
+//   * sixteen warps merge the split partials of the tile's 64 slots (f32, ascending
+//     splits; eight threads per slot, each a 64-dim slice) and write bf16 o_lat
+//     straight into shared memory as the K-major B operand ([8 chunks][64 rows]
+//     [128 B], same swizzle);
 //   * the elected thread then issues 32 MMAs (M = 128 v, N = 64 slots, K = 16)
-//     into a 128 x 64 f32 TMEM accumulator, and the eight warps read it back
+//     into a 128 x 64 f32 TMEM accumulator, and the sixteen warps read it back
 //     (lane = v, column = slot) and store bf16 out.
 // W_UV is read from HBM once per layer per 64 slots; the f32 partials are read
 // once, from L2 where the split kernel just wrote them.
@@ -32,8 +34,8 @@
 namespace k3 {
 
 constexpr int MX_SLOTS = 64;                   // slots per CTA (the MMA's N)
-constexpr int MX_MERGE_WARPS = 8;              // merge + epilogue warps
-constexpr int MX_THREADS = 32 * (MX_MERGE_WARPS + 1);  // + one TMA / MMA warp
+constexpr int MX_MERGE_WARPS = 16;             // merge + epilogue warps
+constexpr int MX_THREADS = 32 * MX_MERGE_WARPS;  // thread 0 also issues the TMA loads and the MMAs
 constexpr int MX_A_BYTES = 8 * VH * 128;       // W_UV[h]: 8 chunks x 128 rows x 128 B
 constexpr int MX_B_BYTES = 8 * MX_SLOTS * 128; // o_lat tile: 8 chunks x 64 rows x 128 B
 constexpr uint32_t MX_IDESC = make_idesc_bf16(128, MX_SLOTS, 0, 0);
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmap_w);
     }
-    if (warp == MX_MERGE_WARPS) {
+    if (warp == 0) {
         tmem_alloc(&tmem_slot, MX_SLOTS);
         tmem_relinquish();
     }
@@ -98,11 +100,85 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
 
-    if (warp == MX_MERGE_WARPS) {
-        if (lane == 0) {
-            // W_UV[h] = w_kv_b rows h*256 + 128 .. h*256 + 255, all 512 columns
-            mbar_arrive_expect_tx(&w_full, MX_A_BYTES);
-            tma_load_3d(sa, &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, 0, &w_full);
+    if (threadIdx.x == 0) {
+        // W_UV[h] = w_kv_b rows h*256 + 128 .. h*256 + 255, all 512 columns
+        mbar_arrive_expect_tx(&w_full, MX_A_BYTES);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            tma_load_3d(sa + c * (VH * 128), &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, c, &w_full);
+    }
+    {
+        // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are 128
+        // float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
+        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
+        const int b = b0 + r;
+        int ns = 0;
+        if (b < p.B) {
+            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
+            ns = (ctx + p.split - 1) / p.split;
+        }
+        float acc[64];
+        // split 0 is loaded before its weight is known (every slot below B has one), so the
+        // partials and the (m, l) records travel together
+        if (b < p.B) {
+            const float4* o0 = reinterpret_cast<const float4*>(p.ws_o + ((size_t)b * p.nsplit * H + h) * LORA);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float4 v = o0[seg + 8 * k];
+                acc[4 * k + 0] = v.x;
+                acc[4 * k + 1] = v.y;
+                acc[4 * k + 2] = v.z;
+                acc[4 * k + 3] = v.w;
+            }
+        }
+        const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
+        float m = -INFINITY, l = 0.f, best = -INFINITY;
+        int best_t = -1;
+        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
+        for (int i = 0; i < ns; ++i) {
+            const float* mi = ml + (size_t)i * H * 4;
+            l += expf(mi[0] - m) * mi[1];
+            if (mi[2] > best) {  // ascending splits: the lowest t wins ties
+                best = mi[2];
+                best_t = __float_as_int(mi[3]);
+            }
+        }
+        if (p.argmax && b < p.B && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
+        if (ns == 0) {  // empty context (or a padding row of the tile): o_lat = 0
+            l = 1.f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
+        } else {
+            const float w0 = expf(ml[0] - m);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f + w0 * acc[k];
+            for (int i = 1; i < ns; ++i) {  // ascending splits
+                const float wgt = expf(ml[(size_t)i * H * 4] - m);
+                const float4* oi =
+                    reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 v = oi[seg + 8 * k];
+                    acc[4 * k + 0] += wgt * v.x;
+                    acc[4 * k + 1] += wgt * v.y;
+                    acc[4 * k + 2] += wgt * v.z;
+                    acc[4 * k + 3] += wgt * v.w;
+                }
+            }
+        }
+        // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int c = k >> 1;
+            const int u = 4 * (k & 1) + (seg >> 1);
+            const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] / l, acc[4 * k + 1] / l),
+                                       mx_pack_bf16x2(acc[4 * k + 2] / l, acc[4 * k + 3] / l));
+            *reinterpret_cast<uint2*>(sb + c * (MX_SLOTS * 128) + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (seg & 1)) =
+                v;
+        }
+        fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
+        mbar_arrive(&b_ready);
+        if (threadIdx.x == 0) {  // the MMAs, once W_UV[h] has landed and every row of o_lat is written
             const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&b_ready, 0, p.dev_err);
             if (ok) {
                 tc_fence_after();
@@ -121,84 +197,29 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             }
             umma_commit(&d_full);  // arrives once every MMA above is complete (at once if none)
         }
-    } else {
-        // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are
-        // 128 float4, float4 f belongs to segment f % 4 (4 threads read 64 contiguous bytes).
-        const int r = threadIdx.x >> 2, seg = threadIdx.x & 3;
-        const int b = b0 + r;
-        int ns = 0;
-        if (b < p.B) {
-            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
-            ns = (ctx + p.split - 1) / p.split;
-        }
-        const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-        float m = -INFINITY, l = 0.f, best = -INFINITY;
-        int best_t = -1;
-        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-        for (int i = 0; i < ns; ++i) {
-            const float* mi = ml + (size_t)i * H * 4;
-            l += expf(mi[0] - m) * mi[1];
-            if (mi[2] > best) {  // ascending splits: the lowest t wins ties
-                best = mi[2];
-                best_t = __float_as_int(mi[3]);
-            }
-        }
-        if (ns == 0) l = 1.f;  // empty context: o_lat = 0
-        if (p.argmax && b < p.B && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {  // dims 256 pass .. 256 pass + 255
-            float acc[64];
-#pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-            for (int i = 0; i < ns; ++i) {
-                const float wgt = expf(ml[(size_t)i * H * 4] - m);
-                const float4* oi = reinterpret_cast<const float4*>(
-                    p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA + 256 * pass);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float4 v = oi[seg + 4 * k];
-                    acc[4 * k + 0] += wgt * v.x;
-                    acc[4 * k + 1] += wgt * v.y;
-                    acc[4 * k + 2] += wgt * v.z;
-                    acc[4 * k + 3] += wgt * v.w;
-                }
-            }
-            // dims d = 256 pass + 16 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int c = 4 * pass + (k >> 2);
-                const int u = 2 * (k & 3) + (seg >> 1);
-                const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] / l, acc[4 * k + 1] / l),
-                                           mx_pack_bf16x2(acc[4 * k + 2] / l, acc[4 * k + 3] / l));
-                *reinterpret_cast<uint2*>(sb + c * (MX_SLOTS * 128) + r * 128 + ((u ^ (r & 7)) << 4) +
-                                          8 * (seg & 1)) = v;
-            }
-        }
-        fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
-        mbar_arrive(&b_ready);
 
-        // ---- epilogue: warp (quarter q, half hf) reads v rows 32q .. 32q+31, slots 32hf .. 32hf+31
-        const int q = warp & 3, hf = warp >> 2;
+        // ---- epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15
+        const int q = warp & 3, cg = warp >> 2;
         const bool got = mx_wait(&d_full, 0, p.dev_err);
         if (__all_sync(0xFFFFFFFFu, got)) {
             tc_fence_after();
-            uint32_t acc32[32];
-            tmem_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * hf), acc32);
+            uint32_t acc16[16];
+            tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * cg), acc16);
             tmem_wait_ld();
             const int v = 32 * q + lane;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int bb = b0 + 32 * hf + j;
+            for (int j = 0; j < 16; ++j) {
+                const int bb = b0 + 16 * cg + j;
                 if (bb < p.B)
                     p.out[((size_t)bb * H + h) * VH + v] =
-                        (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc32[j]), 0.f) & 0xFFFFu);
+                        (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc16[j]), 0.f) & 0xFFFFu);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == MX_MERGE_WARPS) tmem_dealloc(tbase, MX_SLOTS);
+    if (warp == 0) tmem_dealloc(tbase, MX_SLOTS);
 }
 
 
@@ -212,9 +233,9 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
         cudaFuncSetAttribute(k3mla_merge_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = W_UV[h]
+    // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = one chunk of W_UV[h]
     CUtensorMap tmap_w;
-    const int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 8);
+    const int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 1);
     if (rc) return rc;
     const dim3 grid(H, (mp.B + MX_SLOTS - 1) / MX_SLOTS);
     k3mla_merge_expand_kernel<<<grid, dim3(MX_THREADS), smem, st>>>(tmap_w, mp);
