@@ -3,10 +3,14 @@
 // q absorption (pegainfer PR #869, "K3: paged latent MLA KV + absorbed decode",
 // M2 commit: "q_abs = W_UK^T q_nope is precomputed" and "q absorption lands
 // bf16"): q_abs[b][h][j] = bf16(sum_d W_UK[h][d][j] q_nope[b][h][d]) for j < 512,
-// then q_rope is copied to q_abs[b][h][512:576].  Per head this is a small
-// [B x 128] x [128 x 512] product whose cost is reading W_UK (12.6 MB per layer);
-// it runs on tensor cores with mma.sync (f32 accumulation), one CTA per
-// (head, 128 output columns), W_UK staged once in shared memory.
+// then q_rope is copied to q_abs[b][h][512:576].  Per head this is a dense
+// product across slots, Q_abs_h^T [512 x B] = W_UK[h]^T [512 x 128] . Q_nope_h^T
+// [128 x B], whose cost is reading W_UK (12.6 MB per layer).  It runs on the
+// 5th-generation tensor cores, one CTA per (head, tile of 64 slots): W_UK[h] lands
+// as the MN-major A operand ([8 chunks of 64 j][128 d][128 B], 128-byte swizzle) in
+// eight TMA boxes, sixteen warps write the q_nope tile as the K-major B operand
+// ([2 chunks of 64 d][64 slots][128 B]), and 32 MMAs (4 blocks of 128 j x 8 K
+// steps) fill four 128 x 64 f32 TMEM accumulators that the warps read back.
 //
 // Append (same PR, M1 commit): the new token's 512-wide latent and 64-wide rope
 // key land in row ((page * L + layer) * 64 + pos % 64) of the page-first slab,
@@ -17,18 +21,17 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace k3 {
 
-constexpr int AB_THREADS = 256;
-constexpr int AB_NCOLS = 128;             // output columns per CTA
-constexpr int AB_PITCH = AB_NCOLS + 8;    // W tile pitch (elements), 16-byte pad
-constexpr int AQ_PITCH = NOPE + 8;        // q tile pitch (elements)
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+constexpr int AB_SLOTS = 64;                     // slots per CTA (the MMA's N)
+constexpr int AB_WARPS = 16;
+constexpr int AB_THREADS = 32 * AB_WARPS;
+constexpr int AB_A_BYTES = 8 * NOPE * 128;        // W_UK[h]: 8 j-chunks x 128 d rows x 128 B
+constexpr int AB_B_BYTES = 2 * AB_SLOTS * 128;    // q_nope tile: 2 d-chunks x 64 slots x 128 B
+constexpr uint32_t AB_IDESC = make_idesc_bf16(128, AB_SLOTS, 1, 0);  // A MN-major, B K-major
+constexpr uint64_t AB_WAIT_NS = 1000000000ull;
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -37,77 +40,116 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return r;
 }
 
-// grid (512 / 128 column blocks, 96 heads)
-__global__ void __launch_bounds__(AB_THREADS) k3mla_absorb_kernel(const uint16_t* __restrict__ q,
-                                                                    const uint16_t* __restrict__ w,
-                                                                    uint16_t* __restrict__ q_abs, int B)
+// Bounded mbarrier wait: false (and K3MLA_DEV_TIMEOUT when dev_err is given) after 1 s.
+__device__ __noinline__ bool ab_wait(uint64_t* bar, uint32_t parity, int32_t* dev_err)
 {
-    __shared__ __align__(16) uint16_t sw[NOPE * AB_PITCH];   // W_UK[h][d][nb*128 + n]
-    __shared__ __align__(16) uint16_t sq[16 * AQ_PITCH];     // q_nope rows of 16 slots
-    const int nb = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t a = smem_u32(bar);
+    if (mbar_test_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer() - t0 > AB_WAIT_NS) {
+            if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
 
-    const uint16_t* wsrc = w + (size_t)h * WROWS_PER_HEAD * LORA + nb * AB_NCOLS;
-    for (int i = tid; i < NOPE * (AB_NCOLS / 8); i += AB_THREADS) {
-        const int d = i / (AB_NCOLS / 8), c8 = i % (AB_NCOLS / 8);
-        *reinterpret_cast<uint4*>(sw + d * AB_PITCH + c8 * 8) =
-            __ldg(reinterpret_cast<const uint4*>(wsrc + (size_t)d * LORA) + c8);
+// grid (96 heads, ceil(B / 64) slot tiles); block AB_THREADS; thread 0 also issues the loads and MMAs.
+__global__ void __launch_bounds__(AB_THREADS, 1)
+    k3mla_absorb_kernel(const __grid_constant__ CUtensorMap tmap_w, const uint16_t* __restrict__ q,
+                        uint16_t* __restrict__ q_abs, int B)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sb = sa + AB_A_BYTES;
+    __shared__ uint64_t w_full, b_ready, d_full;
+    __shared__ uint32_t tmem_slot;
+    const int h = blockIdx.x;
+    const int b0 = blockIdx.y * AB_SLOTS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&w_full, 1);
+        mbar_init(&b_ready, AB_THREADS);
+        mbar_init(&d_full, 1);
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tmap_w);
     }
-    if (nb == 0) {  // rope half copied through
-        for (int i = tid; i < B * (ROPE / 8); i += AB_THREADS) {
-            const int b = i / (ROPE / 8), c8 = i % (ROPE / 8);
-            *reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW + LORA + c8 * 8) =
-                __ldg(reinterpret_cast<const uint4*>(q + ((size_t)b * H + h) * QDIM + NOPE) + c8);
-        }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 4 * AB_SLOTS);
+        tmem_relinquish();
     }
-    // warp -> output columns 16*warp .. 16*warp+15 (two n8 tiles)
-    const uint32_t a_base = smem_addr(sq) + ((lane & 15) * AQ_PITCH + (lane >> 4) * 8) * 2;
-    // x4.trans over W[k][n]: lane -> k row (lane & 7) + 8*((lane>>3)&1), n block 8*(lane>>4)
-    const uint32_t b_base =
-        smem_addr(sw) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * AB_PITCH + 16 * warp + 8 * (lane >> 4)) * 2;
-    for (int m0 = 0; m0 < B; m0 += 16) {
-        __syncthreads();
-        {
-            const int r = tid >> 4, c8 = tid & 15;  // 16 rows x 16 chunks of 8
-            const int b = m0 + r;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (b < B) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)b * H + h) * QDIM) + c8);
-            *reinterpret_cast<uint4*>(sq + r * AQ_PITCH + c8 * 8) = v;
-        }
-        __syncthreads();
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
+
+    if (threadIdx.x == 0) {  // W_UK[h] = w_kv_b rows h*256 .. h*256 + 127 ([d][j]), one box per 64 j
+        mbar_arrive_expect_tx(&w_full, AB_A_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < NOPE / 16; ++ks) {
-            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(a_base + ks * 32));
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                         : "r"(b_base + ks * 16 * AB_PITCH * 2));
-            asm volatile(
-                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                "{%0,%1,%2,%3};"
-                : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3])
-                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-            asm volatile(
-                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                "{%0,%1,%2,%3};"
-                : "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3])
-                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b2), "r"(b3));
-        }
-        const int g = lane >> 2, t4 = lane & 3;
+        for (int c = 0; c < 8; ++c) tma_load_3d(sa + c * (NOPE * 128), &tmap_w, 0, h * WROWS_PER_HEAD, c, &w_full);
+    }
+    {   // q_nope of the tile -> B operand; q_rope -> q_abs[..][512:576].  thread -> (slot r, segment seg)
+        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
+        const int b = b0 + r;
+        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * H + h) * QDIM);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int col = nb * AB_NCOLS + 16 * warp + 8 * nt + 2 * t4;
-            if (m0 + g < B)
-                *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(m0 + g) * H + h) * ROW + col) =
-                    pack2(acc[nt][0], acc[nt][1]);
-            if (m0 + g + 8 < B)
-                *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(m0 + g + 8) * H + h) * ROW + col) =
-                    pack2(acc[nt][2], acc[nt][3]);
+        for (int e = 0; e < 2; ++e) {  // 16-byte unit u = 2 seg + e: dims 8u .. 8u+7
+            const int u = 2 * seg + e;
+            const uint4 v = (b < B) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+            const int c = u >> 3, uu = u & 7;
+            *reinterpret_cast<uint4*>(sb + c * (AB_SLOTS * 128) + r * 128 + ((uu ^ (r & 7)) << 4)) = v;
+        }
+        if (b < B)
+            reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW + LORA)[seg] = __ldg(src + NOPE / 8 + seg);
+        fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
+        mbar_arrive(&b_ready);
+    }
+    if (threadIdx.x == 0) {
+        const bool ok = ab_wait(&w_full, 0, nullptr) && ab_wait(&b_ready, 0, nullptr);
+        if (ok) {
+            tc_fence_after();
+            const uint64_t ad = make_sdesc(smem_u32(sa), NOPE * 128, 1024);  // LBO: next 64-j chunk
+            const uint64_t bd = make_sdesc(smem_u32(sb), 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < NOPE / 16; ++ks)
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)  // four independent accumulators in turn
+                    umma_ss(tbase + (uint32_t)(AB_SLOTS * mt),
+                            ad + (uint64_t)((mt * 2 * NOPE * 128 + ks * 16 * 128) >> 4),
+                            bd + (uint64_t)(((ks >> 2) * (AB_SLOTS * 128) + (ks & 3) * 32) >> 4), AB_IDESC,
+                            ks > 0 ? 1u : 0u);
+        } else {
+            const uint64_t t0 = globaltimer();  // let an in-flight TMA land before the CTA can exit
+            while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+        }
+        umma_commit(&d_full);
+    }
+    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's 64 slots
+        const int qq = warp & 3, mt = warp >> 2;
+        const bool got = ab_wait(&d_full, 0, nullptr);
+        if (__all_sync(0xFFFFFFFFu, got)) {
+            tc_fence_after();
+            const int j = 128 * mt + 32 * qq + lane;
+#pragma unroll
+            for (int piece = 0; piece < 2; ++piece) {
+                uint32_t acc[32];
+                tmem_ld32(tbase + ((uint32_t)(32 * qq) << 16) + (uint32_t)(AB_SLOTS * mt + 32 * piece), acc);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int b = b0 + 32 * piece + k;
+                    if (b < B)
+                        q_abs[((size_t)b * H + h) * ROW + j] = (uint16_t)(pack2(__uint_as_float(acc[k]), 0.f) & 0xFFFFu);
+                }
+            }
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tbase, 4 * AB_SLOTS);
 }
 
 // one CTA of 96 threads per slot; each thread moves three 32-bit words
@@ -152,8 +194,20 @@ extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_
         return K3MLA_E_INVALID;
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
-    k3mla_absorb_kernel<<<dim3(LORA / AB_NCOLS, H), AB_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        q, w_kv_b, q_abs, B);
+    static bool attr_set[64] = {};
+    const int smem = AB_A_BYTES + AB_B_BYTES + 1024;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaFuncSetAttribute(k3mla_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = 64 columns of W_UK[h]
+    CUtensorMap tmap_w;
+    const int rc = make_tmap_slab_3d(&tmap_w, w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, NOPE, 1);
+    if (rc) return rc;
+    k3mla_absorb_kernel<<<dim3(H, (B + AB_SLOTS - 1) / AB_SLOTS), AB_THREADS, smem,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(tmap_w, q, q_abs, B);
     return check_launch("k3mla_absorb_kernel");
 }
 
