@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
+    griddep_wait();  // the set-up above overlaps the previous kernel in the stream
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {  // W_UK[h] = w_kv_b rows h*256 .. h*256 + 127 ([d][j]), one box per 64 j
         mbar_arrive_expect_tx(&w_full, AB_A_BYTES);
@@ -160,6 +162,8 @@ __global__ void __launch_bounds__(96) k3mla_append_kernel(uint16_t* __restrict__
                                                             const uint16_t* __restrict__ k_rope, int64_t r_stride,
                                                             int32_t* dev_err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.x;
     const int p = pos[b];
     if (p < 0) return;
@@ -206,9 +210,8 @@ extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_
     CUtensorMap tmap_w;
     const int rc = make_tmap_slab_3d(&tmap_w, w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, NOPE, 1);
     if (rc) return rc;
-    k3mla_absorb_kernel<<<dim3(H, (B + AB_SLOTS - 1) / AB_SLOTS), AB_THREADS, smem,
-                          reinterpret_cast<cudaStream_t>(stream)>>>(tmap_w, q, q_abs, B);
-    return check_launch("k3mla_absorb_kernel");
+    return launch_pdl(k3mla_absorb_kernel, dim3(H, (B + AB_SLOTS - 1) / AB_SLOTS), dim3(AB_THREADS), smem,
+                      reinterpret_cast<cudaStream_t>(stream), "k3mla_absorb_kernel", tmap_w, q, q_abs, B);
 }
 
 extern "C" int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
@@ -228,8 +231,7 @@ extern "C" int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, in
         return K3MLA_E_INVALID;
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
-    k3mla_append_kernel<<<B, 96, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, pos, c_kv, c_stride, k_rope, r_stride,
-        dev_err);
-    return check_launch("k3mla_append_kernel");
+    return launch_pdl(k3mla_append_kernel, dim3(B), dim3(96), 0, reinterpret_cast<cudaStream_t>(stream),
+                      "k3mla_append_kernel", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, pos,
+                      c_kv, c_stride, k_rope, r_stride, dev_err);
 }

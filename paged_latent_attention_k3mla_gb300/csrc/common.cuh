@@ -45,6 +45,28 @@ int make_tmap_slab_3d(CUtensorMap* map, const void* base, uint64_t rows, uint32_
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Launch `kernel` on `st` with programmatic stream serialization: it may be scheduled while the
+// kernel before it in the stream is still running, and every kernel of this library calls
+// griddep_wait() before it touches memory that an earlier kernel may write.  Returns K3MLA_OK or
+// K3MLA_E_CUDA (text recorded under `what`).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const char* what,
+               Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, args...);
+    return check_launch(what);
+}
+
 // Split partials -> o_lat -> W_UV expansion (merge_expand.cu).
 struct MergeParams {
     const float* ws_o;     // [B][nsplit][96][512] f32 partial O

@@ -340,11 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
         if (rank == 1)  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
             for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
         fence_mbarrier_init_cluster();
-        if (rank == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
-            tma_prefetch_desc(&tmap_q);
-            mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-            tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, b * H, 0, &sm.q_land);
-        }
+        if (rank == 0) tma_prefetch_desc(&tmap_q);
     }
     if (warp == W_ALLOC) {
         tmem_alloc(&sm.tmem_base, TMEM_COLS);
@@ -358,6 +354,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     cluster_sync();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
+    // everything above overlaps the previous kernel in the stream; q_abs, the slab, the block table
+    // and the context lengths are read only after it has completed
+    griddep_wait();
+    griddep_launch_dependents();
+    if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
+        mbar_arrive_expect_tx(&sm.q_land, QBYTES);
+        for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[1] + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
+    }
 
     if (rank == 0) {
         // =========================== score CTA ===========================
@@ -758,7 +762,7 @@ __global__ void __launch_bounds__(128, 1)
     if (mode == 0) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-            tma_load_3d(sm.u.c0.ring[1], &tmap_q, 0, 0, 0, &sm.q_land);
+            for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[1] + c * QCHUNK, &tmap_q, 0, 0, c, &sm.q_land);
             mbar_arrive_expect_tx(&sm.full[0], SLOT0);
             for (int t = 0; t < 3; ++t) tma_load_3d(sm.u.c0.ring[0] + t * THIRD, &tmap_page, 0, 0, 3 * t, &sm.full[0]);
         }
@@ -841,7 +845,7 @@ static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_
     if (rc) return rc;
     rc = make_tmap_slab_3d(page8, slab, rows, ROW, 9, HALF, 8);
     if (rc) return rc;
-    return make_tmap_slab_3d(qmap, q, q_rows, ROW, 9, H, 9);
+    return make_tmap_slab_3d(qmap, q, q_rows, ROW, 9, H, 1);  // one 64-column chunk per box
 }
 
 static void set_smem_attr(const void* fn, size_t bytes, bool* done)
@@ -940,8 +944,8 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     dp.nsplit = ns;
     dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    k3mla_decode_split_kernel<<<dim3(2 * B * ns), dim3(THREADS), smem, st>>>(tm_page, tm_page8, tm_q, dp);
-    rc = check_launch("k3mla_decode_split_kernel");
+    rc = launch_pdl(k3mla_decode_split_kernel, dim3(2 * B * ns), dim3(THREADS), smem, st, "k3mla_decode_split_kernel",
+                    tm_page, tm_page8, tm_q, dp);
     if (rc) return rc;
 
     MergeParams mp;

@@ -107,6 +107,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         for (int c = 0; c < 8; ++c)
             tma_load_3d(sa + c * (VH * 128), &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, c, &w_full);
     }
+    // W_UV is a layer weight no kernel of this library writes, so its load above overlaps the split
+    // kernel; the split partials, the context lengths and the outputs wait for it
+    griddep_wait();
+    griddep_launch_dependents();
     {
         // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are 128
         // float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
@@ -238,8 +242,8 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
     const int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 1);
     if (rc) return rc;
     const dim3 grid(H, (mp.B + MX_SLOTS - 1) / MX_SLOTS);
-    k3mla_merge_expand_kernel<<<grid, dim3(MX_THREADS), smem, st>>>(tmap_w, mp);
-    return check_launch("k3mla_merge_expand_kernel");
+    return launch_pdl(k3mla_merge_expand_kernel, grid, dim3(MX_THREADS), smem, st, "k3mla_merge_expand_kernel",
+                      tmap_w, mp);
 }
 
 }  // namespace k3

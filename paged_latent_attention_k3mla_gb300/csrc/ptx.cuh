@@ -277,6 +277,18 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on (launched before it in the stream) have completed
+// and their memory is visible; a no-op for a kernel launched without a programmatic dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the grid launched after this one in the stream be scheduled before this one completes.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *dst.
