@@ -124,30 +124,35 @@ def alg_flops(wl):
     return n * H * 2 * (ROW + LORA) + 2 * 2 * wl.B * H * 128 * LORA
 
 
-def cpu_baseline(wl, layer=0, n_slots=None):
-    """The oracle (as it stands) on a bounded sample: n_slots slots of one layer."""
+def cpu_baseline(wl, layers=None, n_slots=None):
+    """The oracle (as it stands) on a bounded sample: n_slots slots of each of the listed layers
+    (by default all slots of up to 8 layers, about 10 s of CPU work on 16 cores)."""
     import oracle
     B = wl.B
     if n_slots is None:
-        n_slots = min(B, 16 if int(wl.ctx_len.max()) <= 4096 else 2)
+        n_slots = B if int(wl.ctx_len.max()) <= 4096 else 2
+    if layers is None:
+        layers = list(range(min(wl.n_layers, 8)))
     slots = list(range(n_slots))
     ncores = os.cpu_count() or 1
     tbl = wl.block_table[slots]
     used = sorted(set(int(x) for x in tbl.ravel() if x >= 0))
     remap = {p: i for i, p in enumerate(used)}
     idx = torch.tensor(used if used else [0], dtype=torch.long, device=wl.slab.device)
-    slab = synth.bf16_bits(wl.slab.index_select(0, idx)[:, layer:layer + 1])
     t2 = np.vectorize(lambda x: remap.get(int(x), -1))(tbl).astype(np.int32)
-    q = synth.bf16_bits(wl.q[layer][slots])
-    w = synth.bf16_bits(wl.w_kv_b[layer])
-    t0 = time.perf_counter()
-    qa = oracle.absorb(q, w)
-    oracle.decode(qa, slab, 0, t2, wl.ctx_len[slots].astype(np.int32), w, wl.scale_bits, nthreads=ncores)
-    dt = time.perf_counter() - t0
-    us_per_layer = dt * 1e6 * (B / n_slots)
+    dt = 0.0
+    for layer in layers:
+        slab = synth.bf16_bits(wl.slab.index_select(0, idx)[:, layer:layer + 1])
+        q = synth.bf16_bits(wl.q[layer][slots])
+        w = synth.bf16_bits(wl.w_kv_b[layer])
+        t0 = time.perf_counter()
+        qa = oracle.absorb(q, w)
+        oracle.decode(qa, slab, 0, t2, wl.ctx_len[slots].astype(np.int32), w, wl.scale_bits, nthreads=ncores)
+        dt += time.perf_counter() - t0
+    us_per_layer = dt * 1e6 / len(layers) * (B / n_slots)
     return {"value": us_per_layer, "unit": "us/layer-call", "cores": ncores, "kind": "oracle",
-            "sample": f"{n_slots} of {B} slots of one layer-call (absorb + decode chain), "
-                      f"{dt:.2f} s wall on {ncores} threads, scaled by {B}/{n_slots}"}
+            "sample": f"{n_slots} of {B} slots x {len(layers)} layer-call(s) (absorb + decode chain), "
+                      f"{dt:.2f} s wall on {ncores} threads, scaled to one {B}-slot layer-call"}
 
 
 def run_reference(args):
@@ -161,7 +166,7 @@ def run_reference(args):
     vals = []
     cb = None
     for _ in range(args.steps):
-        cb = cpu_baseline(wl, 0, n_slots)
+        cb = cpu_baseline(wl, [0], n_slots)
         vals.append(cb["value"])
     v = statistics.mean(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/layer-call",
@@ -333,7 +338,7 @@ def main():
                 traffic = d.get("bytes_per_call")
         except (ValueError, OSError):
             traffic = None
-    cpu = None if args.no_cpu else cpu_baseline(wl, 0)
+    cpu = None if args.no_cpu else cpu_baseline(wl)
     line = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": "us/layer-call", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
