@@ -68,7 +68,9 @@ constexpr int NSLOT = 3;                       // score CTA: page slots (one pro
 constexpr int SLOT0 = 9 * PAGE * 128;          // 73728 B: [9 chunks][64 rows][128 B]
 constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk of a page slot
 constexpr int HALF = 32;                       // PV CTA: tokens per half-page box
-constexpr int THIRD = 3 * 8192;  // score CTA: a third of a page slot (3 chunks), one TMA box
+constexpr int THIRD = 3 * 8192;  // score CTA: a third of a page (3 chunks), one TMA box
+constexpr int NUNIT = 8;         // score CTA: ring of third-page units (2.67 pages)
+constexpr int PSTAGE = 24 * 128; // score CTA: one softmax warp's P rows (24 heads x 64 tokens bf16)
 constexpr int NHSLOT = 5;                      // PV CTA: half-page slots (one producer each)
 constexpr int SLOT1 = 8 * HALF * 128;          // 32768 B: [8 chunks][32 rows][128 B], chunks 0..7 only
 constexpr int HCHUNK = HALF * 128;             // 4096 B per chunk of a half-page slot
@@ -100,7 +102,8 @@ constexpr uint32_t HAND_BAR0 = 1, FIN_BAR0 = 9;
 struct __align__(1024) Smem {
     union {
         struct {
-            uint8_t ring[NSLOT][SLOT0];
+            uint8_t ring[NUNIT][THIRD];  // page thirds; q_abs is staged in units 3.. until it is in TMEM
+            uint8_t pstage[8][PSTAGE];   // each softmax warp's P rows, copied to the PV CTA in bulk
         } c0;
         struct {
             uint8_t ring[NHSLOT][SLOT1];
@@ -117,13 +120,18 @@ struct __align__(1024) Smem {
     float fin_l[4][32];      // ... the odd-page warp's sum of exp, best score and its token
     float fin_s[4][32];
     int32_t fin_t[4][32];
+    // score CTA: the uses of a third-page unit go to different producer and issuer threads; a use
+    // is handled only after the previous use of the unit has passed the same barrier, so a
+    // barrier is never waited on two phases ahead (where its parity would repeat)
+    int32_t unit_loaded[NUNIT];  // uses of the unit whose load has been issued
+    int32_t unit_taken[NUNIT];   // uses of the unit whose MMAs have been issued
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
 static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
-static_assert(QBYTES <= (NSLOT - 1) * SLOT0, "q_abs staging fits in slots 1..2");
+static_assert(QBYTES <= (NUNIT - 3) * THIRD, "q_abs staging fits in units 3..");
 static_assert(PCOPY <= PBUF, "P buffer");
 
 struct DecodeParams {
@@ -182,6 +190,25 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& s
     const uint32_t a = smem_u32(bar);
     if (cluster_scope ? mbar_test_wait_cluster(a, parity) : mbar_test_wait(a, parity)) return true;
     return wait_bar_slow(bar, parity, sm, dev_err, cluster_scope);
+}
+
+// Bounded wait until a shared counter of this CTA reaches `target` (written by another thread of
+// the CTA with a plain store); false when this CTA aborted or the wait timed out.
+__device__ __noinline__ bool wait_count(const int32_t* counter, int32_t target, Smem& sm, int32_t* dev_err)
+{
+    const volatile int32_t* v = counter;
+    if (*v >= target) return true;
+    const uint64_t t0 = globaltimer();
+    while (*v < target) {
+        if (aborted(sm)) return false;
+        if (globaltimer() - t0 > WAIT_NS) {
+            *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
+            if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
 }
 
 // After an abort: let this thread's in-flight TMA copies / MMAs land (bounded, ~2 ms).
@@ -337,6 +364,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
         mbar_init(&sm.epi_req, 1);
         mbar_init(&sm.epi_done, 4);
         sm.abort_flag = 0;
+        for (int i = 0; i < NUNIT; ++i) {
+            sm.unit_loaded[i] = 0;
+            sm.unit_taken[i] = 0;
+        }
         if (rank == 1)  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
             for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
         fence_mbarrier_init_cluster();
@@ -360,27 +391,30 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     griddep_launch_dependents();
     if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
         mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-        for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[1] + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
+        for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[3] + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
     }
 
     if (rank == 0) {
         // =========================== score CTA ===========================
         if (warp >= W_PROD0 && warp < W_PROD0 + NSLOT) {
-            if (lane == 0) {  // producer r streams the pages i = r (mod 3) into slot r, a third at a time
-                const int r = (int)warp - W_PROD0;
+            if (lane == 0) {  // producer t streams third t (chunks 3t .. 3t+2) of every page
+                // third g = 3i + t of the split lives in unit g % NUNIT; a unit's uses are strictly
+                // ordered (a use is loaded only after the MMAs of the previous use released it)
+                const int t = (int)warp - W_PROD0;
                 bool ok = true;
-                if (r > 0) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // slots 1..2 hold q_abs until then
-                for (int i = r; i < npg && ok; i += NSLOT) {
-                    const int k = i / NSLOT;
+                for (int i = 0; i < npg && ok; ++i) {
+                    if (i == 1) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // units 3.. hold q_abs until then
+                    if (!ok) break;
+                    const int g = 3 * i + t, u = g % NUNIT, k = g / NUNIT;
                     const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
-                    for (int t = 0; t < 3; ++t) {  // third t = chunks 3t .. 3t+2, freed as soon as its MMAs end
-                        if (!wait_bar(&sm.empty[3 * r + t], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&sm.full[3 * r + t], THIRD);
-                        tma_load_3d(sm.u.c0.ring[r] + t * THIRD, &tmap_page, 0, y, 3 * t, &sm.full[3 * r + t]);
+                    if (!wait_count(&sm.unit_loaded[u], k, sm, p.dev_err) ||
+                        !wait_bar(&sm.empty[u], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
+                        ok = false;
+                        break;
                     }
+                    *reinterpret_cast<volatile int32_t*>(&sm.unit_loaded[u]) = k + 1;
+                    mbar_arrive_expect_tx(&sm.full[u], THIRD);
+                    tma_load_3d(sm.u.c0.ring[u], &tmap_page, 0, y, 3 * t, &sm.full[u]);
                 }
                 if (!ok) drain_inflight();
             }
@@ -389,7 +423,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 const int r = (int)warp - W_MMA0;
                 bool ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
                 tc_fence_after();
-                const uint32_t slot = smem_u32(sm.u.c0.ring[r]);
                 for (int i = r; i < npg && ok; i += NSLOT) {
                     const int k = i / NSLOT;
                     if (!wait_bar(&sm.s_empty[r], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
@@ -397,13 +430,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                         break;
                     }
                     for (int t = 0; t < 3 && ok; ++t) {
-                        if (!wait_bar(&sm.full[3 * r + t], (uint32_t)(k & 1), sm, p.dev_err)) {
+                        const int g = 3 * i + t, u = g % NUNIT, ku = g / NUNIT;
+                        if (!wait_count(&sm.unit_taken[u], ku, sm, p.dev_err) ||
+                            !wait_bar(&sm.full[u], (uint32_t)(ku & 1), sm, p.dev_err)) {
                             ok = false;
                             break;
                         }
+                        *reinterpret_cast<volatile int32_t*>(&sm.unit_taken[u]) = ku + 1;
                         tc_fence_after();
-                        issue_score_third(tbase, S_COL + 64u * r, slot + (uint32_t)(t * THIRD), t);
-                        umma_commit(&sm.empty[3 * r + t]);
+                        issue_score_third(tbase, S_COL + 64u * r, smem_u32(sm.u.c0.ring[u]), t);
+                        umma_commit(&sm.empty[u]);
                     }
                     if (ok) umma_commit(&sm.s_full[r]);
                 }
@@ -423,7 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
             const uint32_t bar_out = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)par;
             if (par == 0) {
                 const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
-                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
+                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[3]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.q_ready);
@@ -535,18 +571,29 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 }
                 lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
                 const int st = i % NPBUF;
+                // this warp's P rows, laid out as they land (rows 24 qd .. 24 qd + 23 of the P^T
+                // buffer), once the bulk copy of its previous page has read the staging rows
+                uint8_t* stage = sm.u.c0.pstage[warp];
+                if (lane == 0 && i >= 2) bulk_wait_read<0>();
+                __syncwarp();
+                if (has_head) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(stage + pt_chunk_off(h, j) - qd * PSTAGE) =
+                            make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]);
+                }
+                fence_proxy_async_cta();  // the bulk copy reads the rows through the async proxy
+                __syncwarp();
                 // the PV CTA has finished with its buffer from page i - NPBUF
                 bool freed = false;
                 if (ok) freed = wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
                 const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
                 const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
-                if (freed && has_head) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_async_v4(dst + pt_chunk_off(h, j),
-                                    make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]), bar);
-                    st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
+                if (freed && lane == 0) {
+                    bulk_copy_to_cluster(dst + (uint32_t)(qd * PSTAGE), stage, PSTAGE, bar);
+                    bulk_commit();
                 }
+                if (freed && has_head) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
                 if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
             }
@@ -577,10 +624,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 ml[2] = best_s;
                 ml[3] = __int_as_float(best_t);
             }
-            // the PV CTA's last releases of its P buffers land here before exit
-            if (lane == 0)
+            // this warp's bulk copies have read their staging rows, and the PV CTA's last releases
+            // of its P buffers land here, before exit
+            if (lane == 0) {
+                bulk_wait_read<0>();
                 for (int i = max(0, npg - NPBUF); i < npg && !aborted(sm); ++i)
                     wait_bar(&sm.p_empty[i % NPBUF], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err);
+            }
         }
     } else {
         // ============================ PV CTA ============================
@@ -762,12 +812,12 @@ __global__ void __launch_bounds__(128, 1)
     if (mode == 0) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-            for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[1] + c * QCHUNK, &tmap_q, 0, 0, c, &sm.q_land);
+            for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[3] + c * QCHUNK, &tmap_q, 0, 0, c, &sm.q_land);
             mbar_arrive_expect_tx(&sm.full[0], SLOT0);
             for (int t = 0; t < 3; ++t) tma_load_3d(sm.u.c0.ring[0] + t * THIRD, &tmap_page, 0, 0, 3 * t, &sm.full[0]);
         }
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.q_land, 0, sm, nullptr));
-        if (ok) q_smem_to_tmem(tbase, sm.u.c0.ring[1]);
+        if (ok) q_smem_to_tmem(tbase, sm.u.c0.ring[3]);
         tc_fence_before();
         __syncthreads();
         if (threadIdx.x == 0) {
