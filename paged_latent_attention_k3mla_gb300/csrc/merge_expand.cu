@@ -122,9 +122,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             ns = (ctx + p.split - 1) / p.split;
         }
         float acc[64];
-        // split 0 is loaded before its weight is known (every slot below B has one), so the
-        // partials and the (m, l) records travel together
+        // split 0's partial and its (m, l, best, t) record are loaded before the context length is
+        // known (every slot below B has a split 0), so they arrive in one round trip
+        const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
+        float4 r0 = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(-1));
         if (b < p.B) {
+            r0 = *reinterpret_cast<const float4*>(ml);
             const float4* o0 = reinterpret_cast<const float4*>(p.ws_o + ((size_t)b * p.nsplit * H + h) * LORA);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -135,17 +138,21 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                 acc[4 * k + 3] = v.w;
             }
         }
-        const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-        float m = -INFINITY, l = 0.f, best = -INFINITY;
-        int best_t = -1;
-        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-        for (int i = 0; i < ns; ++i) {
-            const float* mi = ml + (size_t)i * H * 4;
-            l += expf(mi[0] - m) * mi[1];
-            if (mi[2] > best) {  // ascending splits: the lowest t wins ties
-                best = mi[2];
-                best_t = __float_as_int(mi[3]);
+        float m = r0.x, best = r0.z, l;
+        int best_t = __float_as_int(r0.w);
+        for (int i = 1; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
+        if (ns > 0) {
+            l = expf(r0.x - m) * r0.y;
+            for (int i = 1; i < ns; ++i) {
+                const float* mi = ml + (size_t)i * H * 4;
+                l += expf(mi[0] - m) * mi[1];
+                if (mi[2] > best) {  // ascending splits: the lowest t wins ties
+                    best = mi[2];
+                    best_t = __float_as_int(mi[3]);
+                }
             }
+        } else {
+            best_t = -1;
         }
         if (p.argmax && b < p.B && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
         if (ns == 0) {  // empty context (or a padding row of the tile): o_lat = 0
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 64; ++k) acc[k] = 0.f;
         } else {
-            const float w0 = expf(ml[0] - m);
+            const float w0 = expf(r0.x - m);
 #pragma unroll
             for (int k = 0; k < 64; ++k) acc[k] = 0.f + w0 * acc[k];
             for (int i = 1; i < ns; ++i) {  // ascending splits
@@ -170,13 +177,14 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                 }
             }
         }
+        const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
         // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const int c = k >> 1;
             const int u = 4 * (k & 1) + (seg >> 1);
-            const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] / l, acc[4 * k + 1] / l),
-                                       mx_pack_bf16x2(acc[4 * k + 2] / l, acc[4 * k + 3] / l));
+            const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] * rl, acc[4 * k + 1] * rl),
+                                       mx_pack_bf16x2(acc[4 * k + 2] * rl, acc[4 * k + 3] * rl));
             *reinterpret_cast<uint2*>(sb + c * (MX_SLOTS * 128) + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (seg & 1)) =
                 v;
         }
