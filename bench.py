@@ -225,10 +225,19 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     q_all, c_all, r_all = wl.q, wl.new_c, wl.new_rope
     stream = torch.cuda.Stream()
+    side = torch.cuda.Stream()          # the append runs beside the absorption (neither reads the other)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+
+    def append_beside(layer, c, r):
+        ev_fork.record(stream)
+        side.wait_event(ev_fork)
+        k3mla.append_latent(wl.slab, layer, table, pos, c, r, dev_err=err, stream=side)
+        ev_join.record(side)
 
     def layer_call(layer, dec_events=None):
-        k3mla.append_latent(wl.slab, layer, table, pos, c_all[layer], r_all[layer], dev_err=err, stream=stream)
+        append_beside(layer, c_all[layer], r_all[layer])
         k3mla.absorb_q(q_all[layer], wl.w_kv_b[layer], q_abs, stream=stream)
+        stream.wait_event(ev_join)
         if dec_events is not None:
             dec_events[0].record(stream)
         k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer], ws,
@@ -304,9 +313,9 @@ def main():
             c_d.copy_(c_h, non_blocking=True)
             r_d.copy_(r_h, non_blocking=True)
             for layer in range(L):
-                k3mla.append_latent(wl.slab, layer, table, pos, c_d[layer], r_d[layer], dev_err=err,
-                                    stream=stream)
+                append_beside(layer, c_d[layer], r_d[layer])
                 k3mla.absorb_q(q_d[layer], wl.w_kv_b[layer], q_abs, stream=stream)
+                stream.wait_event(ev_join)
                 k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
                                    ws, max_ctx, split, dev_err=err, stream=stream)
             out_h.copy_(out, non_blocking=True)
@@ -348,7 +357,8 @@ def main():
                    f"{WORKLOAD_DESC[args.workload]}, first {L} layer(s) only", "slots": B, "layers": L,
                    "context_tokens": int(wl.ctx_len.max()), "split_tokens": split,
                    "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)",
-                   "timing": "24-layer step as one CUDA graph, CUDA events on the launch stream"},
+                   "timing": "24-layer step as one CUDA graph (each layer's append beside its absorption), "
+                             "CUDA events on the launch stream"},
         "latent_gbs": round(ab["latent"] / (us_per_layer * 1e-6) / 1e9, 1),
         "roofline": {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),

@@ -128,9 +128,12 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         }
         umma_commit(&d_full);
     }
-    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's 64 slots
+    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's 64 slots and
+        // lands bf16 values in a [64 slots][512] tile over the (now idle) W_UK buffer; the CTA then
+        // writes each slot's 1 KB row of q_abs with 16-byte stores
         const int qq = warp & 3, mt = warp >> 2;
         const bool got = ab_wait(&d_full, 0, nullptr);
+        uint16_t* tile = reinterpret_cast<uint16_t*>(sa);
         if (__all_sync(0xFFFFFFFFu, got)) {
             tc_fence_after();
             const int j = 128 * mt + 32 * qq + lane;
@@ -140,12 +143,19 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
                 tmem_ld32(tbase + ((uint32_t)(32 * qq) << 16) + (uint32_t)(AB_SLOTS * mt + 32 * piece), acc);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int b = b0 + 32 * piece + k;
-                    if (b < B)
-                        q_abs[((size_t)b * H + h) * ROW + j] = (uint16_t)(pack2(__uint_as_float(acc[k]), 0.f) & 0xFFFFu);
-                }
+                for (int k = 0; k < 32; ++k)
+                    tile[(32 * piece + k) * LORA + j] = (uint16_t)(pack2(__uint_as_float(acc[k]), 0.f) & 0xFFFFu);
             }
+        }
+        __syncthreads();
+        // thread -> (slot r, 16-byte units 8k + seg of its row)
+        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
+        const int b = b0 + r;
+        if (b < B) {
+            const uint4* srow = reinterpret_cast<const uint4*>(tile + r * LORA);
+            uint4* drow = reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) drow[seg + 8 * k] = srow[seg + 8 * k];
         }
     }
     tc_fence_before();
