@@ -81,7 +81,11 @@ const char* k3mla_last_error(void);
  * q      device [B][96][192] bf16 (q_nope | q_rope)
  * w_kv_b device [24576][512] bf16, one layer
  * q_abs  device [B][96][576] bf16, written
- * B >= 0 (B == 0 launches nothing).  Pointers 16-byte aligned. */
+ * B >= 0 (B == 0 launches nothing).  Pointers 16-byte aligned.
+ * The kernel may start while the kernel before it in `stream` is still running
+ * (programmatic dependent launch); it waits for that kernel before it reads q or
+ * writes q_abs, but it starts loading w_kv_b at once, so w_kv_b must not be
+ * written by the kernel immediately before this call in the stream. */
 int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B,
                    void* stream);
 
@@ -139,7 +143,10 @@ int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
  * max_ctx     upper bound of ctx_len, sets the grid (1 <= max_ctx)
  * dev_err     device int32 or NULL (K3MLA_DEV_* bits are ORed in)
  * Runs as two kernels on `stream`: the split decode, then the merge + W_UV
- * expansion. */
+ * expansion.  Both may start while the kernel before them is still running
+ * (programmatic dependent launch); the split kernel reads nothing before the
+ * kernel before it has completed, and the merge kernel loads only w_kv_b early,
+ * after the split kernel (which does not write it) has started. */
 size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens);
 int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
                        int layer, const int32_t* block_table, int max_pages_per_slot,

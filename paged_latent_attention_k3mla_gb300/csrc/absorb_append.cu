@@ -84,14 +84,16 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
-    griddep_wait();  // the set-up above overlaps the previous kernel in the stream
-    griddep_launch_dependents();
-
     if (threadIdx.x == 0) {  // W_UK[h] = w_kv_b rows h*256 .. h*256 + 127 ([d][j]), one box per 64 j
         mbar_arrive_expect_tx(&w_full, AB_A_BYTES);
 #pragma unroll
         for (int c = 0; c < 8; ++c) tma_load_3d(sa + c * (NOPE * 128), &tmap_w, 0, h * WROWS_PER_HEAD, c, &w_full);
     }
+    // the set-up and the weight load above overlap the previous kernel in the stream (the weights
+    // are not written by it: see k3mla_absorb_q); q and q_abs wait for it
+    griddep_wait();
+    griddep_launch_dependents();
+
     {   // q_nope of the tile -> B operand; q_rope -> q_abs[..][512:576].  thread -> (slot r, segment seg)
         const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
         const int b = b0 + r;

@@ -478,19 +478,20 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 uint32_t sp[32];  // bf16 scores: token 2q in the low half, 2q+1 in the high half
                 if (ok) {
                     tc_fence_after();
-#pragma unroll
-                    for (int piece = 0; piece < 2; ++piece) {
-                        uint32_t rr[32];
-                        tmem_ld32(t_lane + 64u * r + 32u * piece, rr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)  // bf16(dot), then bf16(bf16(dot) * scale)
-                            sp[16 * piece + q] = mul_bf16x2(
-                                pack_bf16x2(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1])), p.scale2);
-                    }
+                    uint32_t ra[32], rb[32];  // the page's 64 f32 scores of this thread's head
+                    tmem_ld32(t_lane + 64u * r, ra);
+                    tmem_ld32(t_lane + 64u * r + 32u, rb);
+                    tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.s_empty[r]);
+                    if (lane == 0) mbar_arrive(&sm.s_empty[r]);  // the S buffer is free for page i + 3
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {  // bf16(dot), then bf16(bf16(dot) * scale)
+                        sp[q] = mul_bf16x2(pack_bf16x2(__uint_as_float(ra[2 * q]), __uint_as_float(ra[2 * q + 1])),
+                                           p.scale2);
+                        sp[16 + q] = mul_bf16x2(
+                            pack_bf16x2(__uint_as_float(rb[2 * q]), __uint_as_float(rb[2 * q + 1])), p.scale2);
+                    }
                 } else {
 #pragma unroll
                     for (int q = 0; q < 32; ++q) sp[q] = 0xFF80FF80u;
