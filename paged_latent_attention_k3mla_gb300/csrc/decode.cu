@@ -133,6 +133,7 @@ static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-
 static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
 static_assert(QBYTES <= (NUNIT - 3) * THIRD, "q_abs staging fits in units 3..");
 static_assert(PCOPY <= PBUF, "P buffer");
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
 
 struct DecodeParams {
     const int32_t* table;
