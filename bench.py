@@ -298,27 +298,59 @@ def main():
 
     tbl_pin = torch.from_numpy(host_table.copy()).pin_memory()
 
-    def e2e_step():
-        for b in range(B):                      # a1: claims on 64-token boundaries (none in steady state)
-            pool.ensure(b, int(wl.ctx_len[b]))
-        t_now = pool.table()
-        if not np.array_equal(t_now, tbl_pin.numpy()):
-            torch.cuda.current_stream().synchronize()
-            tbl_pin.numpy()[:] = t_now
+    # inputs stream in layer by layer on a copy stream while earlier layers compute, and each
+    # layer's output is read back as soon as its decode is done
+    copy_s = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(L)]
+    ev_dec = [torch.cuda.Event() for _ in range(L)]
+    ev_out, ev_start = torch.cuda.Event(), torch.cuda.Event()
+
+    def e2e_device_step():
         with torch.cuda.stream(stream):
             table.copy_(tbl_pin, non_blocking=True)
             pos.copy_(pos_h, non_blocking=True)
             ctx.copy_(ctx_h, non_blocking=True)
-            q_d.copy_(q_h, non_blocking=True)
-            c_d.copy_(c_h, non_blocking=True)
-            r_d.copy_(r_h, non_blocking=True)
+        ev_start.record(stream)                 # everything before (the previous step) is done
+        copy_s.wait_event(ev_start)
+        with torch.cuda.stream(copy_s):
             for layer in range(L):
+                q_d[layer].copy_(q_h[layer], non_blocking=True)
+                c_d[layer].copy_(c_h[layer], non_blocking=True)
+                r_d[layer].copy_(r_h[layer], non_blocking=True)
+                ev_in[layer].record(copy_s)
+        for layer in range(L):
+            stream.wait_event(ev_in[layer])
+            with torch.cuda.stream(stream):
                 append_beside(layer, c_d[layer], r_d[layer])
                 k3mla.absorb_q(q_d[layer], wl.w_kv_b[layer], q_abs, stream=stream)
                 stream.wait_event(ev_join)
                 k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
                                    ws, max_ctx, split, dev_err=err, stream=stream)
-            out_h.copy_(out, non_blocking=True)
+                ev_dec[layer].record(stream)
+            copy_s.wait_event(ev_dec[layer])
+            with torch.cuda.stream(copy_s):
+                out_h[layer].copy_(out[layer], non_blocking=True)
+        ev_out.record(copy_s)
+        stream.wait_event(ev_out)
+
+    # the device part of a step (copies in, 24 layer-calls, copies out) as one CUDA graph; the host
+    # part (page claims, table refresh) runs before every replay
+    with torch.cuda.stream(stream):
+        e2e_device_step()
+    torch.cuda.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_device_step()
+
+    def e2e_step():
+        for b in range(B):                      # a1: claims on 64-token boundaries (none in steady state)
+            pool.ensure(b, int(wl.ctx_len[b]))
+        t_now = pool.table()
+        if not np.array_equal(t_now, tbl_pin.numpy()):
+            stream.synchronize()
+            tbl_pin.numpy()[:] = t_now
+        with torch.cuda.stream(stream):
+            e2e_graph.replay()
 
     for _ in range(args.warmup):
         e2e_step()
