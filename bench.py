@@ -18,7 +18,8 @@ JSON line fields beyond the usual ones:
   layer_roofline   the same for the whole layer-call (append + absorb + decode)
   e2e              the same metric through the C ABI with host buffers: pinned
                    H2D of the step's q / new rows / tables and D2H of the outputs
-                   inside the timed region, eager launches
+                   inside the timed region (host page claims, then the step's
+                   copies and kernels replayed as one CUDA graph)
   cpu_baseline     the CPU oracle on a bounded sample of the workload
 """
 from __future__ import annotations
@@ -225,19 +226,14 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     q_all, c_all, r_all = wl.q, wl.new_c, wl.new_rope
     stream = torch.cuda.Stream()
-    side = torch.cuda.Stream()          # the append runs beside the absorption (neither reads the other)
-    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
 
-    def append_beside(layer, c, r):
-        ev_fork.record(stream)
-        side.wait_event(ev_fork)
-        k3mla.append_latent(wl.slab, layer, table, pos, c, r, dev_err=err, stream=side)
-        ev_join.record(side)
+    def absorb_append(layer, q, c, r):
+        # a2 + a3 in one launch: the append rides on the absorption's grid (neither reads the other)
+        k3mla.absorb_q_append(q, wl.w_kv_b[layer], q_abs, wl.slab, layer, table, pos, c, r, dev_err=err,
+                              stream=stream)
 
     def layer_call(layer, dec_events=None):
-        append_beside(layer, c_all[layer], r_all[layer])
-        k3mla.absorb_q(q_all[layer], wl.w_kv_b[layer], q_abs, stream=stream)
-        stream.wait_event(ev_join)
+        absorb_append(layer, q_all[layer], c_all[layer], r_all[layer])
         if dec_events is not None:
             dec_events[0].record(stream)
         k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer], ws,
@@ -321,9 +317,7 @@ def main():
         for layer in range(L):
             stream.wait_event(ev_in[layer])
             with torch.cuda.stream(stream):
-                append_beside(layer, c_d[layer], r_d[layer])
-                k3mla.absorb_q(q_d[layer], wl.w_kv_b[layer], q_abs, stream=stream)
-                stream.wait_event(ev_join)
+                absorb_append(layer, q_d[layer], c_d[layer], r_d[layer])
                 k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
                                    ws, max_ctx, split, dev_err=err, stream=stream)
                 ev_dec[layer].record(stream)
@@ -389,7 +383,7 @@ def main():
                    f"{WORKLOAD_DESC[args.workload]}, first {L} layer(s) only", "slots": B, "layers": L,
                    "context_tokens": int(wl.ctx_len.max()), "split_tokens": split,
                    "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)",
-                   "timing": "24-layer step as one CUDA graph (each layer's append beside its absorption), "
+                   "timing": "24-layer step as one CUDA graph (each layer's append carried by its absorption's launch), "
                              "CUDA events on the launch stream"},
         "latent_gbs": round(ab["latent"] / (us_per_layer * 1e-6) / 1e9, 1),
         "roofline": {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
@@ -402,7 +396,7 @@ def main():
                            "tensor_peak_tflops": tflops},
         "e2e": {"value": round(e2e_ms * 1e3 / L, 3), "unit": "us/layer-call", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * L * 4,
+        "gpu_launches": args.steps * L * 3,   # absorb+append, split decode, merge/expand per layer
         "clocks": clk.summary(),
         "out_sha256_16": digest,
         "cpu_baseline": cpu,

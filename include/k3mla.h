@@ -110,6 +110,24 @@ int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
                         const uint16_t* k_rope, int64_t r_stride, int B,
                         int32_t* dev_err, void* stream);
 
+/* ---- q absorption and append in one launch ------------------------------------
+ * The two calls above, k3mla_absorb_q(q, w_kv_b, q_abs, B) and
+ * k3mla_append_latent(slab, ..., B, dev_err), as one kernel launch: every
+ * argument means what it means there, and so do the results, the alignment
+ * rules and the error codes.  The page's decode step runs the append and the
+ * absorption of a layer back to back and neither reads what the other writes;
+ * carrying both in one grid takes one launch (and its latency) off the chain
+ * that ends in the decode.  The append waits for the kernel before it in
+ * `stream` (like the absorption's q); w_kv_b is read at once, as in
+ * k3mla_absorb_q.  (The page has no single call for the pair: this one is a
+ * launch-level fusion of its two steps.) */
+int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs,
+                          uint16_t* slab, int n_pages, int n_layers, int layer,
+                          const int32_t* block_table, int max_pages_per_slot,
+                          const int32_t* pos, const uint16_t* c_kv, int64_t c_stride,
+                          const uint16_t* k_rope, int64_t r_stride, int B,
+                          int32_t* dev_err, void* stream);
+
 /* ---- paged absorbed decode ---------------------------------------------------
  * For each slot b < B and head h, with n = ctx_len[b] tokens (logical token t
  * lives in page block_table[b][t / 64], row t % 64; a -1 entry is an all-zero

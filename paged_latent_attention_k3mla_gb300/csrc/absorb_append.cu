@@ -55,10 +55,55 @@ __device__ __noinline__ bool ab_wait(uint64_t* bar, uint32_t parity, int32_t* de
     return true;
 }
 
+// The append of one layer-call, carried by the absorption's launch (k3mla_absorb_q_append); B == 0
+// when there is none.
+struct AppendJob {
+    uint16_t* slab;
+    const int32_t* table;
+    const int32_t* pos;
+    const uint16_t* c_kv;
+    const uint16_t* k_rope;
+    int32_t* dev_err;
+    int64_t c_stride, r_stride;
+    int n_pages, n_layers, layer, max_pages, B;
+};
+constexpr int AP_THREADS = 96;  // a row is 288 32-bit words: three per thread
+static_assert(H >= AB_SLOTS, "the absorption grid has a CTA for every appended slot");
+
+// One slot's row: the slab row index (or -1 when the slot writes nothing) and this thread's three
+// words of it (words w = at, at + 96, at + 192; latent below 256, rope from 256).
+__device__ __forceinline__ int64_t append_fetch(const AppendJob& ap, int b, int at, uint32_t (&v)[3])
+{
+    const uint32_t* src_c = reinterpret_cast<const uint32_t*>(ap.c_kv + (size_t)b * ap.c_stride);
+    const uint32_t* src_r = reinterpret_cast<const uint32_t*>(ap.k_rope + (size_t)b * ap.r_stride);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int w = at + AP_THREADS * k;
+        v[k] = (w < LORA / 2) ? src_c[w] : src_r[w - LORA / 2];
+    }
+    const int p = ap.pos[b];
+    if (p < 0) return -1;
+    const int lp = p / PAGE;
+    const int32_t id = (lp < ap.max_pages) ? ap.table[(size_t)b * ap.max_pages + lp] : -1;
+    if (id < 0 || id >= ap.n_pages) {
+        if (at == 0 && ap.dev_err) atomicOr(ap.dev_err, (int)K3MLA_DEV_UNMAPPED);
+        return -1;
+    }
+    return ((int64_t)id * ap.n_layers + ap.layer) * PAGE + p % PAGE;
+}
+
+__device__ __forceinline__ void append_store(const AppendJob& ap, int64_t row, int at, const uint32_t (&v)[3])
+{
+    if (row < 0) return;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(ap.slab + (size_t)row * ROW);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) dst[at + AP_THREADS * k] = v[k];
+}
+
 // grid (96 heads, ceil(B / 64) slot tiles); block AB_THREADS; thread 0 also issues the loads and MMAs.
 __global__ void __launch_bounds__(AB_THREADS, 1)
     k3mla_absorb_kernel(const __grid_constant__ CUtensorMap tmap_w, const uint16_t* __restrict__ q,
-                        uint16_t* __restrict__ q_abs, int B)
+                        uint16_t* __restrict__ q_abs, int B, const AppendJob ap)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -87,12 +132,24 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     if (threadIdx.x == 0) {  // W_UK[h] = w_kv_b rows h*256 .. h*256 + 127 ([d][j]), one box per 64 j
         mbar_arrive_expect_tx(&w_full, AB_A_BYTES);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) tma_load_3d(sa + c * (NOPE * 128), &tmap_w, 0, h * WROWS_PER_HEAD, c, &w_full);
+        for (int c = 0; c < 8; ++c)
+            tma_load_3d_hint(sa + c * (NOPE * 128), &tmap_w, 0, h * WROWS_PER_HEAD, c, &w_full,
+                             policy_evict_first());  // read once per layer
     }
     // the set-up and the weight load above overlap the previous kernel in the stream (the weights
-    // are not written by it: see k3mla_absorb_q); q and q_abs wait for it
+    // are not written by it: see k3mla_absorb_q); q, q_abs and the append's buffers wait for it
     griddep_wait();
     griddep_launch_dependents();
+
+    // The append (when this launch carries one): CTA `lin` writes the row of slot lin (the grid has
+    // 96 ceil(B / 64) >= B CTAs); its last AP_THREADS threads fetch the row here, beside the q_nope
+    // loads, and store it once their share of the B operand is written.
+    const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    const int at = (int)threadIdx.x - (AB_THREADS - AP_THREADS);
+    const bool app_thread = lin < ap.B && at >= 0;
+    uint32_t av[3] = {0u, 0u, 0u};
+    int64_t arow = -1;
+    if (app_thread) arow = append_fetch(ap, lin, at, av);
 
     {   // q_nope of the tile -> B operand; q_rope -> q_abs[..][512:576].  thread -> (slot r, segment seg)
         const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
@@ -110,6 +167,7 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
         mbar_arrive(&b_ready);
     }
+    if (app_thread) append_store(ap, arow, at, av);
     if (threadIdx.x == 0) {
         const bool ok = ab_wait(&w_full, 0, nullptr) && ab_wait(&b_ready, 0, nullptr);
         if (ok) {
@@ -198,17 +256,39 @@ __global__ void __launch_bounds__(96) k3mla_append_kernel(uint16_t* __restrict__
 
 using namespace k3;
 
-extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B, void* stream)
+static int check_absorb(const char* who, const uint16_t* q, const uint16_t* w_kv_b, const uint16_t* q_abs, int B)
 {
     if (B < 0) {
-        set_error("k3mla_absorb_q: B < 0");
+        set_error("%s: B < 0", who);
         return K3MLA_E_INVALID;
     }
-    if (B == 0) return K3MLA_OK;
-    if (!q || !w_kv_b || !q_abs || !aligned(q, 16) || !aligned(w_kv_b, 16) || !aligned(q_abs, 16)) {
-        set_error("k3mla_absorb_q: null or misaligned pointer");
+    if (B > 0 && (!q || !w_kv_b || !q_abs || !aligned(q, 16) || !aligned(w_kv_b, 16) || !aligned(q_abs, 16))) {
+        set_error("%s: null or misaligned pointer", who);
         return K3MLA_E_INVALID;
     }
+    return K3MLA_OK;
+}
+
+static int check_append(const char* who, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                        const int32_t* block_table, int max_pages_per_slot, const int32_t* pos,
+                        const uint16_t* c_kv, int64_t c_stride, const uint16_t* k_rope, int64_t r_stride, int B)
+{
+    if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
+        c_stride < LORA || r_stride < ROPE || (c_stride & 1) || (r_stride & 1)) {
+        set_error("%s: invalid sizes or strides", who);
+        return K3MLA_E_INVALID;
+    }
+    if (B > 0 && (!slab || !block_table || !pos || !c_kv || !k_rope || !aligned(slab, 4) || !aligned(c_kv, 4) ||
+                  !aligned(k_rope, 4))) {
+        set_error("%s: null or misaligned pointer", who);
+        return K3MLA_E_INVALID;
+    }
+    return K3MLA_OK;
+}
+
+static int launch_absorb(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B, const AppendJob& ap,
+                         void* stream)
+{
     if (!device_ok()) return K3MLA_E_DEVICE;
     static bool attr_set[64] = {};
     const int smem = AB_A_BYTES + AB_B_BYTES + 1024;
@@ -223,7 +303,44 @@ extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_
     const int rc = make_tmap_slab_3d(&tmap_w, w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, NOPE, 1);
     if (rc) return rc;
     return launch_pdl(k3mla_absorb_kernel, dim3(H, (B + AB_SLOTS - 1) / AB_SLOTS), dim3(AB_THREADS), smem,
-                      reinterpret_cast<cudaStream_t>(stream), "k3mla_absorb_kernel", tmap_w, q, q_abs, B);
+                      reinterpret_cast<cudaStream_t>(stream), "k3mla_absorb_kernel", tmap_w, q, q_abs, B,
+                      ap);
+}
+
+extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B, void* stream)
+{
+    const int rc = check_absorb("k3mla_absorb_q", q, w_kv_b, q_abs, B);
+    if (rc || B == 0) return rc;
+    AppendJob none{};
+    return launch_absorb(q, w_kv_b, q_abs, B, none, stream);
+}
+
+extern "C" int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, uint16_t* slab,
+                                     int n_pages, int n_layers, int layer, const int32_t* block_table,
+                                     int max_pages_per_slot, const int32_t* pos, const uint16_t* c_kv,
+                                     int64_t c_stride, const uint16_t* k_rope, int64_t r_stride, int B,
+                                     int32_t* dev_err, void* stream)
+{
+    int rc = check_absorb("k3mla_absorb_q_append", q, w_kv_b, q_abs, B);
+    if (!rc)
+        rc = check_append("k3mla_absorb_q_append", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot,
+                          pos, c_kv, c_stride, k_rope, r_stride, B);
+    if (rc || B == 0) return rc;
+    AppendJob ap;
+    ap.slab = slab;
+    ap.table = block_table;
+    ap.pos = pos;
+    ap.c_kv = c_kv;
+    ap.k_rope = k_rope;
+    ap.dev_err = dev_err;
+    ap.c_stride = c_stride;
+    ap.r_stride = r_stride;
+    ap.n_pages = n_pages;
+    ap.n_layers = n_layers;
+    ap.layer = layer;
+    ap.max_pages = max_pages_per_slot;
+    ap.B = B;
+    return launch_absorb(q, w_kv_b, q_abs, B, ap, stream);
 }
 
 extern "C" int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
@@ -231,17 +348,9 @@ extern "C" int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, in
                                    const uint16_t* c_kv, int64_t c_stride, const uint16_t* k_rope,
                                    int64_t r_stride, int B, int32_t* dev_err, void* stream)
 {
-    if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
-        c_stride < LORA || r_stride < ROPE || (c_stride & 1) || (r_stride & 1)) {
-        set_error("k3mla_append_latent: invalid sizes or strides");
-        return K3MLA_E_INVALID;
-    }
-    if (B == 0) return K3MLA_OK;
-    if (!slab || !block_table || !pos || !c_kv || !k_rope || !aligned(slab, 4) || !aligned(c_kv, 4) ||
-        !aligned(k_rope, 4)) {
-        set_error("k3mla_append_latent: null or misaligned pointer");
-        return K3MLA_E_INVALID;
-    }
+    const int rc = check_append("k3mla_append_latent", slab, n_pages, n_layers, layer, block_table,
+                                max_pages_per_slot, pos, c_kv, c_stride, k_rope, r_stride, B);
+    if (rc || B == 0) return rc;
     if (!device_ok()) return K3MLA_E_DEVICE;
     return launch_pdl(k3mla_append_kernel, dim3(B), dim3(96), 0, reinterpret_cast<cudaStream_t>(stream),
                       "k3mla_append_kernel", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, pos,

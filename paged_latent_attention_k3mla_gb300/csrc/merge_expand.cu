@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         mbar_arrive_expect_tx(&w_full, MX_A_BYTES);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            tma_load_3d(sa + c * (VH * 128), &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, c, &w_full);
+            tma_load_3d_hint(sa + c * (VH * 128), &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, c, &w_full,
+                             policy_evict_first());  // read once per layer
     }
     // W_UV is a layer weight no kernel of this library writes, so its load above overlaps the split
     // kernel; the split partials, the context lengths and the outputs wait for it

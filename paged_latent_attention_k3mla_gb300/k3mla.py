@@ -25,6 +25,7 @@ EXPORTS = (
     "k3mla_paged_decode", "k3mla_default_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
+    "k3mla_absorb_q_append",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -65,6 +66,7 @@ def load(build_if_needed: bool = True):
             "k3mla_pool_destroy": ([P], None),
             "k3mla_diag_umma": ([I, P, P, P, P], I),
             "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
+            "k3mla_absorb_q_append": ([P, P, P, P, I, I, I, P, I, P, P, I64, P, I64, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -129,6 +131,31 @@ def append_latent(slab: torch.Tensor, layer: int, block_table: torch.Tensor, pos
         _dev(pos, torch.int32, (B,), "pos"), ctypes.c_void_p(c_kv.data_ptr()), c_kv.stride(0),
         ctypes.c_void_p(k_rope.data_ptr()), k_rope.stride(0), B,
         _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_append_latent")
+
+
+def _rows(t: torch.Tensor, B: int, name: str):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1 or t.shape[0] != B:
+        raise K3mlaError(f"{name} must be a CUDA bf16 [B, n] tensor with unit inner stride")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def absorb_q_append(q: torch.Tensor, w_kv_b: torch.Tensor, q_abs: torch.Tensor, slab: torch.Tensor, layer: int,
+                    block_table: torch.Tensor, pos: torch.Tensor, c_kv: torch.Tensor, k_rope: torch.Tensor,
+                    dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """absorb_q(q, w_kv_b, q_abs) and append_latent(slab, layer, block_table, pos, c_kv, k_rope)
+    in one launch (same arguments, same results)."""
+    B = q.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    lib = load()
+    _check(lib.k3mla_absorb_q_append(
+        _dev(q, torch.bfloat16, (B, H, NOPE + ROPE), "q"),
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"),
+        _dev(q_abs, torch.bfloat16, (B, H, ROW), "q_abs"),
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(pos, torch.int32, (B,), "pos"), _rows(c_kv, B, "c_kv"), c_kv.stride(0),
+        _rows(k_rope, B, "k_rope"), k_rope.stride(0), B,
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_absorb_q_append")
 
 
 def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:

@@ -68,3 +68,35 @@ def test_append_indexes_past_2_31_elements(gpu_lib):
     assert int(torch.count_nonzero(slab)) == int(torch.count_nonzero(c) + torch.count_nonzero(r))
     del slab
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", [6, 67])
+def test_absorb_q_append_is_both_calls_in_one(gpu_lib, B):
+    """The fused launch: q_abs bitwise equal to k3mla_absorb_q's (same kernel) and within the
+    absorption bar of the oracle; the slab bitwise equal to the oracle's append, with a slot that
+    writes nothing (pos -1) and one whose page is unmapped (skipped and flagged)."""
+    ctx = [(7 * i * i + 3 * i) % 300 + 1 for i in range(B)]
+    wl = synth.make_custom(ctx, n_layers=2, seed=300 + B, device="cuda")
+    tbl = wl.block_table.copy()
+    pos = (wl.ctx_len - 1).astype(np.int32)
+    pos[1] = -1
+    tbl[2, pos[2] // 64] = -1
+    slab_ref = synth.bf16_bits(wl.slab).copy()
+    c, r = wl.new_c[1], wl.new_rope[1]
+    assert oracle.append(slab_ref, 1, tbl, pos, synth.bf16_bits(c), synth.bf16_bits(r)) == 1
+    q, w = wl.q[1], wl.w_kv_b[1]
+    q_abs = torch.full((B, 96, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q_abs_sep = torch.full_like(q_abs, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3mla.absorb_q_append(q, w, q_abs, wl.slab, 1, torch.from_numpy(tbl).cuda(), torch.from_numpy(pos).cuda(),
+                          c, r, dev_err=err)
+    k3mla.absorb_q(q, w, q_abs_sep)
+    torch.cuda.synchronize()
+    assert np.array_equal(synth.bf16_bits(wl.slab), slab_ref)
+    assert err.item() == k3mla.DEV_UNMAPPED
+    got = synth.bf16_bits(q_abs)
+    assert np.array_equal(got, synth.bf16_bits(q_abs_sep))
+    ref = oracle.absorb(synth.bf16_bits(q), synth.bf16_bits(w))
+    err_ulp = row_ulp_error(bits_to_f32(got[:, :, :512]), bits_to_f32(ref[:, :, :512]))
+    assert err_ulp.max() <= ULP_TOL
+    assert np.array_equal(got[:, :, 512:], ref[:, :, 512:])

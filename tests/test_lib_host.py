@@ -89,6 +89,15 @@ def test_invalid_arguments_return_status_without_launching():
     assert lib.k3mla_paged_decode(*args) == -1                 # null pointers
     assert b"null or misaligned" in lib.k3mla_last_error()
     assert lib.k3mla_absorb_q(null, null, null, 0, null) == 0   # B == 0: nothing to do
+    # the fused absorption + append checks both halves' arguments
+    fused = [null, null, null, null, 4, 2, 0, null, 1, null, null, 512, null, 64, 1, null, null]
+    assert lib.k3mla_absorb_q_append(*fused) == -1              # null pointers
+    assert b"k3mla_absorb_q_append: null or misaligned" in lib.k3mla_last_error()
+    fused[14] = 0
+    assert lib.k3mla_absorb_q_append(*fused) == 0               # B == 0: nothing to do
+    fused[6] = 2                                                # layer == n_layers
+    assert lib.k3mla_absorb_q_append(*fused) == -1
+    assert b"invalid sizes or strides" in lib.k3mla_last_error()
     assert lib.k3mla_diag_umma(5, null, null, null, null) == -1
 
 
