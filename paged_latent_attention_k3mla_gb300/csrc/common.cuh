@@ -71,6 +71,7 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 struct MergeParams {
     const float* ws_o;     // [B][nsplit][96][512] f32 partial O
     const float* ws_ml;    // [B][nsplit][96][4]: m_ref, l, best score, best t (int bits)
+    const uint16_t* ws_olat;  // nsplit == 1: final o_lat [96][B][512] bf16 (ws_o unused); else null
     const int32_t* ctx_len;
     const uint16_t* w_kv_b;
     uint16_t* out;         // [B][96][128] bf16

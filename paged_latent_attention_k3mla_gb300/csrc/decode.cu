@@ -115,6 +115,9 @@ struct __align__(1024) Smem {
     uint64_t q_land, q_ready;
     uint64_t p_full[NPBUF], p_empty[NPBUF];
     uint64_t o_done, epi_req, epi_done;
+    uint64_t l_full;         // PV CTA: 1 / l of every head has arrived (single-split launches)
+    int32_t fin_ready;       // PV CTA: epilogue warps that saw O complete (4: write it out)
+    float rl[H];             // ... 1 / l by head, stored by the score CTA
     float xm[2][4][32];      // score CTA: reference max after a page, by page parity / quarter / lane
     float xa[2][4][32];      // ... and that page's rescale factor (1 when it kept the reference)
     float fin_l[4][32];      // ... the odd-page warp's sum of exp, best score and its token
@@ -133,6 +136,8 @@ static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-
 static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
 static_assert(QBYTES <= (NUNIT - 3) * THIRD, "q_abs staging fits in units 3..");
 static_assert(PCOPY <= PBUF, "P buffer");
+static_assert(H * LORA * 4 <= NHSLOT * SLOT1 + NPBUF * PBUF,
+              "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
 
 struct DecodeParams {
@@ -140,6 +145,7 @@ struct DecodeParams {
     const int32_t* ctx_len;
     float* ws_o;    // [B][nsplit][96][512]
     float* ws_ml;   // [B][nsplit][96][4]: m_ref, l, best score, best t (int bits)
+    uint16_t* ws_olat;  // nsplit == 1: o_lat [96][B][512] bf16, final (ws_o is then unused); else null
     int32_t* dev_err;
     int max_pages, n_pages, n_layers, layer;
     int B, max_ctx, split, nsplit;
@@ -234,6 +240,14 @@ __device__ __forceinline__ int32_t page_row(const DecodeParams& p, int b, int lp
     return (id * p.n_layers + p.layer) * PAGE;
 }
 
+// An empty context's final o_lat (single-split launches): zero rows [h][b][0:512] for every head.
+__device__ __noinline__ void zero_olat(uint16_t* olat, int B, int b)
+{
+    for (int i = (int)threadIdx.x; i < H * LORA / 8; i += (int)blockDim.x)
+        *reinterpret_cast<uint4*>(olat + ((size_t)(i / (LORA / 8)) * B + b) * LORA + 8 * (i % (LORA / 8))) =
+            make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ---- building blocks shared with the diagnostic kernel -----------------------------
 
 // TMEM lane of head h: 24 heads per 32-lane quarter.
@@ -320,6 +334,56 @@ __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_add
 // Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
 __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_t)(h * 128 + ((j ^ (h & 7)) << 4)); }
 
+// PV CTA, after its roles: O^T [512 dims x 96 heads] f32 lands in the (now idle) page ring and P
+// buffers as [96 heads][512 dims] f32 -- twelve warps, each one TMEM lane quarter x one 32-head
+// piece -- and every thread then copies rows out with 16-byte stores: the f32 partial as it stands,
+// or (single split) o_lat = bf16(O * (1 / l)).  (Four warps alone, straight from the TMEM layout,
+// take several microseconds.)  Kept out of line so that it does not weigh on the register
+// allocation of the pipeline.
+__device__ __noinline__ void pv_write_out(Smem& sm, float* ws_o, uint16_t* ws_olat, int B, int nsplit, uint32_t tbase,
+                                          int b, int s)
+{
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    float* tile = reinterpret_cast<float*>(sm.u.c1.ring[0]);
+    if (warp < 12) {
+        tc_fence_after();
+        const uint32_t q = warp & 3u, pc = warp >> 2;
+        const uint32_t ta = tbase + ((32u * q) << 16) + 32u * pc;
+        float* trow = tile + (32 * pc) * LORA + 32 * q + lane;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            uint32_t rr[32];
+            tmem_ld32(ta + 96u * j, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) trow[c * LORA + 128 * j] = __uint_as_float(rr[c]);
+        }
+    }
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(tile);
+    if (ws_olat) {  // thread -> 16-byte chunk ch of rows h0, h0 + 7, ...
+        constexpr int RSTEP = THREADS / (LORA / 8);
+        static_assert(THREADS % (LORA / 8) == 0, "whole rows per pass");
+        const int ch = (int)threadIdx.x % (LORA / 8), h0 = (int)threadIdx.x / (LORA / 8);
+        uint4* dst = reinterpret_cast<uint4*>(ws_olat + ((size_t)h0 * B + b) * LORA) + ch;
+        const size_t dstep = (size_t)RSTEP * B * (LORA / 8);  // RSTEP heads on, in uint4
+        const float4* s4 = src + h0 * (LORA / 4) + 2 * ch;
+#pragma unroll 1
+        for (int hh = h0; hh < H; hh += RSTEP) {
+            const float r = sm.rl[hh];
+            const float4 x0 = s4[0], x1 = s4[1];
+            *dst = make_uint4(pack_bf16x2(x0.x * r, x0.y * r), pack_bf16x2(x0.z * r, x0.w * r),
+                              pack_bf16x2(x1.x * r, x1.y * r), pack_bf16x2(x1.z * r, x1.w * r));
+            dst += dstep;
+            s4 += RSTEP * (LORA / 4);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(ws_o + (((size_t)b * nsplit + s) * H) * LORA);
+#pragma unroll 4
+        for (int k = (int)threadIdx.x; k < H * (LORA / 4); k += THREADS) dst[k] = src[k];
+    }
+}
+
 // ---- the split decode kernel ---------------------------------------------------------
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
@@ -339,7 +403,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     const int ctx = ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages, p.dev_err,
                                   rank == 0 && threadIdx.x == 0 && s == 0);
     const int start = s * p.split;
-    if (start >= ctx) return;  // empty split: both CTAs leave, nothing was shared
+    if (start >= ctx) {  // empty split: both CTAs leave, nothing was shared
+        if (p.ws_olat && rank == 1) zero_olat(p.ws_olat, p.B, b);  // its only split is this one
+        return;
+    }
     const int ntok = min(ctx, start + p.split) - start;
     const int npg = (ntok + PAGE - 1) / PAGE;
     const int n_lp = (ctx + PAGE - 1) / PAGE;
@@ -364,13 +431,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.epi_req, 1);
         mbar_init(&sm.epi_done, 4);
+        mbar_init(&sm.l_full, 1);
         sm.abort_flag = 0;
+        sm.fin_ready = 0;
         for (int i = 0; i < NUNIT; ++i) {
             sm.unit_loaded[i] = 0;
             sm.unit_taken[i] = 0;
         }
-        if (rank == 1)  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
+        if (rank == 1) {  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
             for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
+            if (p.ws_olat) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
+        }
         fence_mbarrier_init_cluster();
         if (rank == 0) tma_prefetch_desc(&tmap_q);
     }
@@ -621,10 +692,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                     best_t = t1;
                 }
                 float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
+                const float ltot = lsum + sm.fin_l[qd][l];
                 ml[0] = m_ref;
-                ml[1] = lsum + sm.fin_l[qd][l];
+                ml[1] = ltot;
                 ml[2] = best_s;
                 ml[3] = __int_as_float(best_t);
+                // a single split is final: the PV CTA lands o_lat = bf16(O * (1 / l)) itself
+                if (p.ws_olat)
+                    st_async_b32(mapa(smem_u32(&sm.rl[h]), 1), __float_as_uint(1.f / ltot),
+                                 mapa(smem_u32(&sm.l_full), 1));
             }
             // this warp's bulk copies have read their staging rows, and the PV CTA's last releases
             // of its P buffers land here, before exit
@@ -752,23 +828,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                     }
                     fence_proxy_async_cta();
                 }
-                if (cmd & 4u) {  // final: write the split's f32 partial O
-                    const bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
-                    if (!__all_sync(0xFFFFFFFFu, got2)) break;
-                    ++od;
-                    tc_fence_after();
-                    float* o = p.ws_o + (((size_t)b * p.nsplit + s) * H) * LORA;
-                    for (int j = 0; j < 4; ++j) {
-                        const int d = 128 * j + 32 * (int)warp + (int)lane;
-                        for (int piece = 0; piece < 3; ++piece) {
-                            uint32_t rr[32];
-                            tmem_ld32(t_lane + 96u * j + 32u * piece, rr);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                o[(size_t)(32 * piece + c) * LORA + d] = __uint_as_float(rr[c]);
-                        }
-                    }
+                if (cmd & 4u) {  // final: O is complete (and, single split, 1 / l has arrived)
+                    bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
+                    if (p.ws_olat) got2 = got2 && wait_bar(&sm.l_full, 0, sm, p.dev_err, true);
+                    if (__all_sync(0xFFFFFFFFu, got2) && lane == 0) atomicAdd(&sm.fin_ready, 1);
                     break;
                 }
                 tc_fence_before();
@@ -776,6 +839,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 if (lane == 0) mbar_arrive(&sm.epi_done);
             }
         }
+        __syncthreads();  // every role is done: the final write-out takes all warps
+        if (*reinterpret_cast<volatile int32_t*>(&sm.fin_ready) == 4) pv_write_out(sm, p.ws_o, p.ws_olat, p.B, p.nsplit, tbase, b, s);
     }
 
     __syncwarp();
@@ -985,6 +1050,10 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     float* ws_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + o_bytes);
     dp.ws_o = ws_o;
     dp.ws_ml = ws_ml;
+    // one split per slot: the split kernel writes final bf16 o_lat ([96][B][512], in the space of
+    // the f32 partials) and the merge only expands it
+    uint16_t* ws_olat = ns == 1 ? reinterpret_cast<uint16_t*>(workspace) : nullptr;
+    dp.ws_olat = ws_olat;
     dp.dev_err = dev_err;
     dp.max_pages = max_pages_per_slot;
     dp.n_pages = n_pages;
@@ -1003,6 +1072,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     MergeParams mp;
     mp.ws_o = ws_o;
     mp.ws_ml = ws_ml;
+    mp.ws_olat = ws_olat;
     mp.ctx_len = ctx_len;
     mp.w_kv_b = w_kv_b;
     mp.out = out;

@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -71,14 +72,28 @@ __device__ __noinline__ bool mx_wait(uint64_t* bar, uint32_t parity, int32_t* de
     return true;
 }
 
+// OUT_h^T [128 v x 64 slots] = W_UV[h] . O_lat_h^T: 32 MMAs (K = 512) into one accumulator.
+__device__ __forceinline__ void issue_expand(uint32_t tbase, const uint8_t* sa, const uint8_t* sb)
+{
+    const uint64_t ad = make_sdesc(smem_u32(sa), 16, 1024);
+    const uint64_t bd = make_sdesc(smem_u32(sb), 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < LORA / 16; ++ks) {
+        const int c = ks >> 2, kk = ks & 3;
+        umma_ss(tbase, ad + (uint64_t)((c * (VH * 128) + kk * 32) >> 4),
+                bd + (uint64_t)((c * (MX_SLOTS * 128) + kk * 32) >> 4), MX_IDESC, ks > 0 ? 1u : 0u);
+    }
+}
+
 // grid (96 heads, ceil(B / 64) slot tiles); block MX_THREADS.
 __global__ void __launch_bounds__(MX_THREADS, 1)
-    k3mla_merge_expand_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeParams p)
+    k3mla_merge_expand_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_o,
+                              const MergeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sb = sa + MX_A_BYTES;
-    __shared__ uint64_t w_full, b_ready, d_full;
+    __shared__ uint64_t w_full, b_ready, d_full, o_full;
     __shared__ uint32_t tmem_slot;
     const int h = blockIdx.x;
     const int b0 = blockIdx.y * MX_SLOTS;
@@ -88,8 +103,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         mbar_init(&w_full, 1);
         mbar_init(&b_ready, 32 * MX_MERGE_WARPS);
         mbar_init(&d_full, 1);
+        mbar_init(&o_full, 1);
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmap_w);
+        if (p.ws_olat) tma_prefetch_desc(&tmap_o);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, MX_SLOTS);
@@ -112,7 +129,33 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // kernel; the split partials, the context lengths and the outputs wait for it
     griddep_wait();
     griddep_launch_dependents();
-    {
+    if (p.ws_olat) {
+        // ---- one split per slot: the split kernel wrote final bf16 o_lat ([96][B][512]); rows
+        // h B + b0 .. h B + b0 + 63 are the B operand as they stand (rows past the batch belong to
+        // the next head or lie past the array, read as zeros: either way their columns are not stored)
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&o_full, MX_B_BYTES);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                tma_load_3d(sb + c * (MX_SLOTS * 128), &tmap_o, 0, h * p.B + b0, c, &o_full);
+        }
+        if (p.argmax && threadIdx.x < MX_SLOTS && b0 + (int)threadIdx.x < p.B) {
+            const int b = b0 + (int)threadIdx.x;
+            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
+            p.argmax[(size_t)b * H + h] = ctx > 0 ? __float_as_int(p.ws_ml[((size_t)b * H + h) * 4 + 3]) : -1;
+        }
+        if (threadIdx.x == 0) {
+            const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&o_full, 0, p.dev_err);
+            if (ok) {
+                tc_fence_after();
+                issue_expand(tbase, sa, sb);
+            } else {
+                const uint64_t t0 = globaltimer();  // let in-flight TMA copies land before the CTA exits
+                while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+            }
+            umma_commit(&d_full);
+        }
+    } else {
         // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are 128
         // float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
         const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
@@ -195,14 +238,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&b_ready, 0, p.dev_err);
             if (ok) {
                 tc_fence_after();
-                const uint64_t ad = make_sdesc(smem_u32(sa), 16, 1024);
-                const uint64_t bd = make_sdesc(smem_u32(sb), 16, 1024);
-#pragma unroll
-                for (int ks = 0; ks < LORA / 16; ++ks) {
-                    const int c = ks >> 2, kk = ks & 3;
-                    umma_ss(tbase, ad + (uint64_t)((c * (VH * 128) + kk * 32) >> 4),
-                            bd + (uint64_t)((c * (MX_SLOTS * 128) + kk * 32) >> 4), MX_IDESC, ks > 0 ? 1u : 0u);
-                }
+                issue_expand(tbase, sa, sb);
             } else {
                 // a wait gave up: let an in-flight TMA land before the CTA can exit
                 const uint64_t t0 = globaltimer();
@@ -210,7 +246,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             }
             umma_commit(&d_full);  // arrives once every MMA above is complete (at once if none)
         }
-
+    }
+    {
         // ---- epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15
         const int q = warp & 3, cg = warp >> 2;
         const bool got = mx_wait(&d_full, 0, p.dev_err);
@@ -247,12 +284,18 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = one chunk of W_UV[h]
-    CUtensorMap tmap_w;
-    const int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 1);
+    CUtensorMap tmap_w, tmap_o;
+    int rc = make_tmap_slab_3d(&tmap_w, mp.w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, VH, 1);
     if (rc) return rc;
+    // final o_lat viewed as (64 elements, 96 B rows of 512, 8 chunks): one box = 64 slots of a chunk
+    std::memset(&tmap_o, 0, sizeof(tmap_o));
+    if (mp.ws_olat) {
+        rc = make_tmap_slab_3d(&tmap_o, mp.ws_olat, (uint64_t)H * mp.B, LORA, 8, MX_SLOTS, 1);
+        if (rc) return rc;
+    }
     const dim3 grid(H, (mp.B + MX_SLOTS - 1) / MX_SLOTS);
     return launch_pdl(k3mla_merge_expand_kernel, grid, dim3(MX_THREADS), smem, st, "k3mla_merge_expand_kernel",
-                      tmap_w, mp);
+                      tmap_w, tmap_o, mp);
 }
 
 }  // namespace k3

@@ -43,6 +43,16 @@ def test_ragged_tails_and_split_merges(gpu_lib, split):
     _parity(wl, 0, split=split, max_ctx=1024, name=f"ragged_split{split}")
 
 
+def test_single_split_batch_over_one_slot_tile(gpu_lib):
+    # one split per slot (split = max_ctx): the split kernel lands o_lat itself and the expansion
+    # reads it in place; 67 slots cover two 64-slot tiles, two contexts are empty
+    ctx = [(37 * i * i + 11 * i) % 512 + 1 for i in range(67)]
+    ctx[5] = 0
+    ctx[66] = 0
+    wl = synth.make_custom(ctx, seed=302, device="cuda")
+    _parity(wl, 0, split=512, max_ctx=512, name="single_split67")
+
+
 def test_heavy_tailed_rows_force_rescales(gpu_lib):
     # a late token with a much larger score than the early ones moves the
     # reference max by more than the rescale threshold
