@@ -162,8 +162,10 @@ int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q
  * dev_err     device int32 or NULL (K3MLA_DEV_* bits are ORed in)
  * Runs as two kernels on `stream`: the split decode, then the merge + W_UV
  * expansion.  Both may start while the kernel before them is still running
- * (programmatic dependent launch); the split kernel reads nothing before the
- * kernel before it has completed, and the merge kernel loads only w_kv_b early,
+ * (programmatic dependent launch).  Before that kernel has completed, the split
+ * kernel reads ctx_len (to size each split), so the kernel immediately before
+ * this call in `stream` must not write ctx_len; q_abs, the slab and the block
+ * table are read after the wait.  The merge kernel loads only w_kv_b early,
  * after the split kernel (which does not write it) has started. */
 size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens);
 int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,

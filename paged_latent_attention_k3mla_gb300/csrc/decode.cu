@@ -457,8 +457,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     cluster_sync();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
-    // everything above overlaps the previous kernel in the stream; q_abs, the slab, the block table
-    // and the context lengths are read only after it has completed
+    // everything above overlaps the previous kernel in the stream (which must not write ctx_len, read
+    // at the top to size the split); q_abs, the slab and the block table are read after it completed
     griddep_wait();
     griddep_launch_dependents();
     if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
