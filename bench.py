@@ -405,10 +405,11 @@ def main():
 
 
 def kernel_rev() -> str:
-    """Hash of the CUDA sources, so stored ncu traffic is only used for the kernel it measured."""
+    """Hash of the sources of the paged-decode call (split + merge kernels and what they include),
+    so stored ncu traffic is only used for the kernels it measured."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_latent_attention_k3mla_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in ("common.cuh", "decode.cu", "host_common.cu", "merge_expand.cu", "ptx.cuh"):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:12]
 
