@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -405,12 +406,16 @@ def main():
 
 
 def kernel_rev() -> str:
-    """Hash of the sources of the paged-decode call (split + merge kernels and what they include),
-    so stored ncu traffic is only used for the kernels it measured."""
+    """Hash of the code (comments and blank space left out) of the paged-decode call: the split
+    and merge kernels and what they include, so stored ncu traffic is only used for the kernels it
+    measured."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_latent_attention_k3mla_gb300", "csrc")
     for f in ("common.cuh", "decode.cu", "host_common.cu", "merge_expand.cu", "ptx.cuh"):
-        h.update(open(os.path.join(d, f), "rb").read())
+        src = open(os.path.join(d, f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

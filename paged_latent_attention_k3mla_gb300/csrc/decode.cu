@@ -16,26 +16,28 @@
 // pipeline is one 64-token page, held whole in shared memory.
 //   * rank 0, the score CTA, holds q_abs of the slot in TMEM (24 heads in each
 //     32-lane quarter so that all four SM sub-partitions run softmax; 288
-//     columns).  Three page slots of [9 chunks][64 rows][128 B] (one 72 KB 3-D TMA
-//     box per page) rotate; slot r has its own producer thread and its own MMA
-//     issuer thread, so every barrier has one producer and one consumer, and the
-//     three issuers keep the tensor core busy (one thread alone cannot issue
-//     M=128 x N=64 MMAs as fast as the tensor core retires them).  The MMAs
-//     (A = Q from TMEM, B = the page, K-major, 128-byte swizzle) write S^T[heads x
-//     64 tokens] into one of three TMEM buffers.  Four softmax warps (thread =
-//     head) land the scores to bf16 exactly as the chain does -- bf16(dot), then
-//     bf16(. * scale) with packed bf16x2 instructions -- keep a lazily moved
-//     reference max per head, and store bf16 p straight into the partner CTA's
-//     shared memory with st.async (completion counted in bytes on the partner's
-//     mbarrier), laid out as the K-major B operand of the second contraction.
-//   * rank 1, the PV CTA, streams the same pages (chunks 0..7, one 64 KB box per
-//     page, three slots with one producer each; these reads mostly hit L2 right
-//     after the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T
+//     columns).  Pages stream in thirds ([3 chunks][64 rows][128 B], one 24 KB
+//     3-D TMA box each) through a ring of eight units; third t of every page has
+//     its own producer thread, and page i its MMA issuer thread i mod 3 (one
+//     thread alone cannot issue M=128 x N=64 MMAs as fast as the tensor core
+//     retires them).  The MMAs (A = Q from TMEM, B = the page, K-major, 128-byte
+//     swizzle) write S^T[heads x 64 tokens] into one of three TMEM buffers.  Eight
+//     softmax warps (thread = head; the pages of one parity per warp) land the
+//     scores to bf16 exactly as the chain does -- bf16(dot), then bf16(. * scale)
+//     with packed bf16x2 instructions -- keep a lazily moved reference max per
+//     head, and copy bf16 p to the partner CTA's shared memory with one bulk
+//     smem-to-DSMEM copy per warp and page (completion counted in bytes on the
+//     partner's mbarrier), laid out as the K-major B operand of the second
+//     contraction.
+//   * rank 1, the PV CTA, streams the same pages (chunks 0..7 as two 32 KB
+//     half-page boxes into a ring of five half-page slots, one producer each;
+//     these reads mostly hit L2 right after the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T
 //     in TMEM (four M = 128 blocks, N = 96, K = 64 tokens per page; A is the
 //     MN-major latent page).  Its epilogue warps rescale O when the score CTA
-//     moved a head's reference max, zero rows past the context in the final page
-//     (stale rows must never meet p = 0 as 0 * NaN), and write the split's f32
-//     partial.
+//     moved a head's reference max and zero rows past the context in the final
+//     page (stale rows must never meet p = 0 as 0 * NaN); at the end every warp
+//     helps write O out -- the split's f32 partial, or, for a slot with a single
+//     split, final bf16 o_lat = bf16(O * (1 / l)).
 // TMEM holds Q (288 columns) + S (3 x 64) in rank 0 and O (384) in rank 1, which
 // is why the two contractions live in different CTAs.
 //
