@@ -200,9 +200,55 @@ int k3mla_pool_release_slot(k3mla_pool* pool, int slot);
 const int32_t* k3mla_pool_host_table(const k3mla_pool* pool);
 int k3mla_pool_max_pages(const k3mla_pool* pool);
 int k3mla_pool_n_pages(const k3mla_pool* pool);
-/* Pool capacity and pages in use (PR #869 review: expose total / allocated). */
+/* Pool capacity and pages in use (PR #869 review: expose total / allocated).
+ * A page mapped by several slots counts once. */
 int k3mla_pool_stats(const k3mla_pool* pool, int* total, int* used);
 void k3mla_pool_destroy(k3mla_pool* pool);
+
+/* ---- page sharing (PR #869 description, follow-ups: block-pool reuse of cached
+ * prefixes) -------------------------------------------------------------------
+ * Every page carries a reference count: the number of slots that map it (0 =
+ * free).  k3mla_pool_ensure claims pages with count 1; k3mla_pool_release_slot
+ * decrements the counts of the slot's pages and returns a page to the free list
+ * only when its count reaches 0.
+ *
+ * k3mla_pool_share_prefix maps the first ceil(n_tokens / 64) pages of src_slot
+ * into the (empty) dst_slot -- the same physical ids, counts incremented -- so
+ * the two slots share that prefix of the cache with no copy.  K3MLA_E_SLOT for
+ * a slot out of range, K3MLA_E_CTX for n_tokens > max_ctx, K3MLA_E_INVALID when
+ * dst_slot == src_slot, dst_slot maps any page, or src_slot maps fewer pages.
+ *
+ * Before writing token `pos` of `slot` (whose page must be mapped, else
+ * K3MLA_E_CTX), call k3mla_pool_cow: 0 means the slot owns that page alone and
+ * may write it in place; 1 means the page was shared, so the slot now maps a
+ * fresh page (count 1, the old page's count decremented) and *src_page ->
+ * *dst_page names the whole-page copy the caller must run (k3mla_copy_pages)
+ * before the write; K3MLA_E_NO_PAGES leaves everything unchanged.
+ * k3mla_pool_page_refs returns a page's count (K3MLA_E_INVALID for a bad id). */
+int k3mla_pool_share_prefix(k3mla_pool* pool, int dst_slot, int src_slot, int n_tokens);
+int k3mla_pool_cow(k3mla_pool* pool, int slot, int pos, int32_t* src_page, int32_t* dst_page);
+int k3mla_pool_page_refs(const k3mla_pool* pool, int page);
+
+/* ---- whole-page copy (PR #869, M1 commit: "whole-page copy on prefill
+ * adoption") ---------------------------------------------------------------------
+ * For i < n: page dst_ids[i] of dst_slab <- page src_ids[i] of src_slab, all
+ * n_layers layers (a page of the page-first slab is one contiguous block of
+ * n_layers * 64 * 576 bf16).  Adopting a prefilled sequence into a decode slot:
+ * claim the slot's pages (k3mla_pool_ensure), then copy the prefill pool's pages
+ * into them; un-sharing a page: the pair k3mla_pool_cow names, with
+ * src_slab == dst_slab.
+ * dst_slab / src_slab  device, [dst_n_pages | src_n_pages][n_layers][64][576]
+ *                      bf16, 16-byte aligned (may be the same slab)
+ * src_ids / dst_ids    device int32 [n], 0 <= n <= 65535
+ * dev_err              device int32 or NULL: K3MLA_DEV_BAD_PAGE for a pair with
+ *                      an id outside its slab (that pair is skipped)
+ * The dst ids must be distinct and, within one slab, none may also be a src id
+ * of the same call (the copies run concurrently).  One kernel on `stream`; it may
+ * start while the kernel before it is still running and reads the ids and pages
+ * only after that kernel has completed. */
+int k3mla_copy_pages(uint16_t* dst_slab, int dst_n_pages, const uint16_t* src_slab, int src_n_pages,
+                     int n_layers, const int32_t* src_ids, const int32_t* dst_ids, int n,
+                     int32_t* dev_err, void* stream);
 
 /* ---- paged decode with built-in scratch ---------------------------------------
  * The paper has no counterpart to this call.  It is k3mla_paged_decode without the

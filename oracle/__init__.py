@@ -12,6 +12,8 @@ links or calls anything here, and nothing here imports the product path.
   absorbs: it expands per-head K and V from the latent and runs an ordinary
   softmax attention, so that it checks the absorption identity the M2 commit
   relies on.
+* :mod:`oracle.pages` is the whole-page copy of the M1 commit's prefill
+  adoption, as numpy assignments.
 """
 from .chain import (  # noqa: F401
     absorb,
@@ -22,3 +24,4 @@ from .chain import (  # noqa: F401
     MUTATIONS,
 )
 from .expanded import decode_expanded_f64  # noqa: F401
+from .pages import copy_pages  # noqa: F401

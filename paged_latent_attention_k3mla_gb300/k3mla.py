@@ -25,7 +25,8 @@ EXPORTS = (
     "k3mla_paged_decode", "k3mla_default_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
-    "k3mla_absorb_q_append",
+    "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
+    "k3mla_copy_pages",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -67,6 +68,10 @@ def load(build_if_needed: bool = True):
             "k3mla_diag_umma": ([I, P, P, P, P], I),
             "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
             "k3mla_absorb_q_append": ([P, P, P, P, I, I, I, P, I, P, P, I64, P, I64, I, P, P], I),
+            "k3mla_pool_share_prefix": ([P, I, I, I], I),
+            "k3mla_pool_cow": ([P, I, I, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], I),
+            "k3mla_pool_page_refs": ([P, I], I),
+            "k3mla_copy_pages": ([P, I, P, I, I, P, P, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -158,6 +163,22 @@ def absorb_q_append(q: torch.Tensor, w_kv_b: torch.Tensor, q_abs: torch.Tensor, 
         _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_absorb_q_append")
 
 
+def copy_pages(dst_slab: torch.Tensor, src_slab: torch.Tensor, src_ids: torch.Tensor, dst_ids: torch.Tensor,
+               dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Whole-page copies page src_ids[i] of src_slab -> page dst_ids[i] of dst_slab (all layers);
+    slabs [n_pages, L, 64, 576] bf16 with the same L (may be the same tensor)."""
+    n = src_ids.shape[0]
+    L = dst_slab.shape[1]
+    if src_slab.dim() != 4 or src_slab.shape[1] != L:
+        raise K3mlaError("src_slab must be [n_pages, L, 64, 576] with the layer count of dst_slab")
+    lib = load()
+    _check(lib.k3mla_copy_pages(
+        _dev(dst_slab, torch.bfloat16, (dst_slab.shape[0], L, PAGE, ROW), "dst_slab"), dst_slab.shape[0],
+        _dev(src_slab, torch.bfloat16, (src_slab.shape[0], L, PAGE, ROW), "src_slab"), src_slab.shape[0], L,
+        _dev(src_ids, torch.int32, (n,), "src_ids"), _dev(dst_ids, torch.int32, (n,), "dst_ids"), n,
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_copy_pages")
+
+
 def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:
     return int(load().k3mla_decode_workspace_bytes(B, max_ctx, split_tokens))
 
@@ -246,6 +267,22 @@ class Pool:
         t, u = ctypes.c_int(), ctypes.c_int()
         _check(load().k3mla_pool_stats(self._h, ctypes.byref(t), ctypes.byref(u)), "k3mla_pool_stats")
         return t.value, u.value
+
+    def share_prefix(self, dst_slot: int, src_slot: int, n_tokens: int) -> int:
+        """Map src_slot's first ceil(n_tokens / 64) pages into the empty dst_slot (status code)."""
+        return int(load().k3mla_pool_share_prefix(self._h, dst_slot, src_slot, n_tokens))
+
+    def cow(self, slot: int, pos: int):
+        """Before writing token `pos`: None if the slot owns the page (or a negative status code),
+        else the (src_page, dst_page) copy to run first."""
+        s, d = ctypes.c_int32(), ctypes.c_int32()
+        rc = int(load().k3mla_pool_cow(self._h, slot, pos, ctypes.byref(s), ctypes.byref(d)))
+        if rc == 1:
+            return s.value, d.value
+        return None if rc == 0 else rc
+
+    def refs(self, page: int) -> int:
+        return int(load().k3mla_pool_page_refs(self._h, page))
 
     def close(self):
         if self._h:

@@ -76,6 +76,44 @@ def test_pool_shuffle_is_seeded_and_a_permutation():
     assert not np.array_equal(ta.ravel(), np.arange(64))       # actually scattered
 
 
+def test_prefix_sharing_counts_references_and_copies_on_write():
+    pool = k3mla.Pool(n_slots=3, max_ctx=512, n_pages=10)
+    assert pool.ensure(0, 200) == 0                                # 4 pages
+    t0 = pool.table()[0, :4].copy()
+    assert pool.share_prefix(1, 0, 130) == 0                       # 3 pages shared, no copy
+    assert np.array_equal(pool.table()[1, :3], t0[:3]) and pool.table()[1, 3] == -1
+    assert [pool.refs(int(p)) for p in t0] == [2, 2, 2, 1]
+    assert pool.stats() == (10, 4)                                 # shared pages count once
+    assert pool.cow(0, 199) is None                                # page 3 of slot 0 is its own
+    cp = pool.cow(1, 129)                                          # slot 1 writes into shared page 2
+    assert cp is not None and cp[0] == t0[2] and cp[1] not in t0
+    assert pool.table()[1, 2] == cp[1] and pool.refs(int(t0[2])) == 1 and pool.refs(cp[1]) == 1
+    assert pool.cow(1, 129) is None                                # now private
+    assert pool.stats() == (10, 5)
+    assert pool.ensure(1, 300) == 0                                # grows with private pages
+    assert pool.release(0) == 0                                    # slot 1 still holds pages 0, 1
+    assert pool.refs(int(t0[0])) == 1 and pool.refs(int(t0[3])) == 0
+    assert pool.release(1) == 0 and pool.stats() == (10, 0)
+    assert all(pool.refs(p) == 0 for p in range(10))
+    # errors: non-empty destination, same slot, more pages than the source maps, bad slot / page
+    assert pool.ensure(0, 64) == 0 and pool.ensure(1, 1) == 0
+    assert pool.share_prefix(1, 0, 64) == -1 and pool.share_prefix(2, 2, 1) == -1
+    assert pool.share_prefix(2, 0, 65) == -1 and pool.share_prefix(3, 0, 1) == -3
+    assert pool.share_prefix(2, 0, 513) == -4
+    assert pool.cow(2, 0) == -4                                    # position not mapped
+    assert pool.refs(10) == -1
+    pool.close()
+
+
+def test_copy_on_write_is_all_or_nothing_when_the_pool_is_full():
+    pool = k3mla.Pool(n_slots=2, max_ctx=128, n_pages=2)
+    assert pool.ensure(0, 128) == 0 and pool.share_prefix(1, 0, 128) == 0
+    before = pool.table().copy()
+    assert pool.cow(1, 5) == -2                                    # K3MLA_E_NO_PAGES
+    assert np.array_equal(pool.table(), before) and pool.refs(int(before[0, 0])) == 2
+    pool.close()
+
+
 def test_invalid_arguments_return_status_without_launching():
     lib = k3mla.load()
     null = None
@@ -99,6 +137,11 @@ def test_invalid_arguments_return_status_without_launching():
     assert lib.k3mla_absorb_q_append(*fused) == -1
     assert b"invalid sizes or strides" in lib.k3mla_last_error()
     assert lib.k3mla_diag_umma(5, null, null, null, null) == -1
+    assert lib.k3mla_copy_pages(null, 4, null, 4, 2, null, null, 0, null, null) == 0    # n == 0
+    assert lib.k3mla_copy_pages(null, 4, null, 4, 2, null, null, 1, null, null) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    assert lib.k3mla_copy_pages(null, 4, null, 4, 0, null, null, 1, null, null) == -1   # no layers
+    assert lib.k3mla_copy_pages(null, 4, null, 4, 2, null, null, 65536, null, null) == -1
 
 
 def test_workspace_formula():

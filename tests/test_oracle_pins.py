@@ -289,6 +289,23 @@ def test_append_lands_in_the_mapped_row():
     assert np.array_equal(slab[~touched], before[~touched])
 
 
+def test_whole_page_copy_moves_every_layer_of_the_page():
+    """Adoption copy: each page of a tiny slab is filled with its own id (all layers, rows and
+    columns), so after the copy a page's contents name the page it came from."""
+    n_pages, L = 9, 3
+    ids = np.arange(n_pages, dtype=np.uint16)[:, None, None, None]
+    slab = np.broadcast_to(ids, (n_pages, L, PAGE, ROW)).copy()
+    other = np.broadcast_to(ids[:4] + 100, (4, L, PAGE, ROW)).copy()   # a second pool (prefill side)
+    src, dst = [2, 5, 8, 1], [7, 0, 3, 99]                         # the last pair is out of range
+    assert oracle.copy_pages(slab, slab, src, dst) == 1
+    want = np.arange(n_pages)
+    want[[7, 0, 3]] = [2, 5, 8]
+    assert np.array_equal(slab[:, 0, 0, 0], want)
+    assert all((slab[p] == want[p]).all() for p in range(n_pages))   # every layer, row and column
+    assert oracle.copy_pages(slab, other, [3, 0], [4, 6]) == 0      # cross-pool adoption
+    assert (slab[4] == 103).all() and (slab[6] == 100).all() and (slab[5] == 5).all()
+
+
 def test_byte_figures_from_the_page():
     """27.6 KB/token absorbed vs ~1.47 MB/token expanded over the 24 MLA layers."""
     rows = dict(line.split("=", 1) for line in open(os.path.join(GOLDEN, "bytes_per_token.txt"))
