@@ -128,6 +128,39 @@ int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q
                           const uint16_t* k_rope, int64_t r_stride, int B,
                           int32_t* dev_err, void* stream);
 
+/* ---- chunked prefill: many new tokens per slot (PR #869 description,
+ * follow-ups: chunked prefill in place of the token loop) --------------------
+ * A chunk of n_b = row_start[b + 1] - row_start[b] new tokens of slot b sits at
+ * positions pos0[b] .. pos0[b] + n_b - 1 (their pages already mapped, e.g. by
+ * k3mla_pool_ensure(pool, b, pos0[b] + n_b)); the chunk's inputs are rows
+ * row_start[b] .. row_start[b + 1] - 1 of the packed per-token arrays.
+ *
+ * k3mla_append_latent_rows: k3mla_append_latent for every token of every chunk
+ * (row r of c_kv / k_rope lands in the mapped row of its position, size_t
+ * index).  max_rows >= every n_b (sets the grid; rows past n_b are not read).
+ * K3MLA_DEV_UNMAPPED in *dev_err for a row whose page is -1 / out of range or
+ * whose position is negative or past the table (that row is skipped).
+ *
+ * k3mla_chunk_views: for every row r < R of the packed chunk (token j of slot b),
+ * view_table[r][:] = block_table[b][:] and view_ctx[r] = pos0[b] + j + 1, so that
+ * k3mla_paged_decode over the R views (with q_abs of the R tokens, B = R) gives
+ * each token the causal attention of the chunk: token j sees the slot's rows
+ * before the chunk and the chunk's rows 0..j.  Rows r >= row_start[B] get an
+ * empty view (ctx 0, table -1).
+ * block_table [B][max_pages_per_slot], pos0 [B], row_start [B + 1] (non-
+ * decreasing), view_table [R][max_pages_per_slot], view_ctx [R]: device int32.
+ * The decode reads its ctx_len when it starts, so call k3mla_chunk_views before
+ * the absorption (k3mla_absorb_q), not immediately before k3mla_paged_decode. */
+int k3mla_append_latent_rows(uint16_t* slab, int n_pages, int n_layers, int layer,
+                             const int32_t* block_table, int max_pages_per_slot,
+                             const int32_t* pos0, const int32_t* row_start,
+                             const uint16_t* c_kv, int64_t c_stride,
+                             const uint16_t* k_rope, int64_t r_stride, int B, int max_rows,
+                             int32_t* dev_err, void* stream);
+int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
+                      const int32_t* pos0, const int32_t* row_start, int R,
+                      int32_t* view_table, int32_t* view_ctx, void* stream);
+
 /* ---- paged absorbed decode ---------------------------------------------------
  * For each slot b < B and head h, with n = ctx_len[b] tokens (logical token t
  * lives in page block_table[b][t / 64], row t % 64; a -1 entry is an all-zero

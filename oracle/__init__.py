@@ -14,6 +14,8 @@ links or calls anything here, and nothing here imports the product path.
   relies on.
 * :mod:`oracle.pages` is the whole-page copy of the M1 commit's prefill
   adoption, as numpy assignments.
+* :mod:`oracle.chunk` is chunked prefill: the row append once per token and
+  the causal view of each token of a chunk.
 """
 from .chain import (  # noqa: F401
     absorb,
@@ -25,3 +27,4 @@ from .chain import (  # noqa: F401
 )
 from .expanded import decode_expanded_f64  # noqa: F401
 from .pages import copy_pages  # noqa: F401
+from .chunk import append_rows, chunk_views  # noqa: F401

@@ -26,7 +26,7 @@ EXPORTS = (
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
-    "k3mla_copy_pages",
+    "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -72,6 +72,8 @@ def load(build_if_needed: bool = True):
             "k3mla_pool_cow": ([P, I, I, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], I),
             "k3mla_pool_page_refs": ([P, I], I),
             "k3mla_copy_pages": ([P, I, P, I, I, P, P, I, P, P], I),
+            "k3mla_append_latent_rows": ([P, I, I, I, P, I, P, P, P, I64, P, I64, I, I, P, P], I),
+            "k3mla_chunk_views": ([P, I, I, P, P, I, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -177,6 +179,35 @@ def copy_pages(dst_slab: torch.Tensor, src_slab: torch.Tensor, src_ids: torch.Te
         _dev(src_slab, torch.bfloat16, (src_slab.shape[0], L, PAGE, ROW), "src_slab"), src_slab.shape[0], L,
         _dev(src_ids, torch.int32, (n,), "src_ids"), _dev(dst_ids, torch.int32, (n,), "dst_ids"), n,
         _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_copy_pages")
+
+
+def append_latent_rows(slab: torch.Tensor, layer: int, block_table: torch.Tensor, pos0: torch.Tensor,
+                       row_start: torch.Tensor, c_kv: torch.Tensor, k_rope: torch.Tensor, max_rows: int,
+                       dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Chunk append: row r of c_kv [R, >=512] / k_rope [R, >=64] (slot b's rows row_start[b] ..
+    row_start[b+1]-1) lands at position pos0[b] + (r - row_start[b]) of slot b."""
+    n_pages, L = slab.shape[0], slab.shape[1]
+    B = pos0.shape[0]
+    R = c_kv.shape[0]
+    lib = load()
+    _check(lib.k3mla_append_latent_rows(
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(pos0, torch.int32, (B,), "pos0"), _dev(row_start, torch.int32, (B + 1,), "row_start"),
+        _rows(c_kv, R, "c_kv"), c_kv.stride(0), _rows(k_rope, R, "k_rope"), k_rope.stride(0), B, int(max_rows),
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_append_latent_rows")
+
+
+def chunk_views(block_table: torch.Tensor, pos0: torch.Tensor, row_start: torch.Tensor,
+                view_table: torch.Tensor, view_ctx: torch.Tensor, stream=None) -> None:
+    """Per-token views of the chunks: view_table [R, max_pages] and view_ctx [R] (written)."""
+    B, M = block_table.shape
+    R = view_ctx.shape[0]
+    lib = load()
+    _check(lib.k3mla_chunk_views(
+        _dev(block_table, torch.int32, (B, M), "block_table"), B, M, _dev(pos0, torch.int32, (B,), "pos0"),
+        _dev(row_start, torch.int32, (B + 1,), "row_start"), R, _dev(view_table, torch.int32, (R, M), "view_table"),
+        _dev(view_ctx, torch.int32, (R,), "view_ctx"), _stream(stream)), "k3mla_chunk_views")
 
 
 def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:

@@ -1,0 +1,90 @@
+"""Chunked prefill on the GPU against the oracle.
+
+* k3mla_append_latent_rows: bitwise (a copy into the rows the size_t indices name),
+  ragged chunks across page boundaries, an empty chunk and an unmapped page
+  (skipped and flagged).
+* k3mla_chunk_views: the per-token tables and context lengths, bitwise.
+* The chunk's causal attention -- absorption, views, paged decode over one view per
+  token -- against the oracle's chain on the same views, at the decode's bar (4 bf16
+  ULP of each row's largest magnitude, argmax up to the 1-ULP coin flips).  The
+  oracle's views are pinned to the token-by-token loop in the oracle's own tests."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_latent_attention_k3mla_gb300 import k3mla, synth
+from tests.gpu_common import compare
+
+pytestmark = pytest.mark.gpu
+
+H, V, ROW, LORA = 96, 128, 576, 512
+
+
+def _case(prefix, chunk, seed):
+    ctx = [p + n for p, n in zip(prefix, chunk)]
+    wl = synth.make_custom(ctx, n_layers=2, seed=seed, device="cuda")
+    pos0 = np.asarray(prefix, np.int32)
+    row_start = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    R = int(row_start[-1])
+    g = torch.Generator(device="cuda").manual_seed(seed + 1)
+    c = torch.randn(R, LORA, generator=g, device="cuda").to(torch.bfloat16)
+    r = torch.randn(R, ROW - LORA, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn(R, H, 192, generator=g, device="cuda").to(torch.bfloat16)
+    return wl, pos0, row_start, c, r, q, R
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_append_rows_matches_oracle(gpu_lib):
+    wl, pos0, row_start, c, r, _, R = _case([0, 60, 1, 130, 7], [70, 5, 0, 64, 3], seed=600)
+    tbl = wl.block_table.copy()
+    tbl[4, 0] = -1                                       # slot 4's rows 7..9 land in an unmapped page
+    want = synth.bf16_bits(wl.slab).copy()
+    assert oracle.append_rows(want, 1, tbl, pos0, row_start, synth.bf16_bits(c), synth.bf16_bits(r)) == 3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3mla.append_latent_rows(wl.slab, 1, _dev(tbl), _dev(pos0), _dev(row_start), c, r, max_rows=70, dev_err=err)
+    torch.cuda.synchronize()
+    assert np.array_equal(synth.bf16_bits(wl.slab), want)
+    assert err.item() == k3mla.DEV_UNMAPPED
+
+
+def test_chunked_prefill_attention_matches_oracle(gpu_lib):
+    # a prompt prefilled from scratch, chunks after long and short prefixes, a one-token chunk
+    wl, pos0, row_start, c, r, q, R = _case([0, 100, 1, 300], [16, 5, 64, 1], seed=601)
+    B, M = wl.block_table.shape
+    table = _dev(wl.block_table)
+    oslab = synth.bf16_bits(wl.slab).copy()          # the oracle appends on its own copy
+    oracle.append_rows(oslab, 1, wl.block_table, pos0, row_start, synth.bf16_bits(c), synth.bf16_bits(r))
+    k3mla.append_latent_rows(wl.slab, 1, table, _dev(pos0), _dev(row_start), c, r, max_rows=64)
+    vt = torch.full((R + 1, M), 7, dtype=torch.int32, device="cuda")   # one view past the chunk
+    vc = torch.full((R + 1,), 7, dtype=torch.int32, device="cuda")
+    k3mla.chunk_views(table, _dev(pos0), _dev(row_start), vt, vc)
+    q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
+    k3mla.absorb_q(q, wl.w_kv_b[1], q_abs)
+    max_ctx = M * 64
+    split = k3mla.default_split_tokens(R, max_ctx)
+    ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
+    out = torch.full((R, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((R, H), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3mla.paged_decode(q_abs, wl.slab, 1, vt[:R], vc[:R], wl.w_kv_b[1], wl.scale_bits, out, ws, max_ctx, split,
+                       argmax=am, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+    ovt, ovc = oracle.chunk_views(wl.block_table, pos0, row_start, R + 1)
+    assert np.array_equal(vt.cpu().numpy(), ovt) and np.array_equal(vc.cpu().numpy(), ovc)
+    w = synth.bf16_bits(wl.w_kv_b[1])
+    o = oracle.decode(oracle.absorb(synth.bf16_bits(q), w), oslab, 1, ovt[:R], ovc[:R], w, wl.scale_bits,
+                      nthreads=8, probs_stride=int(ovc.max()))
+    o["slots"] = list(range(R))
+    gpu = dict(out=synth.bf16_bits(out), argmax=am.cpu().numpy())
+    ok, stats = compare(gpu, o, ovc[:R], name="chunked_prefill")
+    print("chunked prefill:", stats)
+    assert ok, stats
+    assert np.array_equal(synth.bf16_bits(wl.slab), oslab)   # and the GPU append left the same slab

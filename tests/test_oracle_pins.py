@@ -306,6 +306,64 @@ def test_whole_page_copy_moves_every_layer_of_the_page():
     assert (slab[4] == 103).all() and (slab[6] == 100).all() and (slab[5] == 5).all()
 
 
+def _chunk_case(seed):
+    """Two slots with 70 and 10 tokens cached, then chunks of 5 and 3 new tokens (packed)."""
+    wl = synth.make_custom([75, 13], n_layers=2, seed=seed)
+    pos0 = np.array([70, 10], np.int32)
+    row_start = np.array([0, 5, 8], np.int32)
+    rng = np.random.default_rng(seed)
+    c = synth.bf16_bits(torch.from_numpy(rng.standard_normal((8, LORA)).astype(np.float32)).to(torch.bfloat16))
+    r = synth.bf16_bits(torch.from_numpy(rng.standard_normal((8, ROW - LORA)).astype(np.float32)).to(torch.bfloat16))
+    q = synth.bf16_bits(torch.from_numpy(rng.standard_normal((8, H, NOPE + ROPE)).astype(np.float32)).to(torch.bfloat16))
+    return wl, pos0, row_start, c, r, q
+
+
+def test_chunk_append_is_the_indexed_write_once_per_token():
+    wl, pos0, row_start, c, r, _ = _chunk_case(80)
+    a = synth.bf16_bits(wl.slab).copy()
+    b = a.copy()
+    tbl = wl.block_table.copy()
+    tbl[1, 0] = -1                                          # slot 1's page 0 unmapped: its 3 rows skip
+    assert oracle.append_rows(a, 1, tbl, pos0, row_start, c, r) == 3
+    for j in range(5):                                      # the C oracle's single-row append, row by row
+        pos = np.array([pos0[0] + j, pos0[1] + j if j < 3 else -1], np.int32)
+        rows = [row_start[0] + j, row_start[1] + min(j, 2)]
+        assert oracle.append(b, 1, tbl, pos, c[rows], r[rows]) == (1 if j < 3 else 0)
+    assert np.array_equal(a, b)
+
+
+def test_chunked_views_reproduce_the_token_loop():
+    """Decoding a chunk through per-token views is bitwise the token-by-token loop it replaces:
+    append token j, decode token j with the context grown by one, repeat."""
+    wl, pos0, row_start, c, r, q = _chunk_case(81)
+    w = synth.bf16_bits(wl.w_kv_b[1])
+    q_abs = oracle.absorb(q, w)
+    slab = synth.bf16_bits(wl.slab).copy()
+    loop_out = np.zeros((8, H, V), np.uint16)
+    for j in range(5):
+        for b in range(2):
+            if row_start[b] + j >= row_start[b + 1]:
+                continue
+            row = row_start[b] + j
+            pos = np.full(2, -1, np.int32)
+            pos[b] = pos0[b] + j
+            cc = np.zeros((2, LORA), np.uint16)
+            rr = np.zeros((2, ROW - LORA), np.uint16)
+            cc[b], rr[b] = c[row], r[row]
+            oracle.append(slab, 1, wl.block_table, pos, cc, rr)
+            ctx = np.array([pos0[b] + j + 1], np.int32)
+            o = oracle.decode(q_abs[row:row + 1], slab, 1, wl.block_table[b:b + 1], ctx, w, wl.scale_bits)
+            loop_out[row] = o["out"][0]
+    slab2 = synth.bf16_bits(wl.slab).copy()
+    oracle.append_rows(slab2, 1, wl.block_table, pos0, row_start, c, r)
+    assert np.array_equal(slab, slab2)
+    vt, vc = oracle.chunk_views(wl.block_table, pos0, row_start, 9)   # one row past the chunk
+    assert list(vc) == [71, 72, 73, 74, 75, 11, 12, 13, 0] and (vt[8] == -1).all()
+    assert np.array_equal(vt[3], wl.block_table[0]) and np.array_equal(vt[6], wl.block_table[1])
+    chunked = oracle.decode(q_abs, slab2, 1, vt[:8], vc[:8], w, wl.scale_bits)
+    assert np.array_equal(chunked["out"], loop_out)
+
+
 def test_byte_figures_from_the_page():
     """27.6 KB/token absorbed vs ~1.47 MB/token expanded over the 24 MLA layers."""
     rows = dict(line.split("=", 1) for line in open(os.path.join(GOLDEN, "bytes_per_token.txt"))
