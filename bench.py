@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 from paged_latent_attention_k3mla_gb300 import synth  # noqa: E402
 
 METRIC = "absorbed-MLA decode µs/layer and latent GB/s vs HBM/tensor roofline"
-H, NOPE, ROPE, V, LORA, ROW = 96, 128, 64, 128, 512, 576
+H, NOPE, ROPE, V, LORA, ROW, PAGE = 96, 128, 64, 128, 512, 576, 64
 WORKLOAD_DESC = {
     "steady64": "64 slots x 24 MLA layers x 4096 tokens (seed 2)",
     "ragged16": "16 slots x 24 MLA layers, ctx U[1,4096] (seed 1)",
@@ -190,6 +190,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="steady64", choices=list(WORKLOAD_DESC))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-next", action="store_true", help="skip the page-copy / chunked-prefill figures")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling aid: fewer layers of the same per-layer workload")
     args = ap.parse_args()
@@ -361,6 +362,7 @@ def main():
     digest = hashlib.sha256(out_h.view(torch.int16).numpy().tobytes()).hexdigest()[:16]
 
     hbm, tflops, src = peaks()
+    nxt = None if args.no_next else next_rows(wl, table, max_ctx, stream, hbm, tflops)
     ab = alg_bytes(wl)
     dec_gbs = ab["decode"] / (dec_ms * 1e-3) / 1e9
     layer_gbs = ab["layer"] / (us_per_layer * 1e-6) / 1e9
@@ -401,8 +403,83 @@ def main():
         "clocks": clk.summary(),
         "out_sha256_16": digest,
         "cpu_baseline": cpu,
+        "next_rows": nxt,
     }
     print(json.dumps(line))
+
+
+def _time_ms(fn, stream, warmup=2, reps=5):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def next_rows(wl, table, max_ctx, stream, hbm, tflops):
+    """Figures for the calls beyond the decode step, run after the timed step (they write the
+    cache): a whole-page copy between two slabs (prefill adoption) against the HBM copy bandwidth,
+    and the causal attention of 64-token chunks of 16 slots at their 4096-token contexts."""
+    from paged_latent_attention_k3mla_gb300 import k3mla
+    dev = "cuda"
+    L = wl.n_layers
+    n = 256
+    dst = torch.empty(n, L, PAGE, ROW, dtype=torch.bfloat16, device=dev)
+    src_ids = torch.arange(n, dtype=torch.int32, device=dev)
+    dst_ids = torch.arange(n - 1, -1, -1, dtype=torch.int32, device=dev)
+    ms = _time_ms(lambda: k3mla.copy_pages(dst, wl.slab, src_ids, dst_ids, stream=stream), stream, reps=20)
+    moved = 2 * n * L * PAGE * ROW * 2                 # every page read once and written once
+    gbs = moved / (ms * 1e-3) / 1e9
+    res = {"copy_pages": {"pages": n, "layers": L, "ms": round(ms, 4), "achieved": round(gbs, 1), "peak": hbm,
+                          "unit": "GB/s (read + write)", "frac": round(gbs / hbm, 4)}}
+    del dst
+
+    nb, T = 16, 64
+    B = wl.B
+    tbl = table[:nb].contiguous()
+    pos0 = torch.from_numpy((wl.ctx_len[:nb] - T).astype(np.int32)).to(dev)
+    row_start = torch.arange(0, nb * T + 1, T, dtype=torch.int32, device=dev)
+    R = nb * T
+    M = tbl.shape[1]
+    vt = torch.empty(R, M, dtype=torch.int32, device=dev)
+    vc = torch.empty(R, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    q = torch.randn(R, H, 192, generator=g, device=dev).to(torch.bfloat16)
+    c = torch.randn(R, 512, generator=g, device=dev).to(torch.bfloat16)
+    r = torch.randn(R, 64, generator=g, device=dev).to(torch.bfloat16)
+    q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device=dev)
+    split = k3mla.default_split_tokens(R, max_ctx)
+    ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device=dev)
+    out = torch.empty(R, H, V, dtype=torch.bfloat16, device=dev)
+
+    def chunk_layer():
+        k3mla.append_latent_rows(wl.slab, 0, tbl, pos0, row_start, c, r, max_rows=T, stream=stream)
+        k3mla.chunk_views(tbl, pos0, row_start, vt, vc, stream=stream)
+        k3mla.absorb_q(q, wl.w_kv_b[0], q_abs, stream=stream)
+        k3mla.paged_decode(q_abs, wl.slab, 0, vt, vc, wl.w_kv_b[0], wl.scale_bits, out, ws, max_ctx, split,
+                           stream=stream)
+
+    ms = _time_ms(chunk_layer, stream)
+    # causal attention: token j of a chunk attends over pos0 + j + 1 tokens (scores 576 wide, latent
+    # accumulation 512 wide, 96 heads), plus the absorption and the W_UV expansion of every token
+    seen = int(sum(int(p0) * T + T * (T + 1) // 2 for p0 in (wl.ctx_len[:nb] - T)))
+    flops = seen * H * 2 * (ROW + LORA) + 2 * 2 * R * H * NOPE * LORA
+    tf = flops / (ms * 1e-3) / 1e12
+    res["chunked_prefill"] = {"slots": nb, "chunk_tokens": T, "context_tokens": int(wl.ctx_len[:nb].max()),
+                              "views": R, "us_per_layer": round(ms * 1e3, 1),
+                              "tokens_per_s_per_layer": round(R / (ms * 1e-3), 1),
+                              "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tflops,
+                                           "unit": "TFLOP/s", "frac": round(tf / tflops, 4)},
+                              "how": "row append + per-token causal views + absorption + paged decode over "
+                                     "the views (each view streams its slot's pages)"}
+    del ws, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def kernel_rev() -> str:
