@@ -424,7 +424,8 @@ def _time_ms(fn, stream, warmup=2, reps=5):
 def next_rows(wl, table, max_ctx, stream, hbm, tflops):
     """Figures for the calls beyond the decode step, run after the timed step (they write the
     cache): a whole-page copy between two slabs (prefill adoption) against the HBM copy bandwidth,
-    and the causal attention of 64-token chunks of 16 slots at their 4096-token contexts."""
+    the causal attention of 64-token chunks of 16 slots at their 4096-token contexts, and the
+    exact-chain decode of one layer of the full batch."""
     from paged_latent_attention_k3mla_gb300 import k3mla
     dev = "cuda"
     L = wl.n_layers
@@ -477,6 +478,17 @@ def next_rows(wl, table, max_ctx, stream, hbm, tflops):
                                            "unit": "TFLOP/s", "frac": round(tf / tflops, 4)},
                               "how": "row append + per-token causal views + absorption + paged decode over "
                                      "the views (each view streams its slot's pages)"}
+    del ws, out
+
+    # exact-chain mode (absorption + decode, CUDA-core sequential sums) on the full batch of one layer
+    ws = torch.empty(k3mla.decode_exact_workspace_bytes(B, max_ctx), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, H, V, dtype=torch.bfloat16, device=dev)
+    ctx = torch.from_numpy(wl.ctx_len).to(dev)
+    ms = _time_ms(lambda: k3mla.decode_exact(wl.q[0], wl.slab, 0, table, ctx, wl.w_kv_b[0], wl.scale_bits, out, ws,
+                                             max_ctx, stream=stream), stream, warmup=1, reps=3)
+    res["exact_chain"] = {"slots": B, "context_tokens": int(wl.ctx_len.max()), "us_per_layer": round(ms * 1e3, 1),
+                          "how": "k3mla_decode_exact: the rounding chain's sums in order on CUDA cores, "
+                                 "bitwise equal to the CPU oracle"}
     del ws, out
     torch.cuda.empty_cache()
     return res

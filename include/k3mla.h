@@ -128,6 +128,31 @@ int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q
                           const uint16_t* k_rope, int64_t r_stride, int B,
                           int32_t* dev_err, void* stream);
 
+/* ---- exact-chain decode (PR #869, M2 commit: the certified rounding chain) ----
+ * The same result as k3mla_absorb_q + k3mla_paged_decode, computed landing for
+ * landing as the chain states it: q absorption summed over d ascending, score
+ * dots over the 576 entries ascending, f32 max and sum of exp over t ascending
+ * (exp in double, rounded once to f32), p_t = bf16(e_t / l) with the IEEE
+ * quotient, the latent sum over t ascending, the W_UV expansion over j ascending,
+ * every landing round-to-nearest-even to bf16.  Each sum is one thread's
+ * sequential loop, so the result does not depend on the GPU, the batch or the
+ * page placement, and it matches a CPU run of the same chain bit for bit.  The
+ * fixed orders rule out the tensor cores: this is a CUDA-core path, tens of
+ * times slower than k3mla_paged_decode, meant as a reference mode.
+ * q          device [B][96][192] bf16 (q_nope | q_rope), not q_abs
+ * others     as for k3mla_paged_decode (no split; argmax_t may be NULL)
+ * workspace  device, >= k3mla_decode_exact_workspace_bytes(B, max_ctx) bytes,
+ *            256-byte aligned: bf16 scores then probabilities [B][96][max_ctx
+ *            rounded up to 8], q_abs [B][96][576], o_lat [96][B][512]
+ * Five kernels on `stream`, each reading nothing before the kernel ahead of it
+ * has completed. */
+size_t k3mla_decode_exact_workspace_bytes(int B, int max_ctx);
+int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                       const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
+                       const uint16_t* w_kv_b, uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t,
+                       void* workspace, size_t ws_bytes, int B, int max_ctx, int32_t* dev_err,
+                       void* stream);
+
 /* ---- chunked prefill: many new tokens per slot (PR #869 description,
  * follow-ups: chunked prefill in place of the token loop) --------------------
  * A chunk of n_b = row_start[b + 1] - row_start[b] new tokens of slot b sits at

@@ -1,0 +1,344 @@
+// exact.cu -- the rounding chain, landing for landing, on the GPU.
+//
+// pegainfer PR #869, "K3: paged latent MLA KV + absorbed decode", M2 commit: the
+// certified chain is (1) q absorption lands bf16, (2) an f32 score dot over the 576
+// row entries in ascending order lands bf16, (3) times the bf16 scale, landed bf16,
+// (4) f32 max and f32 sum of exp in a fixed order, (5) probabilities land bf16
+// after normalising, (6) f32 latent accumulation over ascending t lands bf16,
+// (7) f32 W_UV expansion lands bf16.  The page's own kernel kept that chain with
+// three sweeps over the context; the one-pass kernel of decode.cu trades it for a
+// single read of the cache (tensor-core summation order, online softmax).
+//
+// This mode keeps it.  Every sum is one thread's sequential loop in the chain's
+// index order (products of two bf16 values are exact in f32, so a fused
+// multiply-add rounds exactly as the multiply-then-add of the chain), exp is the
+// double-precision exp rounded once to f32, normalisation is the IEEE quotient.
+// Fixed orders rule out the tensor cores, so these are CUDA-core kernels:
+//   E0 absorption   thread per (slot, head, j): sum over d = 0..127
+//   E1 scores       CTA per (slot, 8 pages): Q and each page staged in shared
+//                   memory; thread per (token, 4 heads): sum over k = 0..575
+//   E2 softmax      thread per (slot, head): max, sum of exp over t ascending,
+//                   p_t = bf16(e_t / l), argmax (lowest t with the largest p)
+//   E3 latent sum   CTA per (slot, 128 dims): thread per (dim, 48 heads), sum
+//                   over t ascending, pages staged in shared memory
+//   E4 expansion    thread per (slot, head, v): sum over j = 0..511
+// Interpretation where the pages are silent (the same as the CPU oracle's): a -1
+// table entry is an all-zero row that takes part in the softmax; positions >=
+// ctx_len are never read; ctx_len == 0 gives zeros and argmax -1.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace k3 {
+
+__device__ __forceinline__ float ex_bf(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+__device__ __forceinline__ uint16_t ex_land(float f)  // round to nearest even, f32 -> bf16
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(f));
+    return (uint16_t)(r & 0xFFFFu);
+}
+
+__device__ __forceinline__ int ex_ctx(const int32_t* ctx_len, int b, int max_ctx, int max_pages)
+{
+    int n = ctx_len[b];
+    const int cap = min(max_ctx, max_pages * PAGE);
+    n = n > cap ? cap : n;
+    return n < 0 ? 0 : n;
+}
+
+// Row pointer of logical token t of slot b, or null for a zero row (-1, or a bad id: flagged).
+__device__ __forceinline__ const uint16_t* ex_row(const uint16_t* slab, int n_pages, int n_layers, int layer,
+                                                  const int32_t* table, int max_pages, int b, int t,
+                                                  int32_t* dev_err)
+{
+    const int32_t id = table[(size_t)b * max_pages + t / PAGE];
+    if (id == -1) return nullptr;
+    if (id < -1 || id >= n_pages) {
+        if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_BAD_PAGE);
+        return nullptr;
+    }
+    return slab + (((size_t)id * n_layers + layer) * PAGE + (size_t)(t % PAGE)) * ROW;
+}
+
+// ---- E0: absorption ------------------------------------------------------------------------
+// grid (B, 96); block 512 (j).  q_abs[b][h][j] = bf16(sum_{d ascending} W_UK[h][d][j] q_nope[d]).
+__global__ void __launch_bounds__(LORA) ex_absorb_kernel(const uint16_t* __restrict__ q,
+                                                        const uint16_t* __restrict__ w_kv_b,
+                                                        uint16_t* __restrict__ q_abs)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
+    __shared__ float qn[NOPE];
+    const uint16_t* qb = q + ((size_t)b * H + h) * QDIM;
+    if (j < NOPE) qn[j] = ex_bf(qb[j]);
+    __syncthreads();
+    const uint16_t* w = w_kv_b + (size_t)h * WROWS_PER_HEAD * LORA + j;
+    float acc = 0.f;
+    for (int d = 0; d < NOPE; ++d) acc = __fadd_rn(acc, __fmul_rn(ex_bf(w[(size_t)d * LORA]), qn[d]));
+    uint16_t* qa = q_abs + ((size_t)b * H + h) * ROW;
+    qa[j] = ex_land(acc);
+    if (j < ROPE) qa[LORA + j] = qb[NOPE + j];
+}
+
+// ---- E1: scores ----------------------------------------------------------------------------
+constexpr int E1_PAGES = 8;              // pages per CTA (Q is staged once for them)
+constexpr int E1_THREADS = 256;
+constexpr int E1_QP = ROW + 2;           // padded row pitch (elements): rows start in distinct banks
+constexpr int E1_SMEM = (H + PAGE) * E1_QP * 2;
+
+// grid (B, ceil(max_ctx / (64 * E1_PAGES))); block 256.  s[b][h][t] = bf16(bf16(dot) * scale).
+// Warp w owns heads 12w .. 12w + 11 (three passes of four); lane = token (two passes of 32).
+__global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
+    const uint16_t* __restrict__ q_abs, const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer,
+    const int32_t* __restrict__ table, int max_pages, const int32_t* __restrict__ ctx_len, int max_ctx,
+    uint16_t scale_bf16, uint16_t* __restrict__ s_out, int s_pitch, int32_t* dev_err)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    extern __shared__ uint16_t ex_smem[];
+    uint16_t* Qs = ex_smem;                  // [96][E1_QP]
+    uint16_t* Rs = ex_smem + H * E1_QP;      // [64][E1_QP]
+    const int b = blockIdx.x;
+    const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
+    const int t_begin = blockIdx.y * E1_PAGES * PAGE;
+    if (t_begin >= n) return;
+    const int t_end = min(n, t_begin + E1_PAGES * PAGE);
+    const float scale = ex_bf(scale_bf16);
+    for (int i = threadIdx.x; i < H * (ROW / 2); i += E1_THREADS) {
+        const int h = i / (ROW / 2), k2 = i % (ROW / 2);
+        reinterpret_cast<uint32_t*>(Qs + h * E1_QP)[k2] =
+            reinterpret_cast<const uint32_t*>(q_abs + ((size_t)b * H + h) * ROW)[k2];
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t0 = t_begin; t0 < t_end; t0 += PAGE) {
+        __syncthreads();  // Q staged / the previous page's rows no longer read
+        for (int i = threadIdx.x; i < PAGE * (ROW / 2); i += E1_THREADS) {
+            const int r = i / (ROW / 2), k2 = i % (ROW / 2);
+            const int t = t0 + r;
+            uint32_t v = 0u;
+            if (t < t_end) {
+                const uint16_t* row = ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t,
+                                             k2 == 0 ? dev_err : nullptr);
+                if (row) v = reinterpret_cast<const uint32_t*>(row)[k2];
+            }
+            reinterpret_cast<uint32_t*>(Rs + r * E1_QP)[k2] = v;
+        }
+        __syncthreads();
+        for (int tp = 0; tp < 2; ++tp) {
+            const int r = 32 * tp + lane, t = t0 + r;
+            const uint32_t* rw = reinterpret_cast<const uint32_t*>(Rs + r * E1_QP);
+            for (int hp = 0; hp < 3; ++hp) {
+                const int h0 = 12 * warp + 4 * hp;
+                const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 0) * E1_QP);
+                const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 1) * E1_QP);
+                const uint32_t* q2 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 2) * E1_QP);
+                const uint32_t* q3 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 3) * E1_QP);
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+                for (int k2 = 0; k2 < ROW / 2; ++k2) {  // k = 2 k2, then 2 k2 + 1: ascending
+                    const uint32_t rv = rw[k2];
+                    const float rlo = __uint_as_float(rv << 16), rhi = __uint_as_float(rv & 0xFFFF0000u);
+                    uint32_t qv = q0[k2];
+                    a0 = __fadd_rn(a0, __fmul_rn(__uint_as_float(qv << 16), rlo));
+                    a0 = __fadd_rn(a0, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
+                    qv = q1[k2];
+                    a1 = __fadd_rn(a1, __fmul_rn(__uint_as_float(qv << 16), rlo));
+                    a1 = __fadd_rn(a1, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
+                    qv = q2[k2];
+                    a2 = __fadd_rn(a2, __fmul_rn(__uint_as_float(qv << 16), rlo));
+                    a2 = __fadd_rn(a2, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
+                    qv = q3[k2];
+                    a3 = __fadd_rn(a3, __fmul_rn(__uint_as_float(qv << 16), rlo));
+                    a3 = __fadd_rn(a3, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
+                }
+                if (t < t_end) {
+                    const float acc[4] = {a0, a1, a2, a3};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        s_out[((size_t)b * H + h0 + u) * s_pitch + t] =
+                            ex_land(__fmul_rn(ex_bf(ex_land(acc[u])), scale));
+                }
+            }
+        }
+    }
+}
+
+// ---- E2: softmax -----------------------------------------------------------------------------
+// grid (ceil(B * 96 / 128)); block 128; thread per (slot, head).  Overwrites s with bf16 p.
+__global__ void __launch_bounds__(128) ex_softmax_kernel(const int32_t* __restrict__ ctx_len, int B, int max_ctx,
+                                                        int max_pages, uint16_t* __restrict__ sp, int s_pitch,
+                                                        int32_t* __restrict__ argmax)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int i = blockIdx.x * 128 + threadIdx.x;
+    if (i >= B * H) return;
+    const int b = i / H;
+    const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
+    uint16_t* row = sp + (size_t)i * s_pitch;
+    if (n == 0) {
+        if (argmax) argmax[i] = -1;
+        return;
+    }
+    float m = ex_bf(row[0]);
+    for (int t = 1; t < n; ++t) m = fmaxf(m, ex_bf(row[t]));
+    float l = 0.f;
+    for (int t = 0; t < n; ++t) l = __fadd_rn(l, (float)exp((double)__fsub_rn(ex_bf(row[t]), m)));
+    int am = 0;
+    float best = -1.f;
+    for (int t = 0; t < n; ++t) {
+        const float p = ex_bf(ex_land(__fdiv_rn((float)exp((double)__fsub_rn(ex_bf(row[t]), m)), l)));
+        if (p > best) {
+            best = p;
+            am = t;
+        }
+        row[t] = ex_land(p);
+    }
+    if (argmax) argmax[i] = am;
+}
+
+// ---- E3: latent sum --------------------------------------------------------------------------
+constexpr int E3_THREADS = 256;          // (128 dims) x (2 groups of 48 heads)
+constexpr int E3_SMEM = PAGE * 128 * 4 + H * PAGE * 4;  // c slice [64][128] f32 + p [96][64] f32
+
+// grid (B, 4 blocks of 128 dims); o_lat[h][b][j] = bf16(sum_{t ascending} p_t c_t[j]).
+__global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
+    const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer, const int32_t* __restrict__ table,
+    int max_pages, const int32_t* __restrict__ ctx_len, int B, int max_ctx, const uint16_t* __restrict__ p,
+    int s_pitch, uint16_t* __restrict__ olat)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    extern __shared__ float ex_f[];
+    float* cs = ex_f;                // [64 tokens][128 dims]
+    float* ps = ex_f + PAGE * 128;   // [96 heads][64 tokens]
+    const int b = blockIdx.x, jb = blockIdx.y * 128;
+    const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
+    const int jd = threadIdx.x & 127, hg = (threadIdx.x >> 7) * 48;
+    float acc[48];
+#pragma unroll
+    for (int u = 0; u < 48; ++u) acc[u] = 0.f;
+    for (int t0 = 0; t0 < n; t0 += PAGE) {
+        const int cnt = min(PAGE, n - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < PAGE * 128; i += E3_THREADS) {
+            const int r = i >> 7, j = i & 127;
+            float v = 0.f;
+            if (r < cnt) {
+                const uint16_t* row = ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t0 + r, nullptr);
+                if (row) v = ex_bf(row[jb + j]);
+            }
+            cs[i] = v;
+        }
+        for (int i = threadIdx.x; i < H * PAGE; i += E3_THREADS) {
+            const int h = i >> 6, r = i & 63;
+            ps[i] = r < cnt ? ex_bf(p[((size_t)b * H + h) * s_pitch + t0 + r]) : 0.f;
+        }
+        __syncthreads();
+        for (int r = 0; r < cnt; ++r) {
+            const float c = cs[r * 128 + jd];
+#pragma unroll
+            for (int u = 0; u < 48; ++u) acc[u] = __fadd_rn(acc[u], __fmul_rn(ps[(hg + u) * PAGE + r], c));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 48; ++u) olat[((size_t)(hg + u) * B + b) * LORA + jb + jd] = ex_land(acc[u]);
+}
+
+// ---- E4: expansion ---------------------------------------------------------------------------
+// grid (B, 96); block 128 (v).  out[b][h][v] = bf16(sum_{j ascending} W_UV[h][v][j] o_lat[j]).
+__global__ void __launch_bounds__(VH) ex_expand_kernel(const uint16_t* __restrict__ olat, int B,
+                                                      const uint16_t* __restrict__ w_kv_b,
+                                                      uint16_t* __restrict__ out)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.x, h = blockIdx.y, v = threadIdx.x;
+    __shared__ float ol[LORA];
+    for (int j = threadIdx.x; j < LORA; j += VH) ol[j] = ex_bf(olat[((size_t)h * B + b) * LORA + j]);
+    __syncthreads();
+    const uint16_t* w = w_kv_b + ((size_t)h * WROWS_PER_HEAD + NOPE + v) * LORA;
+    float acc = 0.f;
+    for (int j = 0; j < LORA; ++j) acc = __fadd_rn(acc, __fmul_rn(ex_bf(w[j]), ol[j]));
+    out[((size_t)b * H + h) * VH + v] = ex_land(acc);
+}
+
+}  // namespace k3
+
+using namespace k3;
+
+static size_t ex_pitch(int max_ctx) { return ((size_t)max_ctx + 7) / 8 * 8; }
+
+extern "C" size_t k3mla_decode_exact_workspace_bytes(int B, int max_ctx)
+{
+    if (B <= 0 || max_ctx <= 0) return 0;
+    const size_t sp = ((size_t)B * H * ex_pitch(max_ctx) * 2 + 255) & ~size_t(255);
+    const size_t qa = ((size_t)B * H * ROW * 2 + 255) & ~size_t(255);
+    return sp + qa + (size_t)B * H * LORA * 2;
+}
+
+extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                                  const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
+                                  const uint16_t* w_kv_b, uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t,
+                                  void* workspace, size_t ws_bytes, int B, int max_ctx, int32_t* dev_err,
+                                  void* stream)
+{
+    if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
+        max_ctx <= 0) {
+        set_error("k3mla_decode_exact: invalid sizes");
+        return K3MLA_E_INVALID;
+    }
+    if (B == 0) return K3MLA_OK;
+    if (!q || !slab || !block_table || !ctx_len || !w_kv_b || !out || !workspace || !aligned(q, 4) ||
+        !aligned(slab, 16) || !aligned(out, 2) || !aligned(workspace, 256)) {
+        set_error("k3mla_decode_exact: null or misaligned pointer");
+        return K3MLA_E_INVALID;
+    }
+    const size_t need = k3mla_decode_exact_workspace_bytes(B, max_ctx);
+    if (ws_bytes < need) {
+        set_error("k3mla_decode_exact: workspace %zu < %zu bytes", ws_bytes, need);
+        return K3MLA_E_WORKSPACE;
+    }
+    const int nchunk = (max_ctx + E1_PAGES * PAGE - 1) / (E1_PAGES * PAGE);
+    if (B > 65535 || nchunk > 65535) {
+        set_error("k3mla_decode_exact: grid too large");
+        return K3MLA_E_INVALID;
+    }
+    if (!device_ok()) return K3MLA_E_DEVICE;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaFuncSetAttribute(ex_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E1_SMEM);
+        cudaFuncSetAttribute(ex_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E3_SMEM);
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    const int pitch = (int)ex_pitch(max_ctx);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    uint16_t* sp = reinterpret_cast<uint16_t*>(ws);
+    const size_t sp_bytes = ((size_t)B * H * pitch * 2 + 255) & ~size_t(255);
+    uint16_t* q_abs = reinterpret_cast<uint16_t*>(ws + sp_bytes);
+    const size_t qa_bytes = ((size_t)B * H * ROW * 2 + 255) & ~size_t(255);
+    uint16_t* olat = reinterpret_cast<uint16_t*>(ws + sp_bytes + qa_bytes);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = launch_pdl(ex_absorb_kernel, dim3(B, H), dim3(LORA), 0, st, "ex_absorb_kernel", q, w_kv_b, q_abs);
+    if (rc) return rc;
+    rc = launch_pdl(ex_scores_kernel, dim3(B, nchunk), dim3(E1_THREADS), (size_t)E1_SMEM, st, "ex_scores_kernel",
+                    q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, max_ctx,
+                    scale_bf16, sp, pitch, dev_err);
+    if (rc) return rc;
+    rc = launch_pdl(ex_softmax_kernel, dim3((B * H + 127) / 128), dim3(128), 0, st, "ex_softmax_kernel", ctx_len, B,
+                    max_ctx, max_pages_per_slot, sp, pitch, argmax_t);
+    if (rc) return rc;
+    rc = launch_pdl(ex_latent_kernel, dim3(B, LORA / 128), dim3(E3_THREADS), (size_t)E3_SMEM, st,
+                    "ex_latent_kernel", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, B,
+                    max_ctx, sp, pitch, olat);
+    if (rc) return rc;
+    return launch_pdl(ex_expand_kernel, dim3(B, H), dim3(VH), 0, st, "ex_expand_kernel", olat, B, w_kv_b, out);
+}

@@ -26,7 +26,8 @@ EXPORTS = (
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
-    "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views",
+    "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
+    "k3mla_decode_exact_workspace_bytes",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -74,6 +75,8 @@ def load(build_if_needed: bool = True):
             "k3mla_copy_pages": ([P, I, P, I, I, P, P, I, P, P], I),
             "k3mla_append_latent_rows": ([P, I, I, I, P, I, P, P, P, I64, P, I64, I, I, P, P], I),
             "k3mla_chunk_views": ([P, I, I, P, P, I, P, P, P], I),
+            "k3mla_decode_exact_workspace_bytes": ([I, I], SZ),
+            "k3mla_decode_exact": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -208,6 +211,27 @@ def chunk_views(block_table: torch.Tensor, pos0: torch.Tensor, row_start: torch.
         _dev(block_table, torch.int32, (B, M), "block_table"), B, M, _dev(pos0, torch.int32, (B,), "pos0"),
         _dev(row_start, torch.int32, (B + 1,), "row_start"), R, _dev(view_table, torch.int32, (R, M), "view_table"),
         _dev(view_ctx, torch.int32, (R,), "view_ctx"), _stream(stream)), "k3mla_chunk_views")
+
+
+def decode_exact_workspace_bytes(B: int, max_ctx: int) -> int:
+    return int(load().k3mla_decode_exact_workspace_bytes(B, max_ctx))
+
+
+def decode_exact(q: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor, ctx_len: torch.Tensor,
+                 w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor, workspace: torch.Tensor, max_ctx: int,
+                 argmax: torch.Tensor | None = None, dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """The exact-chain decode (absorption included): q [B,96,192] bf16 -> out [B,96,128] bf16."""
+    B = q.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    lib = load()
+    _check(lib.k3mla_decode_exact(
+        _dev(q, torch.bfloat16, (B, H, NOPE + ROPE), "q"), _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"),
+        n_pages, L, int(layer), _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"), _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"),
+        ctypes.c_uint16(scale_bf16), _dev(out, torch.bfloat16, (B, H, V), "out"),
+        _opt(argmax, torch.int32, (B, H), "argmax"), _dev(workspace, torch.uint8, None, "workspace"),
+        workspace.numel(), B, int(max_ctx), _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)),
+        "k3mla_decode_exact")
 
 
 def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:

@@ -56,7 +56,8 @@ def compact(wl, layer, slots):
     table (page ids never enter the arithmetic, so the oracle may see any ids)."""
     slots = list(slots)
     tbl = wl.block_table[slots]
-    used = sorted(set(int(x) for x in tbl.ravel() if x >= 0))
+    # ids outside [0, n_pages) read as zero rows, like -1: they never reach the page gather below
+    used = sorted(set(int(x) for x in tbl.ravel() if 0 <= x < wl.slab.shape[0]))
     remap = {p: i for i, p in enumerate(used)}
     idx = torch.tensor(used if used else [0], dtype=torch.long, device=wl.slab.device)
     pages = wl.slab.index_select(0, idx)[:, layer:layer + 1]

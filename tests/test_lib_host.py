@@ -144,6 +144,24 @@ def test_invalid_arguments_return_status_without_launching():
     assert lib.k3mla_copy_pages(null, 4, null, 4, 2, null, null, 65536, null, null) == -1
 
 
+def test_exact_workspace_formula_and_arguments():
+    # bf16 scores/probabilities [B][96][max_ctx rounded up to 8] + q_abs [B][96][576] + o_lat [96][B][512],
+    # the first two regions rounded up to 256 bytes
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, max_ctx in ((1, 130), (64, 4096), (3, 1)):
+        want = r256(B * 96 * (-(-max_ctx // 8) * 8) * 2) + r256(B * 96 * 576 * 2) + B * 96 * 512 * 2
+        assert k3mla.decode_exact_workspace_bytes(B, max_ctx) == want
+    assert k3mla.decode_exact_workspace_bytes(0, 10) == 0
+    lib = k3mla.load()
+    args = [None, None, 4, 1, 0, None, 4, None, None, 0x3D94, None, None, None, 0, 1, 256, None, None]
+    assert lib.k3mla_decode_exact(*args) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    args[14] = 0
+    assert lib.k3mla_decode_exact(*args) == 0                   # B == 0: nothing to do
+    args[4] = 1                                                 # layer == n_layers
+    assert lib.k3mla_decode_exact(*args) == -1
+
+
 def test_workspace_formula():
     # [B][nsplit][96][512] f32 partial O (rounded up to 256 B) + [B][nsplit][96][4] f32
     for B, max_ctx, split in ((1, 130, 128), (64, 4096, 4096), (8, 32768, 3712), (128, 256, 256)):
