@@ -140,6 +140,7 @@ int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q
  * fixed orders rule out the tensor cores: this is a CUDA-core path, tens of
  * times slower than k3mla_paged_decode, meant as a reference mode.
  * q          device [B][96][192] bf16 (q_nope | q_rope), not q_abs
+ * max_ctx    1 .. 51,200 (one row's exps are held in shared memory)
  * others     as for k3mla_paged_decode (no split; argmax_t may be NULL)
  * workspace  device, >= k3mla_decode_exact_workspace_bytes(B, max_ctx) bytes,
  *            256-byte aligned: bf16 scores then probabilities [B][96][max_ctx

@@ -17,11 +17,13 @@
 //   E0 absorption   thread per (slot, head, j): sum over d = 0..127
 //   E1 scores       CTA per (slot, 8 pages): Q and each page staged in shared
 //                   memory; thread per (token, 4 heads): sum over k = 0..575
-//   E2 softmax      thread per (slot, head): max, sum of exp over t ascending,
-//                   p_t = bf16(e_t / l), argmax (lowest t with the largest p)
+//   E2 softmax      CTA per (slot, head): max and exps across the block, the sum
+//                   of exp thread 0's loop over t ascending, p_t = bf16(e_t / l),
+//                   argmax (lowest t with the largest p)
 //   E3 latent sum   CTA per (slot, 128 dims): thread per (dim, 48 heads), sum
 //                   over t ascending, pages staged in shared memory
-//   E4 expansion    thread per (slot, head, v): sum over j = 0..511
+//   E4 expansion    CTA per (head, 16 slots): W_UV[h] staged; thread per v:
+//                   sixteen sums over j = 0..511
 // Interpretation where the pages are silent (the same as the CPU oracle's): a -1
 // table entry is an all-zero row that takes part in the softmax; positions >=
 // ctx_len are never read; ctx_len == 0 gives zeros and argmax -1.
@@ -170,37 +172,79 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
 }
 
 // ---- E2: softmax -----------------------------------------------------------------------------
-// grid (ceil(B * 96 / 128)); block 128; thread per (slot, head).  Overwrites s with bf16 p.
-__global__ void __launch_bounds__(128) ex_softmax_kernel(const int32_t* __restrict__ ctx_len, int B, int max_ctx,
-                                                        int max_pages, uint16_t* __restrict__ sp, int s_pitch,
-                                                        int32_t* __restrict__ argmax)
+// grid (B * 96); block E2_THREADS; dynamic smem: e_t for the row (max_ctx f32).  The max, the exps
+// and the landings are independent per token and run across the block; the sum of exp is thread
+// 0's loop over t ascending.  Overwrites s with bf16 p; argmax = lowest t with the largest p.
+constexpr int E2_THREADS = 256;
+constexpr int E2_MAX_SMEM = 200 * 1024;  // e_t of one row: max_ctx <= 51,200
+
+__global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* __restrict__ ctx_len, int max_ctx,
+                                                               int max_pages, uint16_t* __restrict__ sp, int s_pitch,
+                                                               int32_t* __restrict__ argmax)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int i = blockIdx.x * 128 + threadIdx.x;
-    if (i >= B * H) return;
-    const int b = i / H;
+    extern __shared__ float ex_e[];
+    __shared__ float red_f[E2_THREADS / 32];
+    __shared__ int red_i[E2_THREADS / 32];
+    __shared__ float l_sh;
+    const int i = blockIdx.x, b = i / H;
     const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
     uint16_t* row = sp + (size_t)i * s_pitch;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (n == 0) {
-        if (argmax) argmax[i] = -1;
+        if (argmax && threadIdx.x == 0) argmax[i] = -1;
         return;
     }
-    float m = ex_bf(row[0]);
-    for (int t = 1; t < n; ++t) m = fmaxf(m, ex_bf(row[t]));
-    float l = 0.f;
-    for (int t = 0; t < n; ++t) l = __fadd_rn(l, (float)exp((double)__fsub_rn(ex_bf(row[t]), m)));
-    int am = 0;
-    float best = -1.f;
-    for (int t = 0; t < n; ++t) {
-        const float p = ex_bf(ex_land(__fdiv_rn((float)exp((double)__fsub_rn(ex_bf(row[t]), m)), l)));
-        if (p > best) {
-            best = p;
-            am = t;
-        }
-        row[t] = ex_land(p);
+    float m = -INFINITY;  // the max does not depend on the order it is taken in
+    for (int t = threadIdx.x; t < n; t += E2_THREADS) m = fmaxf(m, ex_bf(row[t]));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red_f[warp] = m;
+    __syncthreads();
+    m = red_f[0];
+    for (int w = 1; w < E2_THREADS / 32; ++w) m = fmaxf(m, red_f[w]);
+    for (int t = threadIdx.x; t < n; t += E2_THREADS) ex_e[t] = (float)exp((double)__fsub_rn(ex_bf(row[t]), m));
+    __syncthreads();
+    if (threadIdx.x == 0) {  // l = sum of e_t over t ascending, one rounding per addition
+        float l = 0.f;
+        for (int t = 0; t < n; ++t) l = __fadd_rn(l, ex_e[t]);
+        l_sh = l;
     }
-    if (argmax) argmax[i] = am;
+    __syncthreads();
+    const float l = l_sh;
+    float best = -1.f;
+    int bt = n;
+    for (int t = threadIdx.x; t < n; t += E2_THREADS) {
+        const uint16_t pb = ex_land(__fdiv_rn(ex_e[t], l));
+        const float p = ex_bf(pb);
+        row[t] = pb;
+        if (p > best) {  // t grows within a thread: the first t attaining its best
+            best = p;
+            bt = t;
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {  // largest p, then lowest t
+        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int ot = __shfl_xor_sync(0xFFFFFFFFu, bt, o);
+        if (ob > best || (ob == best && ot < bt)) {
+            best = ob;
+            bt = ot;
+        }
+    }
+    __syncthreads();  // red_f is reused
+    if (lane == 0) {
+        red_f[warp] = best;
+        red_i[warp] = bt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < E2_THREADS / 32; ++w)
+            if (red_f[w] > best || (red_f[w] == best && red_i[w] < bt)) {
+                best = red_f[w];
+                bt = red_i[w];
+            }
+        if (argmax) argmax[i] = bt;
+    }
 }
 
 // ---- E3: latent sum --------------------------------------------------------------------------
@@ -252,21 +296,43 @@ __global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
 }
 
 // ---- E4: expansion ---------------------------------------------------------------------------
-// grid (B, 96); block 128 (v).  out[b][h][v] = bf16(sum_{j ascending} W_UV[h][v][j] o_lat[j]).
+constexpr int E4_SLOTS = 16;             // slots per CTA (W_UV[h] is staged once for them)
+constexpr int E4_WP = LORA + 2;          // padded W_UV row pitch (elements): rows start in distinct banks
+constexpr int E4_SMEM = VH * E4_WP * 2 + E4_SLOTS * LORA * 4;
+
+// grid (96, ceil(B / 16)); block 128 (v).  out[b][h][v] = bf16(sum_{j ascending} W_UV[h][v][j] o_lat[j]),
+// sixteen slots' sums side by side in each thread.
 __global__ void __launch_bounds__(VH) ex_expand_kernel(const uint16_t* __restrict__ olat, int B,
                                                       const uint16_t* __restrict__ w_kv_b,
                                                       uint16_t* __restrict__ out)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x, h = blockIdx.y, v = threadIdx.x;
-    __shared__ float ol[LORA];
-    for (int j = threadIdx.x; j < LORA; j += VH) ol[j] = ex_bf(olat[((size_t)h * B + b) * LORA + j]);
+    extern __shared__ uint16_t ex_w[];
+    float* ol = reinterpret_cast<float*>(ex_w + VH * E4_WP);  // [16][512]
+    const int h = blockIdx.x, b0 = blockIdx.y * E4_SLOTS, v = threadIdx.x;
+    const uint16_t* wsrc = w_kv_b + ((size_t)h * WROWS_PER_HEAD + NOPE) * LORA;
+    for (int k = threadIdx.x; k < VH * (LORA / 2); k += VH) {
+        const int r = k / (LORA / 2), c2 = k % (LORA / 2);
+        reinterpret_cast<uint32_t*>(ex_w + r * E4_WP)[c2] = reinterpret_cast<const uint32_t*>(wsrc + (size_t)r * LORA)[c2];
+    }
+    for (int k = threadIdx.x; k < E4_SLOTS * LORA; k += VH) {
+        const int s = k / LORA, j = k % LORA;
+        ol[k] = (b0 + s < B) ? ex_bf(olat[((size_t)h * B + b0 + s) * LORA + j]) : 0.f;
+    }
     __syncthreads();
-    const uint16_t* w = w_kv_b + ((size_t)h * WROWS_PER_HEAD + NOPE + v) * LORA;
-    float acc = 0.f;
-    for (int j = 0; j < LORA; ++j) acc = __fadd_rn(acc, __fmul_rn(ex_bf(w[j]), ol[j]));
-    out[((size_t)b * H + h) * VH + v] = ex_land(acc);
+    float acc[E4_SLOTS];
+#pragma unroll
+    for (int s = 0; s < E4_SLOTS; ++s) acc[s] = 0.f;
+    const uint16_t* wr = ex_w + v * E4_WP;
+    for (int j = 0; j < LORA; ++j) {
+        const float w = ex_bf(wr[j]);
+#pragma unroll
+        for (int s = 0; s < E4_SLOTS; ++s) acc[s] = __fadd_rn(acc[s], __fmul_rn(w, ol[s * LORA + j]));
+    }
+#pragma unroll
+    for (int s = 0; s < E4_SLOTS; ++s)
+        if (b0 + s < B) out[((size_t)(b0 + s) * H + h) * VH + v] = ex_land(acc[s]);
 }
 
 }  // namespace k3
@@ -306,7 +372,11 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
         return K3MLA_E_WORKSPACE;
     }
     const int nchunk = (max_ctx + E1_PAGES * PAGE - 1) / (E1_PAGES * PAGE);
-    if (B > 65535 || nchunk > 65535) {
+    if ((size_t)max_ctx * 4 > (size_t)E2_MAX_SMEM) {
+        set_error("k3mla_decode_exact: max_ctx above %d", E2_MAX_SMEM / 4);
+        return K3MLA_E_INVALID;
+    }
+    if ((long long)B * H > 0x7FFFFFFFll || B > 65535 || nchunk > 65535) {
         set_error("k3mla_decode_exact: grid too large");
         return K3MLA_E_INVALID;
     }
@@ -317,6 +387,8 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         cudaFuncSetAttribute(ex_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E1_SMEM);
         cudaFuncSetAttribute(ex_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E3_SMEM);
+        cudaFuncSetAttribute(ex_softmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E2_MAX_SMEM);
+        cudaFuncSetAttribute(ex_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E4_SMEM);
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const int pitch = (int)ex_pitch(max_ctx);
@@ -333,12 +405,13 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
                     q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, max_ctx,
                     scale_bf16, sp, pitch, dev_err);
     if (rc) return rc;
-    rc = launch_pdl(ex_softmax_kernel, dim3((B * H + 127) / 128), dim3(128), 0, st, "ex_softmax_kernel", ctx_len, B,
-                    max_ctx, max_pages_per_slot, sp, pitch, argmax_t);
+    rc = launch_pdl(ex_softmax_kernel, dim3(B * H), dim3(E2_THREADS), (size_t)max_ctx * 4, st, "ex_softmax_kernel",
+                    ctx_len, max_ctx, max_pages_per_slot, sp, pitch, argmax_t);
     if (rc) return rc;
     rc = launch_pdl(ex_latent_kernel, dim3(B, LORA / 128), dim3(E3_THREADS), (size_t)E3_SMEM, st,
                     "ex_latent_kernel", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, B,
                     max_ctx, sp, pitch, olat);
     if (rc) return rc;
-    return launch_pdl(ex_expand_kernel, dim3(B, H), dim3(VH), 0, st, "ex_expand_kernel", olat, B, w_kv_b, out);
+    return launch_pdl(ex_expand_kernel, dim3(H, (B + E4_SLOTS - 1) / E4_SLOTS), dim3(VH), (size_t)E4_SMEM, st,
+                      "ex_expand_kernel", olat, B, w_kv_b, out);
 }
