@@ -88,3 +88,48 @@ def test_chunked_prefill_attention_matches_oracle(gpu_lib):
     print("chunked prefill:", stats)
     assert ok, stats
     assert np.array_equal(synth.bf16_bits(wl.slab), oslab)   # and the GPU append left the same slab
+
+
+def test_chunk_path_copy_and_exact_mode_replay_from_a_cuda_graph(gpu_lib):
+    """The calls beyond the decode step are graph-capturable like the rest: a chunk step (row append,
+    views, absorption, decode), a page copy and the exact-chain decode, captured once and replayed,
+    give the eager results bit for bit."""
+    wl, pos0, row_start, c, r, q, R = _case([40, 200], [8, 3], seed=602)
+    B, M = wl.block_table.shape
+    table, p0, rs = _dev(wl.block_table), _dev(pos0), _dev(row_start)
+    vt = torch.empty(R, M, dtype=torch.int32, device="cuda")
+    vc = torch.empty(R, dtype=torch.int32, device="cuda")
+    q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
+    max_ctx = M * 64
+    split = k3mla.default_split_tokens(R, max_ctx)
+    ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
+    out = torch.empty(R, H, V, dtype=torch.bfloat16, device="cuda")
+    ex_ws = torch.empty(k3mla.decode_exact_workspace_bytes(B, max_ctx), dtype=torch.uint8, device="cuda")
+    ex_out = torch.empty(B, H, V, dtype=torch.bfloat16, device="cuda")
+    ctx = torch.from_numpy(wl.ctx_len).cuda()
+    spare = torch.zeros(2, 2, 64, ROW, dtype=torch.bfloat16, device="cuda")
+    src_ids = torch.tensor([int(wl.block_table[1, 0]), int(wl.block_table[0, 0])], dtype=torch.int32, device="cuda")
+    dst_ids = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        k3mla.append_latent_rows(wl.slab, 1, table, p0, rs, c, r, max_rows=8)
+        k3mla.chunk_views(table, p0, rs, vt, vc)
+        k3mla.absorb_q(q, wl.w_kv_b[1], q_abs)
+        k3mla.paged_decode(q_abs, wl.slab, 1, vt, vc, wl.w_kv_b[1], wl.scale_bits, out, ws, max_ctx, split)
+        k3mla.copy_pages(spare, wl.slab, src_ids, dst_ids)
+        k3mla.decode_exact(wl.q[1], wl.slab, 1, table, ctx, wl.w_kv_b[1], wl.scale_bits, ex_out, ex_ws, max_ctx)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (out, spare, ex_out, vc)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for t in (out, spare, ex_out, vc):
+        t.zero_()
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip((out, spare, ex_out, vc), eager))
