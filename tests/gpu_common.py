@@ -16,9 +16,10 @@ NTHREADS = max(1, min(32, os.cpu_count() or 1))
 
 
 def dump(name: str, **arrays):
-    """Keep arrays of a failing comparison for offline study (only if gpurun_out exists)."""
-    d = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-    if os.path.isdir(d):
+    """Keep arrays of a failing comparison for offline study, in the directory that the
+    K3MLA_DUMP_DIR environment variable names (nothing is written when it is unset)."""
+    d = os.environ.get("K3MLA_DUMP_DIR")
+    if d and os.path.isdir(d):
         np.savez_compressed(os.path.join(d, f"{name}.npz"), **arrays)
 
 
