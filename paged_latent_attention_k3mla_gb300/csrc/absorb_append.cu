@@ -15,7 +15,10 @@
 // Append (same PR, M1 commit): the new token's 512-wide latent and 64-wide rope
 // key land in row ((page * L + layer) * 64 + pos % 64) of the page-first slab,
 // page = block_table[b][pos / 64]; the element index is size_t (the slab passes
-// 2^31 elements).
+// 2^31 elements).  The append runs as its own kernel (k3mla_append_latent) or
+// inside the absorption's grid (k3mla_absorb_q_append): the decode step does the
+// two back to back and neither reads what the other writes, so one launch serves
+// both and leaves one launch's latency off the chain into the decode.
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -22,7 +22,11 @@
 //     into a 128 x 64 f32 TMEM accumulator, and the sixteen warps read it back
 //     (lane = v, column = slot) and store bf16 out.
 // W_UV is read from HBM once per layer per 64 slots; the f32 partials are read
-// once, from L2 where the split kernel just wrote them.
+// once, from L2 where the split kernel just wrote them.  When every slot has a
+// single split the split kernel has already landed o_lat itself (same arithmetic:
+// the one partial's weight is exp(0) = 1), so there is nothing to merge: the
+// elected thread TMA-loads o_lat ([96][B][512] bf16) as the B operand and the
+// expansion runs as above.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
