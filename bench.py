@@ -300,6 +300,14 @@ def main():
     # layer's output is read back as soon as its decode is done
     copy_s = torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(L)]
+    # the compute stream waits for its inputs once per group of layers, the groups doubling (1, 1,
+    # 2, 4, 8, ...) so that each group's copies finish while the layers before it compute; a wait on
+    # another stream costs the overlap of the kernels around it, so fewer waits are cheaper
+    first_of_group, start, size = {}, 0, 1
+    while start < L:
+        end = min(L, start + size)
+        first_of_group[start] = end - 1             # wait for the last copy of the group
+        start, size = end, (size if start == 0 else 2 * size)
     ev_dec = [torch.cuda.Event() for _ in range(L)]
     ev_out, ev_start = torch.cuda.Event(), torch.cuda.Event()
 
@@ -317,7 +325,8 @@ def main():
                 r_d[layer].copy_(r_h[layer], non_blocking=True)
                 ev_in[layer].record(copy_s)
         for layer in range(L):
-            stream.wait_event(ev_in[layer])
+            if layer in first_of_group:             # the inputs of this group of layers have landed
+                stream.wait_event(ev_in[first_of_group[layer]])
             with torch.cuda.stream(stream):
                 absorb_append(layer, q_d[layer], c_d[layer], r_d[layer])
                 k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
