@@ -170,3 +170,25 @@ def test_workspace_formula():
         o = (o + 255) // 256 * 256
         assert k3mla.decode_workspace_bytes(B, max_ctx, split) == o + B * ns * 96 * 4 * 4
     assert k3mla.decode_workspace_bytes(0, 4096, 128) == 0
+
+
+def test_product_and_oracle_share_no_code():
+    """The CUDA path and the oracle are independent: no product source imports, includes or names
+    the oracle's modules, and no oracle source imports the product package or includes its
+    headers; only the seeded input generator (synth.py, no method arithmetic) serves both."""
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "paged_latent_attention_k3mla_gb300")
+    product = [os.path.join(pkg, f) for f in os.listdir(pkg) if f.endswith(".py") and f != "synth.py"]
+    product += [os.path.join(pkg, "csrc", f) for f in os.listdir(os.path.join(pkg, "csrc"))]
+    product += [os.path.join(root, "include", f) for f in os.listdir(os.path.join(root, "include"))]
+    for f in product:
+        src = open(f).read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+        assert "k3mla_oracle" not in src and "k3o_" not in src, f
+    for f in os.listdir(os.path.join(root, "oracle")):
+        if not f.endswith((".py", ".c", ".h")):
+            continue
+        src = open(os.path.join(root, "oracle", f)).read()
+        assert "paged_latent_attention_k3mla_gb300" not in src, f
+        assert "k3mla.h" not in src and "csrc" not in src, f
