@@ -78,6 +78,7 @@ struct MergeParams {
     int32_t* argmax;       // [B][96] or null
     int32_t* dev_err;      // K3MLA_DEV_* bits or null
     int B, max_ctx, max_pages, split, nsplit;
+    int tile;              // slots per CTA: 64 (single split), 32 (2-3 splits) or 16 (4 or more)
 };
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st);
 

@@ -1085,6 +1085,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.max_pages = max_pages_per_slot;
     mp.split = split_tokens;
     mp.nsplit = ns;
+    mp.tile = ns == 1 ? 64 : (ns >= 4 ? 16 : 32);  // the merge's split groups: 64 / tile
     return launch_merge_expand(mp, st);
 }
 

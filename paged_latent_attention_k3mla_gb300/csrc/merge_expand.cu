@@ -43,7 +43,6 @@ constexpr int MX_MERGE_WARPS = 16;             // merge + epilogue warps
 constexpr int MX_THREADS = 32 * MX_MERGE_WARPS;  // thread 0 also issues the TMA loads and the MMAs
 constexpr int MX_A_BYTES = 8 * VH * 128;       // W_UV[h]: 8 chunks x 128 rows x 128 B
 constexpr int MX_B_BYTES = 8 * MX_SLOTS * 128; // o_lat tile: 8 chunks x 64 rows x 128 B
-constexpr uint32_t MX_IDESC = make_idesc_bf16(128, MX_SLOTS, 0, 0);
 constexpr uint64_t MX_WAIT_NS = 1000000000ull;  // bounded waits: 1 s
 
 __device__ __forceinline__ uint32_t mx_pack_bf16x2(float lo, float hi)
@@ -76,16 +75,18 @@ __device__ __noinline__ bool mx_wait(uint64_t* bar, uint32_t parity, int32_t* de
     return true;
 }
 
-// OUT_h^T [128 v x 64 slots] = W_UV[h] . O_lat_h^T: 32 MMAs (K = 512) into one accumulator.
-__device__ __forceinline__ void issue_expand(uint32_t tbase, const uint8_t* sa, const uint8_t* sb)
+// OUT_h^T [128 v x tile slots] = W_UV[h] . O_lat_h^T: 32 MMAs (K = 512) into one accumulator; the
+// B operand holds `tile` rows per 64-dim chunk.
+__device__ __forceinline__ void issue_expand(uint32_t tbase, const uint8_t* sa, const uint8_t* sb, int tile)
 {
     const uint64_t ad = make_sdesc(smem_u32(sa), 16, 1024);
     const uint64_t bd = make_sdesc(smem_u32(sb), 16, 1024);
+    const uint32_t idesc = make_idesc_bf16(128, (uint32_t)tile, 0, 0);
 #pragma unroll
     for (int ks = 0; ks < LORA / 16; ++ks) {
         const int c = ks >> 2, kk = ks & 3;
         umma_ss(tbase, ad + (uint64_t)((c * (VH * 128) + kk * 32) >> 4),
-                bd + (uint64_t)((c * (MX_SLOTS * 128) + kk * 32) >> 4), MX_IDESC, ks > 0 ? 1u : 0u);
+                bd + (uint64_t)((c * (tile * 128) + kk * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
     }
 }
 
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     __shared__ uint64_t w_full, b_ready, d_full, o_full;
     __shared__ uint32_t tmem_slot;
     const int h = blockIdx.x;
-    const int b0 = blockIdx.y * MX_SLOTS;
+    const int b0 = blockIdx.y * p.tile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&o_full, 0, p.dev_err);
             if (ok) {
                 tc_fence_after();
-                issue_expand(tbase, sa, sb);
+                issue_expand(tbase, sa, sb, p.tile);
             } else {
                 const uint64_t t0 = globaltimer();  // let in-flight TMA copies land before the CTA exits
                 while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
@@ -160,81 +161,64 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             umma_commit(&d_full);
         }
     } else {
-        // ---- merge: thread -> (row r = slot b0 + r, segment seg); the row's 512 dims are 128
-        // float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
-        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
+        // ---- merge: thread -> (row r = slot b0 + r, split group g, segment seg); the row's 512 dims
+        // are 128 float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
+        // The G = 64 / tile groups of a slot walk its splits i = g, g + G, ... side by side (so that
+        // a slot's partials arrive in ceil(ns / G) round trips, not ns), each summing in ascending
+        // i, and a fixed shuffle tree adds the groups: ((g0 + g1) + (g2 + g3)).  G depends on the
+        // launch's split count only, so a slot's result does not depend on the batch.
+        const int G = MX_SLOTS / p.tile;
+        const int r = (int)threadIdx.x / (8 * G), g = ((int)threadIdx.x >> 3) % G, seg = threadIdx.x & 7;
         const int b = b0 + r;
         int ns = 0;
         if (b < p.B) {
             const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
             ns = (ctx + p.split - 1) / p.split;
         }
-        float acc[64];
-        // split 0's partial and its (m, l, best, t) record are loaded before the context length is
-        // known (every slot below B has a split 0), so they arrive in one round trip
         const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-        float4 r0 = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(-1));
-        if (b < p.B) {
-            r0 = *reinterpret_cast<const float4*>(ml);
-            const float4* o0 = reinterpret_cast<const float4*>(p.ws_o + ((size_t)b * p.nsplit * H + h) * LORA);
+        float m = -INFINITY, best = -INFINITY, l = 0.f;
+        int best_t = -1;
+        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
+        for (int i = 0; i < ns; ++i) {  // ascending splits; the lowest t wins ties
+            const float* mi = ml + (size_t)i * H * 4;
+            l += expf(mi[0] - m) * mi[1];
+            if (mi[2] > best) {
+                best = mi[2];
+                best_t = __float_as_int(mi[3]);
+            }
+        }
+        if (p.argmax && b < p.B && g == 0 && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
+        float acc[64];
+#pragma unroll
+        for (int k = 0; k < 64; ++k) acc[k] = 0.f;
+        for (int i = g; i < ns; i += G) {
+            const float wgt = expf(ml[(size_t)i * H * 4] - m);
+            const float4* oi = reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const float4 v = o0[seg + 8 * k];
-                acc[4 * k + 0] = v.x;
-                acc[4 * k + 1] = v.y;
-                acc[4 * k + 2] = v.z;
-                acc[4 * k + 3] = v.w;
+                const float4 v = oi[seg + 8 * k];
+                acc[4 * k + 0] += wgt * v.x;
+                acc[4 * k + 1] += wgt * v.y;
+                acc[4 * k + 2] += wgt * v.z;
+                acc[4 * k + 3] += wgt * v.w;
             }
         }
-        float m = r0.x, best = r0.z, l;
-        int best_t = __float_as_int(r0.w);
-        for (int i = 1; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-        if (ns > 0) {
-            l = expf(r0.x - m) * r0.y;
-            for (int i = 1; i < ns; ++i) {
-                const float* mi = ml + (size_t)i * H * 4;
-                l += expf(mi[0] - m) * mi[1];
-                if (mi[2] > best) {  // ascending splits: the lowest t wins ties
-                    best = mi[2];
-                    best_t = __float_as_int(mi[3]);
-                }
-            }
-        } else {
-            best_t = -1;
+        for (int o = 8; o < 8 * G; o <<= 1) {  // lanes 8 g + seg of one slot sit in one warp (8 G <= 32)
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
         }
-        if (p.argmax && b < p.B && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
-        if (ns == 0) {  // empty context (or a padding row of the tile): o_lat = 0
-            l = 1.f;
+        if (ns == 0) l = 1.f;  // empty context (or a padding row of the tile): o_lat = 0
+        if (g == 0) {
+            const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
+            // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
 #pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-        } else {
-            const float w0 = expf(r0.x - m);
-#pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] = 0.f + w0 * acc[k];
-            for (int i = 1; i < ns; ++i) {  // ascending splits
-                const float wgt = expf(ml[(size_t)i * H * 4] - m);
-                const float4* oi =
-                    reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float4 v = oi[seg + 8 * k];
-                    acc[4 * k + 0] += wgt * v.x;
-                    acc[4 * k + 1] += wgt * v.y;
-                    acc[4 * k + 2] += wgt * v.z;
-                    acc[4 * k + 3] += wgt * v.w;
-                }
+            for (int k = 0; k < 16; ++k) {
+                const int c = k >> 1;
+                const int u = 4 * (k & 1) + (seg >> 1);
+                const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] * rl, acc[4 * k + 1] * rl),
+                                           mx_pack_bf16x2(acc[4 * k + 2] * rl, acc[4 * k + 3] * rl));
+                *reinterpret_cast<uint2*>(sb + c * (p.tile * 128) + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (seg & 1)) = v;
             }
-        }
-        const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
-        // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int c = k >> 1;
-            const int u = 4 * (k & 1) + (seg >> 1);
-            const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] * rl, acc[4 * k + 1] * rl),
-                                       mx_pack_bf16x2(acc[4 * k + 2] * rl, acc[4 * k + 3] * rl));
-            *reinterpret_cast<uint2*>(sb + c * (MX_SLOTS * 128) + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (seg & 1)) =
-                v;
         }
         fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
         mbar_arrive(&b_ready);
@@ -242,7 +226,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&b_ready, 0, p.dev_err);
             if (ok) {
                 tc_fence_after();
-                issue_expand(tbase, sa, sb);
+                issue_expand(tbase, sa, sb, p.tile);
             } else {
                 // a wait gave up: let an in-flight TMA land before the CTA can exit
                 const uint64_t t0 = globaltimer();
@@ -255,7 +239,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         // ---- epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15
         const int q = warp & 3, cg = warp >> 2;
         const bool got = mx_wait(&d_full, 0, p.dev_err);
-        if (__all_sync(0xFFFFFFFFu, got)) {
+        if (__all_sync(0xFFFFFFFFu, got) && 16 * cg < p.tile) {
             tc_fence_after();
             uint32_t acc16[16];
             tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * cg), acc16);
@@ -297,7 +281,7 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
         rc = make_tmap_slab_3d(&tmap_o, mp.ws_olat, (uint64_t)H * mp.B, LORA, 8, MX_SLOTS, 1);
         if (rc) return rc;
     }
-    const dim3 grid(H, (mp.B + MX_SLOTS - 1) / MX_SLOTS);
+    const dim3 grid(H, (mp.B + mp.tile - 1) / mp.tile);
     return launch_pdl(k3mla_merge_expand_kernel, grid, dim3(MX_THREADS), smem, st, "k3mla_merge_expand_kernel",
                       tmap_w, tmap_o, mp);
 }
