@@ -348,8 +348,8 @@ def main():
         e2e_device_step()
 
     def e2e_step():
-        for b in range(B):                      # a1: claims on 64-token boundaries (none in steady state)
-            pool.ensure(b, int(wl.ctx_len[b]))
+        rc = pool.ensure_all(wl.ctx_len)        # a1: claims on 64-token boundaries (none in steady state)
+        assert rc == 0, rc
         t_now = pool.table()
         if not np.array_equal(t_now, tbl_pin.numpy()):
             stream.synchronize()

@@ -254,6 +254,12 @@ int k3mla_pool_create(int n_pages, int n_slots, int max_ctx, uint64_t shuffle_se
  * [0, new_len) of `slot` are mapped.  All-or-nothing: on K3MLA_E_NO_PAGES no
  * page is claimed.  new_len > max_ctx gives K3MLA_E_CTX. */
 int k3mla_pool_ensure(k3mla_pool* pool, int slot, int new_len);
+/* k3mla_pool_ensure for slots 0 .. n-1 in order, new_len[b] for slot b (host
+ * array), in one call: a decode step's claims for the whole batch.  Stops at
+ * the first slot that fails and returns its status (the slots before it keep
+ * their pages; the failing slot is all-or-nothing as above); K3MLA_E_INVALID
+ * for n < 0 or n > n_slots. */
+int k3mla_pool_ensure_all(k3mla_pool* pool, const int32_t* new_len, int n);
 /* Returns every page of `slot` to the free list and unmaps its table row. */
 int k3mla_pool_release_slot(k3mla_pool* pool, int slot);
 const int32_t* k3mla_pool_host_table(const k3mla_pool* pool);

@@ -95,6 +95,16 @@ extern "C" int k3mla_pool_ensure(k3mla_pool* p, int slot, int new_len)
     return K3MLA_OK;
 }
 
+extern "C" int k3mla_pool_ensure_all(k3mla_pool* p, const int32_t* new_len, int n)
+{
+    if (!p || !new_len || n < 0 || n > p->n_slots) return K3MLA_E_INVALID;
+    for (int b = 0; b < n; ++b) {
+        const int rc = k3mla_pool_ensure(p, b, new_len[b]);
+        if (rc) return rc;
+    }
+    return K3MLA_OK;
+}
+
 extern "C" int k3mla_pool_release_slot(k3mla_pool* p, int slot)
 {
     if (!p) return K3MLA_E_INVALID;

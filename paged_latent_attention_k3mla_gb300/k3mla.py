@@ -27,7 +27,7 @@ EXPORTS = (
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
-    "k3mla_decode_exact_workspace_bytes",
+    "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -60,6 +60,7 @@ def load(build_if_needed: bool = True):
             "k3mla_default_split_tokens": ([I, I], I),
             "k3mla_pool_create": ([I, I, I, ctypes.c_uint64, ctypes.POINTER(P)], I),
             "k3mla_pool_ensure": ([P, I, I], I),
+            "k3mla_pool_ensure_all": ([P, P, I], I),
             "k3mla_pool_release_slot": ([P, I], I),
             "k3mla_pool_host_table": ([P], ctypes.POINTER(ctypes.c_int32)),
             "k3mla_pool_max_pages": ([P], I),
@@ -310,6 +311,11 @@ class Pool:
     def ensure(self, slot: int, new_len: int) -> int:
         """Returns the status code (0 ok, negative K3MLA_E_*)."""
         return int(load().k3mla_pool_ensure(self._h, slot, new_len))
+
+    def ensure_all(self, new_len) -> int:
+        """ensure(b, new_len[b]) for b = 0 .. len-1 in one call (status of the first failure, or 0)."""
+        a = np.ascontiguousarray(new_len, dtype=np.int32)
+        return int(load().k3mla_pool_ensure_all(self._h, a.ctypes.data_as(ctypes.c_void_p), a.shape[0]))
 
     def release(self, slot: int) -> int:
         return int(load().k3mla_pool_release_slot(self._h, slot))

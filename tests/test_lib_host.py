@@ -51,6 +51,22 @@ def test_pool_claims_on_page_boundaries_and_releases():
     pool.close()
 
 
+def test_pool_ensure_all_is_ensure_slot_by_slot():
+    a = k3mla.Pool(n_slots=4, max_ctx=512, n_pages=12, shuffle_seed=3)
+    b = k3mla.Pool(n_slots=4, max_ctx=512, n_pages=12, shuffle_seed=3)
+    lens = np.array([65, 1, 300, 0], np.int32)
+    assert a.ensure_all(lens) == 0
+    for s, n in enumerate(lens):
+        assert b.ensure(s, int(n)) == 0
+    assert np.array_equal(a.table(), b.table()) and a.stats() == b.stats() == (12, 8)
+    # slot 2 takes 3 of the 4 free pages, then slot 3 needs 3 and finds 1: it fails alone, unchanged
+    assert a.ensure_all(np.array([65, 1, 512, 129], np.int32)) == -2
+    assert a.stats() == (12, 11) and (a.table()[3] == -1).all() and (a.table()[2] >= 0).all()
+    assert a.ensure_all(np.array([1, 1, 1, 1, 1], np.int32)) == -1    # more lengths than slots
+    a.close()
+    b.close()
+
+
 def test_pool_errors_are_all_or_nothing():
     pool = k3mla.Pool(n_slots=2, max_ctx=256, n_pages=5)
     assert pool.ensure(0, 256) == 0                            # 4 pages
