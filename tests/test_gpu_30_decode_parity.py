@@ -53,13 +53,37 @@ def test_single_split_batch_over_one_slot_tile(gpu_lib):
     _parity(wl, 0, split=512, max_ctx=512, name="single_split67")
 
 
+RESCALE_TAU = 16.0  # the split kernel moves a head's reference max only past this growth (natural log)
+
+
+def _max_jump(scores, ctx, split):
+    """Largest growth of a page max over the running max of the earlier pages of its split."""
+    best = -np.inf
+    for i, n in enumerate(ctx):
+        for s0 in range(0, int(n), split):
+            for h in range(scores.shape[1]):
+                run = -np.inf
+                for p0 in range(s0, min(int(n), s0 + split), 64):
+                    pm = scores[i, h, p0:min(int(n), p0 + 64, s0 + split)].max()
+                    if run > -np.inf:
+                        best = max(best, pm - run)
+                    run = max(run, pm)
+    return best
+
+
 def test_heavy_tailed_rows_force_rescales(gpu_lib):
-    # a late token with a much larger score than the early ones moves the
-    # reference max by more than the rescale threshold
+    # late tokens with much larger scores than the early ones move the reference max of their
+    # split by more than the rescale threshold, so the PV CTA rescales O (shown on the oracle's
+    # own scores below, not assumed)
     wl = synth.make_custom([700, 1500], seed=301, device="cuda", row_scale=(0.25, 4.0))
-    wl.slab[wl.block_table[0, 9], 0, 5, :] *= 6
-    wl.slab[wl.block_table[1, 20], 0, 17, :] *= 8
-    _parity(wl, 0, split=1024, max_ctx=1536, name="rescale")
+    wl.slab[wl.block_table[0, 9], 0, 5, :] *= 20
+    wl.slab[wl.block_table[1, 20], 0, 17, :] *= 30
+    o = oracle_layer(wl, 0, probs_stride=int(wl.ctx_len.max()))
+    assert _max_jump(o["scores"], wl.ctx_len, 1024) > RESCALE_TAU
+    g = gpu_layer(wl, 0, split=1024, max_ctx=1536)
+    ok, stats = compare(g, o, wl.ctx_len, name="rescale")
+    print(f"rescale: {stats}")
+    assert g["dev_err"] == 0 and ok, stats
 
 
 def test_padding_bucket(gpu_lib):
