@@ -76,8 +76,8 @@ def test_heavy_tailed_rows_force_rescales(gpu_lib):
     # split by more than the rescale threshold, so the PV CTA rescales O (shown on the oracle's
     # own scores below, not assumed)
     wl = synth.make_custom([700, 1500], seed=301, device="cuda", row_scale=(0.25, 4.0))
-    wl.slab[wl.block_table[0, 9], 0, 5, :] *= 20
-    wl.slab[wl.block_table[1, 20], 0, 17, :] *= 30
+    wl.slab[wl.block_table[0, 9], 0, 5, :] *= 100
+    wl.slab[wl.block_table[1, 20], 0, 17, :] *= 150
     o = oracle_layer(wl, 0, probs_stride=int(wl.ctx_len.max()))
     assert _max_jump(o["scores"], wl.ctx_len, 1024) > RESCALE_TAU
     g = gpu_layer(wl, 0, split=1024, max_ctx=1536)
