@@ -86,6 +86,23 @@ def test_heavy_tailed_rows_force_rescales(gpu_lib):
     assert g["dev_err"] == 0 and ok, stats
 
 
+def test_many_slots_over_several_waves_and_tiles(gpu_lib):
+    # 150 slots: 150 clusters (two waves of SM pairs), three 64-slot absorption tiles, and the
+    # two-split merge over tiles of 32 slots (max_ctx 640, split 384)
+    ctx = [(53 * i * i + 17 * i) % 640 + 1 for i in range(150)]
+    wl = synth.make_custom(ctx, seed=303, device="cuda")
+    _parity(wl, 0, split=384, max_ctx=640, name="many_slots150")
+
+
+def test_one_long_slot_many_splits(gpu_lib):
+    # one slot of 20,000 tokens under the default split: 53 splits of 384 tokens, merged by four
+    # split groups; the oracle checks sampled heads of the whole context
+    wl = synth.make_custom([20000], seed=304, device="cuda")
+    split = k3mla.default_split_tokens(1, 20000)
+    assert -(-20000 // split) > 40
+    _parity(wl, 0, split=split, max_ctx=20000, name="long_one_slot")
+
+
 def test_padding_bucket(gpu_lib):
     wl = synth.make_workload("padding128", device="cuda")
     assert (wl.ctx_len == 0).sum() == 1 and (wl.block_table < 0).all(axis=1).sum() > 30
