@@ -6,7 +6,8 @@
 * k3mla_chunk_views: the per-token tables and context lengths, bitwise.
 * The chunk's causal attention -- absorption, views, paged decode over one view per
   token -- against the oracle's chain on the same views, at the decode's bar (4 bf16
-  ULP of each row's largest magnitude, argmax up to the 1-ULP coin flips).  The
+  ULP of each row's largest magnitude, argmax up to the 1-ULP coin flips): short
+  chunks in full, and 300-token chunks after ~3,000-token prefixes on sampled views.  The
   oracle's views are pinned to the token-by-token loop in the oracle's own tests."""
 from __future__ import annotations
 
@@ -88,6 +89,51 @@ def test_chunked_prefill_attention_matches_oracle(gpu_lib):
     print("chunked prefill:", stats)
     assert ok, stats
     assert np.array_equal(synth.bf16_bits(wl.slab), oslab)   # and the GPU append left the same slab
+
+
+def test_long_chunks_after_long_prefixes_sampled(gpu_lib):
+    # two slots, each a 300-token chunk after a prefix of ~3,000 tokens: 600 views (ten absorption
+    # tiles, a multi-wave split grid); the oracle checks sampled views -- each chunk's first token,
+    # the tokens on either side of a page boundary inside it, and its last token
+    prefix, chunk = [3000, 2881], [300, 300]
+    wl, pos0, row_start, c, r, q, R = _case(prefix, chunk, seed=603)
+    B, M = wl.block_table.shape
+    table = _dev(wl.block_table)
+    oslab = synth.bf16_bits(wl.slab).copy()
+    oracle.append_rows(oslab, 1, wl.block_table, pos0, row_start, synth.bf16_bits(c), synth.bf16_bits(r))
+    k3mla.append_latent_rows(wl.slab, 1, table, _dev(pos0), _dev(row_start), c, r, max_rows=300)
+    vt = torch.empty(R, M, dtype=torch.int32, device="cuda")
+    vc = torch.empty(R, dtype=torch.int32, device="cuda")
+    k3mla.chunk_views(table, _dev(pos0), _dev(row_start), vt, vc)
+    q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
+    k3mla.absorb_q(q, wl.w_kv_b[1], q_abs)
+    max_ctx = M * 64
+    split = k3mla.default_split_tokens(R, max_ctx)
+    ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
+    out = torch.full((R, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((R, H), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3mla.paged_decode(q_abs, wl.slab, 1, vt, vc, wl.w_kv_b[1], wl.scale_bits, out, ws, max_ctx, split,
+                       argmax=am, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(synth.bf16_bits(wl.slab), oslab)
+
+    ovt, ovc = oracle.chunk_views(wl.block_table, pos0, row_start, R)
+    assert np.array_equal(vt.cpu().numpy(), ovt) and np.array_equal(vc.cpu().numpy(), ovc)
+    sel = []
+    for b in range(B):
+        j_edge = 64 - prefix[b] % 64           # the chunk's first token on a new page
+        sel += [int(row_start[b]) + j for j in (0, j_edge - 1, j_edge, chunk[b] - 1)]
+    w = synth.bf16_bits(wl.w_kv_b[1])
+    stride = int(ovc[sel].max())
+    o = oracle.decode(oracle.absorb(synth.bf16_bits(q)[sel], w), oslab, 1, ovt[sel], ovc[sel], w, wl.scale_bits,
+                      nthreads=8, probs_stride=stride)
+    o["slots"] = sel
+    gpu = dict(out=synth.bf16_bits(out), argmax=am.cpu().numpy())
+    ok, stats = compare(gpu, o, ovc, name="long_chunks")
+    print("long chunks:", split, stats)
+    assert ok, stats
 
 
 def test_chunk_path_copy_and_exact_mode_replay_from_a_cuda_graph(gpu_lib):

@@ -5,7 +5,8 @@ sequential sums, double exp rounded once to f32, IEEE quotient), so the whole
 output -- out and argmax -- must equal the CPU oracle's bits, not merely fall
 within the one-pass kernel's 4-ULP bar: ragged contexts across page and tile
 boundaries, -1 holes, a bad page id (flagged, read as zero), an empty context,
-heavy-tailed rows, padding slots, and sampled slots of the full-size workload."""
+heavy-tailed rows, the longest context the mode takes, padding slots, and sampled
+slots of the full-size workload."""
 from __future__ import annotations
 
 import numpy as np
@@ -61,6 +62,15 @@ def test_exact_heavy_tailed_rows(gpu_lib):
     wl = synth.make_custom([700, 1500, 33], seed=701, device="cuda", row_scale=(0.25, 4.0))
     wl.slab[wl.block_table[0, 9], 0, 5, :] *= 6
     g = _exact(wl, 0)
+    assert g["dev_err"] == 0
+    _bitwise(g, oracle_layer(wl, 0))
+
+
+def test_exact_at_the_longest_context(gpu_lib):
+    # the mode's largest context (one row's exps fill the softmax kernel's shared memory), heavy-tailed
+    # rows, beside a short slot; max_ctx not a whole number of pages
+    wl = synth.make_custom([51200, 77], seed=702, device="cuda", row_scale=(0.25, 4.0))
+    g = _exact(wl, 0, max_ctx=51200)
     assert g["dev_err"] == 0
     _bitwise(g, oracle_layer(wl, 0))
 
