@@ -200,10 +200,13 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
  *
  * The context of each slot is cut into splits of split_tokens logical tokens
  * (a positive multiple of K3MLA_TILE); each split is reduced on its own and the
- * splits are merged in ascending order.  Split boundaries depend only on the
- * logical position and ctx_len, never on B, the page ids or the GPU, so for a
- * fixed split_tokens the result of a slot is bitwise independent of the other
- * slots in the batch, of padding slots and of which physical pages hold it.
+ * splits are merged in a fixed order: 1, 2 or 4 split groups (by the launch's
+ * split count ceil(max_ctx / split_tokens)), group g summing splits g, g + G, ...
+ * in ascending order, then the groups added as ((g0 + g1) + (g2 + g3)).  Split
+ * boundaries and that order depend only on the logical position, ctx_len,
+ * split_tokens and max_ctx, never on B, the page ids or the GPU, so for fixed
+ * split_tokens and max_ctx the result of a slot is bitwise independent of the
+ * other slots in the batch, of padding slots and of which physical pages hold it.
  *
  * q_abs       device [B][96][576] bf16 (from k3mla_absorb_q)
  * slab        device [n_pages][n_layers][64][576] bf16; n_pages*n_layers*64 < 2^31
