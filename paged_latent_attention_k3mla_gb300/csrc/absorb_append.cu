@@ -6,11 +6,14 @@
 // then q_rope is copied to q_abs[b][h][512:576].  Per head this is a dense
 // product across slots, Q_abs_h^T [512 x B] = W_UK[h]^T [512 x 128] . Q_nope_h^T
 // [128 x B], whose cost is reading W_UK (12.6 MB per layer).  It runs on the
-// 5th-generation tensor cores, one CTA per (head, tile of 64 slots): W_UK[h] lands
+// 5th-generation tensor cores, one CTA per (head, tile of NB slots): W_UK[h] lands
 // as the MN-major A operand ([8 chunks of 64 j][128 d][128 B], 128-byte swizzle) in
 // eight TMA boxes, sixteen warps write the q_nope tile as the K-major B operand
-// ([2 chunks of 64 d][64 slots][128 B]), and 32 MMAs (4 blocks of 128 j x 8 K
-// steps) fill four 128 x 64 f32 TMEM accumulators that the warps read back.
+// ([2 chunks of 64 d][NB slots][128 B]), and 32 MMAs (4 blocks of 128 j x 8 K
+// steps) fill four 128 x NB f32 TMEM accumulators that the warps read back.  NB is
+// 64 for batches of up to 64 slots and 128 above: one CTA per head then covers up to
+// 128 slots (one wave on the GPU, W_UK read once) where 64-slot tiles would take
+// two waves and read every W_UK[h] twice.
 //
 // Append (same PR, M1 commit): the new token's 512-wide latent and 64-wide rope
 // key land in row ((page * L + layer) * 64 + pos % 64) of the page-first slab,
@@ -28,13 +31,22 @@
 
 namespace k3 {
 
-constexpr int AB_SLOTS = 64;                     // slots per CTA (the MMA's N)
 constexpr int AB_WARPS = 16;
 constexpr int AB_THREADS = 32 * AB_WARPS;
+constexpr int AB_ROWS_PER_PASS = AB_THREADS / 8;  // slots staged / written per pass (8 threads a slot)
 constexpr int AB_A_BYTES = 8 * NOPE * 128;        // W_UK[h]: 8 j-chunks x 128 d rows x 128 B
-constexpr int AB_B_BYTES = 2 * AB_SLOTS * 128;    // q_nope tile: 2 d-chunks x 64 slots x 128 B
-constexpr uint32_t AB_IDESC = make_idesc_bf16(128, AB_SLOTS, 1, 0);  // A MN-major, B K-major
 constexpr uint64_t AB_WAIT_NS = 1000000000ull;
+
+// Slots per CTA (the MMA's N): the q_nope tile (2 d-chunks x NB slots x 128 B), the instruction
+// descriptor (A MN-major, B K-major) and the TMEM of the four 128 x NB accumulators.
+template <int NB>
+struct AbTile {
+    static_assert(NB == 64 || NB == 128, "64 or 128 slots per CTA");
+    static constexpr int B_BYTES = 2 * NB * 128;
+    static constexpr uint32_t IDESC = make_idesc_bf16(128, NB, 1, 0);
+    static constexpr uint32_t TMEM = 4 * NB;
+    static_assert(NB * LORA * 2 <= AB_A_BYTES, "the bf16 result tile fits over the W_UK buffer");
+};
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -71,7 +83,6 @@ struct AppendJob {
     int n_pages, n_layers, layer, max_pages, B;
 };
 constexpr int AP_THREADS = 96;  // a row is 288 32-bit words: three per thread
-static_assert(H >= AB_SLOTS, "the absorption grid has a CTA for every appended slot");
 
 // One slot's row: the slab row index (or -1 when the slot writes nothing) and this thread's three
 // words of it (words w = at, at + 96, at + 192; latent below 256, rope from 256).
@@ -103,18 +114,20 @@ __device__ __forceinline__ void append_store(const AppendJob& ap, int64_t row, i
     for (int k = 0; k < 3; ++k) dst[at + AP_THREADS * k] = v[k];
 }
 
-// grid (96 heads, ceil(B / 64) slot tiles); block AB_THREADS; thread 0 also issues the loads and MMAs.
+// grid (96 heads, ceil(B / NB) slot tiles); block AB_THREADS; thread 0 also issues the loads and MMAs.
+template <int NB>
 __global__ void __launch_bounds__(AB_THREADS, 1)
     k3mla_absorb_kernel(const __grid_constant__ CUtensorMap tmap_w, const uint16_t* __restrict__ q,
                         uint16_t* __restrict__ q_abs, int B, const AppendJob ap)
 {
+    using T = AbTile<NB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sb = sa + AB_A_BYTES;
     __shared__ uint64_t w_full, b_ready, d_full;
     __shared__ uint32_t tmem_slot;
     const int h = blockIdx.x;
-    const int b0 = blockIdx.y * AB_SLOTS;
+    const int b0 = blockIdx.y * NB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         tma_prefetch_desc(&tmap_w);
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_slot, 4 * AB_SLOTS);
+        tmem_alloc(&tmem_slot, T::TMEM);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -144,10 +157,12 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     griddep_wait();
     griddep_launch_dependents();
 
-    // The append (when this launch carries one): CTA `lin` writes the row of slot lin (the grid has
-    // 96 ceil(B / 64) >= B CTAs); its last AP_THREADS threads fetch the row here, beside the q_nope
-    // loads, and store it once their share of the B operand is written.
+    // The append (when this launch carries one): CTA `lin` writes the rows of slots lin, lin + ncta,
+    // ... (one slot per CTA unless B exceeds the grid's CTAs); its last AP_THREADS threads fetch the
+    // first row here, beside the q_nope loads, and store it once their share of the B operand is
+    // written.
     const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    const int ncta = (int)(gridDim.x * gridDim.y);
     const int at = (int)threadIdx.x - (AB_THREADS - AP_THREADS);
     const bool app_thread = lin < ap.B && at >= 0;
     uint32_t av[3] = {0u, 0u, 0u};
@@ -155,22 +170,32 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     if (app_thread) arow = append_fetch(ap, lin, at, av);
 
     {   // q_nope of the tile -> B operand; q_rope -> q_abs[..][512:576].  thread -> (slot r, segment seg)
-        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
-        const int b = b0 + r;
-        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * H + h) * QDIM);
+        const int seg = threadIdx.x & 7;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {  // 16-byte unit u = 2 seg + e: dims 8u .. 8u+7
-            const int u = 2 * seg + e;
-            const uint4 v = (b < B) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-            const int c = u >> 3, uu = u & 7;
-            *reinterpret_cast<uint4*>(sb + c * (AB_SLOTS * 128) + r * 128 + ((uu ^ (r & 7)) << 4)) = v;
+        for (int r = threadIdx.x >> 3; r < NB; r += AB_ROWS_PER_PASS) {
+            const int b = b0 + r;
+            const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * H + h) * QDIM);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // 16-byte unit u = 2 seg + e: dims 8u .. 8u+7
+                const int u = 2 * seg + e;
+                const uint4 v = (b < B) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+                const int c = u >> 3, uu = u & 7;
+                *reinterpret_cast<uint4*>(sb + c * (NB * 128) + r * 128 + ((uu ^ (r & 7)) << 4)) = v;
+            }
+            if (b < B)
+                reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW + LORA)[seg] =
+                    __ldg(src + NOPE / 8 + seg);
         }
-        if (b < B)
-            reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW + LORA)[seg] = __ldg(src + NOPE / 8 + seg);
         fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
         mbar_arrive(&b_ready);
     }
-    if (app_thread) append_store(ap, arow, at, av);
+    if (app_thread) {
+        append_store(ap, arow, at, av);
+        for (int sl = lin + ncta; sl < ap.B; sl += ncta) {  // only when B exceeds the grid's CTAs
+            arow = append_fetch(ap, sl, at, av);
+            append_store(ap, arow, at, av);
+        }
+    }
     if (threadIdx.x == 0) {
         const bool ok = ab_wait(&w_full, 0, nullptr) && ab_wait(&b_ready, 0, nullptr);
         if (ok) {
@@ -181,9 +206,9 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
             for (int ks = 0; ks < NOPE / 16; ++ks)
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt)  // four independent accumulators in turn
-                    umma_ss(tbase + (uint32_t)(AB_SLOTS * mt),
+                    umma_ss(tbase + (uint32_t)(NB * mt),
                             ad + (uint64_t)((mt * 2 * NOPE * 128 + ks * 16 * 128) >> 4),
-                            bd + (uint64_t)(((ks >> 2) * (AB_SLOTS * 128) + (ks & 3) * 32) >> 4), AB_IDESC,
+                            bd + (uint64_t)(((ks >> 2) * (NB * 128) + (ks & 3) * 32) >> 4), T::IDESC,
                             ks > 0 ? 1u : 0u);
         } else {
             const uint64_t t0 = globaltimer();  // let an in-flight TMA land before the CTA can exit
@@ -191,8 +216,8 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         }
         umma_commit(&d_full);
     }
-    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's 64 slots and
-        // lands bf16 values in a [64 slots][512] tile over the (now idle) W_UK buffer; the CTA then
+    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's NB slots and
+        // lands bf16 values in a [NB slots][512] tile over the (now idle) W_UK buffer; the CTA then
         // writes each slot's 1 KB row of q_abs with 16-byte stores
         const int qq = warp & 3, mt = warp >> 2;
         const bool got = ab_wait(&d_full, 0, nullptr);
@@ -201,9 +226,9 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
             tc_fence_after();
             const int j = 128 * mt + 32 * qq + lane;
 #pragma unroll
-            for (int piece = 0; piece < 2; ++piece) {
+            for (int piece = 0; piece < NB / 32; ++piece) {
                 uint32_t acc[32];
-                tmem_ld32(tbase + ((uint32_t)(32 * qq) << 16) + (uint32_t)(AB_SLOTS * mt + 32 * piece), acc);
+                tmem_ld32(tbase + ((uint32_t)(32 * qq) << 16) + (uint32_t)(NB * mt + 32 * piece), acc);
                 tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
@@ -212,19 +237,22 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         }
         __syncthreads();
         // thread -> (slot r, 16-byte units 8k + seg of its row)
-        const int r = threadIdx.x >> 3, seg = threadIdx.x & 7;
-        const int b = b0 + r;
-        if (b < B) {
-            const uint4* srow = reinterpret_cast<const uint4*>(tile + r * LORA);
-            uint4* drow = reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW);
+        const int seg = threadIdx.x & 7;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) drow[seg + 8 * k] = srow[seg + 8 * k];
+        for (int r = threadIdx.x >> 3; r < NB; r += AB_ROWS_PER_PASS) {
+            const int b = b0 + r;
+            if (b < B) {
+                const uint4* srow = reinterpret_cast<const uint4*>(tile + r * LORA);
+                uint4* drow = reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) drow[seg + 8 * k] = srow[seg + 8 * k];
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tbase, 4 * AB_SLOTS);
+    if (warp == 0) tmem_dealloc(tbase, T::TMEM);
 }
 
 // one CTA of 96 threads per slot; each thread moves three 32-bit words
@@ -293,21 +321,29 @@ static int launch_absorb(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_
                          void* stream)
 {
     if (!device_ok()) return K3MLA_E_DEVICE;
-    static bool attr_set[64] = {};
-    const int smem = AB_A_BYTES + AB_B_BYTES + 1024;
+    static bool attr_set[2][64] = {};
+    const bool wide = B > 64;  // 128 slots per CTA: one CTA per head up to 128 slots
+    const int nb = wide ? 128 : 64;
+    const int smem = AB_A_BYTES + (wide ? AbTile<128>::B_BYTES : AbTile<64>::B_BYTES) + 1024;
+    const void* fn = wide ? reinterpret_cast<const void*>(k3mla_absorb_kernel<128>)
+                          : reinterpret_cast<const void*>(k3mla_absorb_kernel<64>);
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaFuncSetAttribute(k3mla_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev < 0 || dev >= 64 || !attr_set[wide][dev]) {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (dev >= 0 && dev < 64) attr_set[wide][dev] = true;
     }
     // w_kv_b viewed as (64 elements, 24576 rows of 512, 8 chunks): one box = 64 columns of W_UK[h]
     CUtensorMap tmap_w;
     const int rc = make_tmap_slab_3d(&tmap_w, w_kv_b, (uint64_t)H * WROWS_PER_HEAD, LORA, 8, NOPE, 1);
     if (rc) return rc;
-    return launch_pdl(k3mla_absorb_kernel, dim3(H, (B + AB_SLOTS - 1) / AB_SLOTS), dim3(AB_THREADS), smem,
-                      reinterpret_cast<cudaStream_t>(stream), "k3mla_absorb_kernel", tmap_w, q, q_abs, B,
-                      ap);
+    const dim3 grid(H, (B + nb - 1) / nb);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (wide)
+        return launch_pdl(k3mla_absorb_kernel<128>, grid, dim3(AB_THREADS), smem, st, "k3mla_absorb_kernel", tmap_w,
+                          q, q_abs, B, ap);
+    return launch_pdl(k3mla_absorb_kernel<64>, grid, dim3(AB_THREADS), smem, st, "k3mla_absorb_kernel", tmap_w, q,
+                      q_abs, B, ap);
 }
 
 extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, int B, void* stream)

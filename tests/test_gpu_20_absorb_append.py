@@ -16,8 +16,10 @@ from tests.helpers import bits_to_f32, row_ulp_error, ULP_TOL
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B", [1, 16, 37])
+@pytest.mark.parametrize("B", [1, 16, 37, 64, 65, 128, 200])
 def test_absorb_matches_oracle(gpu_lib, B):
+    # up to 64 slots one CTA per head covers 64 slots; above, 128 (65 and 128: one ragged and one
+    # full tile; 200: a full and a ragged tile)
     g = torch.Generator(device="cuda").manual_seed(100 + B)
     q = torch.randn(B, 96, 192, generator=g, device="cuda").to(torch.bfloat16)
     w = (torch.randn(24576, 512, generator=g, device="cuda") * (1 / 512) ** 0.5).to(torch.bfloat16)
@@ -70,11 +72,12 @@ def test_append_indexes_past_2_31_elements(gpu_lib):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("B", [6, 67])
+@pytest.mark.parametrize("B", [6, 67, 120, 150])
 def test_absorb_q_append_is_both_calls_in_one(gpu_lib, B):
     """The fused launch: q_abs bitwise equal to k3mla_absorb_q's (same kernel) and within the
     absorption bar of the oracle; the slab bitwise equal to the oracle's append, with a slot that
-    writes nothing (pos -1) and one whose page is unmapped (skipped and flagged)."""
+    writes nothing (pos -1) and one whose page is unmapped (skipped and flagged).  At 120 slots the
+    grid has 96 CTAs (one per head), so some CTAs append two rows."""
     ctx = [(7 * i * i + 3 * i) % 300 + 1 for i in range(B)]
     wl = synth.make_custom(ctx, n_layers=2, seed=300 + B, device="cuda")
     tbl = wl.block_table.copy()
