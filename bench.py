@@ -221,7 +221,9 @@ def main():
     table = torch.from_numpy(host_table).to(dev)
     ctx = torch.from_numpy(wl.ctx_len).to(dev)
     pos = torch.from_numpy(wl.pos).to(dev)
-    split = k3mla.default_split_tokens(B, max_ctx)
+    # the split planned for the batch's contexts, known on the host where the pages were claimed (the
+    # default for a batch at full length)
+    split = k3mla.split_tokens_for_contexts(wl.ctx_len, max_ctx)
     q_abs = torch.empty(B, H, ROW, dtype=torch.bfloat16, device=dev)
     out = torch.empty(L, B, H, V, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(k3mla.decode_workspace_bytes(B, max_ctx, split), dtype=torch.uint8, device=dev)

@@ -243,6 +243,24 @@ int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages,
  * once per configuration and reuses it. */
 int k3mla_default_split_tokens(int B, int max_ctx);
 
+/* A split length for a batch whose contexts the caller knows on the host (the
+ * pool that claims the pages does): ctx_host[b] for b < B, clamped to
+ * [0, max_ctx].  pegainfer PR #869 (M2 commit) reduces a context in splits and
+ * merges them in a fixed order; this picks the split length for the contexts at
+ * hand rather than for every slot at max_ctx.  It returns the shortest multiple
+ * of K3MLA_TILE whose splits that hold tokens, sum_b ceil(ctx_b / split), fit
+ * one wave of SM pairs of the current device, so the pairs that short contexts
+ * leave idle take splits of the long ones.  It returns the whole-context length
+ * (max_ctx rounded up to K3MLA_TILE, one split per slot) instead when that
+ * split already covers the longest context, or when no length fits (more slots
+ * with tokens than SM pairs).  With every context at max_ctx the result equals
+ * k3mla_default_split_tokens(B, max_ctx).  B <= 0 or max_ctx <= 0 gives
+ * K3MLA_TILE; a NULL ctx_host with B > 0 gives K3MLA_E_INVALID.  Size the
+ * workspace with k3mla_decode_workspace_bytes for the returned length.  Results
+ * are bitwise invariant only for a fixed split length, so a caller that wants
+ * padding or batch invariance keeps one length. */
+int k3mla_split_tokens_for_contexts(const int32_t* ctx_host, int B, int max_ctx);
+
 /* ---- host page pool: free-list allocator (PR #869, M1 commit) ---------------
  * n_pages == 0 sizes the pool for full coverage: n_slots * ceil(max_ctx / 64)
  * pages, so every slot can reach max_ctx.  The free list holds page ids

@@ -27,7 +27,7 @@ EXPORTS = (
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
-    "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all",
+    "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_split_tokens_for_contexts",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -58,6 +58,7 @@ def load(build_if_needed: bool = True):
             "k3mla_paged_decode": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, P, P],
                                    I),
             "k3mla_default_split_tokens": ([I, I], I),
+            "k3mla_split_tokens_for_contexts": ([P, I, I], I),
             "k3mla_pool_create": ([I, I, I, ctypes.c_uint64, ctypes.POINTER(P)], I),
             "k3mla_pool_ensure": ([P, I, I], I),
             "k3mla_pool_ensure_all": ([P, P, I], I),
@@ -241,6 +242,16 @@ def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:
 
 def default_split_tokens(B: int, max_ctx: int) -> int:
     return int(load().k3mla_default_split_tokens(B, max_ctx))
+
+
+def split_tokens_for_contexts(ctx_len, max_ctx: int) -> int:
+    """The split length for a batch whose context lengths are known on the host (a sequence or
+    array of ints, one per slot); see k3mla_split_tokens_for_contexts."""
+    ctx = np.ascontiguousarray(np.asarray(ctx_len, dtype=np.int32).reshape(-1))
+    rc = int(load().k3mla_split_tokens_for_contexts(ctx.ctypes.data_as(ctypes.c_void_p), int(ctx.size), max_ctx))
+    if rc < 0:
+        _check(rc, "k3mla_split_tokens_for_contexts")
+    return rc
 
 
 def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,

@@ -113,6 +113,10 @@ def test_ragged16_two_layers(gpu_lib):
     wl = synth.make_workload("ragged16", device="cuda", n_layers=24)
     for layer in (0, 23):
         _parity(wl, layer, name=f"ragged16_l{layer}")
+    # and at the split planned for these contexts (shorter than the default: the benchmark's launch)
+    planned = k3mla.split_tokens_for_contexts(wl.ctx_len, 4096)
+    assert planned < k3mla.default_split_tokens(16, 4096)
+    _parity(wl, 11, split=planned, max_ctx=4096, name="ragged16_planned")
     del wl
     torch.cuda.empty_cache()
 

@@ -208,3 +208,52 @@ def test_product_and_oracle_share_no_code():
         src = open(os.path.join(root, "oracle", f)).read()
         assert "paged_latent_attention_k3mla_gb300" not in src, f
         assert "k3mla.h" not in src and "csrc" not in src, f
+
+
+def _pairs():
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(0).multi_processor_count // 2
+    return 148 // 2  # the library's figure when no device answers
+
+
+def _live(ctx, split):
+    return sum(-(-max(int(c), 0) // split) for c in ctx)
+
+
+def test_split_for_contexts_matches_the_default_at_full_length():
+    for B, max_ctx in [(1, 4096), (8, 32768), (16, 4096), (64, 4096), (100, 1000), (3, 130)]:
+        assert k3mla.split_tokens_for_contexts([max_ctx] * B, max_ctx) == k3mla.default_split_tokens(B, max_ctx)
+
+
+def test_split_for_contexts_on_ragged_batches():
+    pairs, tile = _pairs(), 128
+    rng = np.random.default_rng(5)
+    for B, max_ctx in [(16, 4096), (5, 32768), (40, 8192), (2, 640)]:
+        ctx = rng.integers(1, max_ctx + 1, size=B)
+        s = k3mla.split_tokens_for_contexts(ctx, max_ctx)
+        whole = -(-max_ctx // tile) * tile
+        assert s % tile == 0 and tile <= s <= whole
+        if s < whole:  # the shortest length whose live splits fit one wave of SM pairs
+            assert _live(ctx, s) <= pairs
+            assert s == tile or _live(ctx, s - tile) > pairs
+            assert s < int(ctx.max())
+        else:  # no shorter length both fits and splits the longest context
+            shorter = [t for t in range(tile, min(whole, int(ctx.max())), tile) if _live(ctx, t) <= pairs]
+            assert not shorter
+    # one short context under a long max_ctx: a single whole-context split, not many empty ones
+    assert k3mla.split_tokens_for_contexts([100], 32768) == 32768
+    assert k3mla.split_tokens_for_contexts([0, 0, 0], 4096) == 4096
+    # more slots with tokens than SM pairs: one split per slot
+    assert k3mla.split_tokens_for_contexts([200] * (pairs + 1), 256) == 256
+    # clamping: contexts past max_ctx count as max_ctx, negative ones as empty
+    assert k3mla.split_tokens_for_contexts([10**6] * 8, 32768) == k3mla.split_tokens_for_contexts([32768] * 8, 32768)
+    assert k3mla.split_tokens_for_contexts([-5, 100], 32768) == 32768
+
+
+def test_split_for_contexts_arguments():
+    lib = k3mla.load()
+    assert lib.k3mla_split_tokens_for_contexts(None, 0, 4096) == 128
+    assert lib.k3mla_split_tokens_for_contexts(None, 3, 0) == 128
+    assert lib.k3mla_split_tokens_for_contexts(None, 3, 4096) == -1
+    assert b"ctx_host is NULL" in lib.k3mla_last_error()
