@@ -131,7 +131,13 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                              policy_evict_first());  // read once per layer
     }
     // W_UV is a layer weight no kernel of this library writes, so its load above overlaps the split
-    // kernel; the split partials, the context lengths and the outputs wait for it
+    // kernel, and so does the merge's read of the context lengths (the split kernel, which runs just
+    // before in the stream, only reads them); the split partials and the outputs wait for it
+    const int G = p.ws_olat ? 1 : MX_SLOTS / p.tile;
+    const int r = (int)threadIdx.x / (8 * G), g = ((int)threadIdx.x >> 3) % G, seg = threadIdx.x & 7;
+    int ns = 0;  // splits of slot b0 + r that hold tokens (merge path)
+    if (!p.ws_olat && b0 + r < p.B)
+        ns = (mx_ctx_effective(p.ctx_len, b0 + r, p.max_ctx, p.max_pages) + p.split - 1) / p.split;
     griddep_wait();
     griddep_launch_dependents();
     if (p.ws_olat) {
@@ -163,50 +169,60 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     } else {
         // ---- merge: thread -> (row r = slot b0 + r, split group g, segment seg); the row's 512 dims
         // are 128 float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
-        // The G = 64 / tile groups of a slot walk its splits i = g, g + G, ... side by side (so that
-        // a slot's partials arrive in ceil(ns / G) round trips, not ns), each summing in ascending
-        // i, and a fixed shuffle tree adds the groups: ((g0 + g1) + (g2 + g3)).  G depends on the
-        // launch's split count only, so a slot's result does not depend on the batch.
-        const int G = MX_SLOTS / p.tile;
-        const int r = (int)threadIdx.x / (8 * G), g = ((int)threadIdx.x >> 3) % G, seg = threadIdx.x & 7;
+        // The G = 64 / tile groups of a slot walk its splits i = g, g + G, ... side by side, each in
+        // ascending i with a running max: a split's record (m_i, l_i, best score, its token) is
+        // loaded with its partial, so a slot's splits arrive in ceil(ns / G) round trips and no pass
+        // over the records comes first.  A fixed shuffle tree then brings the groups to their common
+        // max and adds them: ((g0 + g1) + (g2 + g3)).  G depends on the launch's split count only,
+        // so a slot's result does not depend on the batch.
         const int b = b0 + r;
-        int ns = 0;
-        if (b < p.B) {
-            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
-            ns = (ctx + p.split - 1) / p.split;
-        }
         const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
         float m = -INFINITY, best = -INFINITY, l = 0.f;
         int best_t = -1;
-        for (int i = 0; i < ns; ++i) m = fmaxf(m, ml[(size_t)i * H * 4]);
-        for (int i = 0; i < ns; ++i) {  // ascending splits; the lowest t wins ties
-            const float* mi = ml + (size_t)i * H * 4;
-            l += expf(mi[0] - m) * mi[1];
-            if (mi[2] > best) {
-                best = mi[2];
-                best_t = __float_as_int(mi[3]);
-            }
-        }
-        if (p.argmax && b < p.B && g == 0 && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
         float acc[64];
 #pragma unroll
         for (int k = 0; k < 64; ++k) acc[k] = 0.f;
         for (int i = g; i < ns; i += G) {
-            const float wgt = expf(ml[(size_t)i * H * 4] - m);
+            const float4 rec = *reinterpret_cast<const float4*>(ml + (size_t)i * H * 4);
             const float4* oi = reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
+            const float mn = fmaxf(m, rec.x);
+            const float a = expf(m - mn);      // 0 before the group's first split (m = -inf)
+            const float wgt = expf(rec.x - mn);
+            l = l * a + wgt * rec.y;
+            if (rec.z > best) {  // ascending splits: the lowest t wins ties
+                best = rec.z;
+                best_t = __float_as_int(rec.w);
+            }
+            m = mn;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const float4 v = oi[seg + 8 * k];
-                acc[4 * k + 0] += wgt * v.x;
-                acc[4 * k + 1] += wgt * v.y;
-                acc[4 * k + 2] += wgt * v.z;
-                acc[4 * k + 3] += wgt * v.w;
+                acc[4 * k + 0] = acc[4 * k + 0] * a + wgt * v.x;
+                acc[4 * k + 1] = acc[4 * k + 1] * a + wgt * v.y;
+                acc[4 * k + 2] = acc[4 * k + 2] * a + wgt * v.z;
+                acc[4 * k + 3] = acc[4 * k + 3] * a + wgt * v.w;
             }
         }
         for (int o = 8; o < 8 * G; o <<= 1) {  // lanes 8 g + seg of one slot sit in one warp (8 G <= 32)
+            const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            const float bo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int to = __shfl_xor_sync(0xFFFFFFFFu, best_t, o);
+            const float mn = fmaxf(m, mo);
+            const float a = (m == mn) ? 1.f : expf(m - mn);  // a group without splits keeps m = -inf
+            l *= a;
+            l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
 #pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
+            for (int k = 0; k < 64; ++k) {
+                acc[k] *= a;
+                acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
+            }
+            if (bo > best || (bo == best && to < best_t && to >= 0)) {  // the lower token on a tie
+                best = bo;
+                best_t = to;
+            }
+            m = mn;
         }
+        if (p.argmax && b < p.B && g == 0 && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
         if (ns == 0) l = 1.f;  // empty context (or a padding row of the tile): o_lat = 0
         if (g == 0) {
             const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
