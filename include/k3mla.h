@@ -202,7 +202,8 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
  * (a positive multiple of K3MLA_TILE); each split is reduced on its own and the
  * splits are merged in a fixed order: 1, 2 or 4 split groups (by the launch's
  * split count ceil(max_ctx / split_tokens)), group g summing splits g, g + G, ...
- * in ascending order, then the groups added as ((g0 + g1) + (g2 + g3)).  Split
+ * in ascending order with a running max, then the groups brought to their
+ * common max and added as ((g0 + g1) + (g2 + g3)).  Split
  * boundaries and that order depend only on the logical position, ctx_len,
  * split_tokens and max_ctx, never on B, the page ids or the GPU, so for fixed
  * split_tokens and max_ctx the result of a slot is bitwise independent of the
@@ -227,8 +228,8 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
  * (programmatic dependent launch).  Before that kernel has completed, the split
  * kernel reads ctx_len (to size each split), so the kernel immediately before
  * this call in `stream` must not write ctx_len; q_abs, the slab and the block
- * table are read after the wait.  The merge kernel loads only w_kv_b early,
- * after the split kernel (which does not write it) has started. */
+ * table are read after the wait.  The merge kernel loads w_kv_b and reads ctx_len
+ * early, while the split kernel (which writes neither) still runs. */
 size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens);
 int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
                        int layer, const int32_t* block_table, int max_pages_per_slot,
