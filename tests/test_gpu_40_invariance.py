@@ -31,14 +31,13 @@ def test_page_permutation_is_bitwise_invisible(gpu_lib):
     assert np.array_equal(base["out"], r["out"]) and np.array_equal(base["argmax"], r["argmax"])
 
 
-def test_padding_slots_leave_real_slots_bitwise_unchanged(gpu_lib):
-    wl = _wl()
-    base = gpu_layer(wl, 0, split=SPLIT, max_ctx=MAXC)
-    # interleave padding rows: all -1 tables (context drawn like the rest) and empty ones
+def _padded(wl, n_pad=1, n_empty=1):
+    """The workload with padding rows interleaved: before each real slot n_pad rows with all -1
+    tables (context drawn like the rest), after it n_empty rows with empty contexts."""
     B = wl.B
     order = []
     for b in range(B):
-        order += [("pad", 500 + b), ("real", b), ("empty", 0)]
+        order += [("pad", 500 + b + 37 * k) for k in range(n_pad)] + [("real", b)] + [("empty", 0)] * n_empty
     tbl = np.full((len(order), wl.block_table.shape[1]), -1, np.int32)
     ctx = np.zeros(len(order), np.int32)
     idx = []
@@ -57,12 +56,23 @@ def test_padding_slots_leave_real_slots_bitwise_unchanged(gpu_lib):
     big = synth.Workload(name="padded", seed=0, n_layers=1, B=len(order), ctx_len=ctx, block_table=tbl,
                          n_pages=wl.n_pages, device="cuda", q=q_big, w_kv_b=wl.w_kv_b, slab=wl.slab,
                          new_c=wl.new_c, new_rope=wl.new_rope)
-    r = gpu_layer(big, 0, split=SPLIT, max_ctx=MAXC)
+    empty_rows = [i for i, (k, _) in enumerate(order) if k == "empty"]
+    pad_rows = [i for i, (k, _) in enumerate(order) if k == "pad"]
+    return big, real_rows, idx, empty_rows, pad_rows
+
+
+@pytest.mark.parametrize("split,n_pad,n_empty", [(SPLIT, 1, 1), (MAXC, 5, 6)])
+def test_padding_slots_leave_real_slots_bitwise_unchanged(gpu_lib, split, n_pad, n_empty):
+    # (MAXC, 5, 6): one split per slot and 72 rows, so the padded batch's absorption runs with 128
+    # slots per CTA and its expansion over two 64-slot tiles, while the 6 slots fit one of each
+    wl = _wl()
+    base = gpu_layer(wl, 0, split=split, max_ctx=MAXC)
+    big, real_rows, idx, empty_rows, pad_rows = _padded(wl, n_pad, n_empty)
+    assert (big.B > 64) == (n_pad + n_empty + 1 > 10)
+    r = gpu_layer(big, 0, split=split, max_ctx=MAXC)
     assert np.array_equal(r["out"][real_rows], base["out"][idx])
     assert np.array_equal(r["argmax"][real_rows], base["argmax"][idx])
-    empty_rows = [i for i, (k, _) in enumerate(order) if k == "empty"]
     assert np.all(r["out"][empty_rows] == 0) and np.all(r["argmax"][empty_rows] == -1)
-    pad_rows = [i for i, (k, _) in enumerate(order) if k == "pad"]
     assert np.all(r["out"][pad_rows] == 0) and np.all(r["argmax"][pad_rows] == 0)
 
 
