@@ -14,13 +14,17 @@ JSON line fields beyond the usual ones:
   value            us per layer-call (24-layer step replayed as a CUDA graph / 24)
   latent_gbs       latent bytes read per layer-call / time
   roofline         the paged-decode call (split decode + merge/expand kernels):
-                   algorithmic bytes / its event-timed duration vs measured HBM
+                   algorithmic bytes / its device time (24 decode calls in one
+                   CUDA graph, timed with events, / 24) vs measured HBM
   layer_roofline   the same for the whole layer-call (append + absorb + decode)
   e2e              the same metric through the C ABI with host buffers: pinned
                    H2D of the step's q / new rows / tables and D2H of the outputs
                    inside the timed region (host page claims, then the step's
                    copies and kernels replayed as one CUDA graph)
-  cpu_baseline     the CPU oracle on a bounded sample of the workload
+  cpu_baseline     the CPU oracle on a bounded sample of the workload (all host
+                   threads, and one thread)
+  workloads        long8, ragged16 and padding128 under the default per-slot
+                   split (and ragged16 under the opt-in batch-planned split)
 """
 from __future__ import annotations
 
@@ -80,13 +84,11 @@ class Clocks:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
-        time.sleep(0.3)
         return self
 
     def __exit__(self, *a):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.2)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -126,17 +128,10 @@ def alg_flops(wl):
     return n * H * 2 * (ROW + LORA) + 2 * 2 * wl.B * H * 128 * LORA
 
 
-def cpu_baseline(wl, layers=None, n_slots=None):
-    """The oracle (as it stands) on a bounded sample: n_slots slots of each of the listed layers
-    (by default all slots of up to 8 layers, about 10 s of CPU work on 16 cores)."""
+def _oracle_sample(wl, layers, slots, nthreads):
+    """Seconds the oracle (absorption + decode chain, as it stands) takes for the listed slots of the
+    listed layers, on `nthreads` host threads."""
     import oracle
-    B = wl.B
-    if n_slots is None:
-        n_slots = B if int(wl.ctx_len.max()) <= 4096 else 2
-    if layers is None:
-        layers = list(range(min(wl.n_layers, 8)))
-    slots = list(range(n_slots))
-    ncores = os.cpu_count() or 1
     tbl = wl.block_table[slots]
     used = sorted(set(int(x) for x in tbl.ravel() if x >= 0))
     remap = {p: i for i, p in enumerate(used)}
@@ -149,12 +144,42 @@ def cpu_baseline(wl, layers=None, n_slots=None):
         w = synth.bf16_bits(wl.w_kv_b[layer])
         t0 = time.perf_counter()
         qa = oracle.absorb(q, w)
-        oracle.decode(qa, slab, 0, t2, wl.ctx_len[slots].astype(np.int32), w, wl.scale_bits, nthreads=ncores)
+        oracle.decode(qa, slab, 0, t2, wl.ctx_len[slots].astype(np.int32), w, wl.scale_bits, nthreads=nthreads)
         dt += time.perf_counter() - t0
-    us_per_layer = dt * 1e6 / len(layers) * (B / n_slots)
-    return {"value": us_per_layer, "unit": "us/layer-call", "cores": ncores, "kind": "oracle",
+    return dt
+
+
+def cpu_baseline(wl):
+    """The oracle (as it stands) on a bounded sample of the workload: all slots of up to 8 layers on
+    every host core (about 10 s), and 2 slots of one layer on one thread; both scaled to one
+    layer-call of the whole batch."""
+    B = wl.B
+    ncores = os.cpu_count() or 1
+    n_slots = B if int(wl.ctx_len.max()) <= 4096 else 2
+    layers = list(range(min(wl.n_layers, 8)))
+    dt = _oracle_sample(wl, layers, list(range(n_slots)), ncores)
+    us = dt * 1e6 / len(layers) * (B / n_slots)
+    n1 = min(B, 2)
+    dt1 = _oracle_sample(wl, [0], list(range(n1)), 1)
+    us1 = dt1 * 1e6 * (B / n1)
+    return {"value": us, "unit": "us/layer-call", "cores": ncores, "kind": "oracle",
             "sample": f"{n_slots} of {B} slots x {len(layers)} layer-call(s) (absorb + decode chain), "
-                      f"{dt:.2f} s wall on {ncores} threads, scaled to one {B}-slot layer-call"}
+                      f"{dt:.2f} s wall on {ncores} threads, scaled to one {B}-slot layer-call",
+            "single_thread": {"value": us1, "unit": "us/layer-call", "cores": 1,
+                              "sample": f"{n1} of {B} slots x 1 layer-call, {dt1:.2f} s wall on 1 thread, "
+                                        f"scaled to one {B}-slot layer-call"}}
+
+
+def config_for(name, wl, split, layers=None):
+    """The bench line's config (both arms print the same dict for the same workload)."""
+    L = wl.n_layers
+    return {"workload": WORKLOAD_DESC[name] if layers is None else f"{WORKLOAD_DESC[name]}, first {L} layer(s) only",
+            "slots": wl.B, "layers": L, "context_tokens": int(wl.ctx_len.max()),
+            "split_tokens": "auto (per slot: ceil(ctx/4096) equal splits)" if split == 0 else split,
+            "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)"
+                  if name in ("steady64", "long8") else "per-layer inputs may be L2-resident",
+            "timing": "24-layer step as one CUDA graph (each layer's append carried by its absorption's launch), "
+                      "CUDA events on the launch stream"}
 
 
 def run_reference(args):
@@ -162,24 +187,260 @@ def run_reference(args):
     if rank != 0:
         return
     wl = synth.make_workload(args.workload, device="cuda" if torch.cuda.is_available() else "cpu")
-    n_slots = min(wl.B, 4 if int(wl.ctx_len.max()) <= 4096 else 1)
+    ncores = os.cpu_count() or 1
+    n_slots = min(wl.B, 16 if int(wl.ctx_len.max()) <= 4096 else 1)
+    slots = list(range(n_slots))
     for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; kept for the contract's shape
-    vals = []
-    cb = None
+        pass  # the oracle keeps no state between calls; nothing to warm
+    step_s = []
     for _ in range(args.steps):
-        cb = cpu_baseline(wl, [0], n_slots)
-        vals.append(cb["value"])
-    v = statistics.mean(vals)
+        step_s.append(_oracle_sample(wl, [0], slots, ncores))   # one step: the sample below, timed
+    ms_step = statistics.mean(step_s) * 1e3
+    v = ms_step * 1e3 * (wl.B / n_slots)   # us per layer-call of the whole batch
+    sample = (f"{n_slots} of {wl.B} slots x 1 layer-call (absorb + decode chain) per step, on {ncores} threads; "
+              f"value scales the measured step by {wl.B}/{n_slots} slots to one {wl.B}-slot layer-call")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/layer-call",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v * wl.n_layers / 1e3,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC[args.workload], "slots": wl.B, "layers": wl.n_layers},
-            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": v,
+            "data": "synthetic", "config": config_for(args.workload, wl, 0, args.layers),
+            "step_is_sample": {"slots": n_slots, "layers": 1,
+                               "scale_to_layer_call": wl.B / n_slots,
+                               "scaled_ms_per_full_step": v * wl.n_layers / 1e3},
+            "cpu_baseline": {"kind": "oracle", "cores": ncores, "sample": sample, "value": v,
                              "unit": "us/layer-call"},
             "e2e": {"value": v, "unit": "us/layer-call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+class Runner:
+    """One workload resident on the device, the hot path captured as CUDA graphs: the 24-layer step
+    (absorption carrying the append, then the paged decode, per layer) and the paged-decode calls
+    alone (24 calls), each replayed and timed with CUDA events on the launch stream."""
+
+    def __init__(self, name, split, layers=None):
+        from paged_latent_attention_k3mla_gb300 import k3mla
+        self.k3mla = k3mla
+        dev = "cuda"
+        self.name = name
+        self.wl = wl = synth.make_workload(name, device=dev, n_layers=layers)
+        self.B, self.L = wl.B, wl.n_layers
+        self.max_ctx = MAX_CTX[name]
+        # a1: page claims from the host free-list pool (shuffled), table to the device
+        self.pool = k3mla.Pool(n_slots=self.B, max_ctx=self.max_ctx, n_pages=wl.n_pages, shuffle_seed=wl.seed + 1)
+        for b in range(self.B):
+            rc = self.pool.ensure(b, int(wl.ctx_len[b]))
+            assert rc == 0, rc
+        self.host_table = self.pool.table()
+        self.table = torch.from_numpy(self.host_table).to(dev)
+        self.ctx = torch.from_numpy(wl.ctx_len).to(dev)
+        self.pos = torch.from_numpy(wl.pos).to(dev)
+        self.split = split
+        self.q_abs = torch.empty(self.B, H, ROW, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(self.L, self.B, H, V, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(k3mla.decode_workspace_bytes(self.B, self.max_ctx, split), dtype=torch.uint8,
+                              device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream()
+
+    def absorb_append(self, layer, q, c, r):
+        # a2 + a3 in one launch: the append rides on the absorption's grid (neither reads the other)
+        wl = self.wl
+        self.k3mla.absorb_q_append(q, wl.w_kv_b[layer], self.q_abs, wl.slab, layer, self.table, self.pos, c, r,
+                                   dev_err=self.err, stream=self.stream)
+
+    def decode(self, layer):
+        wl = self.wl
+        self.k3mla.paged_decode(self.q_abs, wl.slab, layer, self.table, self.ctx, wl.w_kv_b[layer], wl.scale_bits,
+                                self.out[layer], self.ws, self.max_ctx, self.split, dev_err=self.err,
+                                stream=self.stream)
+
+    def step(self):
+        wl = self.wl
+        for layer in range(self.L):
+            self.absorb_append(layer, wl.q[layer], wl.new_c[layer], wl.new_rope[layer])
+            self.decode(layer)
+
+    def decode_calls(self):
+        for layer in range(self.L):
+            self.decode(layer)
+
+    def _graph(self, fn):
+        with torch.cuda.stream(self.stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        return g
+
+    def _load(self, g, seconds):
+        """Untimed replays for about `seconds` (keeps the GPU under this load while clocks are sampled)."""
+        t0 = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            while time.perf_counter() - t0 < seconds:
+                for _ in range(8):
+                    g.replay()
+                torch.cuda.synchronize()
+
+    def _time_graph(self, g, steps, warmup, clocks=None):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ctx = clocks if clocks is not None else _Null()
+        with ctx:
+            if clocks is not None:
+                self._load(g, 0.5)      # the clock samples before the timed region see the same load
+            torch.cuda.synchronize()
+            ev0.record(self.stream)
+            with torch.cuda.stream(self.stream):
+                for _ in range(steps):
+                    g.replay()
+            ev1.record(self.stream)
+            torch.cuda.synchronize()
+            if clocks is not None:
+                self._load(g, 0.5)
+        return ev0.elapsed_time(ev1) / steps
+
+    def measure(self, steps, warmup, clocks=None):
+        """ms per 24-layer step, and ms per paged-decode call (24 decode calls in one graph)."""
+        g_step = self._graph(self.step)
+        ms_step = self._time_graph(g_step, steps, warmup, clocks)
+        assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        g_dec = self._graph(self.decode_calls)
+        ms_dec = self._time_graph(g_dec, steps, warmup) / self.L
+        assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        del g_step, g_dec
+        return ms_step, ms_dec
+
+    def figures(self, ms_step, ms_dec, hbm):
+        ab = alg_bytes(self.wl)
+        us_layer = ms_step * 1e3 / self.L
+        return {"us_per_layer_call": round(us_layer, 3), "decode_call_us": round(ms_dec * 1e3, 3),
+                "decode_hbm_frac": round(ab["decode"] / (ms_dec * 1e-3) / 1e9 / hbm, 4),
+                "layer_hbm_frac": round(ab["layer"] / (us_layer * 1e-6) / 1e9 / hbm, 4),
+                "latent_gbs": round(ab["latent"] / (us_layer * 1e-6) / 1e9, 1)}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def e2e_leg(run, steps, warmup):
+    """The same step through the C ABI with host buffers: every step's inputs copied in from pinned
+    host memory and every layer's output read back inside the timed region (host page claims and
+    table refresh first, then one CUDA graph holding the copies -- on a copy stream, layer by layer,
+    overlapping the compute -- and the 24 layer-calls)."""
+    wl, L, stream = run.wl, run.L, run.stream
+    q_all, c_all, r_all = wl.q, wl.new_c, wl.new_rope
+    q_h = q_all.cpu().pin_memory()
+    c_h = c_all.cpu().pin_memory()
+    r_h = r_all.cpu().pin_memory()
+    pos_h = torch.from_numpy(wl.pos).pin_memory()
+    ctx_h = torch.from_numpy(wl.ctx_len).pin_memory()
+    out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    q_d, c_d, r_d = torch.empty_like(q_all), torch.empty_like(c_all), torch.empty_like(r_all)
+    h2d = (q_h.numel() + c_h.numel() + r_h.numel()) * 2 + (pos_h.numel() + ctx_h.numel()) * 4 + run.host_table.nbytes
+    d2h = out_h.numel() * 2
+    tbl_pin = torch.from_numpy(run.host_table.copy()).pin_memory()
+    copy_s = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(L)]
+    # the compute stream waits for its inputs once per group of layers, the groups doubling (1, 1,
+    # 2, 4, 8, ...) so that each group's copies finish while the layers before it compute; a wait on
+    # another stream costs the overlap of the kernels around it, so fewer waits are cheaper
+    first_of_group, start, size = {}, 0, 1
+    while start < L:
+        end = min(L, start + size)
+        first_of_group[start] = end - 1             # wait for the last copy of the group
+        start, size = end, (size if start == 0 else 2 * size)
+    ev_dec = [torch.cuda.Event() for _ in range(L)]
+    ev_out, ev_start = torch.cuda.Event(), torch.cuda.Event()
+
+    def e2e_device_step():
+        with torch.cuda.stream(stream):
+            run.table.copy_(tbl_pin, non_blocking=True)
+            run.pos.copy_(pos_h, non_blocking=True)
+            run.ctx.copy_(ctx_h, non_blocking=True)
+        ev_start.record(stream)                 # everything before (the previous step) is done
+        copy_s.wait_event(ev_start)
+        with torch.cuda.stream(copy_s):
+            for layer in range(L):
+                q_d[layer].copy_(q_h[layer], non_blocking=True)
+                c_d[layer].copy_(c_h[layer], non_blocking=True)
+                r_d[layer].copy_(r_h[layer], non_blocking=True)
+                ev_in[layer].record(copy_s)
+        for layer in range(L):
+            if layer in first_of_group:             # the inputs of this group of layers have landed
+                stream.wait_event(ev_in[first_of_group[layer]])
+            with torch.cuda.stream(stream):
+                run.absorb_append(layer, q_d[layer], c_d[layer], r_d[layer])
+                run.decode(layer)
+                ev_dec[layer].record(stream)
+            copy_s.wait_event(ev_dec[layer])
+            with torch.cuda.stream(copy_s):
+                out_h[layer].copy_(run.out[layer], non_blocking=True)
+        ev_out.record(copy_s)
+        stream.wait_event(ev_out)
+
+    with torch.cuda.stream(stream):
+        e2e_device_step()
+    torch.cuda.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_device_step()
+
+    def e2e_step():
+        rc = run.pool.ensure_all(wl.ctx_len)    # a1: claims on 64-token boundaries (none in steady state)
+        assert rc == 0, rc
+        t_now = run.pool.table()
+        if not np.array_equal(t_now, tbl_pin.numpy()):
+            stream.synchronize()
+            tbl_pin.numpy()[:] = t_now
+        with torch.cuda.stream(stream):
+            e2e_graph.replay()
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / steps
+    digest = hashlib.sha256(out_h.view(torch.int16).numpy().tobytes()).hexdigest()[:16]
+    return e2e_ms, int(h2d), int(d2h), digest
+
+
+def extra_workloads(hbm, steps, warmup):
+    """The other configurations' figures (parity cases, not the bench's value): each as its own
+    24-layer CUDA-graph step under the default per-slot split, and the ragged batch also under the
+    opt-in batch-planned split (whose numerics depend on the batch)."""
+    from paged_latent_attention_k3mla_gb300 import k3mla
+    res = {}
+    for name, split_kind in (("long8", "auto"), ("ragged16", "auto"), ("ragged16", "planned"),
+                             ("padding128", "auto")):
+        split = 0
+        if split_kind == "planned":
+            wl0 = synth.make_workload(name, device="cpu", n_layers=1)
+            split = k3mla.batch_planned_split_tokens(wl0.ctx_len, MAX_CTX[name])
+        run = Runner(name, split)
+        ms_step, ms_dec = run.measure(steps, warmup)
+        fig = run.figures(ms_step, ms_dec, hbm)
+        fig["split_tokens"] = "auto" if split == 0 else split
+        fig["layers"] = run.L
+        if split_kind == "planned":
+            fig["numerics"] = "batch-dependent (opt-in k3mla_batch_planned_split_tokens)"
+        res[name if split_kind == "auto" else f"{name}_planned"] = fig
+        del run
+        torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -191,6 +452,8 @@ def main():
     ap.add_argument("--workload", default="steady64", choices=list(WORKLOAD_DESC))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-next", action="store_true", help="skip the page-copy / chunked-prefill figures")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads' figures")
+    ap.add_argument("--split", type=int, default=0, help="split_tokens (0: the default per-slot rule)")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling aid: fewer layers of the same per-layer workload")
     args = ap.parse_args()
@@ -208,174 +471,16 @@ def main():
     from paged_latent_attention_k3mla_gb300 import k3mla
     torch.cuda.set_device(0)
     k3mla.load()
-    dev = "cuda"
-    wl = synth.make_workload(args.workload, device=dev, n_layers=args.layers)
-    B, L = wl.B, wl.n_layers
-    max_ctx = MAX_CTX[args.workload]
-    # a1: page claims from the host free-list pool (shuffled), table to the device
-    pool = k3mla.Pool(n_slots=B, max_ctx=max_ctx, n_pages=wl.n_pages, shuffle_seed=wl.seed + 1)
-    for b in range(B):
-        rc = pool.ensure(b, int(wl.ctx_len[b]))
-        assert rc == 0, rc
-    host_table = pool.table()
-    table = torch.from_numpy(host_table).to(dev)
-    ctx = torch.from_numpy(wl.ctx_len).to(dev)
-    pos = torch.from_numpy(wl.pos).to(dev)
-    # the split planned for the batch's contexts, known on the host where the pages were claimed (the
-    # default for a batch at full length)
-    split = k3mla.split_tokens_for_contexts(wl.ctx_len, max_ctx)
-    q_abs = torch.empty(B, H, ROW, dtype=torch.bfloat16, device=dev)
-    out = torch.empty(L, B, H, V, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(k3mla.decode_workspace_bytes(B, max_ctx, split), dtype=torch.uint8, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    q_all, c_all, r_all = wl.q, wl.new_c, wl.new_rope
-    stream = torch.cuda.Stream()
-
-    def absorb_append(layer, q, c, r):
-        # a2 + a3 in one launch: the append rides on the absorption's grid (neither reads the other)
-        k3mla.absorb_q_append(q, wl.w_kv_b[layer], q_abs, wl.slab, layer, table, pos, c, r, dev_err=err,
-                              stream=stream)
-
-    def layer_call(layer, dec_events=None):
-        absorb_append(layer, q_all[layer], c_all[layer], r_all[layer])
-        if dec_events is not None:
-            dec_events[0].record(stream)
-        k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer], ws,
-                           max_ctx, split, dev_err=err, stream=stream)
-        if dec_events is not None:
-            dec_events[1].record(stream)
-
-    def step():
-        for layer in range(L):
-            layer_call(layer)
-
-    # ---- device-timed: the 24-layer step as one CUDA graph ----
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks() as clk:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(args.steps):
-                graph.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
-    ms_per_step = ms_total / args.steps
-    us_per_layer = ms_per_step * 1e3 / L
-    assert err.item() == 0, f"device error bits {err.item()}"
-
-    # ---- the dominant call alone: paged decode (split decode + merge/expand) ----
-    pairs = []
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            layer_call(0)
-        for i in range(args.steps):
-            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            layer_call(i % L, e)
-            pairs.append(e)
-    torch.cuda.synchronize()
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
-
-    # ---- end to end through the C ABI with host buffers ----
-    q_h = q_all.cpu().pin_memory()
-    c_h = c_all.cpu().pin_memory()
-    r_h = r_all.cpu().pin_memory()
-    pos_h = torch.from_numpy(wl.pos).pin_memory()
-    ctx_h = torch.from_numpy(wl.ctx_len).pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d, c_d, r_d = torch.empty_like(q_all), torch.empty_like(c_all), torch.empty_like(r_all)
-    h2d = (q_h.numel() + c_h.numel() + r_h.numel()) * 2 + (pos_h.numel() + ctx_h.numel()) * 4 + host_table.nbytes
-    d2h = out_h.numel() * 2
-
-    tbl_pin = torch.from_numpy(host_table.copy()).pin_memory()
-
-    # inputs stream in layer by layer on a copy stream while earlier layers compute, and each
-    # layer's output is read back as soon as its decode is done
-    copy_s = torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(L)]
-    # the compute stream waits for its inputs once per group of layers, the groups doubling (1, 1,
-    # 2, 4, 8, ...) so that each group's copies finish while the layers before it compute; a wait on
-    # another stream costs the overlap of the kernels around it, so fewer waits are cheaper
-    first_of_group, start, size = {}, 0, 1
-    while start < L:
-        end = min(L, start + size)
-        first_of_group[start] = end - 1             # wait for the last copy of the group
-        start, size = end, (size if start == 0 else 2 * size)
-    ev_dec = [torch.cuda.Event() for _ in range(L)]
-    ev_out, ev_start = torch.cuda.Event(), torch.cuda.Event()
-
-    def e2e_device_step():
-        with torch.cuda.stream(stream):
-            table.copy_(tbl_pin, non_blocking=True)
-            pos.copy_(pos_h, non_blocking=True)
-            ctx.copy_(ctx_h, non_blocking=True)
-        ev_start.record(stream)                 # everything before (the previous step) is done
-        copy_s.wait_event(ev_start)
-        with torch.cuda.stream(copy_s):
-            for layer in range(L):
-                q_d[layer].copy_(q_h[layer], non_blocking=True)
-                c_d[layer].copy_(c_h[layer], non_blocking=True)
-                r_d[layer].copy_(r_h[layer], non_blocking=True)
-                ev_in[layer].record(copy_s)
-        for layer in range(L):
-            if layer in first_of_group:             # the inputs of this group of layers have landed
-                stream.wait_event(ev_in[first_of_group[layer]])
-            with torch.cuda.stream(stream):
-                absorb_append(layer, q_d[layer], c_d[layer], r_d[layer])
-                k3mla.paged_decode(q_abs, wl.slab, layer, table, ctx, wl.w_kv_b[layer], wl.scale_bits, out[layer],
-                                   ws, max_ctx, split, dev_err=err, stream=stream)
-                ev_dec[layer].record(stream)
-            copy_s.wait_event(ev_dec[layer])
-            with torch.cuda.stream(copy_s):
-                out_h[layer].copy_(out[layer], non_blocking=True)
-        ev_out.record(copy_s)
-        stream.wait_event(ev_out)
-
-    # the device part of a step (copies in, 24 layer-calls, copies out) as one CUDA graph; the host
-    # part (page claims, table refresh) runs before every replay
-    with torch.cuda.stream(stream):
-        e2e_device_step()
-    torch.cuda.synchronize()
-    e2e_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(e2e_graph, stream=stream):
-        e2e_device_step()
-
-    def e2e_step():
-        rc = pool.ensure_all(wl.ctx_len)        # a1: claims on 64-token boundaries (none in steady state)
-        assert rc == 0, rc
-        t_now = pool.table()
-        if not np.array_equal(t_now, tbl_pin.numpy()):
-            stream.synchronize()
-            tbl_pin.numpy()[:] = t_now
-        with torch.cuda.stream(stream):
-            e2e_graph.replay()
-
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / args.steps
-    digest = hashlib.sha256(out_h.view(torch.int16).numpy().tobytes()).hexdigest()[:16]
-
     hbm, tflops, src = peaks()
-    nxt = None if args.no_next else next_rows(wl, table, max_ctx, stream, hbm, tflops)
+    run = Runner(args.workload, args.split, args.layers)
+    wl, L, B = run.wl, run.L, run.B
+    clk = Clocks()
+    ms_step, ms_dec = run.measure(args.steps, args.warmup, clocks=clk)
+    us_per_layer = ms_step * 1e3 / L
+    e2e_ms, h2d, d2h, digest = e2e_leg(run, args.steps, args.warmup)
+    nxt = None if args.no_next else next_rows(wl, run.table, run.max_ctx, run.stream, hbm, tflops)
     ab = alg_bytes(wl)
-    dec_gbs = ab["decode"] / (dec_ms * 1e-3) / 1e9
+    dec_gbs = ab["decode"] / (ms_dec * 1e-3) / 1e9
     layer_gbs = ab["layer"] / (us_per_layer * 1e-6) / 1e9
     flops = alg_flops(wl)
     traffic = None
@@ -388,32 +493,33 @@ def main():
         except (ValueError, OSError):
             traffic = None
     cpu = None if args.no_cpu else cpu_baseline(wl)
+    cfg = config_for(args.workload, wl, args.split, args.layers)
+    del run, wl
+    torch.cuda.empty_cache()
+    extra = None if args.no_extra or args.layers is not None else extra_workloads(hbm, min(args.steps, 20), 3)
     line = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": "us/layer-call", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload] if args.layers is None else
-                   f"{WORKLOAD_DESC[args.workload]}, first {L} layer(s) only", "slots": B, "layers": L,
-                   "context_tokens": int(wl.ctx_len.max()), "split_tokens": split,
-                   "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)",
-                   "timing": "24-layer step as one CUDA graph (each layer's append carried by its absorption's launch), "
-                             "CUDA events on the launch stream"},
+        "data": "synthetic", "config": cfg,
         "latent_gbs": round(ab["latent"] / (us_per_layer * 1e-6) / 1e9, 1),
         "roofline": {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
-                     "traffic": traffic, "alg_bytes_per_call": ab["decode"], "avg_call_us": round(dec_ms * 1e3, 3),
+                     "traffic": traffic, "alg_bytes_per_call": ab["decode"], "avg_call_us": round(ms_dec * 1e3, 3),
+                     "timing": f"{L} paged-decode calls in one CUDA graph, replayed; CUDA events on the launch "
+                               f"stream; per call = graph time / {L}",
                      "peak_source": f"{src} hbm_gbs"},
         "layer_roofline": {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": hbm, "unit": "GB/s",
                            "frac": round(layer_gbs / hbm, 4), "alg_bytes_per_layer_call": ab["layer"],
                            "tensor_frac": round(flops / (us_per_layer * 1e-6) / 1e12 / tflops, 4),
                            "tensor_peak_tflops": tflops},
-        "e2e": {"value": round(e2e_ms * 1e3 / L, 3), "unit": "us/layer-call", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+        "e2e": {"value": round(e2e_ms * 1e3 / L, 3), "unit": "us/layer-call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * L * 3,   # absorb+append, split decode, merge/expand per layer
         "clocks": clk.summary(),
         "out_sha256_16": digest,
         "cpu_baseline": cpu,
+        "workloads": extra,
         "next_rows": nxt,
     }
     print(json.dumps(line))
@@ -465,7 +571,7 @@ def next_rows(wl, table, max_ctx, stream, hbm, tflops):
     c = torch.randn(R, 512, generator=g, device=dev).to(torch.bfloat16)
     r = torch.randn(R, 64, generator=g, device=dev).to(torch.bfloat16)
     q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device=dev)
-    split = k3mla.default_split_tokens(R, max_ctx)
+    split = k3mla.SPLIT_AUTO
     ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device=dev)
     out = torch.empty(R, H, V, dtype=torch.bfloat16, device=dev)
 

@@ -27,7 +27,7 @@
  *   - "device" pointers are CUDA device memory owned by the caller; the library
  *     never allocates, frees or synchronises device memory, so every device
  *     call other than k3mla_paged_decode_noalloc can be captured into a CUDA
- *     graph.  `stream` is a cudaStream_t
+ *     graph (nothing is stated here for that one).  `stream` is a cudaStream_t
  *     (NULL = the legacy default stream).
  *   - Return value: K3MLA_OK (0) or a negative K3MLA_E_* code.  Argument errors
  *     are detected on the host before anything is launched.  A launch failure
@@ -57,6 +57,8 @@ extern "C" {
 #define K3MLA_PAGE 64
 #define K3MLA_ROW 576
 #define K3MLA_TILE 128 /* tokens per decode tile; split_tokens must be a multiple */
+#define K3MLA_SPLIT_AUTO 0     /* split_tokens: the default per-slot rule (see k3mla_paged_decode) */
+#define K3MLA_SPLIT_MAX 4096   /* longest split of the default rule, in tokens */
 
 #define K3MLA_OK 0
 #define K3MLA_E_INVALID (-1)   /* bad pointer, size or alignment */
@@ -198,16 +200,21 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
  * (PR #869, M2 commit.)  Rows at positions >= n are never used, whatever they
  * hold.  n == 0 gives out = 0 and argmax -1.
  *
- * The context of each slot is cut into splits of split_tokens logical tokens
- * (a positive multiple of K3MLA_TILE); each split is reduced on its own and the
- * splits are merged in a fixed order: 1, 2 or 4 split groups (by the launch's
- * split count ceil(max_ctx / split_tokens)), group g summing splits g, g + G, ...
- * in ascending order with a running max, then the groups brought to their
- * common max and added as ((g0 + g1) + (g2 + g3)).  Split
- * boundaries and that order depend only on the logical position, ctx_len,
- * split_tokens and max_ctx, never on B, the page ids or the GPU, so for fixed
- * split_tokens and max_ctx the result of a slot is bitwise independent of the
- * other slots in the batch, of padding slots and of which physical pages hold it.
+ * Splits.  The context of each slot is cut into splits; each split is reduced on
+ * its own and a slot's splits are merged in a fixed order.  How a slot is cut is
+ * a function of its own n and of split_tokens only:
+ *   - split_tokens == K3MLA_SPLIT_AUTO (0), the default: ceil(n / K3MLA_SPLIT_MAX)
+ *     splits of equal length, rounded up to a multiple of K3MLA_TILE
+ *     (k3mla_slot_split_tokens gives the length);
+ *   - split_tokens > 0 (a multiple of K3MLA_TILE): a split every split_tokens
+ *     tokens.
+ * A slot with one split (or none) lands its o_lat directly.  A slot with several
+ * is merged by four split groups -- group g sums splits g, g + 4, g + 8, ... in
+ * ascending order with a running max -- and the groups are then brought to their
+ * common max and added as ((g0 + g1) + (g2 + g3)).  Neither the cut nor the merge
+ * depends on B, max_ctx, the other slots, the page ids or the GPU, so for a given
+ * split_tokens a slot's result is bitwise independent of the batch it is in, of
+ * padding slots and of which physical pages hold it.
  *
  * q_abs       device [B][96][576] bf16 (from k3mla_absorb_q)
  * slab        device [n_pages][n_layers][64][576] bf16; n_pages*n_layers*64 < 2^31
@@ -226,10 +233,11 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
  * Runs as two kernels on `stream`: the split decode, then the merge + W_UV
  * expansion.  Both may start while the kernel before them is still running
  * (programmatic dependent launch).  Before that kernel has completed, the split
- * kernel reads ctx_len (to size each split), so the kernel immediately before
- * this call in `stream` must not write ctx_len; q_abs, the slab and the block
- * table are read after the wait.  The merge kernel loads w_kv_b and reads ctx_len
- * early, while the split kernel (which writes neither) still runs. */
+ * kernel reads ctx_len (to cut each slot), so the kernel immediately before
+ * this call in `stream` must not write ctx_len; q_abs, the slab, the block table
+ * and the workspace are read or written only after the wait.  The merge kernel
+ * loads w_kv_b and reads ctx_len early, while the split kernel (which writes
+ * neither) still runs. */
 size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens);
 int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
                        int layer, const int32_t* block_table, int max_pages_per_slot,
@@ -237,30 +245,26 @@ int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages,
                        uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes,
                        int B, int max_ctx, int split_tokens, int32_t* dev_err, void* stream);
 
-/* A split length for a batch of B slots with contexts up to max_ctx on the
- * current device: the smallest multiple of K3MLA_TILE that keeps the number of
- * splits within one wave of SM pairs.  Results are bitwise invariant only for a
- * FIXED split length, so a caller that wants padding invariance computes this
- * once per configuration and reuses it. */
-int k3mla_default_split_tokens(int B, int max_ctx);
+/* The split length a slot of context ctx gets from k3mla_paged_decode:
+ * split_tokens when it is positive, else the default rule's length (at most
+ * K3MLA_SPLIT_MAX; K3MLA_TILE for ctx <= 0).  The slot then has
+ * ceil(ctx / length) splits.  A host-side helper: it touches no GPU. */
+int k3mla_slot_split_tokens(int ctx, int split_tokens);
 
-/* A split length for a batch whose contexts the caller knows on the host (the
- * pool that claims the pages does): ctx_host[b] for b < B, clamped to
- * [0, max_ctx].  pegainfer PR #869 (M2 commit) reduces a context in splits and
- * merges them in a fixed order; this picks the split length for the contexts at
- * hand rather than for every slot at max_ctx.  It returns the shortest multiple
- * of K3MLA_TILE whose splits that hold tokens, sum_b ceil(ctx_b / split), fit
- * one wave of SM pairs of the current device, so the pairs that short contexts
- * leave idle take splits of the long ones.  It returns the whole-context length
- * (max_ctx rounded up to K3MLA_TILE, one split per slot) instead when that
- * split already covers the longest context, or when no length fits (more slots
- * with tokens than SM pairs).  With every context at max_ctx the result equals
- * k3mla_default_split_tokens(B, max_ctx).  B <= 0 or max_ctx <= 0 gives
- * K3MLA_TILE; a NULL ctx_host with B > 0 gives K3MLA_E_INVALID.  Size the
- * workspace with k3mla_decode_workspace_bytes for the returned length.  Results
- * are bitwise invariant only for a fixed split length, so a caller that wants
- * padding or batch invariance keeps one length. */
-int k3mla_split_tokens_for_contexts(const int32_t* ctx_host, int B, int max_ctx);
+/* OPT-IN, BATCH-DEPENDENT NUMERICS.  A fixed split length for a whole batch whose
+ * contexts the caller knows on the host, chosen for throughput: the shortest
+ * multiple of K3MLA_TILE whose splits that hold tokens, sum_b ceil(ctx_b / split),
+ * fit one wave of SM pairs of the current device (or max_ctx rounded up to
+ * K3MLA_TILE when that already gives every slot one split or no length fits).
+ * pegainfer PR #869 (M2 commit) reduces a context in splits merged in a fixed
+ * order; on a ragged batch with few slots this length keeps more SM pairs busy
+ * than the default rule.  The price: the length depends on every slot's context
+ * and on the SM count, so passing it as split_tokens makes a slot's output bits
+ * depend on the rest of the batch, on padding rows and on the GPU.  Callers that
+ * need batch or padding invariance use K3MLA_SPLIT_AUTO instead.
+ * ctx_host[b] for b < B is clamped to [0, max_ctx].  B <= 0 or max_ctx <= 0 gives
+ * K3MLA_TILE; a NULL ctx_host with B > 0 gives K3MLA_E_INVALID. */
+int k3mla_batch_planned_split_tokens(const int32_t* ctx_host, int B, int max_ctx);
 
 /* ---- host page pool: free-list allocator (PR #869, M1 commit) ---------------
  * n_pages == 0 sizes the pool for full coverage: n_slots * ceil(max_ctx / 64)
@@ -346,15 +350,17 @@ int k3mla_copy_pages(uint16_t* dst_slab, int dst_n_pages, const uint16_t* src_sl
  * scratch is a fixed array of K3MLA_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the
  * library; every GPU that loads the library holds it until the process exits.  The
  * call itself allocates and frees nothing.  Arguments, results and error behaviour
- * are those of k3mla_paged_decode, and:
+ * are those of k3mla_paged_decode (same kernels, same bits), and:
  *   - Limit: k3mla_decode_workspace_bytes(B, max_ctx, split_tokens) must not exceed
- *     K3MLA_NOALLOC_SCRATCH_BYTES, i.e. B * ceil(max_ctx / split_tokens) <= 84
- *     (enough for k3mla_default_split_tokens with up to 84 slots).  A larger request
- *     returns K3MLA_E_WORKSPACE before anything is launched; k3mla_last_error() gives
- *     the sizes.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current).  Make that first call before any stream
- *     capture begins.
+ *     K3MLA_NOALLOC_SCRATCH_BYTES: up to 168 slots when every slot has one split
+ *     (max_ctx <= K3MLA_SPLIT_MAX under the default rule), fewer when slots can have
+ *     several.  A larger request returns K3MLA_E_WORKSPACE before anything is
+ *     launched; k3mla_last_error() gives the sizes.
+ *   - The first call in a CUDA context of a device looks up the array's device
+ *     address (once, with that device current); a later call in a new context of the
+ *     same device (after cudaDeviceReset, for instance) looks it up again.  Make the
+ *     first call before any stream capture begins.  This header makes no statement
+ *     either way about capturing this call in a CUDA graph.
  *   - All calls on a device share the one array.  Calls whose kernels overlap on
  *     the GPU (different streams, or threads with no ordering between their calls)
  *     race on it and corrupt each other's results: order them, e.g. on one stream.

@@ -20,6 +20,30 @@ constexpr int ROW = K3MLA_ROW;          // 576
 constexpr int PAGE = K3MLA_PAGE;        // 64
 constexpr int TILE = K3MLA_TILE;        // 128
 constexpr int WROWS_PER_HEAD = NOPE + VH;  // 256
+constexpr int SPLIT_MAX = K3MLA_SPLIT_MAX;  // 4096: longest split of the default rule
+
+// Split length of a slot whose (clamped) context is n tokens: split_tokens when positive, else the
+// default rule -- ceil(n / SPLIT_MAX) splits of equal length rounded up to the 128-token tile.  It
+// depends on n and constants only, never on the batch, the GPU or the page ids, so a slot is cut
+// the same way whatever else is in the launch.
+__host__ __device__ inline int slot_split(int n, int split_tokens)
+{
+    if (split_tokens > 0) return split_tokens;
+    const int ns = n <= SPLIT_MAX ? 1 : (n + SPLIT_MAX - 1) / SPLIT_MAX;
+    const int per = (n + ns - 1) / ns;
+    const int t = (per + TILE - 1) / TILE * TILE;
+    return t < TILE ? TILE : t;
+}
+
+// Splits that hold tokens for a slot of n tokens cut every `split` tokens (0 for an empty context).
+__host__ __device__ inline int slot_nsplit(int n, int split) { return n <= 0 ? 0 : (n + split - 1) / split; }
+
+// Upper bound of slot_nsplit over contexts up to max_ctx: the split count of the launch's grid.
+__host__ __device__ inline int launch_nsplit(int max_ctx, int split_tokens)
+{
+    const int s = split_tokens > 0 ? split_tokens : SPLIT_MAX;
+    return (max_ctx + s - 1) / s;
+}
 
 // Per-thread error text for k3mla_last_error().
 void set_error(const char* fmt, ...);
@@ -67,18 +91,35 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
     return check_launch(what);
 }
 
+// Byte offsets of the decode workspace's regions: final o_lat [96][B][512] bf16 (every slot with at
+// most one split lands it there itself), f32 partial O [B][nsplit][96][512] (only when some slot can
+// have several splits), and the split records [B][nsplit][96][4] f32 (m_ref, l, best score, best t).
+struct WsLayout {
+    size_t olat, o, ml, total;
+};
+inline WsLayout ws_layout(int B, int nsplit)
+{
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    WsLayout w;
+    w.olat = 0;
+    w.o = up((size_t)B * H * LORA * 2);
+    w.ml = w.o + (nsplit > 1 ? up((size_t)B * nsplit * H * LORA * 4) : 0);
+    w.total = w.ml + (size_t)B * nsplit * H * 4 * 4;
+    return w;
+}
+
 // Split partials -> o_lat -> W_UV expansion (merge_expand.cu).
 struct MergeParams {
-    const float* ws_o;     // [B][nsplit][96][512] f32 partial O
+    const float* ws_o;     // [B][nsplit][96][512] f32 partial O (null when nsplit == 1)
     const float* ws_ml;    // [B][nsplit][96][4]: m_ref, l, best score, best t (int bits)
-    const uint16_t* ws_olat;  // nsplit == 1: final o_lat [96][B][512] bf16 (ws_o unused); else null
+    const uint16_t* ws_olat;  // [96][B][512] bf16: final o_lat of the slots with at most one split
     const int32_t* ctx_len;
     const uint16_t* w_kv_b;
     uint16_t* out;         // [B][96][128] bf16
     int32_t* argmax;       // [B][96] or null
     int32_t* dev_err;      // K3MLA_DEV_* bits or null
-    int B, max_ctx, max_pages, split, nsplit;
-    int tile;              // slots per CTA: 64 (single split), 32 (2-3 splits) or 16 (4 or more)
+    int B, max_ctx, max_pages, split_tokens, nsplit;  // split_tokens 0: the default per-slot rule
+    int tile;              // slots per CTA: 64 (nsplit == 1, every o_lat landed) or 16 (merge)
 };
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st);
 

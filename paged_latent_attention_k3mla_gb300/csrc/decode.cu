@@ -11,8 +11,9 @@
 // are in merge_expand.cu.
 //
 // Structure (GB300-first; the page's own 3-sweep kernel is prior art only).
-// The context of a slot is cut into fixed splits of `split` logical tokens;
-// each split is one unit of work for a CLUSTER OF TWO CTAs, and the unit of the
+// The context of a slot is cut into splits (slot_split: a fixed length, or by
+// default ceil(n / 4096) equal splits of the slot's own n tokens); each split
+// is one unit of work for a CLUSTER OF TWO CTAs, and the unit of the
 // pipeline is one 64-token page, held whole in shared memory.
 //   * rank 0, the score CTA, holds q_abs of the slot in TMEM (24 heads in each
 //     32-lane quarter so that all four SM sub-partitions run softmax; 288
@@ -41,9 +42,11 @@
 // TMEM holds Q (288 columns) + S (3 x 64) in rank 0 and O (384) in rank 1, which
 // is why the two contractions live in different CTAs.
 //
-// Split boundaries depend only on the logical position and ctx_len, and no
-// physical page id enters the arithmetic, so a slot's result is bitwise
-// independent of the batch, of padding and of page placement.
+// Split boundaries depend only on the logical position, the slot's own ctx_len
+// and the split_tokens argument; whether a slot lands o_lat itself (one split)
+// or leaves partials for the merge depends on the same; no physical page id
+// enters the arithmetic.  So a slot's result is bitwise independent of the
+// batch, of padding and of page placement.
 //
 // Departures from the chain, all inside the stated tolerance: the tensor cores
 // add the 576 products of a score and the tokens of o_lat in their own order;
@@ -146,12 +149,12 @@ static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with
 struct DecodeParams {
     const int32_t* table;
     const int32_t* ctx_len;
-    float* ws_o;    // [B][nsplit][96][512]
+    float* ws_o;    // [B][nsplit][96][512] f32 partials of slots with several splits (null if nsplit == 1)
     float* ws_ml;   // [B][nsplit][96][4]: m_ref, l, best score, best t (int bits)
-    uint16_t* ws_olat;  // nsplit == 1: o_lat [96][B][512] bf16, final (ws_o is then unused); else null
+    uint16_t* ws_olat;  // [96][B][512] bf16: final o_lat of every slot with at most one split
     int32_t* dev_err;
     int max_pages, n_pages, n_layers, layer;
-    int B, max_ctx, split, nsplit;
+    int B, max_ctx, split_tokens, nsplit;  // split_tokens 0: the default per-slot rule; nsplit: the grid's
     uint32_t scale2;  // the bf16 scale in both halves
 };
 
@@ -405,12 +408,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     const int s = unit % p.nsplit;
     const int ctx = ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages, p.dev_err,
                                   rank == 0 && threadIdx.x == 0 && s == 0);
-    const int start = s * p.split;
+    const int split = slot_split(ctx, p.split_tokens);
+    const bool single = slot_nsplit(ctx, split) <= 1;  // the PV CTA lands final o_lat itself
+    const int start = s * split;
     if (start >= ctx) {  // empty split: both CTAs leave, nothing was shared
-        if (p.ws_olat && rank == 1) zero_olat(p.ws_olat, p.B, b);  // its only split is this one
+        if (s == 0 && rank == 1) {  // an empty context: its o_lat is zero (the workspace is written only
+            griddep_wait();         // after the kernel before has completed: it may still read it)
+            zero_olat(p.ws_olat, p.B, b);
+        }
         return;
     }
-    const int ntok = min(ctx, start + p.split) - start;
+    const int ntok = min(ctx, start + split) - start;
     const int npg = (ntok + PAGE - 1) / PAGE;
     const int n_lp = (ctx + PAGE - 1) / PAGE;
     const int lp0 = start / PAGE;
@@ -443,7 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
         }
         if (rank == 1) {  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
             for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
-            if (p.ws_olat) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
+            if (single) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
         }
         fence_mbarrier_init_cluster();
         if (rank == 0) tma_prefetch_desc(&tmap_q);
@@ -701,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 ml[2] = best_s;
                 ml[3] = __int_as_float(best_t);
                 // a single split is final: the PV CTA lands o_lat = bf16(O * (1 / l)) itself
-                if (p.ws_olat)
+                if (single)
                     st_async_b32(mapa(smem_u32(&sm.rl[h]), 1), __float_as_uint(1.f / ltot),
                                  mapa(smem_u32(&sm.l_full), 1));
             }
@@ -833,7 +841,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 }
                 if (cmd & 4u) {  // final: O is complete (and, single split, 1 / l has arrived)
                     bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
-                    if (p.ws_olat) got2 = got2 && wait_bar(&sm.l_full, 0, sm, p.dev_err, true);
+                    if (single) got2 = got2 && wait_bar(&sm.l_full, 0, sm, p.dev_err, true);
                     if (__all_sync(0xFFFFFFFFu, got2) && lane == 0) atomicAdd(&sm.fin_ready, 1);
                     break;
                 }
@@ -843,7 +851,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
             }
         }
         __syncthreads();  // every role is done: the final write-out takes all warps
-        if (*reinterpret_cast<volatile int32_t*>(&sm.fin_ready) == 4) pv_write_out(sm, p.ws_o, p.ws_olat, p.B, p.nsplit, tbase, b, s);
+        if (*reinterpret_cast<volatile int32_t*>(&sm.fin_ready) == 4)
+            pv_write_out(sm, single ? nullptr : p.ws_o, single ? p.ws_olat : nullptr, p.B, p.nsplit, tbase, b, s);
     }
 
     __syncwarp();
@@ -984,25 +993,17 @@ using namespace k3;
 
 extern "C" size_t k3mla_decode_workspace_bytes(int B, int max_ctx, int split_tokens)
 {
-    if (B <= 0 || max_ctx <= 0 || split_tokens <= 0) return 0;
-    const size_t ns = (size_t)num_splits(max_ctx, split_tokens);
-    const size_t o = (size_t)B * ns * H * LORA * sizeof(float);
-    const size_t ml = (size_t)B * ns * H * 4 * sizeof(float);
-    return ((o + 255) & ~size_t(255)) + ml;
+    if (B <= 0 || max_ctx <= 0 || split_tokens < 0) return 0;
+    return ws_layout(B, launch_nsplit(max_ctx, split_tokens)).total;
 }
 
-extern "C" int k3mla_default_split_tokens(int B, int max_ctx)
+extern "C" int k3mla_slot_split_tokens(int ctx, int split_tokens)
 {
-    if (B <= 0 || max_ctx <= 0) return TILE;
-    int sms = 148;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int clusters = sms / 2;
-    int per_slot = clusters / B;
-    if (per_slot < 1) per_slot = 1;
-    int split = (max_ctx + per_slot - 1) / per_slot;
-    split = (split + TILE - 1) / TILE * TILE;
-    return split < TILE ? TILE : split;
+    if (split_tokens < 0) {
+        set_error("k3mla_slot_split_tokens: split_tokens < 0");
+        return K3MLA_E_INVALID;
+    }
+    return slot_split(ctx < 0 ? 0 : ctx, split_tokens);
 }
 
 extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
@@ -1012,7 +1013,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
                                   int max_ctx, int split_tokens, int32_t* dev_err, void* stream)
 {
     if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
-        max_ctx <= 0 || split_tokens <= 0 || split_tokens % TILE != 0) {
+        max_ctx <= 0 || split_tokens < 0 || split_tokens % TILE != 0) {
         set_error("k3mla_paged_decode: invalid sizes");
         return K3MLA_E_INVALID;
     }
@@ -1033,7 +1034,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
         return K3MLA_E_WORKSPACE;
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
-    const int ns = num_splits(max_ctx, split_tokens);
+    const int ns = launch_nsplit(max_ctx, split_tokens);
     if ((long long)B * ns * 2 > 0x7FFFFFFFll) {
         set_error("k3mla_paged_decode: grid too large");
         return K3MLA_E_INVALID;
@@ -1045,18 +1046,16 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     const size_t smem = smem_bytes();
     set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel), smem, attr_done);
 
+    const WsLayout wl = ws_layout(B, ns);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     DecodeParams dp;
     dp.table = block_table;
     dp.ctx_len = ctx_len;
-    float* ws_o = reinterpret_cast<float*>(workspace);
-    const size_t o_bytes = ((size_t)B * ns * H * LORA * sizeof(float) + 255) & ~size_t(255);
-    float* ws_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + o_bytes);
-    dp.ws_o = ws_o;
-    dp.ws_ml = ws_ml;
-    // one split per slot: the split kernel writes final bf16 o_lat ([96][B][512], in the space of
-    // the f32 partials) and the merge only expands it
-    uint16_t* ws_olat = ns == 1 ? reinterpret_cast<uint16_t*>(workspace) : nullptr;
-    dp.ws_olat = ws_olat;
+    // every slot with at most one split lands final bf16 o_lat ([96][B][512]) in the split kernel; the
+    // f32 partials exist only when some slot of the launch can have several splits
+    dp.ws_olat = reinterpret_cast<uint16_t*>(ws + wl.olat);
+    dp.ws_o = ns > 1 ? reinterpret_cast<float*>(ws + wl.o) : nullptr;
+    dp.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
     dp.dev_err = dev_err;
     dp.max_pages = max_pages_per_slot;
     dp.n_pages = n_pages;
@@ -1064,7 +1063,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     dp.layer = layer;
     dp.B = B;
     dp.max_ctx = max_ctx;
-    dp.split = split_tokens;
+    dp.split_tokens = split_tokens;
     dp.nsplit = ns;
     dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1073,9 +1072,9 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     if (rc) return rc;
 
     MergeParams mp;
-    mp.ws_o = ws_o;
-    mp.ws_ml = ws_ml;
-    mp.ws_olat = ws_olat;
+    mp.ws_o = dp.ws_o;
+    mp.ws_ml = dp.ws_ml;
+    mp.ws_olat = dp.ws_olat;
     mp.ctx_len = ctx_len;
     mp.w_kv_b = w_kv_b;
     mp.out = out;
@@ -1084,9 +1083,9 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.B = B;
     mp.max_ctx = max_ctx;
     mp.max_pages = max_pages_per_slot;
-    mp.split = split_tokens;
+    mp.split_tokens = split_tokens;
     mp.nsplit = ns;
-    mp.tile = ns == 1 ? 64 : (ns >= 4 ? 16 : 32);  // the merge's split groups: 64 / tile
+    mp.tile = ns == 1 ? 64 : 16;  // every o_lat landed: TMA-loaded in 64-slot tiles; else merged, 16 a CTA
     return launch_merge_expand(mp, st);
 }
 
@@ -1097,20 +1096,45 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
 // workspace.  Every device that loads the library holds it until the process exits.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[K3MLA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per device
-// with that device current (in host code the array's name is only a host-side handle).
+// Device address of g_noalloc_scratch in the current CUDA context, looked up with that context's
+// device current (in host code the array's name is only a host-side handle).  The address is cached
+// per device together with the context it belongs to: a new context of the device (after
+// cudaDeviceReset, say) loads the module again, possibly elsewhere, so the lookup is repeated.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+static CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
 static int noalloc_scratch(void** out)
 {
     static std::mutex mu;
     static void* addr[64] = {};
+    static CUcontext owner[64] = {};
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) {
         set_error("k3mla_paged_decode_noalloc: no usable current device (%s)", cudaGetErrorString(e));
         return K3MLA_E_CUDA;
     }
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) {
+        set_error("k3mla_paged_decode_noalloc: cuCtxGetCurrent unavailable");
+        return K3MLA_E_CUDA;
+    }
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;  // none yet: the lookup below makes the primary one current
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!ctx || !addr[dev] || owner[dev] != ctx) {
         void* a = nullptr;
         e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
         if (e != cudaSuccess || !a) {
@@ -1118,7 +1142,12 @@ static int noalloc_scratch(void** out)
                       cudaGetErrorString(e));
             return K3MLA_E_CUDA;
         }
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) {
+            set_error("k3mla_paged_decode_noalloc: no current CUDA context on device %d", dev);
+            return K3MLA_E_CUDA;
+        }
         addr[dev] = a;
+        owner[dev] = ctx;
     }
     *out = addr[dev];
     return K3MLA_OK;
@@ -1130,13 +1159,12 @@ extern "C" int k3mla_paged_decode_noalloc(const uint16_t* q_abs, const uint16_t*
                                           uint16_t* out, int32_t* argmax_t, int B, int max_ctx, int split_tokens,
                                           int32_t* dev_err, void* stream)
 {
-    if (B > 0 && max_ctx > 0 && split_tokens > 0) {
+    if (B > 0 && max_ctx > 0 && split_tokens >= 0) {
         const size_t need = k3mla_decode_workspace_bytes(B, max_ctx, split_tokens);
         if (need > (size_t)K3MLA_NOALLOC_SCRATCH_BYTES) {
             set_error("k3mla_paged_decode_noalloc: B=%d, max_ctx=%d, split_tokens=%d need %zu bytes of scratch; "
-                      "the built-in scratch holds %zu (B * ceil(max_ctx / split_tokens) <= %zu)",
-                      B, max_ctx, split_tokens, need, (size_t)K3MLA_NOALLOC_SCRATCH_BYTES,
-                      (size_t)K3MLA_NOALLOC_SCRATCH_BYTES / k3mla_decode_workspace_bytes(1, 1, TILE));
+                      "the built-in scratch holds %zu",
+                      B, max_ctx, split_tokens, need, (size_t)K3MLA_NOALLOC_SCRATCH_BYTES);
             return K3MLA_E_WORKSPACE;
         }
     }

@@ -9,24 +9,25 @@
 //
 // Per head the expansion is a dense product across slots,
 //     OUT_h^T [128 v x B] = W_UV[h] [128 v x 512] . O_lat_h^T [512 x B],
-// run on the 5th-generation tensor cores.  One CTA per (head, tile of 64 slots):
+// run on the 5th-generation tensor cores.  One CTA per (head, tile of slots):
 //   * one elected thread stages W_UV[h] (128 KB) with eight 3-D TMA boxes, one per
 //     64-column chunk (several boxes in flight load faster than one large box),
 //     landing as the K-major A operand ([8 chunks][128 rows][128 B], 128-byte
 //     swizzle), while
-//   * sixteen warps merge the split partials of the tile's 64 slots (f32, ascending
-//     splits; eight threads per slot, each a 64-dim slice) and write bf16 o_lat
-//     straight into shared memory as the K-major B operand ([8 chunks][64 rows]
-//     [128 B], same swizzle);
-//   * the elected thread then issues 32 MMAs (M = 128 v, N = 64 slots, K = 16)
-//     into a 128 x 64 f32 TMEM accumulator, and the sixteen warps read it back
-//     (lane = v, column = slot) and store bf16 out.
-// W_UV is read from HBM once per layer per 64 slots; the f32 partials are read
-// once, from L2 where the split kernel just wrote them.  When every slot has a
-// single split the split kernel has already landed o_lat itself (same arithmetic:
-// the one partial's weight is exp(0) = 1), so there is nothing to merge: the
-// elected thread TMA-loads o_lat ([96][B][512] bf16) as the B operand and the
-// expansion runs as above.
+//   * the B operand (bf16 o_lat of the tile's slots, [8 chunks][tile rows][128 B],
+//     same swizzle) is put together: a slot whose context had at most one split
+//     already has its final o_lat in the workspace (the split kernel landed it:
+//     the one partial's weight would be exp(0) = 1), and a slot with several
+//     splits is merged here by one warp (four split groups, eight threads each
+//     owning a 64-dim slice) and written straight into shared memory;
+//   * the elected thread then issues 32 MMAs (M = 128 v, N = the tile, K = 16) into
+//     a 128 x tile f32 TMEM accumulator, and the warps read it back (lane = v,
+//     column = slot) and store bf16 out.
+// When no slot of the launch can have more than one split, tiles are 64 slots and
+// the elected thread TMA-loads the tile's o_lat rows ([96][B][512] bf16) as the B
+// operand; otherwise tiles are 16 slots (one warp each).  W_UV is read from HBM
+// once per layer and from L2 by the other tiles; the f32 partials are read once,
+// from L2 where the split kernel just wrote them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +45,10 @@ constexpr int MX_THREADS = 32 * MX_MERGE_WARPS;  // thread 0 also issues the TMA
 constexpr int MX_A_BYTES = 8 * VH * 128;       // W_UV[h]: 8 chunks x 128 rows x 128 B
 constexpr int MX_B_BYTES = 8 * MX_SLOTS * 128; // o_lat tile: 8 chunks x 64 rows x 128 B
 constexpr uint64_t MX_WAIT_NS = 1000000000ull;  // bounded waits: 1 s
+constexpr int MX_G = 4;                        // split groups of a slot with several splits
+constexpr int MX_MERGE_TILE = MX_THREADS / (8 * MX_G);  // 16 slots per CTA when merging
+static_assert(8 * MX_G == 32, "one warp per slot: the group tree is a warp shuffle");
+static_assert(MX_MERGE_TILE == 16, "the launch's merge tile");
 
 __device__ __forceinline__ uint32_t mx_pack_bf16x2(float lo, float hi)
 {
@@ -90,7 +95,7 @@ __device__ __forceinline__ void issue_expand(uint32_t tbase, const uint8_t* sa, 
     }
 }
 
-// grid (96 heads, ceil(B / 64) slot tiles); block MX_THREADS.
+// grid (96 heads, ceil(B / tile) slot tiles); block MX_THREADS.
 __global__ void __launch_bounds__(MX_THREADS, 1)
     k3mla_merge_expand_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_o,
                               const MergeParams p)
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         mbar_init(&o_full, 1);
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmap_w);
-        if (p.ws_olat) tma_prefetch_desc(&tmap_o);
+        if (p.nsplit == 1) tma_prefetch_desc(&tmap_o);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, MX_SLOTS);
@@ -132,17 +137,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     }
     // W_UV is a layer weight no kernel of this library writes, so its load above overlaps the split
     // kernel, and so does the merge's read of the context lengths (the split kernel, which runs just
-    // before in the stream, only reads them); the split partials and the outputs wait for it
-    const int G = p.ws_olat ? 1 : MX_SLOTS / p.tile;
-    const int r = (int)threadIdx.x / (8 * G), g = ((int)threadIdx.x >> 3) % G, seg = threadIdx.x & 7;
-    int ns = 0;  // splits of slot b0 + r that hold tokens (merge path)
-    if (!p.ws_olat && b0 + r < p.B)
-        ns = (mx_ctx_effective(p.ctx_len, b0 + r, p.max_ctx, p.max_pages) + p.split - 1) / p.split;
-    griddep_wait();
-    griddep_launch_dependents();
-    if (p.ws_olat) {
-        // ---- one split per slot: the split kernel wrote final bf16 o_lat ([96][B][512]); rows
-        // h B + b0 .. h B + b0 + 63 are the B operand as they stand (rows past the batch belong to
+    // before in the stream, only reads them); the split results and the outputs wait for it
+    if (p.nsplit == 1) {
+        griddep_wait();
+        griddep_launch_dependents();
+        // ---- every slot has at most one split: the split kernel wrote final bf16 o_lat ([96][B][512]);
+        // rows h B + b0 .. h B + b0 + 63 are the B operand as they stand (rows past the batch belong to
         // the next head or lie past the array, read as zeros: either way their columns are not stored)
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&o_full, MX_B_BYTES);
@@ -167,73 +167,97 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             umma_commit(&d_full);
         }
     } else {
-        // ---- merge: thread -> (row r = slot b0 + r, split group g, segment seg); the row's 512 dims
-        // are 128 float4, float4 f belongs to segment f % 8 (8 threads read 128 contiguous bytes).
-        // The G = 64 / tile groups of a slot walk its splits i = g, g + G, ... side by side, each in
-        // ascending i with a running max: a split's record (m_i, l_i, best score, its token) is
-        // loaded with its partial, so a slot's splits arrive in ceil(ns / G) round trips and no pass
-        // over the records comes first.  A fixed shuffle tree then brings the groups to their common
-        // max and adds them: ((g0 + g1) + (g2 + g3)).  G depends on the launch's split count only,
-        // so a slot's result does not depend on the batch.
+        // ---- tiles of 16 slots, one warp a slot: thread -> (slot r, split group g, segment seg).  A slot
+        // whose context has at most one split (the same rule as the split kernel: its own ctx_len and
+        // split_tokens) has its final o_lat in the workspace already, and its warp copies that row into
+        // the B operand.  A slot with several splits is merged by MX_G = 4 split groups, group g walking
+        // splits g, g + 4, ... in ascending order with a running max: a split's record (m_i, l_i, best
+        // score, its token) is loaded with its partial, so the splits arrive in ceil(ns / 4) round trips
+        // and no pass over the records comes first.  A fixed shuffle tree then brings the groups to
+        // their common max and adds them: ((g0 + g1) + (g2 + g3)).  A group without splits adds exactly
+        // nothing.  The grouping is the same for every slot and launch, so a slot's result depends on
+        // its own splits only.  The row's 512 dims are 128 float4; float4 f belongs to segment f % 8.
+        const int r = (int)threadIdx.x >> 5, g = ((int)threadIdx.x >> 3) & (MX_G - 1), seg = threadIdx.x & 7;
         const int b = b0 + r;
+        int n = 0, ns = 0;
+        if (b < p.B) {
+            n = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
+            ns = slot_nsplit(n, slot_split(n, p.split_tokens));
+        }
+        griddep_wait();
+        griddep_launch_dependents();
         const float* ml = p.ws_ml + ((size_t)b * p.nsplit * H + h) * 4;
-        float m = -INFINITY, best = -INFINITY, l = 0.f;
-        int best_t = -1;
-        float acc[64];
+        if (ns <= 1) {  // warp-uniform: one warp per slot
+            const int l32 = (int)threadIdx.x & 31;
+            const uint4* src = reinterpret_cast<const uint4*>(p.ws_olat + ((size_t)h * p.B + b) * LORA);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-        for (int i = g; i < ns; i += G) {
-            const float4 rec = *reinterpret_cast<const float4*>(ml + (size_t)i * H * 4);
-            const float4* oi = reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
-            const float mn = fmaxf(m, rec.x);
-            const float a = expf(m - mn);      // 0 before the group's first split (m = -inf)
-            const float wgt = expf(rec.x - mn);
-            l = l * a + wgt * rec.y;
-            if (rec.z > best) {  // ascending splits: the lowest t wins ties
-                best = rec.z;
-                best_t = __float_as_int(rec.w);
+            for (int k = 0; k < 2; ++k) {  // 16-byte unit u of the row: dims 8u .. 8u+7, chunk u / 8
+                const int u = 2 * l32 + k, c = u >> 3, uu = u & 7;
+                const uint4 v = b < p.B ? src[u] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sb + c * (p.tile * 128) + r * 128 + ((uu ^ (r & 7)) << 4)) = v;
             }
-            m = mn;
+            if (p.argmax && b < p.B && l32 == 0) p.argmax[(size_t)b * H + h] = n > 0 ? __float_as_int(ml[3]) : -1;
+        } else {
+            float m = -INFINITY, best = -INFINITY, l = 0.f;
+            int best_t = -1;
+            float acc[64];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float4 v = oi[seg + 8 * k];
-                acc[4 * k + 0] = acc[4 * k + 0] * a + wgt * v.x;
-                acc[4 * k + 1] = acc[4 * k + 1] * a + wgt * v.y;
-                acc[4 * k + 2] = acc[4 * k + 2] * a + wgt * v.z;
-                acc[4 * k + 3] = acc[4 * k + 3] * a + wgt * v.w;
-            }
-        }
-        for (int o = 8; o < 8 * G; o <<= 1) {  // lanes 8 g + seg of one slot sit in one warp (8 G <= 32)
-            const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            const float bo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            const int to = __shfl_xor_sync(0xFFFFFFFFu, best_t, o);
-            const float mn = fmaxf(m, mo);
-            const float a = (m == mn) ? 1.f : expf(m - mn);  // a group without splits keeps m = -inf
-            l *= a;
-            l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
+            for (int i = g; i < ns; i += MX_G) {
+                const float4 rec = *reinterpret_cast<const float4*>(ml + (size_t)i * H * 4);
+                const float4* oi =
+                    reinterpret_cast<const float4*>(p.ws_o + (((size_t)b * p.nsplit + i) * H + h) * LORA);
+                const float mn = fmaxf(m, rec.x);
+                const float a = expf(m - mn);      // 0 before the group's first split (m = -inf)
+                const float wgt = expf(rec.x - mn);
+                l = l * a + wgt * rec.y;
+                if (rec.z > best) {  // ascending splits: the lowest t wins ties
+                    best = rec.z;
+                    best_t = __float_as_int(rec.w);
+                }
+                m = mn;
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                acc[k] *= a;
-                acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
+                for (int k = 0; k < 16; ++k) {
+                    const float4 v = oi[seg + 8 * k];
+                    acc[4 * k + 0] = acc[4 * k + 0] * a + wgt * v.x;
+                    acc[4 * k + 1] = acc[4 * k + 1] * a + wgt * v.y;
+                    acc[4 * k + 2] = acc[4 * k + 2] * a + wgt * v.z;
+                    acc[4 * k + 3] = acc[4 * k + 3] * a + wgt * v.w;
+                }
             }
-            if (bo > best || (bo == best && to < best_t && to >= 0)) {  // the lower token on a tie
-                best = bo;
-                best_t = to;
-            }
-            m = mn;
-        }
-        if (p.argmax && b < p.B && g == 0 && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
-        if (ns == 0) l = 1.f;  // empty context (or a padding row of the tile): o_lat = 0
-        if (g == 0) {
-            const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
-            // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int c = k >> 1;
-                const int u = 4 * (k & 1) + (seg >> 1);
-                const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] * rl, acc[4 * k + 1] * rl),
-                                           mx_pack_bf16x2(acc[4 * k + 2] * rl, acc[4 * k + 3] * rl));
-                *reinterpret_cast<uint2*>(sb + c * (p.tile * 128) + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (seg & 1)) = v;
+            for (int o = 8; o < 8 * MX_G; o <<= 1) {  // the groups of one slot are lanes 8 g + seg of its warp
+                const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+                const float bo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                const int to = __shfl_xor_sync(0xFFFFFFFFu, best_t, o);
+                const float mn = fmaxf(m, mo);
+                const float a = (m == mn) ? 1.f : expf(m - mn);  // a group without splits keeps m = -inf
+                l *= a;
+                l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+#pragma unroll
+                for (int k = 0; k < 64; ++k) {
+                    acc[k] *= a;
+                    acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
+                }
+                if (bo > best || (bo == best && to < best_t && to >= 0)) {  // the lower token on a tie
+                    best = bo;
+                    best_t = to;
+                }
+                m = mn;
+            }
+            if (p.argmax && g == 0 && seg == 0) p.argmax[(size_t)b * H + h] = best_t;
+            if (g == 0) {
+                const float rl = 1.f / l;  // o_lat = bf16(o * (1 / l)): one division per thread
+                // dims d = 32 k + 4 seg + (0..3): chunk d / 64, 16-byte unit (d % 64) / 8
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int c = k >> 1;
+                    const int u = 4 * (k & 1) + (seg >> 1);
+                    const uint2 v = make_uint2(mx_pack_bf16x2(acc[4 * k + 0] * rl, acc[4 * k + 1] * rl),
+                                               mx_pack_bf16x2(acc[4 * k + 2] * rl, acc[4 * k + 3] * rl));
+                    *reinterpret_cast<uint2*>(sb + c * (p.tile * 128) + r * 128 + ((u ^ (r & 7)) << 4) +
+                                              8 * (seg & 1)) = v;
+                }
             }
         }
         fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
@@ -293,7 +317,7 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
     if (rc) return rc;
     // final o_lat viewed as (64 elements, 96 B rows of 512, 8 chunks): one box = 64 slots of a chunk
     std::memset(&tmap_o, 0, sizeof(tmap_o));
-    if (mp.ws_olat) {
+    if (mp.nsplit == 1) {
         rc = make_tmap_slab_3d(&tmap_o, mp.ws_olat, (uint64_t)H * mp.B, LORA, 8, MX_SLOTS, 1);
         if (rc) return rc;
     }

@@ -1,13 +1,13 @@
-// plan.cpp -- split length for a batch whose contexts are known on the host.
+// plan.cpp -- an opt-in split length planned for a whole batch (batch-dependent numerics).
 //
 // pegainfer PR #869, "K3: paged latent MLA KV + absorbed decode": the decode
 // reduces each slot's context in splits and merges the partial results in a
-// fixed order.  How long a split is decides how many SM pairs the decode keeps
-// busy.  k3mla_default_split_tokens sees only B and max_ctx and so plans for
-// every slot at max_ctx; on a ragged batch the slots with short contexts then
-// leave part of the wave idle.  The host that claims the pages knows each
-// slot's context, and this call plans the split for those contexts: the
-// shortest split whose non-empty splits still fit one wave.
+// fixed order.  The default rule cuts every slot by its own context alone, so a
+// slot's bits never depend on its batch; on a ragged batch of few slots that
+// leaves most SM pairs idle.  The host that claims the pages knows every slot's
+// context, and this call plans one split length for the batch instead: the
+// shortest whose non-empty splits still fit one wave of SM pairs.  A slot's bits
+// then depend on the other slots' contexts and on the SM count.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,11 +30,11 @@ static long long live_splits(const int32_t* ctx, int B, int max_ctx, int split)
     return n;
 }
 
-extern "C" int k3mla_split_tokens_for_contexts(const int32_t* ctx_host, int B, int max_ctx)
+extern "C" int k3mla_batch_planned_split_tokens(const int32_t* ctx_host, int B, int max_ctx)
 {
     if (B <= 0 || max_ctx <= 0) return K3MLA_TILE;
     if (!ctx_host) {
-        k3::set_error("k3mla_split_tokens_for_contexts: ctx_host is NULL");
+        k3::set_error("k3mla_batch_planned_split_tokens: ctx_host is NULL");
         return K3MLA_E_INVALID;
     }
     int sms = 148;

@@ -16,18 +16,19 @@ import torch
 from . import build as _build
 
 H, NOPE, ROPE, V, LORA, PAGE, ROW, TILE = 96, 128, 64, 128, 512, 64, 576, 128
+SPLIT_AUTO, SPLIT_MAX = 0, 4096   # K3MLA_SPLIT_AUTO (the default per-slot rule), K3MLA_SPLIT_MAX
 
 DEV_BAD_PAGE, DEV_UNMAPPED, DEV_CTX, DEV_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/k3mla.h declares.
 EXPORTS = (
     "k3mla_last_error", "k3mla_absorb_q", "k3mla_append_latent", "k3mla_decode_workspace_bytes",
-    "k3mla_paged_decode", "k3mla_default_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
+    "k3mla_paged_decode", "k3mla_slot_split_tokens", "k3mla_pool_create", "k3mla_pool_ensure",
     "k3mla_pool_release_slot", "k3mla_pool_host_table", "k3mla_pool_max_pages", "k3mla_pool_n_pages",
     "k3mla_pool_stats", "k3mla_pool_destroy", "k3mla_diag_umma", "k3mla_paged_decode_noalloc",
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
-    "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_split_tokens_for_contexts",
+    "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_batch_planned_split_tokens",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -57,8 +58,8 @@ def load(build_if_needed: bool = True):
             "k3mla_decode_workspace_bytes": ([I, I, I], SZ),
             "k3mla_paged_decode": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, P, P],
                                    I),
-            "k3mla_default_split_tokens": ([I, I], I),
-            "k3mla_split_tokens_for_contexts": ([P, I, I], I),
+            "k3mla_slot_split_tokens": ([I, I], I),
+            "k3mla_batch_planned_split_tokens": ([P, I, I], I),
             "k3mla_pool_create": ([I, I, I, ctypes.c_uint64, ctypes.POINTER(P)], I),
             "k3mla_pool_ensure": ([P, I, I], I),
             "k3mla_pool_ensure_all": ([P, P, I], I),
@@ -236,30 +237,38 @@ def decode_exact(q: torch.Tensor, slab: torch.Tensor, layer: int, block_table: t
         "k3mla_decode_exact")
 
 
-def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int) -> int:
+def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int = SPLIT_AUTO) -> int:
     return int(load().k3mla_decode_workspace_bytes(B, max_ctx, split_tokens))
 
 
-def default_split_tokens(B: int, max_ctx: int) -> int:
-    return int(load().k3mla_default_split_tokens(B, max_ctx))
-
-
-def split_tokens_for_contexts(ctx_len, max_ctx: int) -> int:
-    """The split length for a batch whose context lengths are known on the host (a sequence or
-    array of ints, one per slot); see k3mla_split_tokens_for_contexts."""
-    ctx = np.ascontiguousarray(np.asarray(ctx_len, dtype=np.int32).reshape(-1))
-    rc = int(load().k3mla_split_tokens_for_contexts(ctx.ctypes.data_as(ctypes.c_void_p), int(ctx.size), max_ctx))
+def slot_split_tokens(ctx: int, split_tokens: int = SPLIT_AUTO) -> int:
+    """The split length a slot of context ctx gets (k3mla_slot_split_tokens)."""
+    rc = int(load().k3mla_slot_split_tokens(int(ctx), int(split_tokens)))
     if rc < 0:
-        _check(rc, "k3mla_split_tokens_for_contexts")
+        _check(rc, "k3mla_slot_split_tokens")
+    return rc
+
+
+def batch_planned_split_tokens(ctx_len, max_ctx: int) -> int:
+    """OPT-IN, batch-dependent numerics: one split length planned for a batch whose context
+    lengths are known on the host (a sequence or array of ints, one per slot); see
+    k3mla_batch_planned_split_tokens.  Passing it as split_tokens makes a slot's output bits
+    depend on the rest of the batch and on the GPU."""
+    ctx = np.ascontiguousarray(np.asarray(ctx_len, dtype=np.int32).reshape(-1))
+    rc = int(load().k3mla_batch_planned_split_tokens(ctx.ctypes.data_as(ctypes.c_void_p), int(ctx.size), max_ctx))
+    if rc < 0:
+        _check(rc, "k3mla_batch_planned_split_tokens")
     return rc
 
 
 def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
                  ctx_len: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor,
-                 workspace: torch.Tensor, max_ctx: int, split_tokens: int,
+                 workspace: torch.Tensor, max_ctx: int, split_tokens: int = SPLIT_AUTO,
                  argmax: torch.Tensor | None = None, dev_err: torch.Tensor | None = None,
                  stream=None) -> None:
-    """Paged absorbed decode of one layer for B slots; see include/k3mla.h."""
+    """Paged absorbed decode of one layer for B slots; see include/k3mla.h.  split_tokens
+    SPLIT_AUTO (0) cuts each slot by its own context (batch-invariant); a positive multiple of
+    128 cuts every slot at that length."""
     B = q_abs.shape[0]
     n_pages, L = slab.shape[0], slab.shape[1]
     if workspace.dtype != torch.uint8 or not workspace.is_cuda:
@@ -278,12 +287,12 @@ def paged_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_tabl
 
 def paged_decode_noalloc(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
                          ctx_len: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor,
-                         max_ctx: int, split_tokens: int, argmax: torch.Tensor | None = None,
+                         max_ctx: int, split_tokens: int = SPLIT_AUTO, argmax: torch.Tensor | None = None,
                          dev_err: torch.Tensor | None = None, stream=None) -> None:
     """paged_decode without a workspace argument, for callers that cannot allocate
     device memory where they decode: the split results go to the library's built-in
-    16 MiB scratch (B * ceil(max_ctx / split_tokens) <= 84).  Calls that overlap on
-    the GPU share that scratch and race; see include/k3mla.h."""
+    16 MiB scratch (decode_workspace_bytes(B, max_ctx, split_tokens) must fit in it).
+    Calls that overlap on the GPU share that scratch and race; see include/k3mla.h."""
     B = q_abs.shape[0]
     n_pages, L = slab.shape[0], slab.shape[1]
     lib = load()

@@ -32,7 +32,7 @@ def gpu_layer(wl, layer, split=None, max_ctx=None, table=None, ctx=None, slab=No
     """absorb + paged decode of one layer through the C ABI.  Returns numpy bits."""
     B = wl.B
     max_ctx = max_ctx or max(PAGE, int(wl.block_table.shape[1]) * PAGE)
-    split = split or k3mla.default_split_tokens(B, max_ctx)
+    split = k3mla.SPLIT_AUTO if split is None else split
     table = torch.from_numpy(wl.block_table).cuda() if table is None else table
     ctx = torch.from_numpy(wl.ctx_len).cuda() if ctx is None else ctx
     slab = wl.slab if slab is None else slab

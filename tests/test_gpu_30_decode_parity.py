@@ -36,11 +36,21 @@ def test_tiny(gpu_lib):
     _parity(wl, 0, name="tiny")
 
 
-@pytest.mark.parametrize("split", [128, 256, 1024])
+@pytest.mark.parametrize("split", [k3mla.SPLIT_AUTO, 128, 256, 1024])
 def test_ragged_tails_and_split_merges(gpu_lib, split):
     ctx = [1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 640, 1000]
     wl = synth.make_custom(ctx, seed=300, device="cuda")
     _parity(wl, 0, split=split, max_ctx=1024, name=f"ragged_split{split}")
+
+
+def test_default_split_with_single_and_multi_split_slots(gpu_lib):
+    # the default rule (at most 4096 tokens a split) on contexts around its boundaries: slots with one
+    # split land o_lat in the split kernel, slots with two to five are merged, in one launch
+    ctx = [4096, 4097, 100, 8192, 8193, 0, 12000, 1, 20000, 3000]
+    wl = synth.make_custom(ctx, seed=305, device="cuda")
+    ns = [-(-n // k3mla.slot_split_tokens(n)) for n in ctx]
+    assert set(ns) == {0, 1, 2, 3, 5}
+    _parity(wl, 0, split=k3mla.SPLIT_AUTO, max_ctx=20000, name="auto_mixed")
 
 
 def test_single_split_batch_over_one_slot_tile(gpu_lib):
@@ -87,20 +97,18 @@ def test_heavy_tailed_rows_force_rescales(gpu_lib):
 
 
 def test_many_slots_over_several_waves_and_tiles(gpu_lib):
-    # 150 slots: 150 clusters (two waves of SM pairs), three 64-slot absorption tiles, and the
-    # two-split merge over tiles of 32 slots (max_ctx 640, split 384)
+    # 150 slots: 150 clusters (two waves of SM pairs), two 128-slot absorption tiles, and one or two
+    # splits per slot (max_ctx 640, split 384) merged in 16-slot tiles
     ctx = [(53 * i * i + 17 * i) % 640 + 1 for i in range(150)]
     wl = synth.make_custom(ctx, seed=303, device="cuda")
     _parity(wl, 0, split=384, max_ctx=640, name="many_slots150")
 
 
 def test_one_long_slot_many_splits(gpu_lib):
-    # one slot of 20,000 tokens under the default split: 53 splits of 384 tokens, merged by four
-    # split groups; the oracle checks sampled heads of the whole context
+    # one slot of 20,000 tokens at a 384-token split: 53 splits, merged by four split groups of 13-14
+    # splits each; the oracle checks the whole context
     wl = synth.make_custom([20000], seed=304, device="cuda")
-    split = k3mla.default_split_tokens(1, 20000)
-    assert -(-20000 // split) > 40
-    _parity(wl, 0, split=split, max_ctx=20000, name="long_one_slot")
+    _parity(wl, 0, split=384, max_ctx=20000, name="long_one_slot")
 
 
 def test_padding_bucket(gpu_lib):
@@ -113,9 +121,9 @@ def test_ragged16_two_layers(gpu_lib):
     wl = synth.make_workload("ragged16", device="cuda", n_layers=24)
     for layer in (0, 23):
         _parity(wl, layer, name=f"ragged16_l{layer}")
-    # and at the split planned for these contexts (shorter than the default: the benchmark's launch)
-    planned = k3mla.split_tokens_for_contexts(wl.ctx_len, 4096)
-    assert planned < k3mla.default_split_tokens(16, 4096)
+    # and at the opt-in split planned for the whole batch (several splits per slot)
+    planned = k3mla.batch_planned_split_tokens(wl.ctx_len, 4096)
+    assert planned < 4096
     _parity(wl, 11, split=planned, max_ctx=4096, name="ragged16_planned")
     del wl
     torch.cuda.empty_cache()
@@ -123,16 +131,14 @@ def test_ragged16_two_layers(gpu_lib):
 
 def test_steady64_sampled_full_size(gpu_lib):
     wl = synth.make_workload("steady64", device="cuda")
-    split = k3mla.default_split_tokens(64, 4096)
-    _parity(wl, 7, slots=[0, 31, 63], split=split, max_ctx=4096, name="steady64")
+    _parity(wl, 7, slots=[0, 31, 63], split=k3mla.SPLIT_AUTO, max_ctx=4096, name="steady64")
     del wl
     torch.cuda.empty_cache()
 
 
 def test_long8_sampled_full_size(gpu_lib):
     wl = synth.make_workload("long8", device="cuda")
-    split = k3mla.default_split_tokens(8, 32768)
-    _parity(wl, 11, slots=[3], split=split, max_ctx=32768, name="long8")
+    _parity(wl, 11, slots=[3], split=k3mla.SPLIT_AUTO, max_ctx=32768, name="long8")
     del wl
     torch.cuda.empty_cache()
 

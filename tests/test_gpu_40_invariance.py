@@ -162,3 +162,122 @@ def test_repeat_runs_and_graph_replay_are_bitwise_identical(gpu_lib):
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, eager1[0]) and torch.equal(am, eager1[1])
+
+
+def _graph_decode(q, slab, w, table, ctx, max_ctx, scale_bits, split=k3mla.SPLIT_AUTO):
+    """Absorption + paged decode of one layer, run eagerly once and then captured in a CUDA graph and
+    replayed twice into cleared (NaN) outputs; the replay must equal the eager run bit for bit.
+    Returns the replayed out / argmax as numpy arrays and the device error word."""
+    B = q.shape[0]
+    q_abs = torch.empty(B, 96, 576, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((B, 96, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((B, 96), -7, dtype=torch.int32, device="cuda")
+    ws = torch.full((k3mla.decode_workspace_bytes(B, max_ctx, split),), 0xFF, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        k3mla.absorb_q(q, w, q_abs)
+        k3mla.paged_decode(q_abs, slab, 0, table, ctx, w, scale_bits, out, ws, max_ctx, split, argmax=am,
+                           dev_err=err)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager = (synth.bf16_bits(out), am.cpu().numpy())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    out.fill_(float("nan"))
+    am.fill_(-7)
+    ws.fill_(0xFF)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    res = (synth.bf16_bits(out), am.cpu().numpy())
+    assert np.array_equal(res[0], eager[0]) and np.array_equal(res[1], eager[1])
+    return res[0], res[1], int(err.item())
+
+
+def test_padding128_rows_are_bitwise_invariant_under_the_default_split(gpu_lib):
+    """The 128-row padding workload (40 % all -1 padding rows, contexts <= 256, -1 holes, one empty
+    slot) decoded with the library's default split (K3MLA_SPLIT_AUTO, nothing pinned by hand), every
+    batch from a CUDA graph replay.  Its real rows must come out with the same bits when they are
+    decoded (a) in the full 128-row batch; (b) reordered, on physically permuted pages, among added
+    all -1 padding rows and long neighbours with several splits each, under a larger max_ctx (the
+    launch then has f32 partials, the merge path and 16-slot expansion tiles instead of 64-slot
+    ones); (c) five at a time in small batches."""
+    wl = synth.make_workload("padding128", device="cuda")
+    w, q0 = wl.w_kv_b[0], wl.q[0]
+    pad = (wl.block_table < 0).all(axis=1) & (wl.ctx_len > 0)
+    real = [b for b in range(wl.B) if not pad[b]]
+    assert len(real) > 60 and pad.sum() > 30 and (wl.ctx_len[real] == 0).sum() == 1
+    g = torch.Generator(device="cuda").manual_seed(44)
+
+    # (a) the workload as drawn
+    out_a, am_a, err_a = _graph_decode(q0, wl.slab, w, torch.from_numpy(wl.block_table).cuda(),
+                                       torch.from_numpy(wl.ctx_len).cuda(), 256, wl.scale_bits)
+    assert err_a == 0
+    assert np.all(out_a[pad] == 0)
+    empty = [b for b in real if wl.ctx_len[b] == 0][0]
+    assert np.all(out_a[empty] == 0) and np.all(am_a[empty] == -1)
+
+    # (b) reversed real rows, permuted pages, extra padding rows and multi-split neighbours
+    perm = np.random.default_rng(6).permutation(wl.n_pages)
+    slab2 = torch.empty_like(wl.slab)
+    slab2[torch.from_numpy(perm).cuda()] = wl.slab
+    long_ctx = [9000, 4097, 20000]
+    max_ctx = 20000
+    mp = -(-max_ctx // 64)
+    rows = list(reversed(real))
+    n_extra_pad = 10
+    B2 = len(rows) + len(long_ctx) + n_extra_pad
+    tbl = np.full((B2, mp), -1, np.int32)
+    ctx = np.zeros(B2, np.int32)
+    q2 = (torch.randn(B2, 96, 192, generator=g, device="cuda")).to(torch.bfloat16)
+    order = []  # (kind, source row)
+    rng = np.random.default_rng(7)
+    slots = list(range(B2))
+    rng.shuffle(slots)
+    it = iter(slots)
+    for b in rows:
+        i = next(it)
+        t = wl.block_table[b]
+        tbl[i, :t.shape[0]] = np.where(t >= 0, perm[np.maximum(t, 0)], -1)
+        ctx[i] = wl.ctx_len[b]
+        q2[i] = q0[b]
+        order.append((i, b))
+    for n in long_ctx:
+        i = next(it)
+        tbl[i, :-(-n // 64)] = rng.integers(0, wl.n_pages, size=-(-n // 64))
+        ctx[i] = n
+    for _ in range(n_extra_pad):
+        i = next(it)
+        ctx[i] = int(rng.integers(1, 257))
+    assert max(k3mla.slot_split_tokens(n) for n in long_ctx) < 20000  # the neighbours have several splits
+    out_b, am_b, err_b = _graph_decode(q2, slab2, w, torch.from_numpy(tbl).cuda(), torch.from_numpy(ctx).cuda(),
+                                       max_ctx, wl.scale_bits)
+    assert err_b == 0
+    for i, b in order:
+        assert np.array_equal(out_b[i], out_a[b]), f"row {b} differs in the mixed batch"
+        assert np.array_equal(am_b[i], am_a[b]), f"argmax of row {b} differs in the mixed batch"
+
+    # (c) five real rows at a time (absorption and expansion tiles of a small batch)
+    for k in range(0, 20, 5):
+        sel = real[k:k + 5]
+        t = torch.from_numpy(np.ascontiguousarray(wl.block_table[sel])).cuda()
+        c = torch.from_numpy(np.ascontiguousarray(wl.ctx_len[sel])).cuda()
+        out_c, am_c, err_c = _graph_decode(q0[sel].contiguous(), wl.slab, w, t, c, 300, wl.scale_bits)
+        assert err_c == 0
+        assert np.array_equal(out_c, out_a[sel]) and np.array_equal(am_c, am_a[sel])
+
+
+@pytest.mark.parametrize("split", [k3mla.SPLIT_AUTO, 256])
+def test_max_ctx_does_not_change_a_slots_bits(gpu_lib, split):
+    """max_ctx sizes the grid only: the same slots under max_ctx 1024 and 8192 (4 and 32 launch splits
+    at a 256-token split) give the same bits, for the default rule and a fixed split."""
+    wl = _wl()
+    a = gpu_layer(wl, 0, split=split, max_ctx=MAXC)
+    b = gpu_layer(wl, 0, split=split, max_ctx=8192)
+    assert a["dev_err"] == 0 and b["dev_err"] == 0
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["argmax"], b["argmax"])

@@ -68,7 +68,7 @@ def test_chunked_prefill_attention_matches_oracle(gpu_lib):
     q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
     k3mla.absorb_q(q, wl.w_kv_b[1], q_abs)
     max_ctx = M * 64
-    split = k3mla.default_split_tokens(R, max_ctx)
+    split = k3mla.SPLIT_AUTO
     ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
     out = torch.full((R, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
     am = torch.full((R, H), -7, dtype=torch.int32, device="cuda")
@@ -108,7 +108,7 @@ def test_long_chunks_after_long_prefixes_sampled(gpu_lib):
     q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
     k3mla.absorb_q(q, wl.w_kv_b[1], q_abs)
     max_ctx = M * 64
-    split = k3mla.default_split_tokens(R, max_ctx)
+    split = k3mla.SPLIT_AUTO
     ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
     out = torch.full((R, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
     am = torch.full((R, H), -7, dtype=torch.int32, device="cuda")
@@ -147,7 +147,7 @@ def test_chunk_path_copy_and_exact_mode_replay_from_a_cuda_graph(gpu_lib):
     vc = torch.empty(R, dtype=torch.int32, device="cuda")
     q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device="cuda")
     max_ctx = M * 64
-    split = k3mla.default_split_tokens(R, max_ctx)
+    split = k3mla.SPLIT_AUTO
     ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device="cuda")
     out = torch.empty(R, H, V, dtype=torch.bfloat16, device="cuda")
     ex_ws = torch.empty(k3mla.decode_exact_workspace_bytes(B, max_ctx), dtype=torch.uint8, device="cuda")

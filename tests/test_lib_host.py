@@ -139,6 +139,12 @@ def test_invalid_arguments_return_status_without_launching():
     assert lib.k3mla_append_latent(null, 4, 2, 0, null, 1, null, null, 511, null, 64, 1, null, null) == -1
     args = [null, null, 4, 1, 0, null, 4, null, null, 0x3D94, null, null, null, 0, 1, 256, 100, null, null]
     assert lib.k3mla_paged_decode(*args) == -1
+    args[16] = -128                                            # negative split length
+    assert lib.k3mla_paged_decode(*args) == -1
+    assert b"invalid sizes" in lib.k3mla_last_error()
+    args[16] = 0                                               # the default rule: arguments pass, pointers fail
+    assert lib.k3mla_paged_decode(*args) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
     args[16] = 128
     assert lib.k3mla_paged_decode(*args) == -1                 # null pointers
     assert b"null or misaligned" in lib.k3mla_last_error()
@@ -179,13 +185,34 @@ def test_exact_workspace_formula_and_arguments():
 
 
 def test_workspace_formula():
-    # [B][nsplit][96][512] f32 partial O (rounded up to 256 B) + [B][nsplit][96][4] f32
-    for B, max_ctx, split in ((1, 130, 128), (64, 4096, 4096), (8, 32768, 3712), (128, 256, 256)):
-        ns = -(-max_ctx // split)
-        o = B * ns * 96 * 512 * 4
-        o = (o + 255) // 256 * 256
-        assert k3mla.decode_workspace_bytes(B, max_ctx, split) == o + B * ns * 96 * 4 * 4
+    # o_lat [96][B][512] bf16, then -- only when a slot can have several splits -- f32 partial O
+    # [B][nsplit][96][512], each rounded up to 256 B, then the records [B][nsplit][96][4] f32; nsplit
+    # = ceil(max_ctx / split) for a fixed split, ceil(max_ctx / 4096) for the default rule
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, max_ctx, split in ((1, 130, 128), (64, 4096, 4096), (8, 32768, 3712), (128, 256, 256),
+                              (64, 4096, 0), (8, 32768, 0), (3, 4097, 0), (16, 4096, 512)):
+        ns = -(-max_ctx // (split if split else 4096))
+        want = r256(B * 96 * 512 * 2) + (r256(B * ns * 96 * 512 * 4) if ns > 1 else 0) + B * ns * 96 * 4 * 4
+        assert k3mla.decode_workspace_bytes(B, max_ctx, split) == want, (B, max_ctx, split)
     assert k3mla.decode_workspace_bytes(0, 4096, 128) == 0
+    assert k3mla.decode_workspace_bytes(4, 4096, -128) == 0
+
+
+def test_default_split_rule_depends_on_the_slot_alone():
+    """The default rule cuts a slot of n tokens into ceil(n / 4096) splits of equal length rounded up
+    to the 128-token tile: at most 4096 tokens, every split non-empty, a function of n alone."""
+    for n in list(range(0, 300)) + [4095, 4096, 4097, 5000, 8191, 8192, 8193, 20000, 32768, 51200, 131073]:
+        s = k3mla.slot_split_tokens(n)
+        assert s % 128 == 0 and 128 <= s <= 4096, (n, s)
+        ns = -(-n // s)
+        assert ns == -(-n // 4096), (n, s)              # as many splits as 4096-token pieces
+        assert n == 0 or (ns - 1) * s < n, (n, s)       # the last split holds tokens
+        if 0 < n <= 4096:
+            assert s >= n                               # one split: the slot lands o_lat itself
+    assert k3mla.slot_split_tokens(32768) == 4096 and k3mla.slot_split_tokens(5000) == 2560
+    assert k3mla.slot_split_tokens(1000, 256) == 256    # a fixed split length is used as given
+    lib = k3mla.load()
+    assert lib.k3mla_slot_split_tokens(100, -1) == -1
 
 
 def test_product_and_oracle_share_no_code():
@@ -221,17 +248,12 @@ def _live(ctx, split):
     return sum(-(-max(int(c), 0) // split) for c in ctx)
 
 
-def test_split_for_contexts_matches_the_default_at_full_length():
-    for B, max_ctx in [(1, 4096), (8, 32768), (16, 4096), (64, 4096), (100, 1000), (3, 130)]:
-        assert k3mla.split_tokens_for_contexts([max_ctx] * B, max_ctx) == k3mla.default_split_tokens(B, max_ctx)
-
-
-def test_split_for_contexts_on_ragged_batches():
+def test_batch_planned_split_on_ragged_batches():
     pairs, tile = _pairs(), 128
     rng = np.random.default_rng(5)
     for B, max_ctx in [(16, 4096), (5, 32768), (40, 8192), (2, 640)]:
         ctx = rng.integers(1, max_ctx + 1, size=B)
-        s = k3mla.split_tokens_for_contexts(ctx, max_ctx)
+        s = k3mla.batch_planned_split_tokens(ctx, max_ctx)
         whole = -(-max_ctx // tile) * tile
         assert s % tile == 0 and tile <= s <= whole
         if s < whole:  # the shortest length whose live splits fit one wave of SM pairs
@@ -242,18 +264,18 @@ def test_split_for_contexts_on_ragged_batches():
             shorter = [t for t in range(tile, min(whole, int(ctx.max())), tile) if _live(ctx, t) <= pairs]
             assert not shorter
     # one short context under a long max_ctx: a single whole-context split, not many empty ones
-    assert k3mla.split_tokens_for_contexts([100], 32768) == 32768
-    assert k3mla.split_tokens_for_contexts([0, 0, 0], 4096) == 4096
+    assert k3mla.batch_planned_split_tokens([100], 32768) == 32768
+    assert k3mla.batch_planned_split_tokens([0, 0, 0], 4096) == 4096
     # more slots with tokens than SM pairs: one split per slot
-    assert k3mla.split_tokens_for_contexts([200] * (pairs + 1), 256) == 256
+    assert k3mla.batch_planned_split_tokens([200] * (pairs + 1), 256) == 256
     # clamping: contexts past max_ctx count as max_ctx, negative ones as empty
-    assert k3mla.split_tokens_for_contexts([10**6] * 8, 32768) == k3mla.split_tokens_for_contexts([32768] * 8, 32768)
-    assert k3mla.split_tokens_for_contexts([-5, 100], 32768) == 32768
+    assert k3mla.batch_planned_split_tokens([10**6] * 8, 32768) == k3mla.batch_planned_split_tokens([32768] * 8, 32768)
+    assert k3mla.batch_planned_split_tokens([-5, 100], 32768) == 32768
 
 
-def test_split_for_contexts_arguments():
+def test_batch_planned_split_arguments():
     lib = k3mla.load()
-    assert lib.k3mla_split_tokens_for_contexts(None, 0, 4096) == 128
-    assert lib.k3mla_split_tokens_for_contexts(None, 3, 0) == 128
-    assert lib.k3mla_split_tokens_for_contexts(None, 3, 4096) == -1
+    assert lib.k3mla_batch_planned_split_tokens(None, 0, 4096) == 128
+    assert lib.k3mla_batch_planned_split_tokens(None, 3, 0) == 128
+    assert lib.k3mla_batch_planned_split_tokens(None, 3, 4096) == -1
     assert b"ctx_host is NULL" in lib.k3mla_last_error()
