@@ -178,8 +178,8 @@ def config_for(name, wl, split, layers=None):
             "split_tokens": "auto (per slot: ceil(ctx/4096) equal splits)" if split == 0 else split,
             "l2": "inputs larger than L2 (302 MB latent + 25 MB weights per layer, 7.8 GB per step)"
                   if name in ("steady64", "long8") else "per-layer inputs may be L2-resident",
-            "timing": "24-layer step as one CUDA graph (each layer's append carried by its absorption's launch), "
-                      "CUDA events on the launch stream"}
+            "timing": "24-layer step as one CUDA graph of k3mla_decode_layer calls (append carried by the "
+                      "absorption's launch, then split decode and merge/expansion), CUDA events on the launch stream"}
 
 
 def run_reference(args):
@@ -217,12 +217,12 @@ class Runner:
     (absorption carrying the append, then the paged decode, per layer) and the paged-decode calls
     alone (24 calls), each replayed and timed with CUDA events on the launch stream."""
 
-    def __init__(self, name, split, layers=None):
+    def __init__(self, name, split, layers=None, fused=True, wl=None):
         from paged_latent_attention_k3mla_gb300 import k3mla
         self.k3mla = k3mla
         dev = "cuda"
         self.name = name
-        self.wl = wl = synth.make_workload(name, device=dev, n_layers=layers)
+        self.wl = wl = synth.make_workload(name, device=dev, n_layers=layers) if wl is None else wl
         self.B, self.L = wl.B, wl.n_layers
         self.max_ctx = MAX_CTX[name]
         # a1: page claims from the host free-list pool (shuffled), table to the device
@@ -241,6 +241,11 @@ class Runner:
                               device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.Stream()
+        # one public call per layer-call (k3mla_decode_layer: append at ctx - 1, absorption, paged decode
+        # under the default split); a fixed split length goes through the separate calls instead
+        self.fused = fused and split == 0
+        self.lws = (torch.empty(k3mla.decode_layer_workspace_bytes(self.B, self.max_ctx), dtype=torch.uint8,
+                                device=dev) if self.fused else None)
 
     def absorb_append(self, layer, q, c, r):
         # a2 + a3 in one launch: the append rides on the absorption's grid (neither reads the other)
@@ -254,11 +259,19 @@ class Runner:
                                 self.out[layer], self.ws, self.max_ctx, self.split, dev_err=self.err,
                                 stream=self.stream)
 
+    def layer_call(self, layer, q, c, r):
+        if self.fused:
+            wl = self.wl
+            self.k3mla.decode_layer(q, wl.w_kv_b[layer], wl.slab, layer, self.table, self.ctx, c, r, wl.scale_bits,
+                                    self.out[layer], self.lws, self.max_ctx, dev_err=self.err, stream=self.stream)
+        else:
+            self.absorb_append(layer, q, c, r)
+            self.decode(layer)
+
     def step(self):
         wl = self.wl
         for layer in range(self.L):
-            self.absorb_append(layer, wl.q[layer], wl.new_c[layer], wl.new_rope[layer])
-            self.decode(layer)
+            self.layer_call(layer, wl.q[layer], wl.new_c[layer], wl.new_rope[layer])
 
     def decode_calls(self):
         for layer in range(self.L):
@@ -303,14 +316,17 @@ class Runner:
         return ev0.elapsed_time(ev1) / steps
 
     def measure(self, steps, warmup, clocks=None):
-        """ms per 24-layer step, and ms per paged-decode call (24 decode calls in one graph)."""
+        """ms per 24-layer step, and ms per paged-decode call (24 paged-decode calls in one graph)."""
         g_step = self._graph(self.step)
         ms_step = self._time_graph(g_step, steps, warmup, clocks)
         assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        del g_step
+        if self.fused:  # the decode calls below read the absorbed q the layer calls left in their workspace
+            self.q_abs = self.lws[:self.B * H * ROW * 2].view(torch.bfloat16).view(self.B, H, ROW)
         g_dec = self._graph(self.decode_calls)
         ms_dec = self._time_graph(g_dec, steps, warmup) / self.L
         assert self.err.item() == 0, f"device error bits {self.err.item()}"
-        del g_step, g_dec
+        del g_dec
         return ms_step, ms_dec
 
     def figures(self, ms_step, ms_dec, hbm):
@@ -377,8 +393,7 @@ def e2e_leg(run, steps, warmup):
             if layer in first_of_group:             # the inputs of this group of layers have landed
                 stream.wait_event(ev_in[first_of_group[layer]])
             with torch.cuda.stream(stream):
-                run.absorb_append(layer, q_d[layer], c_d[layer], r_d[layer])
-                run.decode(layer)
+                run.layer_call(layer, q_d[layer], c_d[layer], r_d[layer])
                 ev_dec[layer].record(stream)
             copy_s.wait_event(ev_dec[layer])
             with torch.cuda.stream(copy_s):
@@ -435,6 +450,8 @@ def extra_workloads(hbm, steps, warmup):
         fig = run.figures(ms_step, ms_dec, hbm)
         fig["split_tokens"] = "auto" if split == 0 else split
         fig["layers"] = run.L
+        fig["path"] = ("k3mla_decode_layer per layer-call" if run.fused else
+                       "k3mla_absorb_q_append + k3mla_paged_decode per layer-call")
         if split_kind == "planned":
             fig["numerics"] = "batch-dependent (opt-in k3mla_batch_planned_split_tokens)"
         res[name if split_kind == "auto" else f"{name}_planned"] = fig
@@ -480,7 +497,6 @@ def main():
     e2e_ms, h2d, d2h, digest = e2e_leg(run, args.steps, args.warmup)
     nxt = None if args.no_next else next_rows(wl, run.table, run.max_ctx, run.stream, hbm, tflops)
     ab = alg_bytes(wl)
-    dec_gbs = ab["decode"] / (ms_dec * 1e-3) / 1e9
     layer_gbs = ab["layer"] / (us_per_layer * 1e-6) / 1e9
     flops = alg_flops(wl)
     traffic = None
@@ -492,6 +508,13 @@ def main():
                 traffic = d.get("bytes_per_call")
         except (ValueError, OSError):
             traffic = None
+    dec_gbs = ab["decode"] / (ms_dec * 1e-3) / 1e9
+    roofline = {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
+                "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
+                "traffic": traffic, "alg_bytes_per_call": ab["decode"], "avg_call_us": round(ms_dec * 1e3, 3),
+                "timing": f"{L} paged-decode calls in one CUDA graph, replayed; CUDA events on the launch "
+                          f"stream; per call = graph time / {L}",
+                "peak_source": f"{src} hbm_gbs"}
     cpu = None if args.no_cpu else cpu_baseline(wl)
     cfg = config_for(args.workload, wl, args.split, args.layers)
     del run, wl
@@ -503,19 +526,14 @@ def main():
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": cfg,
         "latent_gbs": round(ab["latent"] / (us_per_layer * 1e-6) / 1e9, 1),
-        "roofline": {"kernel": "k3mla_paged_decode (split decode + merge/W_UV expansion)", "bound": "hbm",
-                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
-                     "traffic": traffic, "alg_bytes_per_call": ab["decode"], "avg_call_us": round(ms_dec * 1e3, 3),
-                     "timing": f"{L} paged-decode calls in one CUDA graph, replayed; CUDA events on the launch "
-                               f"stream; per call = graph time / {L}",
-                     "peak_source": f"{src} hbm_gbs"},
+        "roofline": roofline,
         "layer_roofline": {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": hbm, "unit": "GB/s",
                            "frac": round(layer_gbs / hbm, 4), "alg_bytes_per_layer_call": ab["layer"],
                            "tensor_frac": round(flops / (us_per_layer * 1e-6) / 1e12 / tflops, 4),
                            "tensor_peak_tflops": tflops},
         "e2e": {"value": round(e2e_ms * 1e3 / L, 3), "unit": "us/layer-call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * L * 3,   # absorb+append, split decode, merge/expand per layer
+        "gpu_launches": args.steps * L * 3,   # per layer-call: absorption + append, split decode, merge/expansion
         "clocks": clk.summary(),
         "out_sha256_16": digest,
         "cpu_baseline": cpu,

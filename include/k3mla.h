@@ -245,6 +245,32 @@ int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages,
                        uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes,
                        int B, int max_ctx, int split_tokens, int32_t* dev_err, void* stream);
 
+/* ---- one decode step of one layer: append + absorption + paged decode -----------
+ * (PR #869, M1 and M2 commits: the new token's row written into its mapped page,
+ * q absorbed, then the absorbed attention over the slot's pages.)
+ * Exactly k3mla_absorb_q_append with each slot's write position ctx_len[b] - 1
+ * (no write for ctx_len[b] <= 0), followed by k3mla_paged_decode with
+ * split_tokens = K3MLA_SPLIT_AUTO on the q_abs it produced: the same outputs, bit
+ * for bit, and the same error behaviour, in three kernel launches on `stream`
+ * (absorption with the append, split decode, merge / expansion).  ctx_len counts
+ * this step's token.  The call a decode step makes once per MLA layer.
+ * q, w_kv_b, slab, block_table, ctx_len, scale_bf16, out, argmax_t, B, max_ctx,
+ *             dev_err: as for k3mla_absorb_q / k3mla_paged_decode
+ * c_kv, c_stride, k_rope, r_stride: this step's rows, as for k3mla_append_latent
+ * workspace   device, >= k3mla_decode_layer_workspace_bytes(B, max_ctx) bytes,
+ *             256-byte aligned, scratch (q_abs, then the decode workspace); no
+ *             initialisation needed.
+ * As for k3mla_paged_decode, the kernel immediately before this call in `stream`
+ * must not write ctx_len (the split kernel reads it when it starts); the first
+ * kernel of the call reads q, the rows and the tables only after the kernel ahead
+ * of it has completed, and w_kv_b at once. */
+size_t k3mla_decode_layer_workspace_bytes(int B, int max_ctx);
+int k3mla_decode_layer(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* slab, int n_pages, int n_layers,
+                       int layer, const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
+                       const uint16_t* c_kv, int64_t c_stride, const uint16_t* k_rope, int64_t r_stride,
+                       uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes,
+                       int B, int max_ctx, int32_t* dev_err, void* stream);
+
 /* The split length a slot of context ctx gets from k3mla_paged_decode:
  * split_tokens when it is positive, else the default rule's length (at most
  * K3MLA_SPLIT_MAX; K3MLA_TILE for ctx <= 0).  The slot then has
@@ -372,6 +398,21 @@ int k3mla_paged_decode_noalloc(const uint16_t* q_abs, const uint16_t* slab, int 
                                const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
                                uint16_t* out, int32_t* argmax_t, int B, int max_ctx, int split_tokens,
                                int32_t* dev_err, void* stream);
+
+/* ---- diagnostic: the abort path of the bounded waits ---------------------------
+ * Not part of the decode path.  k3mla_paged_decode with two changes that exist only
+ * to exercise what happens when a device wait runs out: in every split, the first
+ * third of logical page `withhold_page` (>= 1) of the split is never loaded, so the
+ * waits on it cannot complete, and every bounded wait of the split kernel gives up
+ * after `wait_us` microseconds (100 .. 100000) instead of 1 s.  The kernels then set
+ * K3MLA_DEV_TIMEOUT in *dev_err, let every copy and MMA they issued land, free their
+ * tensor memory and return; the outputs are invalid.  Returns as k3mla_paged_decode
+ * (K3MLA_E_INVALID for the two arguments out of range). */
+int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                              const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
+                              const uint16_t* w_kv_b, uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t,
+                              void* workspace, size_t ws_bytes, int B, int max_ctx, int split_tokens,
+                              int withhold_page, uint32_t wait_us, int32_t* dev_err, void* stream);
 
 /* ---- diagnostic --------------------------------------------------------------
  * Runs the decode kernel's two tensor-core contractions on one 64-token page in

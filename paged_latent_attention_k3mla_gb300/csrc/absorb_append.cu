@@ -81,6 +81,7 @@ struct AppendJob {
     int32_t* dev_err;
     int64_t c_stride, r_stride;
     int n_pages, n_layers, layer, max_pages, B;
+    int pos_is_ctx;  // `pos` holds context lengths: the write position is pos[b] - 1
 };
 constexpr int AP_THREADS = 96;  // a row is 288 32-bit words: three per thread
 
@@ -95,7 +96,7 @@ __device__ __forceinline__ int64_t append_fetch(const AppendJob& ap, int b, int 
         const int w = at + AP_THREADS * k;
         v[k] = (w < LORA / 2) ? src_c[w] : src_r[w - LORA / 2];
     }
-    const int p = ap.pos[b];
+    const int p = ap.pos[b] - (ap.pos_is_ctx ? 1 : 0);
     if (p < 0) return -1;
     const int lp = p / PAGE;
     const int32_t id = (lp < ap.max_pages) ? ap.table[(size_t)b * ap.max_pages + lp] : -1;
@@ -351,7 +352,7 @@ extern "C" int k3mla_absorb_q(const uint16_t* q, const uint16_t* w_kv_b, uint16_
     const int rc = check_absorb("k3mla_absorb_q", q, w_kv_b, q_abs, B);
     if (rc || B == 0) return rc;
     AppendJob none{};
-    return launch_absorb(q, w_kv_b, q_abs, B, none, stream);
+    return launch_absorb(q, w_kv_b, q_abs, B, none, stream);  // none.B == 0: no append
 }
 
 extern "C" int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, uint16_t* slab,
@@ -379,8 +380,35 @@ extern "C" int k3mla_absorb_q_append(const uint16_t* q, const uint16_t* w_kv_b, 
     ap.layer = layer;
     ap.max_pages = max_pages_per_slot;
     ap.B = B;
+    ap.pos_is_ctx = 0;
     return launch_absorb(q, w_kv_b, q_abs, B, ap, stream);
 }
+
+namespace k3 {
+int launch_absorb_append_at_ctx(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, uint16_t* slab,
+                                int n_pages, int n_layers, int layer, const int32_t* block_table,
+                                int max_pages_per_slot, const int32_t* ctx_len, const uint16_t* c_kv,
+                                int64_t c_stride, const uint16_t* k_rope, int64_t r_stride, int B, int32_t* dev_err,
+                                cudaStream_t stream)
+{
+    AppendJob ap;
+    ap.slab = slab;
+    ap.table = block_table;
+    ap.pos = ctx_len;
+    ap.c_kv = c_kv;
+    ap.k_rope = k_rope;
+    ap.dev_err = dev_err;
+    ap.c_stride = c_stride;
+    ap.r_stride = r_stride;
+    ap.n_pages = n_pages;
+    ap.n_layers = n_layers;
+    ap.layer = layer;
+    ap.max_pages = max_pages_per_slot;
+    ap.B = B;
+    ap.pos_is_ctx = 1;
+    return launch_absorb(q, w_kv_b, q_abs, B, ap, stream);
+}
+}  // namespace k3
 
 extern "C" int k3mla_append_latent(uint16_t* slab, int n_pages, int n_layers, int layer,
                                    const int32_t* block_table, int max_pages_per_slot, const int32_t* pos,

@@ -123,4 +123,12 @@ struct MergeParams {
 };
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st);
 
+// k3mla_absorb_q_append with each slot's write position ctx_len[b] - 1 (none when ctx_len[b] <= 0): the
+// append of a decode step whose context lengths already count the new token (absorb_append.cu).
+int launch_absorb_append_at_ctx(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* q_abs, uint16_t* slab,
+                                int n_pages, int n_layers, int layer, const int32_t* block_table,
+                                int max_pages_per_slot, const int32_t* ctx_len, const uint16_t* c_kv,
+                                int64_t c_stride, const uint16_t* k_rope, int64_t r_stride, int B, int32_t* dev_err,
+                                cudaStream_t stream);
+
 }  // namespace k3

@@ -55,8 +55,9 @@
 // of a head moves only when a page max exceeds it by more than TAU (else
 // exp(s - m_ref) <= e^TAU, far inside f32 / bf16 range); exp is the hardware ex2.
 //
-// Every wait is bounded: after WAIT_NS a wait sets K3MLA_DEV_TIMEOUT in the
-// device error word, lets in-flight copies land and returns (no trap, no hang).
+// Every wait is bounded: after WAIT_NS (1 s; shorter only through the diagnostic
+// entry that tests this path) a wait sets K3MLA_DEV_TIMEOUT in the device error
+// word, lets in-flight copies land and returns (no trap, no hang).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -76,6 +77,8 @@ constexpr int HALF = 32;                       // PV CTA: tokens per half-page b
 constexpr int THIRD = 3 * 8192;  // score CTA: a third of a page (3 chunks), one TMA box
 constexpr int NUNIT = 8;         // score CTA: ring of third-page units (2.67 pages)
 constexpr int PSTAGE = 24 * 128; // score CTA: one softmax warp's P rows (24 heads x 64 tokens bf16)
+constexpr int Q_UNIT0 = 4;       // score CTA: q_abs lands in ring units 4.. (and the P staging area after
+                                 // them) until it is in TMEM, so units 0..3 take pages meanwhile
 constexpr int NHSLOT = 5;                      // PV CTA: half-page slots (one producer each)
 constexpr int SLOT1 = 8 * HALF * 128;          // 32768 B: [8 chunks][32 rows][128 B], chunks 0..7 only
 constexpr int HCHUNK = HALF * 128;             // 4096 B per chunk of a half-page slot
@@ -137,10 +140,12 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
+    uint64_t wait_ns;  // the limit of every bounded wait of this CTA
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
 static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
-static_assert(QBYTES <= (NUNIT - 3) * THIRD, "q_abs staging fits in units 3..");
+static_assert(QBYTES <= (NUNIT - Q_UNIT0) * THIRD + 8 * PSTAGE,
+              "q_abs staging fits in units Q_UNIT0.. and the P staging area that follows them");
 static_assert(PCOPY <= PBUF, "P buffer");
 static_assert(H * LORA * 4 <= NHSLOT * SLOT1 + NPBUF * PBUF,
               "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
@@ -156,6 +161,8 @@ struct DecodeParams {
     int max_pages, n_pages, n_layers, layer;
     int B, max_ctx, split_tokens, nsplit;  // split_tokens 0: the default per-slot rule; nsplit: the grid's
     uint32_t scale2;  // the bf16 scale in both halves
+    uint64_t wait_ns;  // bounded-wait limit: WAIT_NS, shorter only from the diagnostic entry
+    int32_t withhold;  // diagnostic only, 0 otherwise: page k - 1's first third is never loaded
 };
 
 __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int max_ctx, int max_pages,
@@ -175,7 +182,7 @@ __device__ __forceinline__ bool aborted(const Smem& sm)
     return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
 }
 
-// Bounded mbarrier wait, slow path: gives up after WAIT_NS or when this CTA aborted.
+// Bounded mbarrier wait, slow path: gives up after the CTA's wait limit or when this CTA aborted.
 __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
                                            bool cluster_scope)
 {
@@ -186,7 +193,7 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Smem&
         if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
         if ((n & 127u) == 0) {
             if (aborted(sm)) return false;
-            if (globaltimer() - t0 > WAIT_NS) {
+            if (globaltimer() - t0 > sm.wait_ns) {
                 *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
                 if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
                 return false;
@@ -214,7 +221,7 @@ __device__ __noinline__ bool wait_count(const int32_t* counter, int32_t target, 
     const uint64_t t0 = globaltimer();
     while (*v < target) {
         if (aborted(sm)) return false;
-        if (globaltimer() - t0 > WAIT_NS) {
+        if (globaltimer() - t0 > sm.wait_ns) {
             *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
             if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_TIMEOUT);
             return false;
@@ -390,91 +397,79 @@ __device__ __noinline__ void pv_write_out(Smem& sm, float* ws_o, uint16_t* ws_ol
     }
 }
 
-// ---- the split decode kernel ---------------------------------------------------------
+// ---- one split: geometry, barriers -------------------------------------------------------
 
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
-    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
-                              const __grid_constant__ CUtensorMap tmap_page8,
-                              const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
+// Where split s of slot b lies: set from the slot's (clamped) context; false for an empty split.
+struct SplitGeom {
+    int b, s, start, ntok, npg, n_lp, lp0;
+    bool single;      // the slot has at most one split: the PV CTA lands final o_lat itself
+    int32_t oob_row;  // a slab row past the end (a TMA box there reads zeros)
+};
+
+__device__ __forceinline__ bool split_geom(SplitGeom& g, int ctx, const DecodeParams& p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t warp = threadIdx.x >> 5;
-    const uint32_t lane = lane_id();
-
-    const int unit = blockIdx.x >> 1;
-    const int b = unit / p.nsplit;
-    const int s = unit % p.nsplit;
-    const int ctx = ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages, p.dev_err,
-                                  rank == 0 && threadIdx.x == 0 && s == 0);
     const int split = slot_split(ctx, p.split_tokens);
-    const bool single = slot_nsplit(ctx, split) <= 1;  // the PV CTA lands final o_lat itself
-    const int start = s * split;
-    if (start >= ctx) {  // empty split: both CTAs leave, nothing was shared
-        if (s == 0 && rank == 1) {  // an empty context: its o_lat is zero (the workspace is written only
-            griddep_wait();         // after the kernel before has completed: it may still read it)
-            zero_olat(p.ws_olat, p.B, b);
-        }
-        return;
-    }
-    const int ntok = min(ctx, start + split) - start;
-    const int npg = (ntok + PAGE - 1) / PAGE;
-    const int n_lp = (ctx + PAGE - 1) / PAGE;
-    const int lp0 = start / PAGE;
-    const int32_t oob_row = p.n_pages * p.n_layers * PAGE;
+    g.single = slot_nsplit(ctx, split) <= 1;
+    g.start = g.s * split;
+    if (g.start >= ctx) return false;
+    g.ntok = min(ctx, g.start + split) - g.start;
+    g.npg = (g.ntok + PAGE - 1) / PAGE;
+    g.n_lp = (ctx + PAGE - 1) / PAGE;
+    g.lp0 = g.start / PAGE;
+    g.oob_row = p.n_pages * p.n_layers * PAGE;
+    return true;
+}
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 9; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 1);
-        }
-        for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 4);
-        }
-        for (int i = 0; i < NPBUF; ++i) {
-            mbar_init(&sm.p_full[i], 1);
-            mbar_init(&sm.p_empty[i], 1);
-        }
-        mbar_init(&sm.q_land, 1);
-        mbar_init(&sm.q_ready, 4);
-        mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.epi_req, 1);
-        mbar_init(&sm.epi_done, 4);
-        mbar_init(&sm.l_full, 1);
-        sm.abort_flag = 0;
-        sm.fin_ready = 0;
-        for (int i = 0; i < NUNIT; ++i) {
-            sm.unit_loaded[i] = 0;
-            sm.unit_taken[i] = 0;
-        }
-        if (rank == 1) {  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
-            for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
-            if (single) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
-        }
-        fence_mbarrier_init_cluster();
-        if (rank == 0) tma_prefetch_desc(&tmap_q);
+// Score CTA: where q_abs is staged (ring units Q_UNIT0.. and the P staging area after them).
+__device__ __forceinline__ uint8_t* q_stage(Smem& sm) { return reinterpret_cast<uint8_t*>(&sm.u) + Q_UNIT0 * THIRD; }
+
+// Thread 0: the mbarriers and counters of one split (the caller fences them for the cluster).
+__device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bool single, uint64_t wait_ns)
+{
+    sm.wait_ns = wait_ns;
+    for (int i = 0; i < 9; ++i) {
+        mbar_init(&sm.full[i], 1);
+        mbar_init(&sm.empty[i], 1);
     }
-    if (warp == W_ALLOC) {
-        tmem_alloc(&sm.tmem_base, TMEM_COLS);
-        tmem_relinquish();
+    for (int i = 0; i < NSLOT; ++i) {
+        mbar_init(&sm.s_full[i], 1);
+        mbar_init(&sm.s_empty[i], 4);
     }
-    if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tmap_page);
-        tma_prefetch_desc(&tmap_page8);
+    for (int i = 0; i < NPBUF; ++i) {
+        mbar_init(&sm.p_full[i], 1);
+        mbar_init(&sm.p_empty[i], 1);
     }
-    tc_fence_before();
-    cluster_sync();
-    tc_fence_after();
-    const uint32_t tbase = sm.tmem_base;
-    // everything above overlaps the previous kernel in the stream (which must not write ctx_len, read
-    // at the top to size the split); q_abs, the slab and the block table are read after it completed
-    griddep_wait();
-    griddep_launch_dependents();
-    if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in page slots 1..2 until it is in TMEM
+    mbar_init(&sm.q_land, 1);
+    mbar_init(&sm.q_ready, 4);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.epi_req, 1);
+    mbar_init(&sm.epi_done, 4);
+    mbar_init(&sm.l_full, 1);
+    sm.abort_flag = 0;
+    sm.fin_ready = 0;
+    for (int i = 0; i < NUNIT; ++i) {
+        sm.unit_loaded[i] = 0;
+        sm.unit_taken[i] = 0;
+    }
+    if (rank == 1) {  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
+        for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
+        if (single) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
+    }
+}
+
+// The roles of both CTAs for one split: q_abs into TMEM, the page ring, the two contractions, the softmax,
+// and the PV CTA's write-out of O.  Inlined into the kernel: the parameters it reads in its loops stay
+// constant-bank operands (an out-of-line copy, reaching them through a pointer, ran some 50 % slower).
+__device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_page, const CUtensorMap& tmap_page8,
+                                             const CUtensorMap& tmap_q, const DecodeParams& p, const SplitGeom& sg,
+                                             uint32_t tbase, uint32_t rank, uint32_t warp, uint32_t lane)
+{
+    const int b = sg.b, s = sg.s, start = sg.start, ntok = sg.ntok, npg = sg.npg, n_lp = sg.n_lp, lp0 = sg.lp0;
+    const bool single = sg.single;
+    const int32_t oob_row = sg.oob_row;
+    if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in ring units 4.. until it is in TMEM
         mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-        for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[3] + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
+        for (int c = 0; c < 9; ++c) tma_load_3d(q_stage(sm) + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
     }
 
     if (rank == 0) {
@@ -484,11 +479,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                 // third g = 3i + t of the split lives in unit g % NUNIT; a unit's uses are strictly
                 // ordered (a use is loaded only after the MMAs of the previous use released it)
                 const int t = (int)warp - W_PROD0;
-                bool ok = true;
+                bool ok = true, q_in_tmem = false;
                 for (int i = 0; i < npg && ok; ++i) {
-                    if (i == 1) ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);  // units 3.. hold q_abs until then
-                    if (!ok) break;
                     const int g = 3 * i + t, u = g % NUNIT, k = g / NUNIT;
+                    if (!q_in_tmem && g >= Q_UNIT0) {  // units Q_UNIT0.. hold q_abs until it is in TMEM
+                        ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
+                        q_in_tmem = true;
+                    }
+                    if (!ok || (t == 0 && i + 1 == p.withhold)) break;  // (diagnostic: a load never issued)
                     const int32_t y = page_row(p, b, lp0 + i, n_lp, oob_row);
                     if (!wait_count(&sm.unit_loaded[u], k, sm, p.dev_err) ||
                         !wait_bar(&sm.empty[u], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
@@ -542,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
             const uint32_t bar_out = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)par;
             if (par == 0) {
                 const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
-                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, sm.u.c0.ring[3]);
+                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, q_stage(sm));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.q_ready);
@@ -713,10 +711,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                     st_async_b32(mapa(smem_u32(&sm.rl[h]), 1), __float_as_uint(1.f / ltot),
                                  mapa(smem_u32(&sm.l_full), 1));
             }
-            // this warp's bulk copies have read their staging rows, and the PV CTA's last releases
-            // of its P buffers land here, before exit
+            // this warp's bulk copies are complete (their bytes have landed in the PV CTA), and the PV
+            // CTA's last releases of its P buffers land here, before exit
             if (lane == 0) {
-                bulk_wait_read<0>();
+                bulk_wait<0>();
                 for (int i = max(0, npg - NPBUF); i < npg && !aborted(sm); ++i)
                     wait_bar(&sm.p_empty[i % NPBUF], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err);
             }
@@ -855,6 +853,58 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
             pv_write_out(sm, single ? nullptr : p.ws_o, single ? p.ws_olat : nullptr, p.B, p.nsplit, tbase, b, s);
     }
 
+}
+
+// ---- the split decode kernel ---------------------------------------------------------
+
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
+    k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
+                              const __grid_constant__ CUtensorMap tmap_page8,
+                              const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+
+    const int unit = blockIdx.x >> 1;
+    SplitGeom sg;
+    sg.b = unit / p.nsplit;
+    sg.s = unit % p.nsplit;
+    const int ctx = ctx_effective(p.ctx_len, sg.b, p.max_ctx, p.max_pages, p.dev_err,
+                                  rank == 0 && threadIdx.x == 0 && sg.s == 0);
+    if (!split_geom(sg, ctx, p)) {  // empty split: both CTAs leave, nothing was shared
+        if (sg.s == 0 && rank == 1) {  // an empty context: its o_lat is zero (the workspace is written only
+            griddep_wait();            // after the kernel before has completed: it may still read it)
+            zero_olat(p.ws_olat, p.B, sg.b);
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        init_decode_barriers(sm, rank, sg.single, p.wait_ns);
+        fence_mbarrier_init_cluster();
+        if (rank == 0) tma_prefetch_desc(&tmap_q);
+    }
+    if (warp == W_ALLOC) {
+        tmem_alloc(&sm.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmap_page);
+        tma_prefetch_desc(&tmap_page8);
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+    // everything above overlaps the previous kernel in the stream (which must not write ctx_len, read
+    // at the top to size the split); q_abs, the slab and the block table are read after it completed
+    griddep_wait();
+    griddep_launch_dependents();
+    decode_roles(sm, tmap_page, tmap_page8, tmap_q, p, sg, tbase, rank, warp, lane);
+
     __syncwarp();
     tc_fence_before();
     cluster_sync();
@@ -876,6 +926,7 @@ __global__ void __launch_bounds__(128, 1)
         mbar_init(&sm.q_land, 1);
         mbar_init(&sm.o_done, 1);
         sm.abort_flag = 0;
+        sm.wait_ns = WAIT_NS;
         fence_mbarrier_init_cluster();
     }
     if (warp == 0) {
@@ -965,7 +1016,6 @@ __global__ void __launch_bounds__(128, 1)
 
 static size_t smem_bytes() { return sizeof(Smem) + 1024; }
 
-static int num_splits(int max_ctx, int split) { return (max_ctx + split - 1) / split; }
 
 static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_rows, CUtensorMap* page,
                      CUtensorMap* page8, CUtensorMap* qmap)
@@ -1006,11 +1056,11 @@ extern "C" int k3mla_slot_split_tokens(int ctx, int split_tokens)
     return slot_split(ctx < 0 ? 0 : ctx, split_tokens);
 }
 
-extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
-                                  int layer, const int32_t* block_table, int max_pages_per_slot,
-                                  const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
-                                  uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes, int B,
-                                  int max_ctx, int split_tokens, int32_t* dev_err, void* stream)
+static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                        const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
+                        const uint16_t* w_kv_b, uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t,
+                        void* workspace, size_t ws_bytes, int B, int max_ctx, int split_tokens, int32_t* dev_err,
+                        void* stream, uint64_t wait_ns, int withhold)
 {
     if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
         max_ctx <= 0 || split_tokens < 0 || split_tokens % TILE != 0) {
@@ -1066,6 +1116,8 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     dp.split_tokens = split_tokens;
     dp.nsplit = ns;
     dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
+    dp.wait_ns = wait_ns;
+    dp.withhold = withhold;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     rc = launch_pdl(k3mla_decode_split_kernel, dim3(2 * B * ns), dim3(THREADS), smem, st, "k3mla_decode_split_kernel",
                     tm_page, tm_page8, tm_q, dp);
@@ -1087,6 +1139,81 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
     mp.nsplit = ns;
     mp.tile = ns == 1 ? 64 : 16;  // every o_lat landed: TMA-loaded in 64-slot tiles; else merged, 16 a CTA
     return launch_merge_expand(mp, st);
+}
+
+extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
+                                  int layer, const int32_t* block_table, int max_pages_per_slot,
+                                  const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
+                                  uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes, int B,
+                                  int max_ctx, int split_tokens, int32_t* dev_err, void* stream)
+{
+    return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
+                        scale_bf16, out, argmax_t, workspace, ws_bytes, B, max_ctx, split_tokens, dev_err, stream,
+                        WAIT_NS, 0);
+}
+
+extern "C" int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
+                                         int layer, const int32_t* block_table, int max_pages_per_slot,
+                                         const int32_t* ctx_len, const uint16_t* w_kv_b, uint16_t scale_bf16,
+                                         uint16_t* out, int32_t* argmax_t, void* workspace, size_t ws_bytes, int B,
+                                         int max_ctx, int split_tokens, int withhold_page, uint32_t wait_us,
+                                         int32_t* dev_err, void* stream)
+{
+    if (withhold_page < 1 || wait_us < 100 || wait_us > 100000) {
+        set_error("k3mla_diag_decode_timeout: withhold_page >= 1 and 100 <= wait_us <= 100000");
+        return K3MLA_E_INVALID;
+    }
+    return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
+                        scale_bf16, out, argmax_t, workspace, ws_bytes, B, max_ctx, split_tokens, dev_err, stream,
+                        (uint64_t)wait_us * 1000ull, withhold_page + 1);
+}
+
+// ---- one decode step of one layer ------------------------------------------------------
+
+static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+extern "C" size_t k3mla_decode_layer_workspace_bytes(int B, int max_ctx)
+{
+    if (B <= 0 || max_ctx <= 0) return 0;
+    return up256((size_t)B * H * ROW * 2) + ws_layout(B, launch_nsplit(max_ctx, 0)).total;
+}
+
+extern "C" int k3mla_decode_layer(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* slab, int n_pages,
+                                  int n_layers, int layer, const int32_t* block_table, int max_pages_per_slot,
+                                  const int32_t* ctx_len, const uint16_t* c_kv, int64_t c_stride,
+                                  const uint16_t* k_rope, int64_t r_stride, uint16_t scale_bf16, uint16_t* out,
+                                  int32_t* argmax_t, void* workspace, size_t ws_bytes, int B, int max_ctx,
+                                  int32_t* dev_err, void* stream)
+{
+    if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
+        max_ctx <= 0 || c_stride < LORA || r_stride < ROPE || (c_stride & 1) || (r_stride & 1)) {
+        set_error("k3mla_decode_layer: invalid sizes or strides");
+        return K3MLA_E_INVALID;
+    }
+    if (B == 0) return K3MLA_OK;
+    if (!q || !w_kv_b || !slab || !block_table || !ctx_len || !c_kv || !k_rope || !out || !workspace ||
+        !aligned(q, 16) || !aligned(w_kv_b, 16) || !aligned(slab, 16) || !aligned(out, 4) || !aligned(c_kv, 4) ||
+        !aligned(k_rope, 4) || !aligned(workspace, 256)) {
+        set_error("k3mla_decode_layer: null or misaligned pointer");
+        return K3MLA_E_INVALID;
+    }
+    const size_t need = k3mla_decode_layer_workspace_bytes(B, max_ctx);
+    if (ws_bytes < need) {
+        set_error("k3mla_decode_layer: workspace %zu < %zu bytes", ws_bytes, need);
+        return K3MLA_E_WORKSPACE;
+    }
+    if (!device_ok()) return K3MLA_E_DEVICE;
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    uint16_t* q_abs = reinterpret_cast<uint16_t*>(ws);
+    uint8_t* dws = ws + up256((size_t)B * H * ROW * 2);
+    const size_t dws_bytes = ws_bytes - (size_t)(dws - ws);
+    const int rc = launch_absorb_append_at_ctx(q, w_kv_b, q_abs, slab, n_pages, n_layers, layer, block_table,
+                                               max_pages_per_slot, ctx_len, c_kv, c_stride, k_rope, r_stride, B,
+                                               dev_err, reinterpret_cast<cudaStream_t>(stream));
+    if (rc) return rc;
+    return k3mla_paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
+                              scale_bf16, out, argmax_t, dws, dws_bytes, B, max_ctx, K3MLA_SPLIT_AUTO, dev_err,
+                              stream);
 }
 
 // ---- decode with built-in scratch ----------------------------------------------------

@@ -151,6 +151,7 @@ __device__ __forceinline__ void fence_proxy_async_cluster()
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)

@@ -29,6 +29,7 @@ EXPORTS = (
     "k3mla_absorb_q_append", "k3mla_pool_share_prefix", "k3mla_pool_cow", "k3mla_pool_page_refs",
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
     "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_batch_planned_split_tokens",
+    "k3mla_decode_layer_workspace_bytes", "k3mla_decode_layer", "k3mla_diag_decode_timeout",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -70,6 +71,8 @@ def load(build_if_needed: bool = True):
             "k3mla_pool_stats": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "k3mla_pool_destroy": ([P], None),
             "k3mla_diag_umma": ([I, P, P, P, P], I),
+            "k3mla_diag_decode_timeout": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, I,
+                                           ctypes.c_uint32, P, P], I),
             "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
             "k3mla_absorb_q_append": ([P, P, P, P, I, I, I, P, I, P, P, I64, P, I64, I, P, P], I),
             "k3mla_pool_share_prefix": ([P, I, I, I], I),
@@ -79,6 +82,9 @@ def load(build_if_needed: bool = True):
             "k3mla_append_latent_rows": ([P, I, I, I, P, I, P, P, P, I64, P, I64, I, I, P, P], I),
             "k3mla_chunk_views": ([P, I, I, P, P, I, P, P, P], I),
             "k3mla_decode_exact_workspace_bytes": ([I, I], SZ),
+            "k3mla_decode_layer_workspace_bytes": ([I, I], SZ),
+            "k3mla_decode_layer": ([P, P, P, I, I, I, P, I, P, P, I64, P, I64, ctypes.c_uint16, P, P, P, SZ, I, I, P, P],
+                                   I),
             "k3mla_decode_exact": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
@@ -237,6 +243,33 @@ def decode_exact(q: torch.Tensor, slab: torch.Tensor, layer: int, block_table: t
         "k3mla_decode_exact")
 
 
+def decode_layer_workspace_bytes(B: int, max_ctx: int) -> int:
+    return int(load().k3mla_decode_layer_workspace_bytes(B, max_ctx))
+
+
+
+def decode_layer(q: torch.Tensor, w_kv_b: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
+                 ctx_len: torch.Tensor, c_kv: torch.Tensor, k_rope: torch.Tensor, scale_bf16: int, out: torch.Tensor,
+                 workspace: torch.Tensor, max_ctx: int, argmax: torch.Tensor | None = None,
+                 dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """One decode step of one layer (append at ctx_len - 1, absorption, paged decode under the
+    default split); see k3mla_decode_layer.  `workspace`: uint8, >= decode_layer_workspace_bytes."""
+    B = q.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise K3mlaError("workspace must be a CUDA uint8 tensor")
+    lib = load()
+    _check(lib.k3mla_decode_layer(
+        _dev(q, torch.bfloat16, (B, H, NOPE + ROPE), "q"), _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"),
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"), _rows(c_kv, B, "c_kv"), c_kv.stride(0),
+        _rows(k_rope, B, "k_rope"), k_rope.stride(0), ctypes.c_uint16(scale_bf16),
+        _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), B, int(max_ctx),
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_decode_layer")
+
+
 def decode_workspace_bytes(B: int, max_ctx: int, split_tokens: int = SPLIT_AUTO) -> int:
     return int(load().k3mla_decode_workspace_bytes(B, max_ctx, split_tokens))
 
@@ -305,6 +338,26 @@ def paged_decode_noalloc(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, bl
         _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
         B, int(max_ctx), int(split_tokens), _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)),
         "k3mla_paged_decode_noalloc")
+
+
+def diag_decode_timeout(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
+                        ctx_len: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int, out: torch.Tensor,
+                        workspace: torch.Tensor, max_ctx: int, split_tokens: int, withhold_page: int, wait_us: int,
+                        dev_err: torch.Tensor, stream=None) -> None:
+    """Diagnostic: paged_decode with page `withhold_page` of every split never loaded and every
+    bounded wait limited to wait_us; see k3mla_diag_decode_timeout."""
+    B = q_abs.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    lib = load()
+    _check(lib.k3mla_diag_decode_timeout(
+        _dev(q_abs, torch.bfloat16, (B, H, ROW), "q_abs"),
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"),
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"), int(scale_bf16),
+        _dev(out, torch.bfloat16, (B, H, V), "out"), None, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+        B, int(max_ctx), int(split_tokens), int(withhold_page), ctypes.c_uint32(wait_us),
+        _dev(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_diag_decode_timeout")
 
 
 def diag_umma(mode: int, a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, stream=None) -> None:

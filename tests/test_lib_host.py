@@ -215,6 +215,23 @@ def test_default_split_rule_depends_on_the_slot_alone():
     assert lib.k3mla_slot_split_tokens(100, -1) == -1
 
 
+def test_layer_call_sizes_and_arguments():
+    # q_abs [B][96][576] bf16 (256-aligned), then the decode workspace of the default split
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, max_ctx in ((1, 130), (64, 4096), (8, 32768)):
+        want = r256(B * 96 * 576 * 2) + k3mla.decode_workspace_bytes(B, max_ctx, 0)
+        assert k3mla.decode_layer_workspace_bytes(B, max_ctx) == want
+    lib = k3mla.load()
+    args = [None, None, None, 4, 1, 0, None, 4, None, None, 512, None, 64, 0x3D94, None, None, None, 0, 1, 256,
+            None, None]
+    assert lib.k3mla_decode_layer(*args) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    args[18] = 0
+    assert lib.k3mla_decode_layer(*args) == 0                   # B == 0: nothing to do
+    args[18], args[10] = 1, 511                                 # c_stride below a latent row
+    assert lib.k3mla_decode_layer(*args) == -1
+
+
 def test_product_and_oracle_share_no_code():
     """The CUDA path and the oracle are independent: no product source imports, includes or names
     the oracle's modules, and no oracle source imports the product package or includes its
