@@ -16,11 +16,11 @@
 // Fixed orders rule out the tensor cores, so these are CUDA-core kernels:
 //   E0 absorption   thread per (slot, head, j): sum over d = 0..127
 //   E1 scores       CTA per (slot, 8 pages): Q and each page staged in shared
-//                   memory; thread per (token, 4 heads): sum over k = 0..575
+//                   memory; thread per (4 tokens, 3 heads): sums over k = 0..575
 //   E2 softmax      CTA per (slot, head): max and exps across the block, the sum
 //                   of exp thread 0's loop over t ascending, p_t = bf16(e_t / l),
 //                   argmax (lowest t with the largest p)
-//   E3 latent sum   CTA per (slot, 128 dims): thread per (dim, 48 heads), sum
+//   E3 latent sum   CTA per (slot, 64 dims): thread per (4 dims, 6 heads), sums
 //                   over t ascending, pages staged in shared memory
 //   E4 expansion    CTA per (head, 16 slots): W_UV[h] staged; thread per v:
 //                   sixteen sums over j = 0..511
@@ -90,12 +90,15 @@ __global__ void __launch_bounds__(LORA) ex_absorb_kernel(const uint16_t* __restr
 
 // ---- E1: scores ----------------------------------------------------------------------------
 constexpr int E1_PAGES = 8;              // pages per CTA (Q is staged once for them)
-constexpr int E1_THREADS = 256;
+constexpr int E1_THREADS = 512;
 constexpr int E1_QP = ROW + 2;           // padded row pitch (elements): rows start in distinct banks
 constexpr int E1_SMEM = (H + PAGE) * E1_QP * 2;
+constexpr int E1_TOK = 4, E1_HEADS = 3;  // register tile of one thread: 4 tokens x 3 heads
 
-// grid (B, ceil(max_ctx / (64 * E1_PAGES))); block 256.  s[b][h][t] = bf16(bf16(dot) * scale).
-// Warp w owns heads 12w .. 12w + 11 (three passes of four); lane = token (two passes of 32).
+// grid (B, ceil(max_ctx / (64 * E1_PAGES))); block 512.  s[b][h][t] = bf16(bf16(dot) * scale).
+// Thread (warp w, lane l): tokens g, g + 16, g + 32, g + 48 of the page (g = l % 16) and heads
+// 3 (2 w + l / 16) .. + 2; each of its 12 dots is one sequential sum over k = 0..575 ascending (a fused
+// multiply-add of two bf16 values rounds as the chain's multiply-then-add: the product is exact).
 __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     const uint16_t* __restrict__ q_abs, const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer,
     const int32_t* __restrict__ table, int max_pages, const int32_t* __restrict__ ctx_len, int max_ctx,
@@ -118,6 +121,7 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
             reinterpret_cast<const uint32_t*>(q_abs + ((size_t)b * H + h) * ROW)[k2];
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane & 15, h0 = E1_HEADS * (2 * warp + (lane >> 4));
     for (int t0 = t_begin; t0 < t_end; t0 += PAGE) {
         __syncthreads();  // Q staged / the previous page's rows no longer read
         for (int i = threadIdx.x; i < PAGE * (ROW / 2); i += E1_THREADS) {
@@ -132,41 +136,42 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
             reinterpret_cast<uint32_t*>(Rs + r * E1_QP)[k2] = v;
         }
         __syncthreads();
-        for (int tp = 0; tp < 2; ++tp) {
-            const int r = 32 * tp + lane, t = t0 + r;
-            const uint32_t* rw = reinterpret_cast<const uint32_t*>(Rs + r * E1_QP);
-            for (int hp = 0; hp < 3; ++hp) {
-                const int h0 = 12 * warp + 4 * hp;
-                const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 0) * E1_QP);
-                const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 1) * E1_QP);
-                const uint32_t* q2 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 2) * E1_QP);
-                const uint32_t* q3 = reinterpret_cast<const uint32_t*>(Qs + (h0 + 3) * E1_QP);
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-                for (int k2 = 0; k2 < ROW / 2; ++k2) {  // k = 2 k2, then 2 k2 + 1: ascending
-                    const uint32_t rv = rw[k2];
-                    const float rlo = __uint_as_float(rv << 16), rhi = __uint_as_float(rv & 0xFFFF0000u);
-                    uint32_t qv = q0[k2];
-                    a0 = __fadd_rn(a0, __fmul_rn(__uint_as_float(qv << 16), rlo));
-                    a0 = __fadd_rn(a0, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
-                    qv = q1[k2];
-                    a1 = __fadd_rn(a1, __fmul_rn(__uint_as_float(qv << 16), rlo));
-                    a1 = __fadd_rn(a1, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
-                    qv = q2[k2];
-                    a2 = __fadd_rn(a2, __fmul_rn(__uint_as_float(qv << 16), rlo));
-                    a2 = __fadd_rn(a2, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
-                    qv = q3[k2];
-                    a3 = __fadd_rn(a3, __fmul_rn(__uint_as_float(qv << 16), rlo));
-                    a3 = __fadd_rn(a3, __fmul_rn(__uint_as_float(qv & 0xFFFF0000u), rhi));
-                }
-                if (t < t_end) {
-                    const float acc[4] = {a0, a1, a2, a3};
+        float acc[E1_TOK][E1_HEADS];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        s_out[((size_t)b * H + h0 + u) * s_pitch + t] =
-                            ex_land(__fmul_rn(ex_bf(ex_land(acc[u])), scale));
+        for (int a = 0; a < E1_TOK; ++a)
+#pragma unroll
+            for (int c = 0; c < E1_HEADS; ++c) acc[a][c] = 0.f;
+        const uint32_t* rw[E1_TOK];
+#pragma unroll
+        for (int a = 0; a < E1_TOK; ++a) rw[a] = reinterpret_cast<const uint32_t*>(Rs + (g + 16 * a) * E1_QP);
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(Qs + h0 * E1_QP);
+#pragma unroll 2
+        for (int k2 = 0; k2 < ROW / 2; ++k2) {  // k = 2 k2, then 2 k2 + 1: ascending
+            float rlo[E1_TOK], rhi[E1_TOK];
+#pragma unroll
+            for (int a = 0; a < E1_TOK; ++a) {
+                const uint32_t rv = rw[a][k2];
+                rlo[a] = __uint_as_float(rv << 16);
+                rhi[a] = __uint_as_float(rv & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int c = 0; c < E1_HEADS; ++c) {
+                const uint32_t qv = qw[c * (E1_QP / 2) + k2];
+                const float qlo = __uint_as_float(qv << 16), qhi = __uint_as_float(qv & 0xFFFF0000u);
+#pragma unroll
+                for (int a = 0; a < E1_TOK; ++a) {
+                    acc[a][c] = __fmaf_rn(qlo, rlo[a], acc[a][c]);
+                    acc[a][c] = __fmaf_rn(qhi, rhi[a], acc[a][c]);
                 }
             }
+        }
+#pragma unroll
+        for (int a = 0; a < E1_TOK; ++a) {
+            const int t = t0 + g + 16 * a;
+            if (t < t_end)
+#pragma unroll
+                for (int c = 0; c < E1_HEADS; ++c)
+                    s_out[((size_t)b * H + h0 + c) * s_pitch + t] = ex_land(__fmul_rn(ex_bf(ex_land(acc[a][c])), scale));
         }
     }
 }
@@ -248,10 +253,14 @@ __global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* _
 }
 
 // ---- E3: latent sum --------------------------------------------------------------------------
-constexpr int E3_THREADS = 256;          // (128 dims) x (2 groups of 48 heads)
-constexpr int E3_SMEM = PAGE * 128 * 4 + H * PAGE * 4;  // c slice [64][128] f32 + p [96][64] f32
+constexpr int E3_THREADS = 256;          // (16 groups of 4 dims) x (16 groups of 6 heads)
+constexpr int E3_DIMS = 64;              // latent dims per CTA
+constexpr int E3_PP = 100;               // ps row pitch (floats): 8-byte aligned 6-head groups
+constexpr int E3_SMEM = PAGE * E3_DIMS * 4 + PAGE * E3_PP * 4;  // c slice [64][64] f32 + p [64][100] f32
 
-// grid (B, 4 blocks of 128 dims); o_lat[h][b][j] = bf16(sum_{t ascending} p_t c_t[j]).
+// grid (B, 512 / 64); o_lat[h][b][j] = bf16(sum_{t ascending} p_t c_t[j]).  Thread (warp w, lane l),
+// i = 32 w + l: dims 4 (i % 16) .. + 3 of the block and heads 6 (i / 16) .. + 5, each of its 24 sums one
+// sequential loop over t ascending (fused multiply-add of two bf16 values: the product is exact).
 __global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
     const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer, const int32_t* __restrict__ table,
     int max_pages, const int32_t* __restrict__ ctx_len, int B, int max_ctx, const uint16_t* __restrict__ p,
@@ -260,39 +269,63 @@ __global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
     griddep_wait();
     griddep_launch_dependents();
     extern __shared__ float ex_f[];
-    float* cs = ex_f;                // [64 tokens][128 dims]
-    float* ps = ex_f + PAGE * 128;   // [96 heads][64 tokens]
-    const int b = blockIdx.x, jb = blockIdx.y * 128;
+    float* cs = ex_f;                   // [64 tokens][64 dims]
+    float* ps = ex_f + PAGE * E3_DIMS;  // [64 tokens][E3_PP] (heads 0..95)
+    const int b = blockIdx.x, jb = blockIdx.y * E3_DIMS;
     const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
-    const int jd = threadIdx.x & 127, hg = (threadIdx.x >> 7) * 48;
-    float acc[48];
+    const int dg = threadIdx.x & 15, hg = 6 * (threadIdx.x >> 4);
+    float acc[6][4];
 #pragma unroll
-    for (int u = 0; u < 48; ++u) acc[u] = 0.f;
+    for (int u = 0; u < 6; ++u)
+#pragma unroll
+        for (int d = 0; d < 4; ++d) acc[u][d] = 0.f;
     for (int t0 = 0; t0 < n; t0 += PAGE) {
         const int cnt = min(PAGE, n - t0);
         __syncthreads();
-        for (int i = threadIdx.x; i < PAGE * 128; i += E3_THREADS) {
-            const int r = i >> 7, j = i & 127;
-            float v = 0.f;
+        for (int i = threadIdx.x; i < PAGE * (E3_DIMS / 8); i += E3_THREADS) {  // 16 bytes = 8 dims each
+            const int r = i >> 3, u = i & 7;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (r < cnt) {
                 const uint16_t* row = ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t0 + r, nullptr);
-                if (row) v = ex_bf(row[jb + j]);
+                if (row) v = *reinterpret_cast<const uint4*>(row + jb + 8 * u);
             }
-            cs[i] = v;
+            float4* dst = reinterpret_cast<float4*>(cs + r * E3_DIMS + 8 * u);
+            dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                 __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+            dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                 __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
         }
-        for (int i = threadIdx.x; i < H * PAGE; i += E3_THREADS) {
-            const int h = i >> 6, r = i & 63;
-            ps[i] = r < cnt ? ex_bf(p[((size_t)b * H + h) * s_pitch + t0 + r]) : 0.f;
+        for (int i = threadIdx.x; i < H * (PAGE / 8); i += E3_THREADS) {  // 8 tokens of one head each
+            const int h = i >> 3, r0 = 8 * (i & 7);
+            const uint16_t* src = p + ((size_t)b * H + h) * s_pitch + t0 + r0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ps[(r0 + e) * E3_PP + h] = (r0 + e < cnt) ? ex_bf(src[e]) : 0.f;
         }
         __syncthreads();
         for (int r = 0; r < cnt; ++r) {
-            const float c = cs[r * 128 + jd];
+            const float4 c = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 4 * dg);
+            const float2* pr = reinterpret_cast<const float2*>(ps + r * E3_PP + hg);
 #pragma unroll
-            for (int u = 0; u < 48; ++u) acc[u] = __fadd_rn(acc[u], __fmul_rn(ps[(hg + u) * PAGE + r], c));
+            for (int q2 = 0; q2 < 3; ++q2) {
+                const float2 pv = pr[q2];
+                const float pp[2] = {pv.x, pv.y};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float* a = acc[2 * q2 + e];
+                    a[0] = __fmaf_rn(pp[e], c.x, a[0]);
+                    a[1] = __fmaf_rn(pp[e], c.y, a[1]);
+                    a[2] = __fmaf_rn(pp[e], c.z, a[2]);
+                    a[3] = __fmaf_rn(pp[e], c.w, a[3]);
+                }
+            }
         }
     }
 #pragma unroll
-    for (int u = 0; u < 48; ++u) olat[((size_t)(hg + u) * B + b) * LORA + jb + jd] = ex_land(acc[u]);
+    for (int u = 0; u < 6; ++u) {
+        const uint32_t lo = (uint32_t)ex_land(acc[u][0]) | ((uint32_t)ex_land(acc[u][1]) << 16);
+        const uint32_t hi = (uint32_t)ex_land(acc[u][2]) | ((uint32_t)ex_land(acc[u][3]) << 16);
+        *reinterpret_cast<uint2*>(olat + ((size_t)(hg + u) * B + b) * LORA + jb + 4 * dg) = make_uint2(lo, hi);
+    }
 }
 
 // ---- E4: expansion ---------------------------------------------------------------------------
@@ -408,7 +441,7 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
     rc = launch_pdl(ex_softmax_kernel, dim3(B * H), dim3(E2_THREADS), (size_t)max_ctx * 4, st, "ex_softmax_kernel",
                     ctx_len, max_ctx, max_pages_per_slot, sp, pitch, argmax_t);
     if (rc) return rc;
-    rc = launch_pdl(ex_latent_kernel, dim3(B, LORA / 128), dim3(E3_THREADS), (size_t)E3_SMEM, st,
+    rc = launch_pdl(ex_latent_kernel, dim3(B, LORA / E3_DIMS), dim3(E3_THREADS), (size_t)E3_SMEM, st,
                     "ex_latent_kernel", slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, B,
                     max_ctx, sp, pitch, olat);
     if (rc) return rc;
