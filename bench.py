@@ -48,6 +48,7 @@ from paged_latent_attention_k3mla_gb300 import synth  # noqa: E402
 
 METRIC = "absorbed-MLA decode µs/layer and latent GB/s vs HBM/tensor roofline"
 H, NOPE, ROPE, V, LORA, ROW, PAGE = 96, 128, 64, 128, 512, 576, 64
+XR = NOPE + ROPE + V   # one head's row of the expanded cache: K nope, K rope, V
 WORKLOAD_DESC = {
     "steady64": "64 slots x 24 MLA layers x 4096 tokens (seed 2)",
     "ragged16": "16 slots x 24 MLA layers, ctx U[1,4096] (seed 1)",
@@ -495,7 +496,7 @@ def main():
     ms_step, ms_dec = run.measure(args.steps, args.warmup, clocks=clk)
     us_per_layer = ms_step * 1e3 / L
     e2e_ms, h2d, d2h, digest = e2e_leg(run, args.steps, args.warmup)
-    nxt = None if args.no_next else next_rows(wl, run.table, run.max_ctx, run.stream, hbm, tflops)
+    nxt = None if args.no_next else next_rows(wl, run.table, run.max_ctx, run.stream, hbm, tflops, ms_dec * 1e3)
     ab = alg_bytes(wl)
     layer_gbs = ab["layer"] / (us_per_layer * 1e-6) / 1e9
     flops = alg_flops(wl)
@@ -556,11 +557,12 @@ def _time_ms(fn, stream, warmup=2, reps=5):
     return e0.elapsed_time(e1) / reps
 
 
-def next_rows(wl, table, max_ctx, stream, hbm, tflops):
+def next_rows(wl, table, max_ctx, stream, hbm, tflops, absorbed_call_us):
     """Figures for the calls beyond the decode step, run after the timed step (they write the
     cache): a whole-page copy between two slabs (prefill adoption) against the HBM copy bandwidth,
-    the causal attention of 64-token chunks of 16 slots at their 4096-token contexts, and the
-    exact-chain decode of one layer of the full batch."""
+    the causal attention of 64-token chunks of 16 slots at their 4096-token contexts, the
+    exact-chain decode of one layer of the full batch, and the expanded-cache design (per-head K and
+    V rows built from the latent, ordinary attention over them) on one layer of the full batch."""
     from paged_latent_attention_k3mla_gb300 import k3mla
     dev = "cuda"
     L = wl.n_layers
@@ -625,6 +627,35 @@ def next_rows(wl, table, max_ctx, stream, hbm, tflops):
                           "how": "k3mla_decode_exact: the rounding chain's sums in order on CUDA cores, "
                                  "bitwise equal to the CPU oracle"}
     del ws, out
+    torch.cuda.empty_cache()
+
+    # the expanded-cache design, A/B: layer 0's per-head K (192) and V (128) rows for every page, then
+    # ordinary attention over them; the cache (61,440 B a token) is far larger than L2
+    n_pages = wl.slab.shape[0]
+    x = torch.empty(n_pages, PAGE, H, XR, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(B, H, V, dtype=torch.bfloat16, device=dev)
+    ms_build = _time_ms(lambda: k3mla.expand_latent_cache(wl.slab, 0, wl.w_kv_b[0], x, stream=stream), stream,
+                        warmup=1, reps=3)
+    ms_xd = _time_ms(lambda: k3mla.expanded_decode(wl.q[0], x, table, ctx, wl.scale_bits, out, max_ctx,
+                                                   stream=stream), stream, warmup=2, reps=10)
+    tokens = int(wl.ctx_len.sum())
+    xd_bytes = tokens * H * XR * 2 + B * H * (192 + V) * 2      # K and V rows read, q read, out written
+    xd_gbs = xd_bytes / (ms_xd * 1e-3) / 1e9
+    build_bytes = n_pages * PAGE * (H * XR * 2 + ROW * 2)        # the cache written, each latent row read
+    res["expanded_ab"] = {
+        "layer": 0, "slots": B, "tokens": tokens, "cache_bytes": x.numel() * 2,
+        "bytes_per_token_per_layer": H * XR * 2, "latent_bytes_per_token_per_layer": ROW * 2,
+        "build_ms": round(ms_build, 3),
+        "build_gbs": round(build_bytes / (ms_build * 1e-3) / 1e9, 1),
+        "decode_us": round(ms_xd * 1e3, 1),
+        "roofline": {"bound": "hbm", "achieved": round(xd_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(xd_gbs / hbm, 4)},
+        "absorbed_decode_call_us": round(absorbed_call_us, 3),
+        "expanded_over_absorbed": round(ms_xd * 1e3 / absorbed_call_us, 2),
+        "how": "k3mla_expand_latent_cache (tcgen05, W_UK / W_UV of a head x a page's latent) then "
+               "k3mla_expanded_decode (a warp per slot and head, CUDA cores); absorbed figure: the "
+               "paged-decode call timed above"}
+    del x, out
     torch.cuda.empty_cache()
     return res
 

@@ -399,6 +399,44 @@ int k3mla_paged_decode_noalloc(const uint16_t* q_abs, const uint16_t* slab, int 
                                uint16_t* out, int32_t* argmax_t, int B, int max_ctx, int split_tokens,
                                int32_t* dev_err, void* stream);
 
+/* ---- the expanded-cache design, as an A/B baseline (PR #869, M2 commit) --------
+ * The design the absorbed decode replaces: every token's latent expanded by kv_b
+ * into per-head K (192 = 128 nope + the 64-wide rope key) and V (128) rows, about
+ * 1.47 MB per token over 24 MLA layers (61,440 bytes per token and layer) against
+ * the latent's 27.6 KB, and ordinary attention over them.  For timing the two
+ * designs on the same workload; not part of the absorbed path.
+ *
+ * k3mla_expand_latent_cache: for every page p < n_pages of the slab, token t and
+ * head h, at this layer:
+ *   xcache[p][t][h][0:128]   = bf16( W_UK[h] c_t )      (f32 accumulation)
+ *   xcache[p][t][h][128:192] = k_rope_t                  (copied)
+ *   xcache[p][t][h][192:320] = bf16( W_UV[h] c_t )
+ * slab   device [n_pages][n_layers][64][576] bf16, 16-byte aligned
+ * w_kv_b device [24576][512] bf16, the layer's weights, 16-byte aligned
+ * xcache device, k3mla_expanded_cache_bytes(n_pages) bytes, 16-byte aligned
+ * One kernel on `stream`; it reads nothing before the kernel ahead of it completed.
+ *
+ * k3mla_expanded_decode: for each slot b < B and head h, over its n = ctx_len[b]
+ * tokens (token t at page block_table[b][t / 64], row t % 64; -1 is a zero K / V
+ * row that takes part in the softmax; ids outside [-1, n_pages) read as zero and
+ * set K3MLA_DEV_BAD_PAGE; n is clamped to min(max_ctx, 64 * max_pages_per_slot)
+ * with K3MLA_DEV_CTX):
+ *   s_t = bf16( bf16( q[b][h] . K_h[t] ) * scale ),  p = softmax(s),
+ *   out[b][h] = bf16( sum_t p_t V_h[t] )             (f32 online softmax)
+ * q device [B][96][192] bf16 (q_nope | q_rope, not absorbed), 4-byte aligned;
+ * out device [B][96][128] bf16, 8-byte aligned; n == 0 gives zeros.  One kernel on
+ * `stream`, no workspace.
+ * Both return K3MLA_E_INVALID, with nothing launched, for sizes out of range (a
+ * layer past the slab, no pages, a grid past 65535 slots) or a null or misaligned
+ * pointer; k3mla_expanded_decode with B == 0 does nothing.  The caller owns every
+ * buffer. */
+size_t k3mla_expanded_cache_bytes(int n_pages);
+int k3mla_expand_latent_cache(const uint16_t* slab, int n_pages, int n_layers, int layer, const uint16_t* w_kv_b,
+                              uint16_t* xcache, int32_t* dev_err, void* stream);
+int k3mla_expanded_decode(const uint16_t* q, const uint16_t* xcache, int n_pages, const int32_t* block_table,
+                          int max_pages_per_slot, const int32_t* ctx_len, uint16_t scale_bf16, uint16_t* out, int B,
+                          int max_ctx, int32_t* dev_err, void* stream);
+
 /* ---- diagnostic: the abort path of the bounded waits ---------------------------
  * Not part of the decode path.  k3mla_paged_decode with two changes that exist only
  * to exercise what happens when a device wait runs out: in every split, the first

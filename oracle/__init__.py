@@ -25,6 +25,6 @@ from .chain import (  # noqa: F401
     f32_to_bf16,
     MUTATIONS,
 )
-from .expanded import decode_expanded_f64  # noqa: F401
+from .expanded import decode_expanded_f64, expand_pages_f64  # noqa: F401
 from .pages import copy_pages  # noqa: F401
 from .chunk import append_rows, chunk_views  # noqa: F401

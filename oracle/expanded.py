@@ -73,3 +73,23 @@ def decode_expanded_f64(q, slab, layer, block_table, ctx_len, w_kv_b, scale, slo
             out[b, h] = p @ v
             am[b, h] = int(np.argmax(p))
     return out, am
+
+
+def expand_pages_f64(slab, layer, w_kv_b, pages) -> np.ndarray:
+    """The expanded cache of the listed pages at one layer, in float64, unlanded.
+
+    pegainfer PR #869, M2 commit: kv_b expands each token's latent into per-head
+    K and V rows, the cache the absorbed decode does away with.  Returns [len(pages), 64 tokens, 96 heads, 320] with,
+    for head h and the token at page position t, the row
+        [ W_UK[h] c_t (128) | k_rope_t (64) | W_UV[h] c_t (128) ]
+    where c_t and k_rope_t are the first 512 and last 64 values of its latent row.
+    """
+    w = bf16_bits_to_f64(w_kv_b).reshape(H, NOPE + V, LORA)
+    out = np.zeros((len(pages), PAGE, H, NOPE + ROPE + V), np.float64)
+    for i, pid in enumerate(pages):
+        rows = bf16_bits_to_f64(slab[int(pid), layer])            # [64, 576]
+        c, k_rope = rows[:, :LORA], rows[:, LORA:]
+        out[i, :, :, :NOPE] = np.einsum("hdj,tj->thd", w[:, :NOPE, :], c)
+        out[i, :, :, NOPE:NOPE + ROPE] = k_rope[:, None, :]
+        out[i, :, :, NOPE + ROPE:] = np.einsum("hdj,tj->thd", w[:, NOPE:, :], c)
+    return out

@@ -17,7 +17,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libk3mla.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["host_common.cu", "decode.cu", "merge_expand.cu", "absorb_append.cu", "pages.cu", "chunk.cu", "exact.cu", "pool.cpp", "plan.cpp"]
+SOURCES = ["host_common.cu", "decode.cu", "merge_expand.cu", "absorb_append.cu", "pages.cu", "chunk.cu", "exact.cu",
+           "expanded.cu", "pool.cpp", "plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

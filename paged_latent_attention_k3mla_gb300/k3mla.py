@@ -30,6 +30,7 @@ EXPORTS = (
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
     "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_batch_planned_split_tokens",
     "k3mla_decode_layer_workspace_bytes", "k3mla_decode_layer", "k3mla_diag_decode_timeout",
+    "k3mla_expanded_cache_bytes", "k3mla_expand_latent_cache", "k3mla_expanded_decode",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -71,6 +72,9 @@ def load(build_if_needed: bool = True):
             "k3mla_pool_stats": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "k3mla_pool_destroy": ([P], None),
             "k3mla_diag_umma": ([I, P, P, P, P], I),
+            "k3mla_expanded_cache_bytes": ([I], SZ),
+            "k3mla_expand_latent_cache": ([P, I, I, I, P, P, P, P], I),
+            "k3mla_expanded_decode": ([P, P, I, P, I, P, ctypes.c_uint16, P, I, I, P, P], I),
             "k3mla_diag_decode_timeout": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, I,
                                            ctypes.c_uint32, P, P], I),
             "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
@@ -338,6 +342,39 @@ def paged_decode_noalloc(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, bl
         _dev(out, torch.bfloat16, (B, H, V), "out"), _opt(argmax, torch.int32, (B, H), "argmax"),
         B, int(max_ctx), int(split_tokens), _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)),
         "k3mla_paged_decode_noalloc")
+
+
+def expanded_cache_bytes(n_pages: int) -> int:
+    return int(load().k3mla_expanded_cache_bytes(int(n_pages)))
+
+
+def expand_latent_cache(slab: torch.Tensor, layer: int, w_kv_b: torch.Tensor, xcache: torch.Tensor,
+                        dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """The expanded-cache baseline's cache for one layer: xcache [n_pages, 64, 96, 320] bf16 (K nope |
+    K rope | V per head) from the latent slab; see k3mla_expand_latent_cache."""
+    n_pages, L = slab.shape[0], slab.shape[1]
+    lib = load()
+    _check(lib.k3mla_expand_latent_cache(
+        _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"), n_pages, L, int(layer),
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"),
+        _dev(xcache, torch.bfloat16, (n_pages, PAGE, H, NOPE + ROPE + V), "xcache"),
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_expand_latent_cache")
+
+
+def expanded_decode(q: torch.Tensor, xcache: torch.Tensor, block_table: torch.Tensor, ctx_len: torch.Tensor,
+                    scale_bf16: int, out: torch.Tensor, max_ctx: int, dev_err: torch.Tensor | None = None,
+                    stream=None) -> None:
+    """Ordinary attention over the expanded cache: q [B,96,192] bf16 -> out [B,96,128] bf16."""
+    B = q.shape[0]
+    n_pages = xcache.shape[0]
+    lib = load()
+    _check(lib.k3mla_expanded_decode(
+        _dev(q, torch.bfloat16, (B, H, NOPE + ROPE), "q"),
+        _dev(xcache, torch.bfloat16, (n_pages, PAGE, H, NOPE + ROPE + V), "xcache"), n_pages,
+        _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(ctx_len, torch.int32, (B,), "ctx_len"), ctypes.c_uint16(scale_bf16),
+        _dev(out, torch.bfloat16, (B, H, V), "out"), B, int(max_ctx), _opt(dev_err, torch.int32, (1,), "dev_err"),
+        _stream(stream)), "k3mla_expanded_decode")
 
 
 def diag_decode_timeout(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,

@@ -232,6 +232,25 @@ def test_layer_call_sizes_and_arguments():
     assert lib.k3mla_decode_layer(*args) == -1
 
 
+def test_expanded_baseline_sizes_and_arguments():
+    # the expanded cache: [n_pages][64 tokens][96 heads][128 K nope | 64 K rope | 128 V] bf16
+    assert k3mla.expanded_cache_bytes(0) == 0
+    assert k3mla.expanded_cache_bytes(3) == 3 * 64 * 96 * 320 * 2
+    lib = k3mla.load()
+    assert lib.k3mla_expand_latent_cache(None, 4, 2, 2, None, None, None, None) == -1   # layer past the slab
+    assert b"invalid sizes" in lib.k3mla_last_error()
+    assert lib.k3mla_expand_latent_cache(None, 4, 2, 1, None, None, None, None) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    args = [None, None, 4, None, 2, None, 0x3D94, None, 0, 128, None, None]
+    assert lib.k3mla_expanded_decode(*args) == 0                # B == 0: nothing to do
+    args[8] = 1
+    assert lib.k3mla_expanded_decode(*args) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    args[2] = 0                                                 # no pages
+    assert lib.k3mla_expanded_decode(*args) == -1
+    assert b"invalid sizes" in lib.k3mla_last_error()
+
+
 def test_product_and_oracle_share_no_code():
     """The CUDA path and the oracle are independent: no product source imports, includes or names
     the oracle's modules, and no oracle source imports the product package or includes its

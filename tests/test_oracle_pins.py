@@ -137,6 +137,44 @@ def test_chain_matches_expanded_float64(case):
                                       int(r["argmax"][b, h]), int(am[b, h]))
 
 
+def test_expanded_pages_select_the_latent_entries_a_permutation_weight_picks():
+    # closed form: with W_UK[h][i, j] = [j == (i + h) mod 512] and W_UV[h][i, j] = 2 [j == (511 - i - h) mod 512]
+    # the expansion is a gather, so a transposed weight, a head mixed up or K and V swapped all fail
+    wl = synth.make_custom([130], seed=21)
+    d = np_inputs(wl)
+    w = np.zeros((H, NOPE + V, LORA), np.float32)
+    for h in range(H):
+        for i in range(NOPE):
+            w[h, i, (i + h) % LORA] = 1.0
+            w[h, NOPE + i, (LORA - 1 - i - h) % LORA] = 2.0
+    wbits = synth.bf16_bits(torch.from_numpy(w.reshape(H * (NOPE + V), LORA)).to(torch.bfloat16))
+    pages = [int(wl.block_table[0, 1]), int(wl.block_table[0, 0])]
+    x = oracle.expand_pages_f64(d["slab"], 0, wbits, pages)
+    for k, pid in enumerate(pages):
+        rows = bf16_bits_to_f64(d["slab"][pid, 0])
+        for h in (0, 1, 57, 95):
+            i = np.arange(NOPE)
+            assert np.array_equal(x[k, :, h, :NOPE], rows[:, (i + h) % LORA])
+            assert np.array_equal(x[k, :, h, NOPE:NOPE + 64], rows[:, LORA:])
+            assert np.array_equal(x[k, :, h, NOPE + 64:], 2.0 * rows[:, (LORA - 1 - i - h) % LORA])
+
+
+def test_expanded_scores_equal_the_absorbed_association():
+    # q . [W_UK c ; k_rope] against (W_UK^T q) . c + q_rope . k_rope, both in float64: the absorption identity
+    wl = synth.make_custom([64], seed=22)
+    d = np_inputs(wl)
+    pid = int(wl.block_table[0, 0])
+    x = oracle.expand_pages_f64(d["slab"], 0, d["w"], [pid])[0]              # [64, 96, 320]
+    q = bf16_bits_to_f64(d["q"])[0]                                           # [96, 192]
+    w = bf16_bits_to_f64(d["w"]).reshape(H, NOPE + V, LORA)
+    rows = bf16_bits_to_f64(d["slab"][pid, 0])
+    s_exp = np.einsum("thd,hd->th", x[:, :, :NOPE + 64], q)
+    q_abs = np.einsum("hd,hdj->hj", q[:, :NOPE], w[:, :NOPE, :])
+    s_abs = rows[:, :LORA] @ q_abs.T + rows[:, LORA:] @ q[:, NOPE:].T
+    scale = np.abs(rows[:, :LORA]) @ np.abs(np.einsum("hd,hdj->hj", np.abs(q[:, :NOPE]), np.abs(w[:, :NOPE, :]))).T
+    assert np.all(np.abs(s_exp - s_abs) <= 1e-12 * (scale + 1.0))
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_single_token_closed_form_and_q_independence():
