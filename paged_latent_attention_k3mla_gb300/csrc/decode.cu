@@ -140,6 +140,7 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
+    int32_t early_n[NHSLOT];  // producer q: leading uses of its ring units loaded before the grid wait
     uint64_t wait_ns;  // the limit of every bounded wait of this CTA
 };
 static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
@@ -149,6 +150,7 @@ static_assert(QBYTES <= (NUNIT - Q_UNIT0) * THIRD + 8 * PSTAGE,
 static_assert(PCOPY <= PBUF, "P buffer");
 static_assert(H * LORA * 4 <= NHSLOT * SLOT1 + NPBUF * PBUF,
               "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
+static_assert((H * 256 * 2) % 128 == 0 && (H * 128 * 4) % 128 == 0, "store boxes start 128-byte aligned");
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
 
 struct DecodeParams {
@@ -163,6 +165,7 @@ struct DecodeParams {
     uint32_t scale2;  // the bf16 scale in both halves
     uint64_t wait_ns;  // bounded-wait limit: WAIT_NS, shorter only from the diagnostic entry
     int32_t withhold;  // diagnostic only, 0 otherwise: page k - 1's first third is never loaded
+    int32_t early;     // 1 only from k3mla_decode_layer: see early_loads
 };
 
 __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int max_ctx, int max_pages,
@@ -347,53 +350,54 @@ __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_add
 // Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
 __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_t)(h * 128 + ((j ^ (h & 7)) << 4)); }
 
-// PV CTA, after its roles: O^T [512 dims x 96 heads] f32 lands in the (now idle) page ring and P
-// buffers as [96 heads][512 dims] f32 -- twelve warps, each one TMEM lane quarter x one 32-head
-// piece -- and every thread then copies rows out with 16-byte stores: the f32 partial as it stands,
-// or (single split) o_lat = bf16(O * (1 / l)).  (Four warps alone, straight from the TMEM layout,
-// take several microseconds.)  Kept out of line so that it does not weigh on the register
-// allocation of the pipeline.
-__device__ __noinline__ void pv_write_out(Smem& sm, float* ws_o, uint16_t* ws_olat, int B, int nsplit, uint32_t tbase,
-                                          int b, int s)
+// PV CTA, after its roles: O^T [512 dims x 96 heads] f32 leaves TMEM through the (now idle) page ring
+// and P buffers, laid out there as the boxes of bulk tensor stores.  Twelve warps, each one TMEM lane
+// quarter (dims 32 q .. 32 q + 31 of every 128-dim block) x one 32-head piece, write either final o_lat
+// = bf16(O * (1 / l)) of a slot with a single split, as [2 halves of 256 dims][96 heads][256] bf16, or
+// the split's f32 partial as it stands, as [4 quarters of 128 dims][96 heads][128] f32 (a warp's 32
+// lanes write 32 consecutive dims of one head: one shared-memory wavefront).  One thread then stores
+// the tile with two or four bulk tensor stores and waits until they are complete.  Kept out of line
+// so that it does not weigh on the register allocation of the pipeline.
+__device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, const CUtensorMap* tm_part,
+                                          bool single, int nsplit, uint32_t tbase, int b, int s)
 {
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-    float* tile = reinterpret_cast<float*>(sm.u.c1.ring[0]);
+    uint8_t* tile = sm.u.c1.ring[0];
     if (warp < 12) {
         tc_fence_after();
-        const uint32_t q = warp & 3u, pc = warp >> 2;
-        const uint32_t ta = tbase + ((32u * q) << 16) + 32u * pc;
-        float* trow = tile + (32 * pc) * LORA + 32 * q + lane;
+        const int q = (int)(warp & 3u), pc = (int)(warp >> 2);
+        const uint32_t ta = tbase + ((32u * (uint32_t)q) << 16) + 32u * (uint32_t)pc;
+        float rl[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) rl[c] = single ? sm.rl[32 * pc + c] : 1.f;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
             uint32_t rr[32];
-            tmem_ld32(ta + 96u * j, rr);
+            tmem_ld32(ta + 96u * (uint32_t)j, rr);
             tmem_wait_ld();
+            const int d = 128 * j + 32 * q + (int)lane;
+            if (single) {
+                uint16_t* t16 = reinterpret_cast<uint16_t*>(tile) + (d >> 8) * (H * 256) + (32 * pc) * 256 + (d & 255);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) trow[c * LORA + 128 * j] = __uint_as_float(rr[c]);
+                for (int c = 0; c < 32; ++c)
+                    t16[c * 256] = (uint16_t)(pack_bf16x2(__uint_as_float(rr[c]) * rl[c], 0.f) & 0xFFFFu);
+            } else {
+                float* t32 = reinterpret_cast<float*>(tile) + (d >> 7) * (H * 128) + (32 * pc) * 128 + (d & 127);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) t32[c * 128] = __uint_as_float(rr[c]);
+            }
         }
     }
+    fence_proxy_async_cta();  // the tile is read by the bulk tensor stores (async proxy)
     __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(tile);
-    if (ws_olat) {  // thread -> 16-byte chunk ch of rows h0, h0 + 7, ...
-        constexpr int RSTEP = THREADS / (LORA / 8);
-        static_assert(THREADS % (LORA / 8) == 0, "whole rows per pass");
-        const int ch = (int)threadIdx.x % (LORA / 8), h0 = (int)threadIdx.x / (LORA / 8);
-        uint4* dst = reinterpret_cast<uint4*>(ws_olat + ((size_t)h0 * B + b) * LORA) + ch;
-        const size_t dstep = (size_t)RSTEP * B * (LORA / 8);  // RSTEP heads on, in uint4
-        const float4* s4 = src + h0 * (LORA / 4) + 2 * ch;
-#pragma unroll 1
-        for (int hh = h0; hh < H; hh += RSTEP) {
-            const float r = sm.rl[hh];
-            const float4 x0 = s4[0], x1 = s4[1];
-            *dst = make_uint4(pack_bf16x2(x0.x * r, x0.y * r), pack_bf16x2(x0.z * r, x0.w * r),
-                              pack_bf16x2(x1.x * r, x1.y * r), pack_bf16x2(x1.z * r, x1.w * r));
-            dst += dstep;
-            s4 += RSTEP * (LORA / 4);
+    if (threadIdx.x == 0) {
+        if (single) {  // o_lat [96][B][512] viewed as (512 dims, B slots, 96 heads), box (256, 1, 96)
+            for (int k = 0; k < 2; ++k) tma_store_3d(tm_olat, tile + k * (H * 256 * 2), 256 * k, b, 0);
+        } else {  // partials [B][nsplit][96][512] viewed as (512 dims, rows), box (128, 96)
+            for (int k = 0; k < 4; ++k) tma_store_2d(tm_part, tile + k * (H * 128 * 4), 128 * k, (b * nsplit + s) * H);
         }
-    } else {
-        float4* dst = reinterpret_cast<float4*>(ws_o + (((size_t)b * nsplit + s) * H) * LORA);
-#pragma unroll 4
-        for (int k = (int)threadIdx.x; k < H * (LORA / 4); k += THREADS) dst[k] = src[k];
+        bulk_commit();
+        bulk_wait<0>();
     }
 }
 
@@ -447,6 +451,7 @@ __device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bo
     mbar_init(&sm.l_full, 1);
     sm.abort_flag = 0;
     sm.fin_ready = 0;
+    for (int i = 0; i < NHSLOT; ++i) sm.early_n[i] = 0;
     for (int i = 0; i < NUNIT; ++i) {
         sm.unit_loaded[i] = 0;
         sm.unit_taken[i] = 0;
@@ -461,7 +466,8 @@ __device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bo
 // and the PV CTA's write-out of O.  Inlined into the kernel: the parameters it reads in its loops stay
 // constant-bank operands (an out-of-line copy, reaching them through a pointer, ran some 50 % slower).
 __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_page, const CUtensorMap& tmap_page8,
-                                             const CUtensorMap& tmap_q, const DecodeParams& p, const SplitGeom& sg,
+                                             const CUtensorMap& tmap_q, const CUtensorMap& tmap_olat,
+                                             const CUtensorMap& tmap_part, const DecodeParams& p, const SplitGeom& sg,
                                              uint32_t tbase, uint32_t rank, uint32_t warp, uint32_t lane)
 {
     const int b = sg.b, s = sg.s, start = sg.start, ntok = sg.ntok, npg = sg.npg, n_lp = sg.n_lp, lp0 = sg.lp0;
@@ -480,7 +486,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 // ordered (a use is loaded only after the MMAs of the previous use released it)
                 const int t = (int)warp - W_PROD0;
                 bool ok = true, q_in_tmem = false;
-                for (int i = 0; i < npg && ok; ++i) {
+                for (int i = sm.early_n[t]; i < npg && ok; ++i) {
                     const int g = 3 * i + t, u = g % NUNIT, k = g / NUNIT;
                     if (!q_in_tmem && g >= Q_UNIT0) {  // units Q_UNIT0.. hold q_abs until it is in TMEM
                         ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
@@ -726,7 +732,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 const uint64_t pol = policy_evict_first();  // last reader of the latent
                 const int q = (int)warp - 4;
                 bool ok = true;
-                for (int u = q; u < 2 * npg && ok; u += NHSLOT) {
+                for (int u = q + NHSLOT * sm.early_n[q]; u < 2 * npg && ok; u += NHSLOT) {
                     const int k = u / NHSLOT;
                     const int32_t y = page_row(p, b, lp0 + u / 2, n_lp, oob_row) + HALF * (u & 1);
                     if (!wait_bar(&sm.empty[q], (uint32_t)(k & 1) ^ 1u, sm, p.dev_err)) {
@@ -850,9 +856,45 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
         }
         __syncthreads();  // every role is done: the final write-out takes all warps
         if (*reinterpret_cast<volatile int32_t*>(&sm.fin_ready) == 4)
-            pv_write_out(sm, single ? nullptr : p.ws_o, single ? p.ws_olat : nullptr, p.B, p.nsplit, tbase, b, s);
+            pv_write_out(sm, &tmap_olat, &tmap_part, single, p.nsplit, tbase, b, s);
     }
 
+}
+
+// The first uses of both page rings, issued before the grid wait when the kernel before in the stream
+// is this library's absorption-append launch of the same layer-call (k3mla_decode_layer).  That
+// launch writes only q_abs and the step's row of each slot, which lies in the slot's last logical
+// page, so every other page is loaded here: the loads overlap the absorption.  Nothing else writes
+// the slab or the block table meanwhile: the absorption-append grid lets this kernel start only
+// after each of its CTAs has waited for the kernel before it to complete.  Producer lanes only.
+__device__ __forceinline__ void early_loads(Smem& sm, const CUtensorMap& tmap_page, const CUtensorMap& tmap_page8,
+                                            const DecodeParams& p, const SplitGeom& sg, uint32_t rank,
+                                            uint32_t warp, uint32_t lane)
+{
+    if (lane != 0) return;
+    if (rank == 0 && warp >= W_PROD0 && warp < W_PROD0 + NSLOT) {
+        // producer t: third t of pages 0, 1, ... while they fall in the units q_abs leaves free
+        const int t = (int)warp - W_PROD0;
+        int i = 0;
+        for (; 3 * i + t < Q_UNIT0 && i < sg.npg && sg.lp0 + i < sg.n_lp - 1; ++i) {
+            const int u = 3 * i + t;  // the unit's first use
+            *reinterpret_cast<volatile int32_t*>(&sm.unit_loaded[u]) = 1;
+            mbar_arrive_expect_tx(&sm.full[u], THIRD);
+            tma_load_3d(sm.u.c0.ring[u], &tmap_page, 0, page_row(p, sg.b, sg.lp0 + i, sg.n_lp, sg.oob_row), 3 * t,
+                        &sm.full[u]);
+        }
+        sm.early_n[t] = i;
+    } else if (rank == 1 && warp >= 4 && warp <= 8) {
+        // producer q: half page q into half-slot q (its first use)
+        const int q = (int)warp - 4;
+        if (q < 2 * sg.npg && sg.lp0 + q / 2 < sg.n_lp - 1) {
+            mbar_arrive_expect_tx(&sm.full[q], SLOT1);
+            tma_load_3d_hint(sm.u.c1.ring[q], &tmap_page8, 0,
+                             page_row(p, sg.b, sg.lp0 + q / 2, sg.n_lp, sg.oob_row) + HALF * (q & 1), 0, &sm.full[q],
+                             policy_evict_first());
+            sm.early_n[q] = 1;
+        }
+    }
 }
 
 // ---- the split decode kernel ---------------------------------------------------------
@@ -860,7 +902,9 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
                               const __grid_constant__ CUtensorMap tmap_page8,
-                              const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p)
+                              const __grid_constant__ CUtensorMap tmap_q,
+                              const __grid_constant__ CUtensorMap tmap_olat,
+                              const __grid_constant__ CUtensorMap tmap_part, const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -894,16 +938,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tmap_page);
         tma_prefetch_desc(&tmap_page8);
+        if (rank == 1) tma_prefetch_desc(sg.single ? &tmap_olat : &tmap_part);
     }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     // everything above overlaps the previous kernel in the stream (which must not write ctx_len, read
-    // at the top to size the split); q_abs, the slab and the block table are read after it completed
+    // at the top to size the split); q_abs, the slab and the block table are read after it completed,
+    // but for the early page loads of a layer-call
+    if (p.early) early_loads(sm, tmap_page, tmap_page8, p, sg, rank, warp, lane);
     griddep_wait();
     griddep_launch_dependents();
-    decode_roles(sm, tmap_page, tmap_page8, tmap_q, p, sg, tbase, rank, warp, lane);
+    decode_roles(sm, tmap_page, tmap_page8, tmap_q, tmap_olat, tmap_part, p, sg, tbase, rank, warp, lane);
 
     __syncwarp();
     tc_fence_before();
@@ -1060,7 +1107,7 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
                         const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
                         const uint16_t* w_kv_b, uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t,
                         void* workspace, size_t ws_bytes, int B, int max_ctx, int split_tokens, int32_t* dev_err,
-                        void* stream, uint64_t wait_ns, int withhold)
+                        void* stream, uint64_t wait_ns, int withhold, int early)
 {
     if (B < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers || max_pages_per_slot <= 0 ||
         max_ctx <= 0 || split_tokens < 0 || split_tokens % TILE != 0) {
@@ -1085,7 +1132,7 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
     }
     if (!device_ok()) return K3MLA_E_DEVICE;
     const int ns = launch_nsplit(max_ctx, split_tokens);
-    if ((long long)B * ns * 2 > 0x7FFFFFFFll) {
+    if ((long long)B * ns * H > 0x7FFFFFFFll) {  // grid and partial-row coordinates
         set_error("k3mla_paged_decode: grid too large");
         return K3MLA_E_INVALID;
     }
@@ -1118,9 +1165,29 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
     dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
     dp.wait_ns = wait_ns;
     dp.withhold = withhold;
+    dp.early = early;
+    // the PV CTAs' stores: o_lat [96][B][512] bf16 as (512 dims, B slots, 96 heads), and the f32 partials
+    // [B][ns][96][512] as (512 dims, B ns 96 rows)
+    CUtensorMap tm_olat, tm_part;
+    {
+        const uint64_t dims[3] = {LORA, (uint64_t)B, H};
+        const uint64_t strides[2] = {LORA * 2, (uint64_t)B * LORA * 2};
+        const uint32_t box[3] = {256, 1, H};
+        rc = make_tmap_plain(&tm_olat, false, 3, dp.ws_olat, dims, strides, box);
+        if (rc) return rc;
+    }
+    if (ns > 1) {
+        const uint64_t dims[2] = {LORA, (uint64_t)B * ns * H};
+        const uint64_t strides[1] = {LORA * 4};
+        const uint32_t box[2] = {128, H};
+        rc = make_tmap_plain(&tm_part, true, 2, dp.ws_o, dims, strides, box);
+        if (rc) return rc;
+    } else {
+        tm_part = tm_olat;  // not used: no slot of this launch has several splits
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     rc = launch_pdl(k3mla_decode_split_kernel, dim3(2 * B * ns), dim3(THREADS), smem, st, "k3mla_decode_split_kernel",
-                    tm_page, tm_page8, tm_q, dp);
+                    tm_page, tm_page8, tm_q, tm_olat, tm_part, dp);
     if (rc) return rc;
 
     MergeParams mp;
@@ -1149,7 +1216,7 @@ extern "C" int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, i
 {
     return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
                         scale_bf16, out, argmax_t, workspace, ws_bytes, B, max_ctx, split_tokens, dev_err, stream,
-                        WAIT_NS, 0);
+                        WAIT_NS, 0, 0);
 }
 
 extern "C" int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers,
@@ -1165,7 +1232,7 @@ extern "C" int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* 
     }
     return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
                         scale_bf16, out, argmax_t, workspace, ws_bytes, B, max_ctx, split_tokens, dev_err, stream,
-                        (uint64_t)wait_us * 1000ull, withhold_page + 1);
+                        (uint64_t)wait_us * 1000ull, withhold_page + 1, 0);
 }
 
 // ---- one decode step of one layer ------------------------------------------------------
@@ -1211,9 +1278,11 @@ extern "C" int k3mla_decode_layer(const uint16_t* q, const uint16_t* w_kv_b, uin
                                                max_pages_per_slot, ctx_len, c_kv, c_stride, k_rope, r_stride, B,
                                                dev_err, reinterpret_cast<cudaStream_t>(stream));
     if (rc) return rc;
-    return k3mla_paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
-                              scale_bf16, out, argmax_t, dws, dws_bytes, B, max_ctx, K3MLA_SPLIT_AUTO, dev_err,
-                              stream);
+    // the split kernel loads pages before the absorption-append launch has completed (early_loads): all
+    // but the page each slot's row goes into
+    return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
+                        scale_bf16, out, argmax_t, dws, dws_bytes, B, max_ctx, K3MLA_SPLIT_AUTO, dev_err, stream,
+                        WAIT_NS, 0, 1);
 }
 
 // ---- decode with built-in scratch ----------------------------------------------------
