@@ -28,18 +28,20 @@
 //     with packed bf16x2 instructions -- keep a lazily moved reference max per
 //     head, and copy bf16 p to the partner CTA's shared memory with one bulk
 //     smem-to-DSMEM copy per warp and page (completion counted in bytes on the
-//     partner's mbarrier), laid out as the K-major B operand of the second
+//     partner's mbarrier), laid out as the K-major A operand of the second
 //     contraction.
 //   * rank 1, the PV CTA, streams the same pages (chunks 0..7 as two 32 KB
 //     half-page boxes into a ring of five half-page slots, one producer each;
-//     these reads mostly hit L2 right after the score CTA's) and accumulates O^T[512 dims x 96 heads] += C^T . P^T
-//     in TMEM (four M = 128 blocks, N = 96, K = 64 tokens per page; A is the
-//     MN-major latent page).  Its epilogue warps rescale O when the score CTA
-//     moved a head's reference max and zero rows past the context in the final
-//     page (stale rows must never meet p = 0 as 0 * NaN); at the end every warp
-//     helps write O out -- the split's f32 partial, or, for a slot with a single
-//     split, final bf16 o_lat = bf16(O * (1 / l)).
-// TMEM holds Q (288 columns) + S (3 x 64) in rank 0 and O (384) in rank 1, which
+//     these reads mostly hit L2 right after the score CTA's) and accumulates
+//     O[heads x 512 dims] += P . C in TMEM (M = 128 rows, the 96 heads first;
+//     two N = 256 halves; K = 64 tokens per page; B is the MN-major latent
+//     page), so that a thread reading its TMEM lane holds one head's O row.  Its
+//     epilogue warps rescale O when the score CTA moved a head's reference max
+//     and zero rows past the context in the final page (stale rows must never
+//     meet p = 0 as 0 * NaN); at the end six warps write O out -- the split's f32
+//     partial, or, for a slot with a single split, final bf16 o_lat = bf16(O *
+//     (1 / l)) -- in swizzled boxes that bulk tensor stores copy out.
+// TMEM holds Q (288 columns) + S (3 x 64) in rank 0 and O (512) in rank 1, which
 // is why the two contractions live in different CTAs.
 //
 // Split boundaries depend only on the logical position, the slot's own ctx_len
@@ -98,7 +100,7 @@ constexpr float TAU = 16.0f;                   // max growth (natural log) befor
                                                // l <= n e^16 stays far inside f32 for any context here
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
-constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 96, 1, 0);   // O^T block = C^T . P^T (A MN-major)
+constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 256, 0, 1);  // O half = P . C (B MN-major)
 // rank 0: warps 0-7 softmax, 8-10 producers, 11-13 MMA issuers; rank 1: warps 0-3
 // epilogue, 4-8 producers, 9 MMA issuer, 10-13 idle.  Warp 8 allocates TMEM in both.
 constexpr int THREADS = 448;
@@ -106,6 +108,8 @@ constexpr int W_PROD0 = 8, W_MMA0 = 11, W_ALLOC = 8;
 // named barriers of the score CTA (0 is __syncthreads): the decision hand-off between the two
 // softmax warps of a quarter (2 per quarter) and their final combine
 constexpr uint32_t HAND_BAR0 = 1, FIN_BAR0 = 9;
+// named barrier of the PV CTA's write-out (its six writing warps)
+constexpr uint32_t WO_BAR = 13;
 // 14 warps put four on some SM sub-partitions (16K registers each): at most 128 registers per thread.
 
 struct __align__(1024) Smem {
@@ -150,7 +154,10 @@ static_assert(QBYTES <= (NUNIT - Q_UNIT0) * THIRD + 8 * PSTAGE,
 static_assert(PCOPY <= PBUF, "P buffer");
 static_assert(H * LORA * 4 <= NHSLOT * SLOT1 + NPBUF * PBUF,
               "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
-static_assert((H * 256 * 2) % 128 == 0 && (H * 128 * 4) % 128 == 0, "store boxes start 128-byte aligned");
+static_assert((H * 128) % 1024 == 0, "store boxes start 1024-byte aligned (128-byte swizzle)");
+static_assert(16 * H * 128 <= NHSLOT * SLOT1 + NPBUF * PBUF, "the write-out boxes fit in the ring and P buffers");
+static_assert(NHSLOT * SLOT1 + (NPBUF - 1) * PBUF + 128 * 128 <= sizeof(Smem::u),
+              "rows 96..127 of the last P buffer, read as the A operand's unused rows, lie in this CTA's tile area");
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
 
 struct DecodeParams {
@@ -326,22 +333,25 @@ __device__ __forceinline__ void issue_score_third(uint32_t tbase, uint32_t d_col
     }
 }
 
-// PV CTA: O^T (+)= C^T . P^T over one 64-token page held as two half-page slots
-// ([8 chunks][32 rows][128 B] each): 4 blocks of 128 dims x 4 K-steps of 16 tokens.
+// PV CTA: O[128 rows = heads (rows 96.. unused) x 512 dims] (+)= P . C over one 64-token page held as
+// two half-page slots ([8 chunks][32 rows][128 B] each).  A = P, K-major (the P buffer's rows are heads,
+// 64 tokens each; rows 96..127 read whatever follows the buffer in this CTA's shared memory and only
+// land in TMEM lanes nobody reads); B = C, MN-major (dims contiguous).  Two N = 256 halves of the dims
+// x 4 K-steps of 16 tokens.
 __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_addr, uint32_t half1_addr,
                                               uint32_t pt_addr, bool accumulate_first)
 {
-    const uint64_t b0 = make_sdesc(pt_addr, 16, 1024);
+    const uint64_t a0 = make_sdesc(pt_addr, 16, 1024);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-        const uint64_t a0 = make_sdesc(hh ? half1_addr : half0_addr, HCHUNK, 1024);
+        const uint64_t b0 = make_sdesc(hh ? half1_addr : half0_addr, HCHUNK, 1024);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t ad = a0 + (uint64_t)((uint32_t)((2 * hh + ks) * 32) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t ad = a0 + (uint64_t)((uint32_t)(2 * j * HCHUNK + ks * 2048) >> 4);
-                const uint64_t bd = b0 + (uint64_t)((uint32_t)((2 * hh + ks) * 32) >> 4);
-                umma_ss(tbase + 96u * j, ad, bd, IDESC_PV, (accumulate_first || hh > 0 || ks > 0) ? 1u : 0u);
+            for (int n = 0; n < 2; ++n) {
+                const uint64_t bd = b0 + (uint64_t)((uint32_t)(4 * n * HCHUNK + ks * 2048) >> 4);
+                umma_ss(tbase + 256u * n, ad, bd, IDESC_PV, (accumulate_first || hh > 0 || ks > 0) ? 1u : 0u);
             }
         }
     }
@@ -350,54 +360,65 @@ __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_add
 // Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
 __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_t)(h * 128 + ((j ^ (h & 7)) << 4)); }
 
-// PV CTA, after its roles: O^T [512 dims x 96 heads] f32 leaves TMEM through the (now idle) page ring
-// and P buffers, laid out there as the boxes of bulk tensor stores.  Twelve warps, each one TMEM lane
-// quarter (dims 32 q .. 32 q + 31 of every 128-dim block) x one 32-head piece, write either final o_lat
-// = bf16(O * (1 / l)) of a slot with a single split, as [2 halves of 256 dims][96 heads][256] bf16, or
-// the split's f32 partial as it stands, as [4 quarters of 128 dims][96 heads][128] f32 (a warp's 32
-// lanes write 32 consecutive dims of one head: one shared-memory wavefront).  One thread then stores
-// the tile with two or four bulk tensor stores and waits until they are complete.  Kept out of line
-// so that it does not weigh on the register allocation of the pipeline.
+// PV CTA, after its roles: O [heads x 512 dims] f32 leaves TMEM through the (now idle) page ring and P
+// buffers, laid out there as the 128-byte-swizzled boxes of bulk tensor stores: [96 heads][64 dims]
+// bf16 boxes of final o_lat = bf16(O * (1 / l)) when the slot has a single split, else [96 heads][32
+// dims] f32 boxes of the split's partial as it stands.  Six warps write, thread = head (TMEM lane),
+// warps 0-2 the dims 0..255 and warps 4-6 the dims 256..511, 16 bytes at a time; whenever a box of
+// each half is complete, thread 0 stores the two while the warps go on.  At the end it waits until
+// the stores have read the tile (the writes reach global memory before the grid counts as complete,
+// which is what the merge kernel waits for).  Kept out of line so that it does not weigh on the
+// register allocation of the pipeline.
 __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, const CUtensorMap* tm_part,
                                           bool single, int nsplit, uint32_t tbase, int b, int s)
 {
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     uint8_t* tile = sm.u.c1.ring[0];
-    if (warp < 12) {
+    if (warp < 8 && (warp & 3u) < 3u) {
         tc_fence_after();
-        const int q = (int)(warp & 3u), pc = (int)(warp >> 2);
-        const uint32_t ta = tbase + ((32u * (uint32_t)q) << 16) + 32u * (uint32_t)pc;
-        float rl[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) rl[c] = single ? sm.rl[32 * pc + c] : 1.f;
+        const int h = 32 * (int)(warp & 3u) + (int)lane, half = (int)(warp >> 2);
+        const uint32_t ta = tbase + ((32u * (warp & 3u)) << 16) + 256u * (uint32_t)half;
+        const float r = single ? sm.rl[h] : 1.f;
+        const uint32_t sw = (uint32_t)(h & 7);
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+        for (int k = 0; k < 8; ++k) {  // dims 256 half + 32 k .. + 31
             uint32_t rr[32];
-            tmem_ld32(ta + 96u * (uint32_t)j, rr);
+            tmem_ld32(ta + 32u * (uint32_t)k, rr);
             tmem_wait_ld();
-            const int d = 128 * j + 32 * q + (int)lane;
-            if (single) {
-                uint16_t* t16 = reinterpret_cast<uint16_t*>(tile) + (d >> 8) * (H * 256) + (32 * pc) * 256 + (d & 255);
+            if (single) {  // box 4 half + k / 2 (64 dims), 16-byte chunks 4 (k & 1) .. + 3 of row h
+                uint8_t* row = tile + (4 * half + (k >> 1)) * (H * 128) + h * 128;
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    t16[c * 256] = (uint16_t)(pack_bf16x2(__uint_as_float(rr[c]) * rl[c], 0.f) & 0xFFFFu);
-            } else {
-                float* t32 = reinterpret_cast<float*>(tile) + (d >> 7) * (H * 128) + (32 * pc) * 128 + (d & 127);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t ch = (uint32_t)(4 * (k & 1) + i);
+                    *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) =
+                        make_uint4(pack_bf16x2(__uint_as_float(rr[8 * i]) * r, __uint_as_float(rr[8 * i + 1]) * r),
+                                   pack_bf16x2(__uint_as_float(rr[8 * i + 2]) * r, __uint_as_float(rr[8 * i + 3]) * r),
+                                   pack_bf16x2(__uint_as_float(rr[8 * i + 4]) * r, __uint_as_float(rr[8 * i + 5]) * r),
+                                   pack_bf16x2(__uint_as_float(rr[8 * i + 6]) * r, __uint_as_float(rr[8 * i + 7]) * r));
+                }
+            } else {  // box 8 half + k (32 dims), all eight 16-byte chunks of row h
+                uint8_t* row = tile + (8 * half + k) * (H * 128) + h * 128;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) t32[c * 128] = __uint_as_float(rr[c]);
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<uint4*>(row + (((uint32_t)i ^ sw) << 4)) =
+                        make_uint4(rr[4 * i], rr[4 * i + 1], rr[4 * i + 2], rr[4 * i + 3]);
+            }
+            if (single && !(k & 1)) continue;  // a bf16 box takes two passes
+            fence_proxy_async_cta();  // the boxes are read by bulk tensor stores (async proxy)
+            named_bar(WO_BAR, 6 * 32);
+            if (threadIdx.x == 0) {
+                if (single) {  // o_lat [96][B][512] as (512 dims, B slots, 96 heads), box (64, 1, 96)
+                    const int bi = k >> 1;
+                    tma_store_3d(tm_olat, tile + bi * (H * 128), 64 * bi, b, 0);
+                    tma_store_3d(tm_olat, tile + (4 + bi) * (H * 128), 256 + 64 * bi, b, 0);
+                } else {  // partials [B][nsplit][96][512] as (512 dims, rows), box (32, 96)
+                    tma_store_2d(tm_part, tile + k * (H * 128), 32 * k, (b * nsplit + s) * H);
+                    tma_store_2d(tm_part, tile + (8 + k) * (H * 128), 256 + 32 * k, (b * nsplit + s) * H);
+                }
+                bulk_commit();
             }
         }
-    }
-    fence_proxy_async_cta();  // the tile is read by the bulk tensor stores (async proxy)
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (single) {  // o_lat [96][B][512] viewed as (512 dims, B slots, 96 heads), box (256, 1, 96)
-            for (int k = 0; k < 2; ++k) tma_store_3d(tm_olat, tile + k * (H * 256 * 2), 256 * k, b, 0);
-        } else {  // partials [B][nsplit][96][512] viewed as (512 dims, rows), box (128, 96)
-            for (int k = 0; k < 4; ++k) tma_store_2d(tm_part, tile + k * (H * 128 * 4), 128 * k, (b * nsplit + s) * H);
-        }
-        bulk_commit();
-        bulk_wait<0>();
+        if (threadIdx.x == 0) bulk_wait_read<0>();
     }
 }
 
@@ -798,7 +819,8 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 }
             }
         } else if (warp < 4) {
-            // epilogue warps 0..3: thread owns TMEM lane 32*warp + lane (one latent dim per block)
+            // epilogue warps 0..3: thread owns TMEM lane 32*warp + lane, the O row of that head (lanes
+            // 96.. are not heads)
             const uint32_t t_lane = tbase + ((32u * warp) << 16);
             uint32_t k = 0, od = 0;
             for (;;) {
@@ -806,29 +828,25 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 if (!__all_sync(0xFFFFFFFFu, got)) break;
                 ++k;
                 const uint32_t cmd = *reinterpret_cast<volatile uint32_t*>(&sm.epi_cmd);
-                if (cmd & 1u) {  // rescale O^T columns by alpha[head]
+                if (cmd & 1u) {  // rescale each head's O row by its alpha
                     const bool got2 = wait_bar(&sm.o_done, od & 1u, sm, p.dev_err);
                     if (!__all_sync(0xFFFFFFFFu, got2)) break;
                     ++od;
                     tc_fence_after();
                     const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + META_ALPHA);
+                    const float a = warp < 3 ? al[32 * warp + lane] : 1.f;
+                    if (__any_sync(0xFFFFFFFFu, a != 1.f)) {  // some head of this warp moved its reference
 #pragma unroll 1
-                    for (int piece = 0; piece < 3; ++piece) {  // heads 32 piece .. 32 piece + 31
-                        float a32[32];
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) a32[c] = al[32 * piece + c];
-#pragma unroll 1
-                        for (int j = 0; j < 4; ++j) {
+                        for (int cb = 0; cb < LORA / 32; ++cb) {
                             uint32_t rr[32];
-                            const uint32_t ta = t_lane + 96u * j + 32u * piece;
-                            tmem_ld32(ta, rr);
+                            tmem_ld32(t_lane + 32u * cb, rr);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * a32[c]);
-                            tmem_st32(ta, rr);
+                            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * a);
+                            tmem_st32(t_lane + 32u * cb, rr);
                         }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
                     tc_fence_before();
                 }
                 if (cmd & 2u) {  // zero rows >= vrows of chunks 0..7 of the final page (two half slots)
@@ -1043,15 +1061,14 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.o_done, 0, sm, nullptr));
         tc_fence_after();
-        if (ok)
-            for (int j = 0; j < 4; ++j)
-                for (int piece = 0; piece < 3; ++piece) {
-                    uint32_t r[32];
-                    tmem_ld32(t_lane + 96u * j + 32u * piece, r);
-                    tmem_wait_ld();
-                    for (int c = 0; c < 32; ++c)
-                        d[(size_t)(128 * j + 32 * warp + lane) * H + 32 * piece + c] = __uint_as_float(r[c]);
-                }
+        if (ok)  // TMEM lane = head (warps 0..2), column = dim; d is [512 dims][96 heads]
+            for (int cb = 0; cb < LORA / 32; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + 32u * cb, r);
+                tmem_wait_ld();
+                if (warp < 3)
+                    for (int c = 0; c < 32; ++c) d[(size_t)(32 * cb + c) * H + 32 * warp + lane] = __uint_as_float(r[c]);
+            }
     }
     if (!ok) drain_inflight();
     __syncwarp();
@@ -1172,15 +1189,15 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
     {
         const uint64_t dims[3] = {LORA, (uint64_t)B, H};
         const uint64_t strides[2] = {LORA * 2, (uint64_t)B * LORA * 2};
-        const uint32_t box[3] = {256, 1, H};
-        rc = make_tmap_plain(&tm_olat, false, 3, dp.ws_olat, dims, strides, box);
+        const uint32_t box[3] = {64, 1, H};
+        rc = make_tmap_sw128(&tm_olat, false, 3, dp.ws_olat, dims, strides, box);
         if (rc) return rc;
     }
     if (ns > 1) {
         const uint64_t dims[2] = {LORA, (uint64_t)B * ns * H};
         const uint64_t strides[1] = {LORA * 4};
-        const uint32_t box[2] = {128, H};
-        rc = make_tmap_plain(&tm_part, true, 2, dp.ws_o, dims, strides, box);
+        const uint32_t box[2] = {32, H};
+        rc = make_tmap_sw128(&tm_part, true, 2, dp.ws_o, dims, strides, box);
         if (rc) return rc;
     } else {
         tm_part = tm_olat;  // not used: no slot of this launch has several splits
