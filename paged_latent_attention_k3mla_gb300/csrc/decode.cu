@@ -364,8 +364,9 @@ __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_
 // buffers, laid out there as the 128-byte-swizzled boxes of bulk tensor stores: [96 heads][64 dims]
 // bf16 boxes of final o_lat = bf16(O * (1 / l)) when the slot has a single split, else [96 heads][32
 // dims] f32 boxes of the split's partial as it stands.  Six warps write, thread = head (TMEM lane),
-// warps 0-2 the dims 0..255 and warps 4-6 the dims 256..511, 16 bytes at a time; whenever a box of
-// each half is complete, thread 0 stores the two while the warps go on.  At the end it waits until
+// warps 0-2 the dims 0..255 and warps 4-6 the dims 256..511, 64 dims (two TMEM loads, one wait) at a
+// time, 16 bytes per store; whenever both halves have written theirs, thread 0 stores those boxes
+// while the warps go on.  At the end it waits until
 // the stores have read the tile (the writes reach global memory before the grid counts as complete,
 // which is what the merge kernel waits for).  Kept out of line so that it does not weigh on the
 // register allocation of the pipeline.
@@ -381,39 +382,44 @@ __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, 
         const float r = single ? sm.rl[h] : 1.f;
         const uint32_t sw = (uint32_t)(h & 7);
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {  // dims 256 half + 32 k .. + 31
-            uint32_t rr[32];
-            tmem_ld32(ta + 32u * (uint32_t)k, rr);
+        for (int k2 = 0; k2 < 4; ++k2) {  // dims 256 half + 64 k2 .. + 63: two loads, one wait
+            uint32_t rr[2][32];
+            tmem_ld32(ta + 64u * (uint32_t)k2, rr[0]);
+            tmem_ld32(ta + 64u * (uint32_t)k2 + 32u, rr[1]);
             tmem_wait_ld();
-            if (single) {  // box 4 half + k / 2 (64 dims), 16-byte chunks 4 (k & 1) .. + 3 of row h
-                uint8_t* row = tile + (4 * half + (k >> 1)) * (H * 128) + h * 128;
+            if (single) {  // box 4 half + k2 (64 dims): the eight 16-byte chunks of row h
+                uint8_t* row = tile + (4 * half + k2) * (H * 128) + h * 128;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t ch = (uint32_t)(4 * (k & 1) + i);
-                    *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) =
-                        make_uint4(pack_bf16x2(__uint_as_float(rr[8 * i]) * r, __uint_as_float(rr[8 * i + 1]) * r),
-                                   pack_bf16x2(__uint_as_float(rr[8 * i + 2]) * r, __uint_as_float(rr[8 * i + 3]) * r),
-                                   pack_bf16x2(__uint_as_float(rr[8 * i + 4]) * r, __uint_as_float(rr[8 * i + 5]) * r),
-                                   pack_bf16x2(__uint_as_float(rr[8 * i + 6]) * r, __uint_as_float(rr[8 * i + 7]) * r));
-                }
-            } else {  // box 8 half + k (32 dims), all eight 16-byte chunks of row h
-                uint8_t* row = tile + (8 * half + k) * (H * 128) + h * 128;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t* v = rr[i >> 2] + 8 * (i & 3);
                     *reinterpret_cast<uint4*>(row + (((uint32_t)i ^ sw) << 4)) =
-                        make_uint4(rr[4 * i], rr[4 * i + 1], rr[4 * i + 2], rr[4 * i + 3]);
+                        make_uint4(pack_bf16x2(__uint_as_float(v[0]) * r, __uint_as_float(v[1]) * r),
+                                   pack_bf16x2(__uint_as_float(v[2]) * r, __uint_as_float(v[3]) * r),
+                                   pack_bf16x2(__uint_as_float(v[4]) * r, __uint_as_float(v[5]) * r),
+                                   pack_bf16x2(__uint_as_float(v[6]) * r, __uint_as_float(v[7]) * r));
+                }
+            } else {  // boxes 8 half + 2 k2 and + 1 (32 dims each): all chunks of row h
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint8_t* row = tile + (8 * half + 2 * k2 + e) * (H * 128) + h * 128;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4*>(row + (((uint32_t)i ^ sw) << 4)) =
+                            make_uint4(rr[e][4 * i], rr[e][4 * i + 1], rr[e][4 * i + 2], rr[e][4 * i + 3]);
+                }
             }
-            if (single && !(k & 1)) continue;  // a bf16 box takes two passes
             fence_proxy_async_cta();  // the boxes are read by bulk tensor stores (async proxy)
             named_bar(WO_BAR, 6 * 32);
             if (threadIdx.x == 0) {
                 if (single) {  // o_lat [96][B][512] as (512 dims, B slots, 96 heads), box (64, 1, 96)
-                    const int bi = k >> 1;
-                    tma_store_3d(tm_olat, tile + bi * (H * 128), 64 * bi, b, 0);
-                    tma_store_3d(tm_olat, tile + (4 + bi) * (H * 128), 256 + 64 * bi, b, 0);
+                    tma_store_3d(tm_olat, tile + k2 * (H * 128), 64 * k2, b, 0);
+                    tma_store_3d(tm_olat, tile + (4 + k2) * (H * 128), 256 + 64 * k2, b, 0);
                 } else {  // partials [B][nsplit][96][512] as (512 dims, rows), box (32, 96)
-                    tma_store_2d(tm_part, tile + k * (H * 128), 32 * k, (b * nsplit + s) * H);
-                    tma_store_2d(tm_part, tile + (8 + k) * (H * 128), 256 + 32 * k, (b * nsplit + s) * H);
+                    const int row0 = (b * nsplit + s) * H;
+                    for (int e = 0; e < 2; ++e) {
+                        tma_store_2d(tm_part, tile + (2 * k2 + e) * (H * 128), 64 * k2 + 32 * e, row0);
+                        tma_store_2d(tm_part, tile + (8 + 2 * k2 + e) * (H * 128), 256 + 64 * k2 + 32 * e, row0);
+                    }
                 }
                 bulk_commit();
             }
