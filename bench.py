@@ -436,13 +436,14 @@ def e2e_leg(run, steps, warmup):
 
 def extra_workloads(hbm, steps, warmup):
     """The other configurations' figures (parity cases, not the bench's value): each as its own
-    24-layer CUDA-graph step under the default per-slot split, and the ragged batch also under the
-    opt-in batch-planned split (whose numerics depend on the batch)."""
+    24-layer CUDA-graph step under the default per-slot split; the ragged batch also under a fixed
+    512-token split (as batch-invariant as the default: the latency setting for small batches) and
+    under the opt-in batch-planned split (whose numerics depend on the batch)."""
     from paged_latent_attention_k3mla_gb300 import k3mla
     res = {}
-    for name, split_kind in (("long8", "auto"), ("ragged16", "auto"), ("ragged16", "planned"),
-                             ("padding128", "auto")):
-        split = 0
+    for name, split_kind in (("long8", "auto"), ("ragged16", "auto"), ("ragged16", "split512"),
+                             ("ragged16", "planned"), ("padding128", "auto")):
+        split = 512 if split_kind == "split512" else 0
         if split_kind == "planned":
             wl0 = synth.make_workload(name, device="cpu", n_layers=1)
             split = k3mla.batch_planned_split_tokens(wl0.ctx_len, MAX_CTX[name])
@@ -455,7 +456,9 @@ def extra_workloads(hbm, steps, warmup):
                        "k3mla_absorb_q_append + k3mla_paged_decode per layer-call")
         if split_kind == "planned":
             fig["numerics"] = "batch-dependent (opt-in k3mla_batch_planned_split_tokens)"
-        res[name if split_kind == "auto" else f"{name}_planned"] = fig
+        elif split_kind == "split512":
+            fig["numerics"] = "batch-invariant (a fixed split length the caller chooses once)"
+        res[name if split_kind == "auto" else f"{name}_{split_kind}"] = fig
         del run
         torch.cuda.empty_cache()
     return res
