@@ -159,16 +159,13 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     griddep_launch_dependents();
 
     // The append (when this launch carries one): CTA `lin` writes the rows of slots lin, lin + ncta,
-    // ... (one slot per CTA unless B exceeds the grid's CTAs); its last AP_THREADS threads fetch the
-    // first row here, beside the q_nope loads, and store it once their share of the B operand is
-    // written.
+    // ... (one slot per CTA unless B exceeds the grid's CTAs) with its last AP_THREADS threads, once
+    // their share of the B operand is written: the row's position and page id are two dependent
+    // loads, which would hold the B operand (and the MMAs) back if they came first.
     const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x);
     const int ncta = (int)(gridDim.x * gridDim.y);
     const int at = (int)threadIdx.x - (AB_THREADS - AP_THREADS);
     const bool app_thread = lin < ap.B && at >= 0;
-    uint32_t av[3] = {0u, 0u, 0u};
-    int64_t arow = -1;
-    if (app_thread) arow = append_fetch(ap, lin, at, av);
 
     {   // q_nope of the tile -> B operand; q_rope -> q_abs[..][512:576].  thread -> (slot r, segment seg)
         const int seg = threadIdx.x & 7;
@@ -191,9 +188,9 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         mbar_arrive(&b_ready);
     }
     if (app_thread) {
-        append_store(ap, arow, at, av);
-        for (int sl = lin + ncta; sl < ap.B; sl += ncta) {  // only when B exceeds the grid's CTAs
-            arow = append_fetch(ap, sl, at, av);
+        for (int sl = lin; sl < ap.B; sl += ncta) {  // more than one slot only when B exceeds the grid's CTAs
+            uint32_t av[3];
+            const int64_t arow = append_fetch(ap, sl, at, av);
             append_store(ap, arow, at, av);
         }
     }
@@ -219,7 +216,8 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
     }
     {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's NB slots and
         // lands bf16 values in a [NB slots][512] tile over the (now idle) W_UK buffer; the CTA then
-        // writes each slot's 1 KB row of q_abs with 16-byte stores
+        // writes each slot's 1 KB row of q_abs with 16-byte stores (measured faster here than one
+        // thread's bulk tensor stores of the same tile)
         const int qq = warp & 3, mt = warp >> 2;
         const bool got = ab_wait(&d_full, 0, nullptr);
         uint16_t* tile = reinterpret_cast<uint16_t*>(sa);

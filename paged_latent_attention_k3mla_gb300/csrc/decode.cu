@@ -1196,14 +1196,14 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
         const uint64_t dims[3] = {LORA, (uint64_t)B, H};
         const uint64_t strides[2] = {LORA * 2, (uint64_t)B * LORA * 2};
         const uint32_t box[3] = {64, 1, H};
-        rc = make_tmap_sw128(&tm_olat, false, 3, dp.ws_olat, dims, strides, box);
+        rc = make_tmap_store(&tm_olat, false, 3, dp.ws_olat, dims, strides, box, true);
         if (rc) return rc;
     }
     if (ns > 1) {
         const uint64_t dims[2] = {LORA, (uint64_t)B * ns * H};
         const uint64_t strides[1] = {LORA * 4};
         const uint32_t box[2] = {32, H};
-        rc = make_tmap_sw128(&tm_part, true, 2, dp.ws_o, dims, strides, box);
+        rc = make_tmap_store(&tm_part, true, 2, dp.ws_o, dims, strides, box, true);
         if (rc) return rc;
     } else {
         tm_part = tm_olat;  // not used: no slot of this launch has several splits

@@ -112,8 +112,8 @@ int make_tmap_slab_3d(CUtensorMap* map, const void* base, uint64_t rows, uint32_
     return K3MLA_OK;
 }
 
-int make_tmap_sw128(CUtensorMap* map, bool f32, uint32_t rank, const void* base, const uint64_t* dims,
-                    const uint64_t* strides, const uint32_t* box)
+int make_tmap_store(CUtensorMap* map, bool f32, uint32_t rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box, bool swizzle128)
 {
     auto fn = encode_fn();
     if (!fn) {
@@ -129,10 +129,11 @@ int make_tmap_sw128(CUtensorMap* map, bool f32, uint32_t rank, const void* base,
         if (i + 1 < rank) st[i] = strides[i];
     }
     CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-                    const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
-        set_error("cuTensorMapEncodeTiled (swizzled store view) failed (%d)", (int)r);
+        set_error("cuTensorMapEncodeTiled (store view) failed (%d)", (int)r);
         return K3MLA_E_CUDA;
     }
     return K3MLA_OK;
