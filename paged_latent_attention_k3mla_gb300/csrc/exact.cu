@@ -15,12 +15,13 @@
 // double-precision exp rounded once to f32, normalisation is the IEEE quotient.
 // Fixed orders rule out the tensor cores, so these are CUDA-core kernels:
 //   E0 absorption   thread per (slot, head, j): sum over d = 0..127
-//   E1 scores       CTA per (slot, 8 pages): Q and each page staged in shared
-//                   memory; thread per (4 tokens, 3 heads): sums over k = 0..575
+//   E1 scores       CTA per (slot, 128 tokens): Q and the rows staged in shared
+//                   memory by 32-dim chunks; thread per (8 tokens, 6 heads): sums
+//                   over k = 0..575
 //   E2 softmax      CTA per (slot, head): max and exps across the block, the sum
 //                   of exp thread 0's loop over t ascending, p_t = bf16(e_t / l),
 //                   argmax (lowest t with the largest p)
-//   E3 latent sum   CTA per (slot, 64 dims): thread per (4 dims, 6 heads), sums
+//   E3 latent sum   CTA per (slot, 64 dims): thread per (8 dims, 6 heads), sums
 //                   over t ascending, pages staged in shared memory
 //   E4 expansion    CTA per (head, 16 slots): W_UV[h] staged; thread per v:
 //                   sixteen sums over j = 0..511
@@ -89,15 +90,23 @@ __global__ void __launch_bounds__(LORA) ex_absorb_kernel(const uint16_t* __restr
 }
 
 // ---- E1: scores ----------------------------------------------------------------------------
-constexpr int E1_PAGES = 8;              // pages per CTA (Q is staged once for them)
-constexpr int E1_THREADS = 512;
-constexpr int E1_QP = ROW + 2;           // padded row pitch (elements): rows start in distinct banks
-constexpr int E1_SMEM = (H + PAGE) * E1_QP * 2;
-constexpr int E1_TOK = 4, E1_HEADS = 3;  // register tile of one thread: 4 tokens x 3 heads
+constexpr int E1_TB = 2 * PAGE;          // tokens per CTA
+constexpr int E1_KC = 32;                // dims per staged chunk (576 = 18 chunks)
+constexpr int E1_NKC = ROW / E1_KC;
+constexpr int E1_THREADS = 256;          // 16 token groups x 16 head groups
+constexpr int E1_TT = 8, E1_HT = 6;      // register tile of one thread: 8 tokens x 6 heads
+constexpr int E1_RP = E1_TB + 4;         // Rs row pitch (floats): 16-byte rows, rows 4 banks apart
+constexpr int E1_BUF = E1_KC * (E1_RP + H);  // one stage: Rs [KC][RP] + Qs [KC][96], f32
+constexpr int E1_SMEM = 2 * E1_BUF * 4;
+static_assert(E1_TB * E1_KC == 2 * 8 * E1_THREADS, "R staging: two 8-dim pieces per thread");
+static_assert(H * E1_KC <= 2 * 8 * E1_THREADS && H * E1_KC > 8 * E1_THREADS, "Q staging: one or two pieces per thread");
+static_assert(H * E1_TB * 2 <= E1_SMEM, "the bf16 score tile fits in the staging buffers");
 
-// grid (B, ceil(max_ctx / (64 * E1_PAGES))); block 512.  s[b][h][t] = bf16(bf16(dot) * scale).
-// Thread (warp w, lane l): tokens g, g + 16, g + 32, g + 48 of the page (g = l % 16) and heads
-// 3 (2 w + l / 16) .. + 2; each of its 12 dots is one sequential sum over k = 0..575 ascending (a fused
+// grid (B, ceil(max_ctx / 128)); block 256.  s[b][h][t] = bf16(bf16(dot) * scale).  Q and the 128
+// tokens' rows are staged in chunks of 32 dims as f32, transposed ([k][token], [k][head]) and
+// double-buffered (the next chunk's loads are in flight while this one is used).  Thread (warp w,
+// lane l): tokens 8 tg .. 8 tg + 7 with tg = 8 (w & 1) + (l & 7), heads 6 hg .. 6 hg + 5 with hg =
+// 4 (w >> 1) + (l >> 3); each of its 48 dots is one sequential sum over k = 0..575 ascending (a fused
 // multiply-add of two bf16 values rounds as the chain's multiply-then-add: the product is exact).
 __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     const uint16_t* __restrict__ q_abs, const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer,
@@ -106,72 +115,108 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
 {
     griddep_wait();
     griddep_launch_dependents();
-    extern __shared__ uint16_t ex_smem[];
-    uint16_t* Qs = ex_smem;                  // [96][E1_QP]
-    uint16_t* Rs = ex_smem + H * E1_QP;      // [64][E1_QP]
+    extern __shared__ float ex_sf[];
     const int b = blockIdx.x;
     const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
-    const int t_begin = blockIdx.y * E1_PAGES * PAGE;
+    const int t_begin = blockIdx.y * E1_TB;
     if (t_begin >= n) return;
-    const int t_end = min(n, t_begin + E1_PAGES * PAGE);
-    const float scale = ex_bf(scale_bf16);
-    for (int i = threadIdx.x; i < H * (ROW / 2); i += E1_THREADS) {
-        const int h = i / (ROW / 2), k2 = i % (ROW / 2);
-        reinterpret_cast<uint32_t*>(Qs + h * E1_QP)[k2] =
-            reinterpret_cast<const uint32_t*>(q_abs + ((size_t)b * H + h) * ROW)[k2];
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane & 15, h0 = E1_HEADS * (2 * warp + (lane >> 4));
-    for (int t0 = t_begin; t0 < t_end; t0 += PAGE) {
-        __syncthreads();  // Q staged / the previous page's rows no longer read
-        for (int i = threadIdx.x; i < PAGE * (ROW / 2); i += E1_THREADS) {
-            const int r = i / (ROW / 2), k2 = i % (ROW / 2);
-            const int t = t0 + r;
-            uint32_t v = 0u;
-            if (t < t_end) {
-                const uint16_t* row = ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t,
-                                             k2 == 0 ? dev_err : nullptr);
-                if (row) v = reinterpret_cast<const uint32_t*>(row)[k2];
-            }
-            reinterpret_cast<uint32_t*>(Rs + r * E1_QP)[k2] = v;
+    const int t_end = min(n, t_begin + E1_TB);
+    const int tid = (int)threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tg = 8 * (warp & 1) + (lane & 7), hg = 4 * (warp >> 1) + (lane >> 3);
+    // staging roles: token st (dims 16 sp .. 16 sp + 15 of each chunk); Q pieces i = tid, tid + 256
+    const int st = tid & (E1_TB - 1), sp = tid >> 7;
+    const uint16_t* srow = (t_begin + st < t_end)
+                               ? ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t_begin + st, dev_err)
+                               : nullptr;
+    const uint16_t* qrow = q_abs + (size_t)b * H * ROW;
+    const bool q2 = tid + E1_THREADS < H * E1_KC / 8;
+    uint4 rv[2], qv[2];
+    auto load = [&](int kc) {
+        const int k0 = kc * E1_KC;
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            rv[e] = srow ? *reinterpret_cast<const uint4*>(srow + k0 + 16 * sp + 8 * e) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = tid + E1_THREADS * e;
+            if (e == 0 || q2)
+                qv[e] = *reinterpret_cast<const uint4*>(qrow + (size_t)(i >> 2) * ROW + k0 + 8 * (i & 3));
         }
-        __syncthreads();
-        float acc[E1_TOK][E1_HEADS];
+    };
+    auto store = [&](int buf) {
+        float* Rs = ex_sf + buf * E1_BUF;
+        float* Qs = Rs + E1_KC * E1_RP;
 #pragma unroll
-        for (int a = 0; a < E1_TOK; ++a)
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t w[4] = {rv[e].x, rv[e].y, rv[e].z, rv[e].w};
 #pragma unroll
-            for (int c = 0; c < E1_HEADS; ++c) acc[a][c] = 0.f;
-        const uint32_t* rw[E1_TOK];
-#pragma unroll
-        for (int a = 0; a < E1_TOK; ++a) rw[a] = reinterpret_cast<const uint32_t*>(Rs + (g + 16 * a) * E1_QP);
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(Qs + h0 * E1_QP);
-#pragma unroll 2
-        for (int k2 = 0; k2 < ROW / 2; ++k2) {  // k = 2 k2, then 2 k2 + 1: ascending
-            float rlo[E1_TOK], rhi[E1_TOK];
-#pragma unroll
-            for (int a = 0; a < E1_TOK; ++a) {
-                const uint32_t rv = rw[a][k2];
-                rlo[a] = __uint_as_float(rv << 16);
-                rhi[a] = __uint_as_float(rv & 0xFFFF0000u);
+            for (int u = 0; u < 4; ++u) {
+                Rs[(16 * sp + 8 * e + 2 * u) * E1_RP + st] = __uint_as_float(w[u] << 16);
+                Rs[(16 * sp + 8 * e + 2 * u + 1) * E1_RP + st] = __uint_as_float(w[u] & 0xFFFF0000u);
             }
+        }
 #pragma unroll
-            for (int c = 0; c < E1_HEADS; ++c) {
-                const uint32_t qv = qw[c * (E1_QP / 2) + k2];
-                const float qlo = __uint_as_float(qv << 16), qhi = __uint_as_float(qv & 0xFFFF0000u);
+        for (int e = 0; e < 2; ++e) {
+            const int i = tid + E1_THREADS * e;
+            if (e == 0 || q2) {
+                const uint32_t w[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
+                const int h = i >> 2, kb = 8 * (i & 3);
 #pragma unroll
-                for (int a = 0; a < E1_TOK; ++a) {
-                    acc[a][c] = __fmaf_rn(qlo, rlo[a], acc[a][c]);
-                    acc[a][c] = __fmaf_rn(qhi, rhi[a], acc[a][c]);
+                for (int u = 0; u < 4; ++u) {
+                    Qs[(kb + 2 * u) * H + h] = __uint_as_float(w[u] << 16);
+                    Qs[(kb + 2 * u + 1) * H + h] = __uint_as_float(w[u] & 0xFFFF0000u);
                 }
             }
         }
+    };
+    float acc[E1_TT][E1_HT];
 #pragma unroll
-        for (int a = 0; a < E1_TOK; ++a) {
-            const int t = t0 + g + 16 * a;
-            if (t < t_end)
+    for (int a = 0; a < E1_TT; ++a)
 #pragma unroll
-                for (int c = 0; c < E1_HEADS; ++c)
-                    s_out[((size_t)b * H + h0 + c) * s_pitch + t] = ex_land(__fmul_rn(ex_bf(ex_land(acc[a][c])), scale));
+        for (int c = 0; c < E1_HT; ++c) acc[a][c] = 0.f;
+    load(0);
+    store(0);
+    __syncthreads();
+#pragma unroll 1
+    for (int kc = 0; kc < E1_NKC; ++kc) {
+        if (kc + 1 < E1_NKC) load(kc + 1);  // in flight while chunk kc is used
+        const float* Rs = ex_sf + (kc & 1) * E1_BUF;
+        const float* Qs = Rs + E1_KC * E1_RP;
+#pragma unroll 4
+        for (int k = 0; k < E1_KC; ++k) {
+            const float4 r0 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg);
+            const float4 r1 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg + 4);
+            const float2 qa = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg);
+            const float2 qb = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg + 2);
+            const float2 qc = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg + 4);
+            const float r[E1_TT] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            const float q[E1_HT] = {qa.x, qa.y, qb.x, qb.y, qc.x, qc.y};
+#pragma unroll
+            for (int a = 0; a < E1_TT; ++a)
+#pragma unroll
+                for (int c = 0; c < E1_HT; ++c) acc[a][c] = __fmaf_rn(q[c], r[a], acc[a][c]);
+        }
+        if (kc + 1 < E1_NKC) store((kc + 1) & 1);
+        __syncthreads();
+    }
+    // the landed scores through shared memory ([96 heads][128 tokens] bf16), then row by row
+    const float scale = ex_bf(scale_bf16);
+    uint16_t* S = reinterpret_cast<uint16_t*>(ex_sf);
+#pragma unroll
+    for (int a = 0; a < E1_TT; ++a)
+#pragma unroll
+        for (int c = 0; c < E1_HT; ++c)
+            S[(6 * hg + c) * E1_TB + 8 * tg + a] = ex_land(__fmul_rn(ex_bf(ex_land(acc[a][c])), scale));
+    __syncthreads();
+    const int cnt = t_end - t_begin;
+    for (int i = tid; i < H * (E1_TB / 8); i += E1_THREADS) {
+        const int h = i / (E1_TB / 8), j = 8 * (i % (E1_TB / 8));
+        uint16_t* dst = s_out + ((size_t)b * H + h) * s_pitch + t_begin + j;
+        const uint16_t* src = S + h * E1_TB + j;
+        if (j + 8 <= cnt) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        } else {
+            for (int e = 0; j + e < cnt; ++e) dst[e] = src[e];
         }
     }
 }
@@ -253,15 +298,19 @@ __global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* _
 }
 
 // ---- E3: latent sum --------------------------------------------------------------------------
-constexpr int E3_THREADS = 256;          // (16 groups of 4 dims) x (16 groups of 6 heads)
+constexpr int E3_THREADS = 128;          // (8 groups of 8 dims) x (16 groups of 6 heads)
 constexpr int E3_DIMS = 64;              // latent dims per CTA
 constexpr int E3_PP = 100;               // ps row pitch (floats): 8-byte aligned 6-head groups
 constexpr int E3_SMEM = PAGE * E3_DIMS * 4 + PAGE * E3_PP * 4;  // c slice [64][64] f32 + p [64][100] f32
+constexpr int E3_CV = PAGE * E3_DIMS / 8 / E3_THREADS;           // 16-byte c pieces per thread and page (4)
+constexpr int E3_PV = H * PAGE / 8 / E3_THREADS;                 // 16-byte p pieces per thread and page (6)
+static_assert(E3_CV * 8 * E3_THREADS == PAGE * E3_DIMS && E3_PV * 8 * E3_THREADS == H * PAGE, "staging split");
 
-// grid (B, 512 / 64); o_lat[h][b][j] = bf16(sum_{t ascending} p_t c_t[j]).  Thread (warp w, lane l),
-// i = 32 w + l: dims 4 (i % 16) .. + 3 of the block and heads 6 (i / 16) .. + 5, each of its 24 sums one
-// sequential loop over t ascending (fused multiply-add of two bf16 values: the product is exact).
-__global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
+// grid (B, 512 / 64); o_lat[h][b][j] = bf16(sum_{t ascending} p_t c_t[j]).  Thread i: dims 8 (i % 8) ..
+// + 7 of the block and heads 6 (i / 8) .. + 5, each of its 48 sums one sequential loop over t ascending
+// (fused multiply-add of two bf16 values: the product is exact).  A page's c slice and probabilities
+// are staged in shared memory as f32; the next page's are loaded into registers while this one is used.
+__global__ void __launch_bounds__(E3_THREADS, 4) ex_latent_kernel(
     const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer, const int32_t* __restrict__ table,
     int max_pages, const int32_t* __restrict__ ctx_len, int B, int max_ctx, const uint16_t* __restrict__ p,
     int s_pitch, uint16_t* __restrict__ olat)
@@ -273,58 +322,87 @@ __global__ void __launch_bounds__(E3_THREADS) ex_latent_kernel(
     float* ps = ex_f + PAGE * E3_DIMS;  // [64 tokens][E3_PP] (heads 0..95)
     const int b = blockIdx.x, jb = blockIdx.y * E3_DIMS;
     const int n = ex_ctx(ctx_len, b, max_ctx, max_pages);
-    const int dg = threadIdx.x & 15, hg = 6 * (threadIdx.x >> 4);
-    float acc[6][4];
+    const int tid = (int)threadIdx.x;
+    const int dg = tid & 7, hg = 6 * (tid >> 3);
+    const uint16_t* prow = p + (size_t)b * H * s_pitch;
+    uint4 cv[E3_CV], pv[E3_PV];
+    // c piece m: token (tid + 128 m) / 8, dims 8 ((tid + 128 m) % 8); p piece m: head (tid + 128 m) % 96,
+    // tokens 8 ((tid + 128 m) / 96) .. + 7 (a warp's lanes take 32 heads of one token group)
+    auto load = [&](int t0) {
+        const int cnt = min(PAGE, n - t0);
+#pragma unroll
+        for (int m = 0; m < E3_CV; ++m) {
+            const int i = tid + E3_THREADS * m, r = i >> 3, u = i & 7;
+            const uint16_t* row = r < cnt ? ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t0 + r, nullptr)
+                                          : nullptr;
+            cv[m] = row ? *reinterpret_cast<const uint4*>(row + jb + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int m = 0; m < E3_PV; ++m) {
+            const int i = tid + E3_THREADS * m, h = i % H, r0 = 8 * (i / H);
+            if (r0 + 8 <= cnt) {
+                pv[m] = *reinterpret_cast<const uint4*>(prow + (size_t)h * s_pitch + t0 + r0);
+            } else {  // the last, partial group of the context: zeros past it
+                uint16_t e[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) e[k] = r0 + k < cnt ? prow[(size_t)h * s_pitch + t0 + r0 + k] : (uint16_t)0;
+                pv[m] = make_uint4((uint32_t)e[0] | ((uint32_t)e[1] << 16), (uint32_t)e[2] | ((uint32_t)e[3] << 16),
+                                   (uint32_t)e[4] | ((uint32_t)e[5] << 16), (uint32_t)e[6] | ((uint32_t)e[7] << 16));
+            }
+        }
+    };
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+    float acc[6][8];
 #pragma unroll
     for (int u = 0; u < 6; ++u)
 #pragma unroll
-        for (int d = 0; d < 4; ++d) acc[u][d] = 0.f;
+        for (int d = 0; d < 8; ++d) acc[u][d] = 0.f;
+    if (n > 0) load(0);
     for (int t0 = 0; t0 < n; t0 += PAGE) {
         const int cnt = min(PAGE, n - t0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < PAGE * (E3_DIMS / 8); i += E3_THREADS) {  // 16 bytes = 8 dims each
-            const int r = i >> 3, u = i & 7;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < cnt) {
-                const uint16_t* row = ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t0 + r, nullptr);
-                if (row) v = *reinterpret_cast<const uint4*>(row + jb + 8 * u);
-            }
+        __syncthreads();  // the previous page is no longer read
+#pragma unroll
+        for (int m = 0; m < E3_CV; ++m) {
+            const int i = tid + E3_THREADS * m, r = i >> 3, u = i & 7;
             float4* dst = reinterpret_cast<float4*>(cs + r * E3_DIMS + 8 * u);
-            dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
-                                 __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-            dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
-                                 __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+            dst[0] = make_float4(lo(cv[m].x), hi(cv[m].x), lo(cv[m].y), hi(cv[m].y));
+            dst[1] = make_float4(lo(cv[m].z), hi(cv[m].z), lo(cv[m].w), hi(cv[m].w));
         }
-        for (int i = threadIdx.x; i < H * (PAGE / 8); i += E3_THREADS) {  // 8 tokens of one head each
-            const int h = i >> 3, r0 = 8 * (i & 7);
-            const uint16_t* src = p + ((size_t)b * H + h) * s_pitch + t0 + r0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ps[(r0 + e) * E3_PP + h] = (r0 + e < cnt) ? ex_bf(src[e]) : 0.f;
+        for (int m = 0; m < E3_PV; ++m) {
+            const int i = tid + E3_THREADS * m, h = i % H, r0 = 8 * (i / H);
+            const uint32_t w[4] = {pv[m].x, pv[m].y, pv[m].z, pv[m].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                ps[(r0 + 2 * k) * E3_PP + h] = lo(w[k]);
+                ps[(r0 + 2 * k + 1) * E3_PP + h] = hi(w[k]);
+            }
         }
         __syncthreads();
+        if (t0 + PAGE < n) load(t0 + PAGE);  // in flight while this page is used
+#pragma unroll 2
         for (int r = 0; r < cnt; ++r) {
-            const float4 c = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 4 * dg);
+            const float4 c0 = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 8 * dg);
+            const float4 c1 = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 8 * dg + 4);
             const float2* pr = reinterpret_cast<const float2*>(ps + r * E3_PP + hg);
+            const float2 p0 = pr[0], p1 = pr[1], p2 = pr[2];
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const float pp[6] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y};
 #pragma unroll
-            for (int q2 = 0; q2 < 3; ++q2) {
-                const float2 pv = pr[q2];
-                const float pp[2] = {pv.x, pv.y};
+            for (int u = 0; u < 6; ++u)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float* a = acc[2 * q2 + e];
-                    a[0] = __fmaf_rn(pp[e], c.x, a[0]);
-                    a[1] = __fmaf_rn(pp[e], c.y, a[1]);
-                    a[2] = __fmaf_rn(pp[e], c.z, a[2]);
-                    a[3] = __fmaf_rn(pp[e], c.w, a[3]);
-                }
-            }
+                for (int d = 0; d < 8; ++d) acc[u][d] = __fmaf_rn(pp[u], c[d], acc[u][d]);
         }
     }
 #pragma unroll
     for (int u = 0; u < 6; ++u) {
-        const uint32_t lo = (uint32_t)ex_land(acc[u][0]) | ((uint32_t)ex_land(acc[u][1]) << 16);
-        const uint32_t hi = (uint32_t)ex_land(acc[u][2]) | ((uint32_t)ex_land(acc[u][3]) << 16);
-        *reinterpret_cast<uint2*>(olat + ((size_t)(hg + u) * B + b) * LORA + jb + 4 * dg) = make_uint2(lo, hi);
+        uint4 o;
+        o.x = (uint32_t)ex_land(acc[u][0]) | ((uint32_t)ex_land(acc[u][1]) << 16);
+        o.y = (uint32_t)ex_land(acc[u][2]) | ((uint32_t)ex_land(acc[u][3]) << 16);
+        o.z = (uint32_t)ex_land(acc[u][4]) | ((uint32_t)ex_land(acc[u][5]) << 16);
+        o.w = (uint32_t)ex_land(acc[u][6]) | ((uint32_t)ex_land(acc[u][7]) << 16);
+        *reinterpret_cast<uint4*>(olat + ((size_t)(hg + u) * B + b) * LORA + jb + 8 * dg) = o;
     }
 }
 
@@ -404,7 +482,7 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
         set_error("k3mla_decode_exact: workspace %zu < %zu bytes", ws_bytes, need);
         return K3MLA_E_WORKSPACE;
     }
-    const int nchunk = (max_ctx + E1_PAGES * PAGE - 1) / (E1_PAGES * PAGE);
+    const int nchunk = (max_ctx + E1_TB - 1) / E1_TB;
     if ((size_t)max_ctx * 4 > (size_t)E2_MAX_SMEM) {
         set_error("k3mla_decode_exact: max_ctx above %d", E2_MAX_SMEM / 4);
         return K3MLA_E_INVALID;
