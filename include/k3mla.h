@@ -452,6 +452,15 @@ int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* slab, int n
                               void* workspace, size_t ws_bytes, int B, int max_ctx, int split_tokens,
                               int withhold_page, uint32_t wait_us, int32_t* dev_err, void* stream);
 
+/* ---- diagnostic: the exact-chain mode's exponential ------------------------------
+ * y[i] = the f32 nearest to e^(x[i]) as the exact-chain mode computes it (the double
+ * exponential rounded once to f32 -- the chain's definition of e_t -- evaluated first in
+ * f32 pairs, the double exponential deciding where the pair is too close to a rounding
+ * boundary); fast[i] (optional, may be NULL) = 1 where the f32 pair decided, else 0.
+ * x, y, fast: device arrays of n elements, 4-byte aligned.  One kernel on `stream`.
+ * Returns K3MLA_E_INVALID for n < 0 or a null / misaligned x or y; n == 0 does nothing. */
+int k3mla_diag_exact_exp(const float* x, float* y, int32_t* fast, int n, void* stream);
+
 /* ---- diagnostic --------------------------------------------------------------
  * Runs the decode kernel's two tensor-core contractions on one 64-token page in
  * isolation so that their operand layouts can be checked against a plain matrix

@@ -182,15 +182,23 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
         if (kc + 1 < E1_NKC) load(kc + 1);  // in flight while chunk kc is used
         const float* Rs = ex_sf + (kc & 1) * E1_BUF;
         const float* Qs = Rs + E1_KC * E1_RP;
+        // operands of step k + 1 are loaded while step k's 48 fmas run (shared-memory latency)
+        float4 r0 = *reinterpret_cast<const float4*>(Rs + 8 * tg);
+        float4 r1 = *reinterpret_cast<const float4*>(Rs + 8 * tg + 4);
+        float2 qa = *reinterpret_cast<const float2*>(Qs + 6 * hg);
+        float2 qb = *reinterpret_cast<const float2*>(Qs + 6 * hg + 2);
+        float2 qc = *reinterpret_cast<const float2*>(Qs + 6 * hg + 4);
 #pragma unroll 4
         for (int k = 0; k < E1_KC; ++k) {
-            const float4 r0 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg);
-            const float4 r1 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg + 4);
-            const float2 qa = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg);
-            const float2 qb = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg + 2);
-            const float2 qc = *reinterpret_cast<const float2*>(Qs + k * H + 6 * hg + 4);
             const float r[E1_TT] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
             const float q[E1_HT] = {qa.x, qa.y, qb.x, qb.y, qc.x, qc.y};
+            if (k + 1 < E1_KC) {
+                r0 = *reinterpret_cast<const float4*>(Rs + (k + 1) * E1_RP + 8 * tg);
+                r1 = *reinterpret_cast<const float4*>(Rs + (k + 1) * E1_RP + 8 * tg + 4);
+                qa = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg);
+                qb = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg + 2);
+                qc = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg + 4);
+            }
 #pragma unroll
             for (int a = 0; a < E1_TT; ++a)
 #pragma unroll
@@ -221,6 +229,92 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     }
 }
 
+// ---- the chain's exp: f32 of the exact exponential --------------------------------------------
+// The chain takes e_t as the double exponential rounded once to f32, which is the f32 nearest to
+// e^x unless e^x lies within a double rounding error of a point halfway between two f32 values.
+// FP64 runs at a small fraction of the FP32 rate here, so the exp is first evaluated in f32 pairs
+// (an unevaluated sum hi + lo; Knuth's and Dekker's error-free sums, the exact product from the fused
+// multiply-add), by table-driven argument reduction (Tang, 1989) with a Cody-Waite split constant:
+//   x = k ln2 / 32 + r, |r| <= ln2 / 64, with ln2 / 32 split as L1 + L2 + L3 (L1, L2 short enough that
+//   k L1 and k L2 are exact for |k| < 2^12, so x - k L1 is exact);
+//   e^r = 1 + r + r^2 / 2 + tail, tail = r^3 / 6 + r^4 / 24 + r^5 / 120 in plain f32 (|tail| < 2.2e-7;
+//   the truncation r^6 / 720 < 2^-48);
+//   e^x = 2^(k >> 5) * 2^((k & 31) / 32) * e^r, the 32 values 2^(j/32) as f32 pairs (X_TH, X_TL, each
+//   the f32 nearest to 2^(j/32) and to the remainder).
+// The pair's error is below 2^-43 of e^x over the whole range used (measured over every f32 in
+// [-87, 0] against a long-double reference).  When the pair lies farther than 2^-40 e^x from every
+// rounding boundary of the f32 grid, its rounding is the rounding of e^x, and is returned; otherwise
+// (a few in 10^5 arguments), and for x outside [-87, 0], the double exponential decides.
+__device__ __constant__ float X_TH[32] = {
+    0x1.000000p+0f, 0x1.059b0ep+0f, 0x1.0b5586p+0f, 0x1.11301ep+0f, 0x1.172b84p+0f, 0x1.1d4874p+0f, 0x1.2387a6p+0f,
+    0x1.29e9e0p+0f, 0x1.306fe0p+0f, 0x1.371a74p+0f, 0x1.3dea64p+0f, 0x1.44e086p+0f, 0x1.4bfdaep+0f, 0x1.5342b6p+0f,
+    0x1.5ab07ep+0f, 0x1.6247ecp+0f, 0x1.6a09e6p+0f, 0x1.71f75ep+0f, 0x1.7a1148p+0f, 0x1.82589ap+0f, 0x1.8ace54p+0f,
+    0x1.93737cp+0f, 0x1.9c4918p+0f, 0x1.a5503cp+0f, 0x1.ae89fap+0f, 0x1.b7f770p+0f, 0x1.c199bep+0f, 0x1.cb720ep+0f,
+    0x1.d5818ep+0f, 0x1.dfc974p+0f, 0x1.ea4afap+0f, 0x1.f50766p+0f};
+__device__ __constant__ float X_TL[32] = {
+    0.0f, -0x1.9d4f52p-25f, 0x1.9f3122p-25f, -0x1.fdb496p-25f, -0x1.c15742p-27f, -0x1.d2e8cap-25f, 0x1.ceac48p-25f,
+    -0x1.5c0424p-25f, 0x1.4636e2p-25f, -0x1.18aac6p-25f, 0x1.824684p-25f, 0x1.8624b4p-30f, -0x1.593abcp-25f,
+    -0x1.2c5610p-25f, -0x1.5bd5ecp-27f, -0x1.f8b550p-25f, 0x1.9fcef4p-26f, 0x1.1d8beep-25f, -0x1.829fd0p-25f,
+    -0x1.accc7cp-26f, 0x1.15506ep-27f, -0x1.e64744p-25f, 0x1.51f848p-27f, -0x1.b83b54p-25f, -0x1.a94b14p-26f,
+    -0x1.a09438p-25f, -0x1.3d56b2p-27f, -0x1.8837ccp-27f, -0x1.822dbcp-27f, -0x1.908c94p-25f, 0x1.52486cp-27f,
+    -0x1.246eb0p-26f};
+
+// Error-free transformations: a + b = s + e exactly (any order of magnitude; Knuth), and the same when
+// |a| >= |b| (Dekker).
+__device__ __forceinline__ void x_two_sum(float a, float b, float& s, float& e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void x_fast_two_sum(float a, float b, float& s, float& e)
+{
+    s = __fadd_rn(a, b);
+    e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// f32 of e^x as the chain defines it; `tl` / `th`: the 2^(j/32) pairs (shared or constant memory).
+// *fast (optional) tells whether the f32 pair decided.
+__device__ __forceinline__ float ex_exp(float x, const float* th, const float* tl, bool* fast = nullptr)
+{
+    if (x >= -87.0f && x <= 0.0f) {
+        const float kf = rintf(__fmul_rn(x, 0x1.715476p+5f));  // 32 / ln2
+        const int k = (int)kf;
+        const float rhi = __fsub_rn(x, __fmul_rn(kf, 0x1.62ep-6f));  // exact
+        float rh, rl;
+        x_two_sum(rhi, -__fmul_rn(kf, 0x1.0cp-20f), rh, rl);
+        rl = __fmaf_rn(-kf, -0x1.05c61p-34f, rl);
+        x_fast_two_sum(rh, rl, rh, rl);  // |rl| <= ulp(rh) / 2
+        const float a = __fmul_rn(rh, rh);
+        const float ae = __fmaf_rn(rh, rh, -a);  // rh^2 = a + ae
+        float t = __fmaf_rn(rh, 1.0f / 120.0f, 1.0f / 24.0f);
+        t = __fmaf_rn(rh, t, 1.0f / 6.0f);
+        const float tail = __fmul_rn(__fmul_rn(a, rh), t);
+        float s, se, s2, se2;
+        x_two_sum(1.0f, rh, s, se);
+        x_two_sum(s, __fmul_rn(0.5f, a), s2, se2);
+        const float lo = __fadd_rn(
+            __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(se, se2), __fmul_rn(0.5f, ae)), tail), rl), __fmul_rn(rh, rl));
+        float eh, el;
+        x_fast_two_sum(s2, lo, eh, el);
+        const int j = k & 31, m = k >> 5;
+        const float ph = __fmul_rn(eh, th[j]);
+        const float pe = __fmaf_rn(eh, th[j], -ph);
+        const float q = __fadd_rn(__fadd_rn(pe, __fmul_rn(eh, tl[j])), __fmul_rn(el, th[j]));
+        float yh, yl;
+        x_fast_two_sum(ph, q, yh, yl);
+        const uint32_t bits = __float_as_uint(yh);
+        const float ulp = __uint_as_float((((bits >> 23) & 0xFFu) - 23u) << 23);
+        const float h = (yl < 0.0f && (bits & 0x7FFFFFu) == 0u) ? 0.25f * ulp : 0.5f * ulp;
+        if (__fadd_rn(fabsf(yl), __fmul_rn(0x1p-40f, yh)) < h) {
+            if (fast) *fast = true;
+            return __fmul_rn(yh, __uint_as_float((uint32_t)(m + 127) << 23));  // exact: a normal f32
+        }
+    }
+    if (fast) *fast = false;
+    return (float)exp((double)x);
+}
+
 // ---- E2: softmax -----------------------------------------------------------------------------
 // grid (B * 96); block E2_THREADS; dynamic smem: e_t for the row (max_ctx f32).  The max, the exps
 // and the landings are independent per token and run across the block; the sum of exp is thread
@@ -236,6 +330,11 @@ __global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* _
     griddep_launch_dependents();
     extern __shared__ float ex_e[];
     __shared__ float red_f[E2_THREADS / 32];
+    __shared__ float x_th[32], x_tl[32];  // indexed per thread: shared, not constant, memory
+    if (threadIdx.x < 32) {
+        x_th[threadIdx.x] = X_TH[threadIdx.x];
+        x_tl[threadIdx.x] = X_TL[threadIdx.x];
+    }
     __shared__ int red_i[E2_THREADS / 32];
     __shared__ float l_sh;
     const int i = blockIdx.x, b = i / H;
@@ -253,7 +352,7 @@ __global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* _
     __syncthreads();
     m = red_f[0];
     for (int w = 1; w < E2_THREADS / 32; ++w) m = fmaxf(m, red_f[w]);
-    for (int t = threadIdx.x; t < n; t += E2_THREADS) ex_e[t] = (float)exp((double)__fsub_rn(ex_bf(row[t]), m));
+    for (int t = threadIdx.x; t < n; t += E2_THREADS) ex_e[t] = ex_exp(__fsub_rn(ex_bf(row[t]), m), x_th, x_tl);
     __syncthreads();
     if (threadIdx.x == 0) {  // l = sum of e_t over t ascending, one rounding per addition
         float l = 0.f;
@@ -295,6 +394,17 @@ __global__ void __launch_bounds__(E2_THREADS) ex_softmax_kernel(const int32_t* _
             }
         if (argmax) argmax[i] = bt;
     }
+}
+
+// Diagnostic: the chain's exp on n arguments; fast[i] = 1 where the f32 pair decided.
+__global__ void ex_exp_diag_kernel(const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ fast,
+                                   int n)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    bool f = false;
+    y[i] = ex_exp(x[i], X_TH, X_TL, &f);
+    if (fast) fast[i] = f ? 1 : 0;
 }
 
 // ---- E3: latent sum --------------------------------------------------------------------------
@@ -381,14 +491,23 @@ __global__ void __launch_bounds__(E3_THREADS, 4) ex_latent_kernel(
         }
         __syncthreads();
         if (t0 + PAGE < n) load(t0 + PAGE);  // in flight while this page is used
+        // operands of token r + 1 are loaded while token r's 48 fmas run (shared-memory latency); the
+        // staged rows past cnt are zeros, so the load one past the last token stays in the tile
+        float4 c0 = *reinterpret_cast<const float4*>(cs + 8 * dg);
+        float4 c1 = *reinterpret_cast<const float4*>(cs + 8 * dg + 4);
+        float2 p0 = *reinterpret_cast<const float2*>(ps + hg);
+        float2 p1 = *reinterpret_cast<const float2*>(ps + hg + 2);
+        float2 p2 = *reinterpret_cast<const float2*>(ps + hg + 4);
 #pragma unroll 2
         for (int r = 0; r < cnt; ++r) {
-            const float4 c0 = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 8 * dg);
-            const float4 c1 = *reinterpret_cast<const float4*>(cs + r * E3_DIMS + 8 * dg + 4);
-            const float2* pr = reinterpret_cast<const float2*>(ps + r * E3_PP + hg);
-            const float2 p0 = pr[0], p1 = pr[1], p2 = pr[2];
             const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             const float pp[6] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y};
+            const int rn = r + 1 < PAGE ? r + 1 : r;
+            c0 = *reinterpret_cast<const float4*>(cs + rn * E3_DIMS + 8 * dg);
+            c1 = *reinterpret_cast<const float4*>(cs + rn * E3_DIMS + 8 * dg + 4);
+            p0 = *reinterpret_cast<const float2*>(ps + rn * E3_PP + hg);
+            p1 = *reinterpret_cast<const float2*>(ps + rn * E3_PP + hg + 2);
+            p2 = *reinterpret_cast<const float2*>(ps + rn * E3_PP + hg + 4);
 #pragma unroll
             for (int u = 0; u < 6; ++u)
 #pragma unroll
@@ -525,4 +644,16 @@ extern "C" int k3mla_decode_exact(const uint16_t* q, const uint16_t* slab, int n
     if (rc) return rc;
     return launch_pdl(ex_expand_kernel, dim3(H, (B + E4_SLOTS - 1) / E4_SLOTS), dim3(VH), (size_t)E4_SMEM, st,
                       "ex_expand_kernel", olat, B, w_kv_b, out);
+}
+
+extern "C" int k3mla_diag_exact_exp(const float* x, float* y, int32_t* fast, int n, void* stream)
+{
+    if (n < 0 || (n > 0 && (!x || !y || !aligned(x, 4) || !aligned(y, 4)))) {
+        set_error("k3mla_diag_exact_exp: invalid arguments");
+        return K3MLA_E_INVALID;
+    }
+    if (n == 0) return K3MLA_OK;
+    if (!device_ok()) return K3MLA_E_DEVICE;
+    return launch_pdl(ex_exp_diag_kernel, dim3((n + 255) / 256), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                      "ex_exp_diag_kernel", x, y, fast, n);
 }

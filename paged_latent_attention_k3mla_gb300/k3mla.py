@@ -30,7 +30,7 @@ EXPORTS = (
     "k3mla_copy_pages", "k3mla_append_latent_rows", "k3mla_chunk_views", "k3mla_decode_exact",
     "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_batch_planned_split_tokens",
     "k3mla_decode_layer_workspace_bytes", "k3mla_decode_layer", "k3mla_diag_decode_timeout",
-    "k3mla_expanded_cache_bytes", "k3mla_expand_latent_cache", "k3mla_expanded_decode",
+    "k3mla_expanded_cache_bytes", "k3mla_expand_latent_cache", "k3mla_expanded_decode", "k3mla_diag_exact_exp",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -75,6 +75,7 @@ def load(build_if_needed: bool = True):
             "k3mla_expanded_cache_bytes": ([I], SZ),
             "k3mla_expand_latent_cache": ([P, I, I, I, P, P, P, P], I),
             "k3mla_expanded_decode": ([P, P, I, P, I, P, ctypes.c_uint16, P, I, I, P, P], I),
+            "k3mla_diag_exact_exp": ([P, P, P, I, P], I),
             "k3mla_diag_decode_timeout": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, P, SZ, I, I, I, I,
                                            ctypes.c_uint32, P, P], I),
             "k3mla_paged_decode_noalloc": ([P, P, I, I, I, P, I, P, P, ctypes.c_uint16, P, P, I, I, I, P, P], I),
@@ -395,6 +396,16 @@ def diag_decode_timeout(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, blo
         _dev(out, torch.bfloat16, (B, H, V), "out"), None, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
         B, int(max_ctx), int(split_tokens), int(withhold_page), ctypes.c_uint32(wait_us),
         _dev(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_diag_decode_timeout")
+
+
+def diag_exact_exp(x: torch.Tensor, y: torch.Tensor, fast: torch.Tensor | None = None, stream=None) -> None:
+    """Diagnostic: the exact-chain mode's exponential of every element of x (f32) into y; fast[i] = 1
+    where the f32 evaluation decided; see k3mla_diag_exact_exp."""
+    n = x.numel()
+    lib = load()
+    _check(lib.k3mla_diag_exact_exp(_dev(x, torch.float32, (n,), "x"), _dev(y, torch.float32, (n,), "y"),
+                                    _opt(fast, torch.int32, (n,), "fast"), n, _stream(stream)),
+           "k3mla_diag_exact_exp")
 
 
 def diag_umma(mode: int, a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, stream=None) -> None:

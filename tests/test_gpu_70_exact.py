@@ -88,3 +88,37 @@ def test_exact_full_size_sampled(gpu_lib):
     _bitwise(g, oracle_layer(wl, 0, slots=[0, 63]), slots=[0, 63])
     del wl
     torch.cuda.empty_cache()
+
+
+def test_the_chains_exp_equals_the_double_exponential_rounded_to_f32(gpu_lib):
+    # The mode's e_t = f32 of the double exponential (the chain's definition), evaluated first in f32
+    # pairs: wherever the pair decided, the result must be the f32 nearest to e^x, the same bits as
+    # numpy's double exp rounded once; where it handed over to the double exp (arguments whose e^x lies
+    # close to an f32 rounding boundary, or outside [-87, 0]), the two double exponentials may differ by
+    # one f32 unit at most.  Arguments: 4M uniform in [-90, 0.5], every landed score difference s - m of
+    # two bf16 values in [-16, 16] against m in a few rows' maxima, and edge values.
+    g = np.random.default_rng(701)
+    xs = [g.uniform(-90.0, 0.5, size=4 << 20).astype(np.float32)]
+    b = np.arange(0, 1 << 16, dtype=np.uint32)
+    bf = (b << 16).view(np.float32)
+    bf = bf[np.isfinite(bf) & (np.abs(bf) <= 16.0)]
+    for m in (np.float32(0.0), np.float32(3.1875), np.float32(7.5), np.float32(15.875)):
+        d = (bf[bf <= m] - m).astype(np.float32)
+        xs.append(d)
+    xs.append(np.array([0.0, -0.0, -1e-30, -1.4e-45, -87.0, -87.00001, -86.99999, -88.7, -103.9, -104.0, 1.0,
+                        -0.5, -0.34657359, -0.01083, 0.01083], np.float32))
+    x = np.concatenate(xs)
+    xt = torch.from_numpy(x).cuda()
+    y = torch.empty_like(xt)
+    fast = torch.empty(x.size, dtype=torch.int32, device="cuda")
+    k3mla.diag_exact_exp(xt, y, fast)
+    torch.cuda.synchronize()
+    y, fast = y.cpu().numpy(), fast.cpu().numpy().astype(bool)
+    with np.errstate(over="ignore", under="ignore"):
+        ref = np.exp(x.astype(np.float64)).astype(np.float32)
+    yb, rb = y.view(np.uint32).astype(np.int64), ref.view(np.uint32).astype(np.int64)
+    assert np.array_equal(yb[fast], rb[fast]), f"{int((yb[fast] != rb[fast]).sum())} fast-path results differ"
+    assert np.all(np.abs(yb[~fast] - rb[~fast]) <= 1)
+    inside = (x >= -87.0) & (x <= 0.0)
+    assert fast[inside].mean() > 0.999, fast[inside].mean()          # the double exp is the exception
+    assert not fast[~inside].any()
