@@ -16,7 +16,7 @@
 // Fixed orders rule out the tensor cores, so these are CUDA-core kernels:
 //   E0 absorption   thread per (slot, head, j): sum over d = 0..127
 //   E1 scores       CTA per (slot, 128 tokens): Q and the rows staged in shared
-//                   memory by 32-dim chunks; thread per (8 tokens, 6 heads): sums
+//                   memory by 32-dim chunks; thread per (8 tokens, 8 heads): sums
 //                   over k = 0..575
 //   E2 softmax      CTA per (slot, head): max and exps across the block, the sum
 //                   of exp thread 0's loop over t ascending, p_t = bf16(e_t / l),
@@ -93,20 +93,21 @@ __global__ void __launch_bounds__(LORA) ex_absorb_kernel(const uint16_t* __restr
 constexpr int E1_TB = 2 * PAGE;          // tokens per CTA
 constexpr int E1_KC = 32;                // dims per staged chunk (576 = 18 chunks)
 constexpr int E1_NKC = ROW / E1_KC;
-constexpr int E1_THREADS = 256;          // 16 token groups x 16 head groups
-constexpr int E1_TT = 8, E1_HT = 6;      // register tile of one thread: 8 tokens x 6 heads
+constexpr int E1_TT = 8, E1_HT = 8;      // register tile of one thread: 8 tokens x 8 heads
+constexpr int E1_THREADS = (E1_TB / E1_TT) * (H / E1_HT);  // 16 token groups x 12 head groups = 192
 constexpr int E1_RP = E1_TB + 4;         // Rs row pitch (floats): 16-byte rows, rows 4 banks apart
 constexpr int E1_BUF = E1_KC * (E1_RP + H);  // one stage: Rs [KC][RP] + Qs [KC][96], f32
 constexpr int E1_SMEM = 2 * E1_BUF * 4;
-static_assert(E1_TB * E1_KC == 2 * 8 * E1_THREADS, "R staging: two 8-dim pieces per thread");
-static_assert(H * E1_KC <= 2 * 8 * E1_THREADS && H * E1_KC > 8 * E1_THREADS, "Q staging: one or two pieces per thread");
+constexpr int E1_RPIECES = E1_TB * E1_KC / 8;  // 512 pieces of 8 dims of a row per chunk
+constexpr int E1_QPIECES = H * E1_KC / 8;      // 384 pieces of 8 dims of Q per chunk
+static_assert(E1_THREADS == 192 && E1_QPIECES == 2 * E1_THREADS && E1_RPIECES <= 3 * E1_THREADS, "staging split");
 static_assert(H * E1_TB * 2 <= E1_SMEM, "the bf16 score tile fits in the staging buffers");
 
-// grid (B, ceil(max_ctx / 128)); block 256.  s[b][h][t] = bf16(bf16(dot) * scale).  Q and the 128
+// grid (B, ceil(max_ctx / 128)); block 192.  s[b][h][t] = bf16(bf16(dot) * scale).  Q and the 128
 // tokens' rows are staged in chunks of 32 dims as f32, transposed ([k][token], [k][head]) and
 // double-buffered (the next chunk's loads are in flight while this one is used).  Thread (warp w,
-// lane l): tokens 8 tg .. 8 tg + 7 with tg = 8 (w & 1) + (l & 7), heads 6 hg .. 6 hg + 5 with hg =
-// 4 (w >> 1) + (l >> 3); each of its 48 dots is one sequential sum over k = 0..575 ascending (a fused
+// lane l): tokens 8 tg .. 8 tg + 7 with tg = 8 (w & 1) + (l & 7), heads 8 hg .. 8 hg + 7 with hg =
+// 4 (w >> 1) + (l >> 3); each of its 64 dots is one sequential sum over k = 0..575 ascending (a fused
 // multiply-add of two bf16 values rounds as the chain's multiply-then-add: the product is exact).
 __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     const uint16_t* __restrict__ q_abs, const uint16_t* __restrict__ slab, int n_pages, int n_layers, int layer,
@@ -123,49 +124,55 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     const int t_end = min(n, t_begin + E1_TB);
     const int tid = (int)threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tg = 8 * (warp & 1) + (lane & 7), hg = 4 * (warp >> 1) + (lane >> 3);
-    // staging roles: token st (dims 16 sp .. 16 sp + 15 of each chunk); Q pieces i = tid, tid + 256
-    const int st = tid & (E1_TB - 1), sp = tid >> 7;
-    const uint16_t* srow = (t_begin + st < t_end)
-                               ? ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t_begin + st, dev_err)
-                               : nullptr;
+    // staging roles: row piece i = tid + 192 e (e < 3, i < 512): token i % 128, dims 8 (i / 128) .. + 7;
+    // Q piece i = tid + 192 e (e < 2): head i / 4, dims 8 (i % 4) .. + 7
+    const uint16_t* srow[3];
+#pragma unroll
+    for (int e = 0; e < 3; ++e) {
+        const int i = tid + E1_THREADS * e, t = t_begin + (i & (E1_TB - 1));
+        srow[e] = (i < E1_RPIECES && t < t_end) ? ex_row(slab, n_pages, n_layers, layer, table, max_pages, b, t, dev_err)
+                                                : nullptr;
+    }
     const uint16_t* qrow = q_abs + (size_t)b * H * ROW;
-    const bool q2 = tid + E1_THREADS < H * E1_KC / 8;
-    uint4 rv[2], qv[2];
+    uint4 rv[3], qv[2];
     auto load = [&](int kc) {
         const int k0 = kc * E1_KC;
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-            rv[e] = srow ? *reinterpret_cast<const uint4*>(srow + k0 + 16 * sp + 8 * e) : make_uint4(0u, 0u, 0u, 0u);
+        for (int e = 0; e < 3; ++e) {
+            const int i = tid + E1_THREADS * e;
+            rv[e] = srow[e] ? *reinterpret_cast<const uint4*>(srow[e] + k0 + 8 * (i >> 7)) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int i = tid + E1_THREADS * e;
-            if (e == 0 || q2)
-                qv[e] = *reinterpret_cast<const uint4*>(qrow + (size_t)(i >> 2) * ROW + k0 + 8 * (i & 3));
+            qv[e] = *reinterpret_cast<const uint4*>(qrow + (size_t)(i >> 2) * ROW + k0 + 8 * (i & 3));
         }
     };
     auto store = [&](int buf) {
         float* Rs = ex_sf + buf * E1_BUF;
         float* Qs = Rs + E1_KC * E1_RP;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const uint32_t w[4] = {rv[e].x, rv[e].y, rv[e].z, rv[e].w};
+        for (int e = 0; e < 3; ++e) {
+            const int i = tid + E1_THREADS * e;
+            if (i < E1_RPIECES) {
+                const uint32_t w[4] = {rv[e].x, rv[e].y, rv[e].z, rv[e].w};
+                const int t = i & (E1_TB - 1), kb = 8 * (i >> 7);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                Rs[(16 * sp + 8 * e + 2 * u) * E1_RP + st] = __uint_as_float(w[u] << 16);
-                Rs[(16 * sp + 8 * e + 2 * u + 1) * E1_RP + st] = __uint_as_float(w[u] & 0xFFFF0000u);
+                for (int u = 0; u < 4; ++u) {
+                    Rs[(kb + 2 * u) * E1_RP + t] = __uint_as_float(w[u] << 16);
+                    Rs[(kb + 2 * u + 1) * E1_RP + t] = __uint_as_float(w[u] & 0xFFFF0000u);
+                }
             }
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int i = tid + E1_THREADS * e;
-            if (e == 0 || q2) {
-                const uint32_t w[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
-                const int h = i >> 2, kb = 8 * (i & 3);
+            const uint32_t w[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
+            const int h = i >> 2, kb = 8 * (i & 3);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    Qs[(kb + 2 * u) * H + h] = __uint_as_float(w[u] << 16);
-                    Qs[(kb + 2 * u + 1) * H + h] = __uint_as_float(w[u] & 0xFFFF0000u);
-                }
+            for (int u = 0; u < 4; ++u) {
+                Qs[(kb + 2 * u) * H + h] = __uint_as_float(w[u] << 16);
+                Qs[(kb + 2 * u + 1) * H + h] = __uint_as_float(w[u] & 0xFFFF0000u);
             }
         }
     };
@@ -182,23 +189,14 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
         if (kc + 1 < E1_NKC) load(kc + 1);  // in flight while chunk kc is used
         const float* Rs = ex_sf + (kc & 1) * E1_BUF;
         const float* Qs = Rs + E1_KC * E1_RP;
-        // operands of step k + 1 are loaded while step k's 48 fmas run (shared-memory latency)
-        float4 r0 = *reinterpret_cast<const float4*>(Rs + 8 * tg);
-        float4 r1 = *reinterpret_cast<const float4*>(Rs + 8 * tg + 4);
-        float2 qa = *reinterpret_cast<const float2*>(Qs + 6 * hg);
-        float2 qb = *reinterpret_cast<const float2*>(Qs + 6 * hg + 2);
-        float2 qc = *reinterpret_cast<const float2*>(Qs + 6 * hg + 4);
 #pragma unroll 4
         for (int k = 0; k < E1_KC; ++k) {
+            const float4 r0 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg);
+            const float4 r1 = *reinterpret_cast<const float4*>(Rs + k * E1_RP + 8 * tg + 4);
+            const float4 q0 = *reinterpret_cast<const float4*>(Qs + k * H + 8 * hg);
+            const float4 q1 = *reinterpret_cast<const float4*>(Qs + k * H + 8 * hg + 4);
             const float r[E1_TT] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            const float q[E1_HT] = {qa.x, qa.y, qb.x, qb.y, qc.x, qc.y};
-            if (k + 1 < E1_KC) {
-                r0 = *reinterpret_cast<const float4*>(Rs + (k + 1) * E1_RP + 8 * tg);
-                r1 = *reinterpret_cast<const float4*>(Rs + (k + 1) * E1_RP + 8 * tg + 4);
-                qa = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg);
-                qb = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg + 2);
-                qc = *reinterpret_cast<const float2*>(Qs + (k + 1) * H + 6 * hg + 4);
-            }
+            const float q[E1_HT] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
             for (int a = 0; a < E1_TT; ++a)
 #pragma unroll
@@ -214,7 +212,7 @@ __global__ void __launch_bounds__(E1_THREADS) ex_scores_kernel(
     for (int a = 0; a < E1_TT; ++a)
 #pragma unroll
         for (int c = 0; c < E1_HT; ++c)
-            S[(6 * hg + c) * E1_TB + 8 * tg + a] = ex_land(__fmul_rn(ex_bf(ex_land(acc[a][c])), scale));
+            S[(8 * hg + c) * E1_TB + 8 * tg + a] = ex_land(__fmul_rn(ex_bf(ex_land(acc[a][c])), scale));
     __syncthreads();
     const int cnt = t_end - t_begin;
     for (int i = tid; i < H * (E1_TB / 8); i += E1_THREADS) {
