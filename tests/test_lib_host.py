@@ -251,6 +251,14 @@ def test_expanded_baseline_sizes_and_arguments():
     assert b"invalid sizes" in lib.k3mla_last_error()
 
 
+def test_exact_exp_diagnostic_arguments():
+    lib = k3mla.load()
+    assert lib.k3mla_diag_exact_exp(None, None, None, 0, None) == 0     # nothing to do
+    assert lib.k3mla_diag_exact_exp(None, None, None, -1, None) == -1
+    assert lib.k3mla_diag_exact_exp(None, None, None, 5, None) == -1
+    assert b"invalid arguments" in lib.k3mla_last_error()
+
+
 def test_product_and_oracle_share_no_code():
     """The CUDA path and the oracle are independent: no product source imports, includes or names
     the oracle's modules, and no oracle source imports the product package or includes its
