@@ -113,6 +113,18 @@ def test_many_slots_and_several_splits(gpu_lib, case):
         _same_as_the_calls(wl, [0], 9000)
 
 
+def test_splits_with_every_page_unmapped(gpu_lib):
+    # the layer call gives a split whose pages are all -1 its known result without streaming zero rows;
+    # the bits must be those of the full pass: a padding slot of one split, a padding slot of several
+    # splits, a slot whose first split is unmapped and whose second is not, and an ordinary slot
+    wl = synth.make_custom([300, 9000, 5000, 700], seed=452, device="cuda")
+    wl.block_table[0, :] = -1                    # one split, all unmapped (its append is flagged)
+    wl.block_table[1, :] = -1                    # three splits, all unmapped
+    split = int(k3mla.slot_split_tokens(5000, k3mla.SPLIT_AUTO))
+    wl.block_table[2, :split // 64] = -1         # slot 2: its first split unmapped
+    _same_as_the_calls(wl, [0], 9000, expect_err=k3mla.DEV_UNMAPPED)
+
+
 def test_matches_the_oracle(gpu_lib):
     wl = synth.make_workload("ragged16", device="cuda", n_layers=2)
     slab_before = synth.bf16_bits(wl.slab).copy()
