@@ -263,7 +263,10 @@ int k3mla_paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages,
  * As for k3mla_paged_decode, the kernel immediately before this call in `stream`
  * must not write ctx_len (the split kernel reads it when it starts); the first
  * kernel of the call reads q, the rows and the tables only after the kernel ahead
- * of it has completed, and w_kv_b at once. */
+ * of it has completed, and w_kv_b at once.  Within the call the split kernel starts
+ * loading each slot's pages, all but the one the step's row goes into, before the
+ * append has finished: a page that receives a row must not be read by another slot
+ * of the same call (the pool's copy on write keeps a slot's last page its own). */
 size_t k3mla_decode_layer_workspace_bytes(int B, int max_ctx);
 int k3mla_decode_layer(const uint16_t* q, const uint16_t* w_kv_b, uint16_t* slab, int n_pages, int n_layers,
                        int layer, const int32_t* block_table, int max_pages_per_slot, const int32_t* ctx_len,
