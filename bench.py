@@ -606,29 +606,47 @@ def next_rows(wl, table, max_ctx, stream, hbm, tflops, absorbed_call_us):
     r = torch.randn(R, 64, generator=g, device=dev).to(torch.bfloat16)
     q_abs = torch.empty(R, H, ROW, dtype=torch.bfloat16, device=dev)
     split = k3mla.SPLIT_AUTO
-    ws = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(k3mla.decode_workspace_bytes(R, max_ctx, split), dtype=torch.uint8, device=dev)
+    ws = torch.empty(k3mla.chunk_decode_workspace_bytes(nb, R, max_ctx), dtype=torch.uint8, device=dev)
     out = torch.empty(R, H, V, dtype=torch.bfloat16, device=dev)
+    out_v = torch.empty(R, H, V, dtype=torch.bfloat16, device=dev)
 
-    def chunk_layer():
+    def chunk_layer():  # multi-query: up to four token rows of a slot share each page load
+        k3mla.append_latent_rows(wl.slab, 0, tbl, pos0, row_start, c, r, max_rows=T, stream=stream)
+        k3mla.absorb_q(q, wl.w_kv_b[0], q_abs, stream=stream)
+        k3mla.chunk_decode(q_abs, wl.slab, 0, tbl, pos0, row_start, wl.w_kv_b[0], wl.scale_bits, out, ws, max_ctx,
+                           stream=stream)
+
+    def chunk_layer_views():  # one view per token row, each streaming its slot's pages
         k3mla.append_latent_rows(wl.slab, 0, tbl, pos0, row_start, c, r, max_rows=T, stream=stream)
         k3mla.chunk_views(tbl, pos0, row_start, vt, vc, stream=stream)
         k3mla.absorb_q(q, wl.w_kv_b[0], q_abs, stream=stream)
-        k3mla.paged_decode(q_abs, wl.slab, 0, vt, vc, wl.w_kv_b[0], wl.scale_bits, out, ws, max_ctx, split,
+        k3mla.paged_decode(q_abs, wl.slab, 0, vt, vc, wl.w_kv_b[0], wl.scale_bits, out_v, ws_v, max_ctx, split,
                            stream=stream)
 
     ms = _time_ms(chunk_layer, stream)
+    ms_v = _time_ms(chunk_layer_views, stream)
+    torch.cuda.synchronize()
+    # every context here fits one split, so the two forms agree bit for bit
+    same = bool(torch.equal(out.view(torch.int16), out_v.view(torch.int16)))
     # causal attention: token j of a chunk attends over pos0 + j + 1 tokens (scores 576 wide, latent
     # accumulation 512 wide, 96 heads), plus the absorption and the W_UV expansion of every token
     seen = int(sum(int(p0) * T + T * (T + 1) // 2 for p0 in (wl.ctx_len[:nb] - T)))
     flops = seen * H * 2 * (ROW + LORA) + 2 * 2 * R * H * NOPE * LORA
     tf = flops / (ms * 1e-3) / 1e12
     res["chunked_prefill"] = {"slots": nb, "chunk_tokens": T, "context_tokens": int(wl.ctx_len[:nb].max()),
-                              "views": R, "us_per_layer": round(ms * 1e3, 1),
+                              "token_rows": R, "us_per_layer": round(ms * 1e3, 1),
                               "tokens_per_s_per_layer": round(R / (ms * 1e-3), 1),
                               "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tflops,
                                            "unit": "TFLOP/s", "frac": round(tf / tflops, 4)},
-                              "how": "row append + per-token causal views + absorption + paged decode over "
-                                     "the views (each view streams its slot's pages)"}
+                              "how": "row append + absorption + k3mla_chunk_decode (multi-query: up to four "
+                                     "token rows of a slot share each page load, 32 heads of each)",
+                              "views_us_per_layer": round(ms_v * 1e3, 1),
+                              "views_tokens_per_s_per_layer": round(R / (ms_v * 1e-3), 1),
+                              "views_how": "row append + per-token causal views + absorption + paged decode over "
+                                           "the views (each view streams its slot's pages)",
+                              "views_equal_bitwise": same}
+    del ws_v, out_v
     del ws, out
 
     # exact-chain mode (absorption + decode, CUDA-core sequential sums) on the full batch of one layer

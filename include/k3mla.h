@@ -189,6 +189,34 @@ int k3mla_chunk_views(const int32_t* block_table, int B, int max_pages_per_slot,
                       const int32_t* pos0, const int32_t* row_start, int R,
                       int32_t* view_table, int32_t* view_ctx, void* stream);
 
+/* k3mla_chunk_decode: the same causal attention of every token of the chunks
+ * (row j of slot b over the slot's first pos0[b] + j + 1 tokens) in multi-query
+ * form: up to four consecutive rows of one slot share each page load, one row
+ * per 32-lane quarter of the contractions, 32 heads of each (all 128 rows of
+ * an M = 128 MMA used), so a slot's pages are streamed ceil(n_b / 4) x 3 times
+ * instead of n_b times, and no view table is needed.  Each row's context is
+ * one split (the whole context: the split kernel's unit streams the pages up
+ * to its longest row), and every row's result equals k3mla_paged_decode of
+ * that row's view with a split_tokens at least the context, bit for bit.
+ * q_abs      device [R][96][576] bf16: k3mla_absorb_q of the R token rows
+ * block_table, pos0 [B], row_start [B + 1] (non-decreasing): as for
+ *            k3mla_chunk_views; rows outside every slot's range, or whose
+ *            context pos0[b] + j + 1 is < 1, get zero output (argmax -1)
+ * out        device [R][96][128] bf16; argmax_t [R][96] int32 or NULL
+ * max_ctx    >= every row's context (a longer one is clamped and flagged
+ *            K3MLA_DEV_CTX, like ctx_len in k3mla_paged_decode)
+ * workspace  device, >= k3mla_chunk_decode_workspace_bytes(B, R, max_ctx)
+ *            bytes, 256-byte aligned: o_lat [96][R][512], the rows' records,
+ *            the groups of rows and the rows' context lengths
+ * Three kernels on `stream` (groups, split kernel, merge / expansion), each
+ * reading nothing the one before writes until it has completed. */
+size_t k3mla_chunk_decode_workspace_bytes(int B, int R, int max_ctx);
+int k3mla_chunk_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                       const int32_t* block_table, int max_pages_per_slot, const int32_t* pos0,
+                       const int32_t* row_start, int B, int R, const uint16_t* w_kv_b,
+                       uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t, void* workspace,
+                       size_t ws_bytes, int max_ctx, int32_t* dev_err, void* stream);
+
 /* ---- paged absorbed decode ---------------------------------------------------
  * For each slot b < B and head h, with n = ctx_len[b] tokens (logical token t
  * lives in page block_table[b][t / 64], row t % 64; a -1 entry is an all-zero

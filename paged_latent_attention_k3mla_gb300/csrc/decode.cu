@@ -63,6 +63,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -77,22 +78,34 @@ constexpr int SLOT0 = 9 * PAGE * 128;          // 73728 B: [9 chunks][64 rows][1
 constexpr int CHUNK = PAGE * 128;              // 8192 B per chunk of a page slot
 constexpr int HALF = 32;                       // PV CTA: tokens per half-page box
 constexpr int THIRD = 3 * 8192;  // score CTA: a third of a page (3 chunks), one TMA box
-constexpr int NUNIT = 8;         // score CTA: ring of third-page units (2.67 pages)
-constexpr int PSTAGE = 24 * 128; // score CTA: one softmax warp's P rows (24 heads x 64 tokens bf16)
-constexpr int Q_UNIT0 = 4;       // score CTA: q_abs lands in ring units 4.. (and the P staging area after
-                                 // them) until it is in TMEM, so units 0..3 take pages meanwhile
 constexpr int NHSLOT = 5;                      // PV CTA: half-page slots (one producer each)
 constexpr int SLOT1 = 8 * HALF * 128;          // 32768 B: [8 chunks][32 rows][128 B], chunks 0..7 only
 constexpr int HCHUNK = HALF * 128;             // 4096 B per chunk of a half-page slot
-constexpr int NPBUF = 4;                       // P buffers in the PV CTA
-constexpr int QBYTES = H * ROW * 2;            // 110592 B: q_abs of one slot, [9 chunks][96 rows][128 B]
-constexpr int QCHUNK = H * 128;                // 12288 B per chunk of Q
-constexpr int HPW = 24;                        // heads per softmax warp (lanes 0..23 of each quarter)
-constexpr int PT_BYTES = H * 128;              // 12288 B: P^T [96 heads][64 tokens] bf16, K-major SW128
-constexpr int META_ALPHA = PT_BYTES;           // f32 alpha[96]
-constexpr int META_FLAGS = PT_BYTES + 4 * H;   // u32 flags[4]: "some head of warp w rescaled"
-constexpr int PCOPY = PT_BYTES + 4 * H + 16;   // bytes stored per page (12688)
-constexpr int PBUF = 13 * 1024;                // buffer pitch, keeps every P^T 1024-byte aligned
+
+// The rows of a unit of work, one per TMEM lane of the score and PV contractions.  Decode: the 96 heads
+// of one slot, 24 in each 32-lane quarter (lanes 24..31 idle), so that all four SM sub-partitions run
+// softmax.  Multi-query (a prefill chunk): 32 heads of up to four consecutive tokens of one slot's chunk,
+// one token per quarter, every lane a row; its larger Q and P tiles take a ring unit and a P buffer.
+template <bool MQ> struct Cfg {
+    static constexpr int RPQ = MQ ? 32 : 24;            // rows per 32-lane quarter
+    static constexpr int ROWS = 4 * RPQ;                 // rows of the unit: 96 or 128
+    static constexpr int NUNIT = MQ ? 7 : 8;             // score CTA: ring of third-page units
+    static constexpr int Q_UNIT0 = MQ ? 2 : 4;           // score CTA: q_abs lands in ring units Q_UNIT0..
+                                                         // (and the P staging area after them) until it is
+                                                         // in TMEM, so the units before take pages meanwhile
+    static constexpr int NPBUF = MQ ? 3 : 4;             // PV CTA: P buffers
+    static constexpr int PSTAGE = RPQ * 128;             // score CTA: one softmax warp's P rows (x 64 tokens)
+    static constexpr int QCHUNK = ROWS * 128;            // one 64-column chunk of Q, [rows][128 B]
+    static constexpr int QBYTES = 9 * QCHUNK;            // q_abs of a unit (110592 B for decode)
+    static constexpr int PT_BYTES = ROWS * 128;          // P^T [rows][64 tokens] bf16, K-major SW128
+    static constexpr int META_ALPHA = PT_BYTES;          // f32 alpha[rows]
+    static constexpr int META_FLAGS = PT_BYTES + 4 * ROWS;  // u32 flags[4]: "some row of quarter w rescaled"
+    static constexpr int PCOPY = PT_BYTES + 4 * ROWS + 16;  // bytes stored per page (12688 for decode)
+    static constexpr int PBUF = (PCOPY + 1023) / 1024 * 1024;  // buffer pitch: every P^T 1024-byte aligned
+    static constexpr int WO_WARPS = MQ ? 8 : 6;          // PV CTA: warps writing O out
+};
+using CD = Cfg<false>;
+constexpr int HPW = CD::RPQ;  // heads per softmax warp of the decode layout (lanes 0..23 of each quarter)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL = 0;                  // score CTA: S^T buffers r = 0..2 at 64 r
 constexpr uint32_t Q_COL = 192;                // score CTA: Q, 288 columns (576 bf16)
@@ -112,25 +125,26 @@ constexpr uint32_t HAND_BAR0 = 1, FIN_BAR0 = 9;
 constexpr uint32_t WO_BAR = 13;
 // 14 warps put four on some SM sub-partitions (16K registers each): at most 128 registers per thread.
 
-struct __align__(1024) Smem {
+template <bool MQ> struct __align__(1024) SmemT {
+    using C = Cfg<MQ>;
     union {
         struct {
-            uint8_t ring[NUNIT][THIRD];  // page thirds; q_abs is staged in units 3.. until it is in TMEM
-            uint8_t pstage[8][PSTAGE];   // each softmax warp's P rows, copied to the PV CTA in bulk
+            uint8_t ring[C::NUNIT][THIRD];  // page thirds; q_abs is staged in units Q_UNIT0.. until in TMEM
+            uint8_t pstage[8][C::PSTAGE];   // each softmax warp's P rows, copied to the PV CTA in bulk
         } c0;
         struct {
             uint8_t ring[NHSLOT][SLOT1];
-            uint8_t recv[NPBUF][PBUF];
+            uint8_t recv[C::NPBUF][C::PBUF];
         } c1;
     } u;
     uint64_t full[9], empty[9];  // score CTA: one pair per third of a page slot; PV CTA: per half-slot
     uint64_t s_full[NSLOT], s_empty[NSLOT];
     uint64_t q_land, q_ready;
-    uint64_t p_full[NPBUF], p_empty[NPBUF];
+    uint64_t p_full[C::NPBUF], p_empty[C::NPBUF];
     uint64_t o_done, epi_req, epi_done;
-    uint64_t l_full;         // PV CTA: 1 / l of every head has arrived (single-split launches)
+    uint64_t l_full;         // PV CTA: 1 / l of every row has arrived (single-split launches)
     int32_t fin_ready;       // PV CTA: epilogue warps that saw O complete (4: write it out)
-    float rl[H];             // ... 1 / l by head, stored by the score CTA
+    float rl[C::ROWS];       // ... 1 / l by row, stored by the score CTA
     float xm[2][4][32];      // score CTA: reference max after a page, by page parity / quarter / lane
     float xa[2][4][32];      // ... and that page's rescale factor (1 when it kept the reference)
     float fin_l[4][32];      // ... the odd-page warp's sum of exp, best score and its token
@@ -139,26 +153,38 @@ struct __align__(1024) Smem {
     // score CTA: the uses of a third-page unit go to different producer and issuer threads; a use
     // is handled only after the previous use of the unit has passed the same barrier, so a
     // barrier is never waited on two phases ahead (where its parity would repeat)
-    int32_t unit_loaded[NUNIT];  // uses of the unit whose load has been issued
-    int32_t unit_taken[NUNIT];   // uses of the unit whose MMAs have been issued
+    int32_t unit_loaded[C::NUNIT];  // uses of the unit whose load has been issued
+    int32_t unit_taken[C::NUNIT];   // uses of the unit whose MMAs have been issued
     uint32_t tmem_base;
     uint32_t epi_cmd, epi_slot0, epi_slot1, epi_stage, epi_vrows;
     int32_t abort_flag;
     int32_t early_n[NHSLOT];  // producer q: leading uses of its ring units loaded before the grid wait
     uint64_t wait_ns;  // the limit of every bounded wait of this CTA
+    // multi-query: the token row of quarter w (-1: none) and its context length
+    int32_t mq_row[4], mq_ntok[4];
 };
-static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && PBUF % 1024 == 0, "1024-byte aligned operand tiles");
-static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
-static_assert(QBYTES <= (NUNIT - Q_UNIT0) * THIRD + 8 * PSTAGE,
-              "q_abs staging fits in units Q_UNIT0.. and the P staging area that follows them");
-static_assert(PCOPY <= PBUF, "P buffer");
-static_assert(H * LORA * 4 <= NHSLOT * SLOT1 + NPBUF * PBUF,
-              "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
-static_assert((H * 128) % 1024 == 0, "store boxes start 1024-byte aligned (128-byte swizzle)");
-static_assert(16 * H * 128 <= NHSLOT * SLOT1 + NPBUF * PBUF, "the write-out boxes fit in the ring and P buffers");
-static_assert(NHSLOT * SLOT1 + (NPBUF - 1) * PBUF + 128 * 128 <= sizeof(Smem::u),
-              "rows 96..127 of the last P buffer, read as the A operand's unused rows, lie in this CTA's tile area");
-static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
+template <bool MQ> constexpr bool smem_fits()
+{
+    using C = Cfg<MQ>;
+    using S = SmemT<MQ>;
+    static_assert(SLOT0 % 1024 == 0 && SLOT1 % 1024 == 0 && C::PBUF % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(NHSLOT <= 9 && 3 * NSLOT <= 9, "barrier arrays");
+    static_assert(C::QBYTES <= (C::NUNIT - C::Q_UNIT0) * THIRD + 8 * C::PSTAGE,
+                  "q_abs staging fits in units Q_UNIT0.. and the P staging area that follows them");
+    static_assert((C::Q_UNIT0 * THIRD) % 1024 == 0 && C::PSTAGE % 128 == 0, "TMA and bulk-copy alignment");
+    static_assert(C::PCOPY <= C::PBUF, "P buffer");
+    static_assert(MQ || H * LORA * 4 <= NHSLOT * SLOT1 + C::NPBUF * C::PBUF,
+                  "the final [96][512] f32 tile fits in the PV CTA's page ring and P buffers");
+    static_assert((C::ROWS * 128) % 1024 == 0, "store boxes start 1024-byte aligned (128-byte swizzle)");
+    static_assert((MQ ? 8 : 16) * C::ROWS * 128 <= NHSLOT * SLOT1 + C::NPBUF * C::PBUF,
+                  "the write-out boxes fit in the ring and P buffers");
+    static_assert(NHSLOT * SLOT1 + (C::NPBUF - 1) * C::PBUF + 128 * 128 <= sizeof(S::u),
+                  "all 128 rows of the last P buffer, read as the A operand, lie in this CTA's tile area");
+    static_assert(sizeof(S) + 1024 <= 227 * 1024, "shared memory of one CTA (with 1024-byte alignment slack)");
+    return true;
+}
+static_assert(smem_fits<false>() && smem_fits<true>(), "shared-memory layouts");
+using Smem = SmemT<false>;
 
 struct DecodeParams {
     const int32_t* table;
@@ -173,6 +199,9 @@ struct DecodeParams {
     uint64_t wait_ns;  // bounded-wait limit: WAIT_NS, shorter only from the diagnostic entry
     int32_t withhold;  // diagnostic only, 0 otherwise: page k - 1's first third is never loaded
     int32_t early;     // 1 only from k3mla_decode_layer: see early_loads
+    // multi-query units (a prefill chunk) only
+    const int4* mq_groups;   // per group of up to four token rows: slot, first row, rows (0: no group)
+    const int32_t* mq_ctx;   // per token row: its context length, clamped to the table
 };
 
 __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int max_ctx, int max_pages,
@@ -187,13 +216,14 @@ __device__ __forceinline__ int ctx_effective(const int32_t* ctx_len, int b, int 
     return n < 0 ? 0 : n;
 }
 
-__device__ __forceinline__ bool aborted(const Smem& sm)
+template <class S> __device__ __forceinline__ bool aborted(const S& sm)
 {
     return *reinterpret_cast<const volatile int32_t*>(&sm.abort_flag) != 0;
 }
 
 // Bounded mbarrier wait, slow path: gives up after the CTA's wait limit or when this CTA aborted.
-__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
+template <class S>
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, S& sm, int32_t* dev_err,
                                            bool cluster_scope)
 {
     const uint32_t a = smem_u32(bar);
@@ -214,7 +244,8 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Smem&
 
 // Bounded mbarrier wait: an inline non-blocking test first (most waits are already
 // satisfied when they are reached), then the suspending slow path.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& sm, int32_t* dev_err,
+template <class S>
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, S& sm, int32_t* dev_err,
                                          bool cluster_scope = false)
 {
     const uint32_t a = smem_u32(bar);
@@ -224,7 +255,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Smem& s
 
 // Bounded wait until a shared counter of this CTA reaches `target` (written by another thread of
 // the CTA with a plain store); false when this CTA aborted or the wait timed out.
-__device__ __noinline__ bool wait_count(const int32_t* counter, int32_t target, Smem& sm, int32_t* dev_err)
+template <class S>
+__device__ __noinline__ bool wait_count(const int32_t* counter, int32_t target, S& sm, int32_t* dev_err)
 {
     const volatile int32_t* v = counter;
     if (*v >= target) return true;
@@ -273,16 +305,14 @@ __device__ __noinline__ void zero_olat(uint16_t* olat, int B, int b)
 
 // ---- building blocks shared with the diagnostic kernel -----------------------------
 
-// TMEM lane of head h: 24 heads per 32-lane quarter.
-__device__ __forceinline__ int head_lane(int h) { return 32 * (h / HPW) + (h % HPW); }
-
-// Score CTA, warps 0..3: copy Q (smem, [9 chunks][96 rows][128 B], 128-byte
-// swizzle, as a 3-D TMA box lands it) into TMEM columns [Q_COL, Q_COL + 288):
-// lane 32w + l <- head 24w + l (l < 24), other lanes zero.
-__device__ __forceinline__ void q_smem_to_tmem(uint32_t tbase, const uint8_t* qs)
+// Score CTA, warps 0..3: copy Q (smem, [9 chunks][rows][128 B], 128-byte swizzle, as the TMA boxes
+// land it) into TMEM columns [Q_COL, Q_COL + 288): lane 32w + l <- row RPQ w + l (l < RPQ), other
+// lanes zero.
+template <bool MQ> __device__ __forceinline__ void q_smem_to_tmem(uint32_t tbase, const uint8_t* qs)
 {
+    using C = Cfg<MQ>;
     const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31);
-    const int h = HPW * w + l;
+    const int h = C::RPQ * w + l;
     const uint32_t taddr = tbase + ((32u * w) << 16) + Q_COL;
 #pragma unroll 1
     for (int c = 0; c < 9; ++c) {
@@ -290,7 +320,7 @@ __device__ __forceinline__ void q_smem_to_tmem(uint32_t tbase, const uint8_t* qs
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (l < HPW) v = *reinterpret_cast<const uint4*>(qs + c * QCHUNK + h * 128 + ((j ^ (h & 7)) << 4));
+            if (l < C::RPQ) v = *reinterpret_cast<const uint4*>(qs + c * C::QCHUNK + h * 128 + ((j ^ (h & 7)) << 4));
             r[4 * j + 0] = v.x;
             r[4 * j + 1] = v.y;
             r[4 * j + 2] = v.z;
@@ -360,22 +390,25 @@ __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_add
 // Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
 __device__ __forceinline__ uint32_t pt_chunk_off(int h, int j) { return (uint32_t)(h * 128 + ((j ^ (h & 7)) << 4)); }
 
-// PV CTA, after its roles: O [heads x 512 dims] f32 leaves TMEM through the (now idle) page ring and P
-// buffers, laid out there as the 128-byte-swizzled boxes of bulk tensor stores: [96 heads][64 dims]
-// bf16 boxes of final o_lat = bf16(O * (1 / l)) when the slot has a single split, else [96 heads][32
-// dims] f32 boxes of the split's partial as it stands.  Six warps write, thread = head (TMEM lane),
-// warps 0-2 the dims 0..255 and warps 4-6 the dims 256..511, 64 dims (two TMEM loads, one wait) at a
-// time, 16 bytes per store; whenever both halves have written theirs, thread 0 stores those boxes
-// while the warps go on.  At the end it waits until
-// the stores have read the tile (the writes reach global memory before the grid counts as complete,
-// which is what the merge kernel waits for).  Kept out of line so that it does not weigh on the
-// register allocation of the pipeline.
-__device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, const CUtensorMap* tm_part,
-                                          bool single, int nsplit, uint32_t tbase, int b, int s)
+// PV CTA, after its roles: O [rows x 512 dims] f32 leaves TMEM through the (now idle) page ring and P
+// buffers, laid out there as the 128-byte-swizzled boxes of bulk tensor stores: [rows][64 dims] bf16
+// boxes of final o_lat = bf16(O * (1 / l)) when the unit is the row's only split, else [96 heads][32
+// dims] f32 boxes of the split's partial as it stands (decode only: a multi-query unit always holds
+// whole contexts).  Thread = row (TMEM lane); warps 0-2 (multi-query: 0-3) write the dims 0..255 and
+// warps 4-6 (4-7) the dims 256..511, 64 dims (two TMEM loads, one wait) at a time, 16 bytes per store;
+// whenever both halves have written theirs, thread 0 stores those boxes while the warps go on.  At the
+// end it waits until the stores have read the tile (the writes reach global memory before the grid
+// counts as complete, which is what the merge kernel waits for).  Kept out of line so that it does not
+// weigh on the register allocation of the pipeline.  b: the slot; hb: a multi-query unit's head block.
+template <bool MQ>
+__device__ __noinline__ void pv_write_out(SmemT<MQ>& sm, const CUtensorMap* tm_olat, const CUtensorMap* tm_part,
+                                          bool single, int nsplit, uint32_t tbase, int b, int s, int hb)
 {
+    using C = Cfg<MQ>;
+    constexpr int BOX = C::ROWS * 128;  // one box of every row of the unit
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     uint8_t* tile = sm.u.c1.ring[0];
-    if (warp < 8 && (warp & 3u) < 3u) {
+    if (warp < 8 && (MQ || (warp & 3u) < 3u)) {
         tc_fence_after();
         const int h = 32 * (int)(warp & 3u) + (int)lane, half = (int)(warp >> 2);
         const uint32_t ta = tbase + ((32u * (warp & 3u)) << 16) + 256u * (uint32_t)half;
@@ -387,8 +420,8 @@ __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, 
             tmem_ld32(ta + 64u * (uint32_t)k2, rr[0]);
             tmem_ld32(ta + 64u * (uint32_t)k2 + 32u, rr[1]);
             tmem_wait_ld();
-            if (single) {  // box 4 half + k2 (64 dims): the eight 16-byte chunks of row h
-                uint8_t* row = tile + (4 * half + k2) * (H * 128) + h * 128;
+            if (MQ || single) {  // box 4 half + k2 (64 dims): the eight 16-byte chunks of row h
+                uint8_t* row = tile + (4 * half + k2) * BOX + h * 128;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint32_t* v = rr[i >> 2] + 8 * (i & 3);
@@ -398,10 +431,10 @@ __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, 
                                    pack_bf16x2(__uint_as_float(v[4]) * r, __uint_as_float(v[5]) * r),
                                    pack_bf16x2(__uint_as_float(v[6]) * r, __uint_as_float(v[7]) * r));
                 }
-            } else {  // boxes 8 half + 2 k2 and + 1 (32 dims each): all chunks of row h
+            } else if constexpr (!MQ) {  // boxes 8 half + 2 k2 and + 1 (32 dims each): all chunks of row h
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    uint8_t* row = tile + (8 * half + 2 * k2 + e) * (H * 128) + h * 128;
+                    uint8_t* row = tile + (8 * half + 2 * k2 + e) * BOX + h * 128;
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         *reinterpret_cast<uint4*>(row + (((uint32_t)i ^ sw) << 4)) =
@@ -409,9 +442,16 @@ __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, 
                 }
             }
             fence_proxy_async_cta();  // the boxes are read by bulk tensor stores (async proxy)
-            named_bar(WO_BAR, 6 * 32);
+            named_bar(WO_BAR, C::WO_WARPS * 32);
             if (threadIdx.x == 0) {
-                if (single) {  // o_lat [96][B][512] as (512 dims, B slots, 96 heads), box (64, 1, 96)
+                if constexpr (MQ) {  // o_lat [96][R][512] as (512 dims, R rows, 96 heads), box (64, 1, 32)
+                    for (int w = 0; w < 4; ++w) {
+                        const int row = sm.mq_row[w];
+                        if (row < 0) continue;
+                        tma_store_3d(tm_olat, tile + k2 * BOX + 32 * w * 128, 64 * k2, row, 32 * hb);
+                        tma_store_3d(tm_olat, tile + (4 + k2) * BOX + 32 * w * 128, 256 + 64 * k2, row, 32 * hb);
+                    }
+                } else if (single) {  // o_lat [96][B][512] as (512 dims, B slots, 96 heads), box (64, 1, 96)
                     tma_store_3d(tm_olat, tile + k2 * (H * 128), 64 * k2, b, 0);
                     tma_store_3d(tm_olat, tile + (4 + k2) * (H * 128), 256 + 64 * k2, b, 0);
                 } else {  // partials [B][nsplit][96][512] as (512 dims, rows), box (32, 96)
@@ -433,6 +473,7 @@ __device__ __noinline__ void pv_write_out(Smem& sm, const CUtensorMap* tm_olat, 
 // Where split s of slot b lies: set from the slot's (clamped) context; false for an empty split.
 struct SplitGeom {
     int b, s, start, ntok, npg, n_lp, lp0;
+    int hb;           // a multi-query unit's head block (heads 32 hb .. 32 hb + 31)
     bool single;      // the slot has at most one split: the PV CTA lands final o_lat itself
     int32_t oob_row;  // a slab row past the end (a TMA box there reads zeros)
 };
@@ -452,11 +493,16 @@ __device__ __forceinline__ bool split_geom(SplitGeom& g, int ctx, const DecodePa
 }
 
 // Score CTA: where q_abs is staged (ring units Q_UNIT0.. and the P staging area after them).
-__device__ __forceinline__ uint8_t* q_stage(Smem& sm) { return reinterpret_cast<uint8_t*>(&sm.u) + Q_UNIT0 * THIRD; }
+template <bool MQ> __device__ __forceinline__ uint8_t* q_stage(SmemT<MQ>& sm)
+{
+    return reinterpret_cast<uint8_t*>(&sm.u) + Cfg<MQ>::Q_UNIT0 * THIRD;
+}
 
 // Thread 0: the mbarriers and counters of one split (the caller fences them for the cluster).
-__device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bool single, uint64_t wait_ns)
+template <bool MQ>
+__device__ __forceinline__ void init_decode_barriers(SmemT<MQ>& sm, uint32_t rank, bool single, uint64_t wait_ns)
 {
+    using C = Cfg<MQ>;
     sm.wait_ns = wait_ns;
     for (int i = 0; i < 9; ++i) {
         mbar_init(&sm.full[i], 1);
@@ -466,7 +512,7 @@ __device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bo
         mbar_init(&sm.s_full[i], 1);
         mbar_init(&sm.s_empty[i], 4);
     }
-    for (int i = 0; i < NPBUF; ++i) {
+    for (int i = 0; i < C::NPBUF; ++i) {
         mbar_init(&sm.p_full[i], 1);
         mbar_init(&sm.p_empty[i], 1);
     }
@@ -479,30 +525,45 @@ __device__ __forceinline__ void init_decode_barriers(Smem& sm, uint32_t rank, bo
     sm.abort_flag = 0;
     sm.fin_ready = 0;
     for (int i = 0; i < NHSLOT; ++i) sm.early_n[i] = 0;
-    for (int i = 0; i < NUNIT; ++i) {
+    for (int i = 0; i < C::NUNIT; ++i) {
         sm.unit_loaded[i] = 0;
         sm.unit_taken[i] = 0;
     }
     if (rank == 1) {  // the P buffers of pages 0 .. NPBUF-1 are expected before anything is sent
-        for (int i = 0; i < NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], PCOPY);
-        if (single) mbar_arrive_expect_tx(&sm.l_full, 4 * H);
+        for (int i = 0; i < C::NPBUF; ++i) mbar_arrive_expect_tx(&sm.p_full[i], C::PCOPY);
+        if (single) mbar_arrive_expect_tx(&sm.l_full, 4 * C::ROWS);
     }
 }
 
 // The roles of both CTAs for one split: q_abs into TMEM, the page ring, the two contractions, the softmax,
 // and the PV CTA's write-out of O.  Inlined into the kernel: the parameters it reads in its loops stay
 // constant-bank operands (an out-of-line copy, reaching them through a pointer, ran some 50 % slower).
-__device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_page, const CUtensorMap& tmap_page8,
+// A multi-query unit (MQ) runs the same roles over its rows: quarter w holds heads 32 hb .. 32 hb + 31 of
+// token row mq_row[w], whose context is the first mq_ntok[w] tokens of the unit's pages.
+template <bool MQ>
+__device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& tmap_page, const CUtensorMap& tmap_page8,
                                              const CUtensorMap& tmap_q, const CUtensorMap& tmap_olat,
                                              const CUtensorMap& tmap_part, const DecodeParams& p, const SplitGeom& sg,
                                              uint32_t tbase, uint32_t rank, uint32_t warp, uint32_t lane)
 {
+    using C = Cfg<MQ>;
     const int b = sg.b, s = sg.s, start = sg.start, ntok = sg.ntok, npg = sg.npg, n_lp = sg.n_lp, lp0 = sg.lp0;
     const bool single = sg.single;
     const int32_t oob_row = sg.oob_row;
-    if (rank == 0 && threadIdx.x == 0) {  // q_abs of the slot, staged in ring units 4.. until it is in TMEM
-        mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-        for (int c = 0; c < 9; ++c) tma_load_3d(q_stage(sm) + c * QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
+    if (rank == 0 && threadIdx.x == 0) {  // q_abs of the unit, staged in ring units Q_UNIT0.. until in TMEM
+        if constexpr (MQ) {  // 32 rows of each present token row per chunk, at row 32 w of the chunk
+            int nq = 0;
+            for (int w = 0; w < 4; ++w) nq += sm.mq_row[w] >= 0 ? 1 : 0;
+            mbar_arrive_expect_tx(&sm.q_land, 9 * nq * C::PSTAGE);
+            for (int c = 0; c < 9; ++c)
+                for (int w = 0; w < 4; ++w)
+                    if (sm.mq_row[w] >= 0)
+                        tma_load_3d(q_stage(sm) + c * C::QCHUNK + w * C::PSTAGE, &tmap_q, 0,
+                                    sm.mq_row[w] * H + 32 * sg.hb, c, &sm.q_land);
+        } else {
+            mbar_arrive_expect_tx(&sm.q_land, C::QBYTES);
+            for (int c = 0; c < 9; ++c) tma_load_3d(q_stage(sm) + c * C::QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
+        }
     }
 
     if (rank == 0) {
@@ -514,8 +575,8 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 const int t = (int)warp - W_PROD0;
                 bool ok = true, q_in_tmem = false;
                 for (int i = sm.early_n[t]; i < npg && ok; ++i) {
-                    const int g = 3 * i + t, u = g % NUNIT, k = g / NUNIT;
-                    if (!q_in_tmem && g >= Q_UNIT0) {  // units Q_UNIT0.. hold q_abs until it is in TMEM
+                    const int g = 3 * i + t, u = g % C::NUNIT, k = g / C::NUNIT;
+                    if (!q_in_tmem && g >= C::Q_UNIT0) {  // units Q_UNIT0.. hold q_abs until it is in TMEM
                         ok = wait_bar(&sm.q_ready, 0, sm, p.dev_err);
                         q_in_tmem = true;
                     }
@@ -544,7 +605,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                         break;
                     }
                     for (int t = 0; t < 3 && ok; ++t) {
-                        const int g = 3 * i + t, u = g % NUNIT, ku = g / NUNIT;
+                        const int g = 3 * i + t, u = g % C::NUNIT, ku = g / C::NUNIT;
                         if (!wait_count(&sm.unit_taken[u], ku, sm, p.dev_err) ||
                             !wait_bar(&sm.full[u], (uint32_t)(ku & 1), sm, p.dev_err)) {
                             ok = false;
@@ -560,20 +621,22 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 if (!ok) drain_inflight();
             }
         } else if (warp < 8) {
-            // softmax warps 0..7: warp (qd = warp % 4, par = warp / 4) owns heads 24 qd .. 24 qd + 23
-            // (thread l < 24 -> head 24 qd + l) for all 64 tokens of the pages of parity par.  The
+            // softmax warps 0..7: warp (qd = warp % 4, par = warp / 4) owns rows RPQ qd .. RPQ qd + RPQ-1
+            // (thread l < RPQ -> row RPQ qd + l; decode: head 24 qd + l) for all 64 tokens of the pages
+            // of parity par.  The
             // reference max is a chain through the pages: each warp hands its page's decision (new
             // reference max, rescale factor) to the other warp of its quarter through shared memory
             // and a named barrier, and takes the previous page's decision from it; everything else
             // (scores, max, argmax, exp, the P store) of the two pages runs in parallel.
             const int qd = (int)(warp & 3u), par = (int)(warp >> 2), l = (int)lane;
-            const int h = HPW * qd + l;
-            const bool has_head = l < HPW;
+            const int h = C::RPQ * qd + l;  // the row (decode: the head)
+            const bool has_head = l < C::RPQ;
+            const int ntok_q = MQ ? sm.mq_ntok[qd] : ntok;  // the row's tokens in this split
             const uint32_t bar_in = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)(par ^ 1);
             const uint32_t bar_out = HAND_BAR0 + 2u * (uint32_t)qd + (uint32_t)par;
             if (par == 0) {
                 const bool qok = wait_bar(&sm.q_land, 0, sm, p.dev_err);
-                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem(tbase, q_stage(sm));
+                if (__all_sync(0xFFFFFFFFu, qok)) q_smem_to_tmem<MQ>(tbase, q_stage(sm));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.q_ready);
@@ -588,7 +651,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
             for (int i = par; i < npg; i += 2) {
                 const int r = i % NSLOT, k = i / NSLOT;
                 if (ok) ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.s_full[r], (uint32_t)(k & 1), sm, p.dev_err));
-                const int nvalid = min(PAGE, ntok - PAGE * i);
+                const int nvalid = min(PAGE, ntok_q - PAGE * i);
                 uint32_t sp[32];  // bf16 scores: token 2q in the low half, 2q+1 in the high half
                 if (ok) {
                     tc_fence_after();
@@ -669,7 +732,8 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 sm.xm[i & 1][qd][l] = m_ref;  // hand this page's decision on
                 sm.xa[i & 1][qd][l] = alpha;
                 named_bar_arrive(bar_out, 64);
-                const float mb = m_ref * LOG2E;
+                // (multi-query: a row with no token yet keeps m_ref = -inf, and its p~ = exp(-inf) = 0)
+                const float mb = (MQ && m_ref == -INFINITY) ? 0.f : m_ref * LOG2E;
                 float part[8];  // independent partial sums, combined in a fixed order below
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {  // tokens 8j .. 8j+7: p~ = bf16(exp(s - m_ref)), in place of s
@@ -685,7 +749,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                     part[j] = acc;
                 }
                 lsum += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                const int st = i % NPBUF;
+                const int st = i % C::NPBUF;
                 // this warp's P rows, laid out as they land (rows 24 qd .. 24 qd + 23 of the P^T
                 // buffer), once the bulk copy of its previous page has read the staging rows
                 uint8_t* stage = sm.u.c0.pstage[warp];
@@ -694,23 +758,23 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 if (has_head) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(stage + pt_chunk_off(h, j) - qd * PSTAGE) =
+                        *reinterpret_cast<uint4*>(stage + pt_chunk_off(h, j) - qd * C::PSTAGE) =
                             make_uint4(sp[4 * j], sp[4 * j + 1], sp[4 * j + 2], sp[4 * j + 3]);
                 }
                 fence_proxy_async_cta();  // the bulk copy reads the rows through the async proxy
                 __syncwarp();
                 // the PV CTA has finished with its buffer from page i - NPBUF
                 bool freed = false;
-                if (ok) freed = wait_bar(&sm.p_empty[st], (uint32_t)((i / NPBUF) & 1) ^ 1u, sm, p.dev_err);
-                const uint32_t dst = recv0 + (uint32_t)(st * PBUF);
+                if (ok) freed = wait_bar(&sm.p_empty[st], (uint32_t)((i / C::NPBUF) & 1) ^ 1u, sm, p.dev_err);
+                const uint32_t dst = recv0 + (uint32_t)(st * C::PBUF);
                 const uint32_t bar = pfull0 + (uint32_t)(st * sizeof(uint64_t));
                 if (freed && lane == 0) {
-                    bulk_copy_to_cluster(dst + (uint32_t)(qd * PSTAGE), stage, PSTAGE, bar);
+                    bulk_copy_to_cluster(dst + (uint32_t)(qd * C::PSTAGE), stage, C::PSTAGE, bar);
                     bulk_commit();
                 }
-                if (freed && has_head) st_async_b32(dst + META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
+                if (freed && has_head) st_async_b32(dst + C::META_ALPHA + 4 * h, __float_as_uint(alpha), bar);
                 const uint32_t any = __ballot_sync(0xFFFFFFFFu, resc && has_head);
-                if (freed && lane == 0) st_async_b32(dst + META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
+                if (freed && lane == 0) st_async_b32(dst + C::META_FLAGS + 4 * qd, any ? 1u : 0u, bar);
             }
             // the other warp's decision on the last page, when that page was not this warp's
             const int last = npg - 1;
@@ -733,23 +797,30 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                     best_s = s1;
                     best_t = t1;
                 }
-                float* ml = p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
                 const float ltot = lsum + sm.fin_l[qd][l];
-                ml[0] = m_ref;
-                ml[1] = ltot;
-                ml[2] = best_s;
-                ml[3] = __int_as_float(best_t);
+                // multi-query: row (token row mq_row[qd], head 32 hb + l); a quarter without a token row
+                // writes no record, and a row without tokens lands zeros (1 / l taken as 0)
+                const int row = MQ ? sm.mq_row[qd] : b;
+                if (!MQ || row >= 0) {
+                    float* ml = MQ ? p.ws_ml + ((size_t)row * H + 32 * sg.hb + l) * 4
+                                   : p.ws_ml + (((size_t)b * p.nsplit + s) * H + h) * 4;
+                    ml[0] = m_ref;
+                    ml[1] = ltot;
+                    ml[2] = best_s;
+                    ml[3] = __int_as_float(best_t);
+                }
                 // a single split is final: the PV CTA lands o_lat = bf16(O * (1 / l)) itself
                 if (single)
-                    st_async_b32(mapa(smem_u32(&sm.rl[h]), 1), __float_as_uint(1.f / ltot),
+                    st_async_b32(mapa(smem_u32(&sm.rl[h]), 1),
+                                 __float_as_uint((MQ && !(ltot > 0.f)) ? 0.f : 1.f / ltot),
                                  mapa(smem_u32(&sm.l_full), 1));
             }
             // this warp's bulk copies are complete (their bytes have landed in the PV CTA), and the PV
             // CTA's last releases of its P buffers land here, before exit
             if (lane == 0) {
                 bulk_wait<0>();
-                for (int i = max(0, npg - NPBUF); i < npg && !aborted(sm); ++i)
-                    wait_bar(&sm.p_empty[i % NPBUF], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err);
+                for (int i = max(0, npg - C::NPBUF); i < npg && !aborted(sm); ++i)
+                    wait_bar(&sm.p_empty[i % C::NPBUF], (uint32_t)((i / C::NPBUF) & 1), sm, p.dev_err);
             }
         }
     } else {
@@ -776,14 +847,14 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                 uint32_t epi_k = 0;
                 bool ok = true;
                 for (int i = 0; i < npg && ok; ++i) {
-                    const int st = i % NPBUF;
-                    if (!wait_bar(&sm.p_full[st], (uint32_t)((i / NPBUF) & 1), sm, p.dev_err, true)) {
+                    const int st = i % C::NPBUF;
+                    if (!wait_bar(&sm.p_full[st], (uint32_t)((i / C::NPBUF) & 1), sm, p.dev_err, true)) {
                         ok = false;
                         break;
                     }
                     fence_proxy_async_cta();  // the P tile arrived through st.async; the MMA reads it
                     const volatile uint32_t* rf =
-                        reinterpret_cast<const volatile uint32_t*>(sm.u.c1.recv[st] + META_FLAGS);
+                        reinterpret_cast<const volatile uint32_t*>(sm.u.c1.recv[st] + C::META_FLAGS);
                     const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2] | rf[3]) != 0u);
                     const int nvalid = min(PAGE, ntok - PAGE * i);
                     const bool tail = nvalid < PAGE;
@@ -813,7 +884,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                     umma_commit(&sm.empty[q0]);
                     umma_commit(&sm.empty[q1]);
                     umma_commit_mc(&sm.p_empty[st], (uint16_t)0x1);
-                    if (i + NPBUF < npg) mbar_arrive_expect_tx(&sm.p_full[st], PCOPY);
+                    if (i + C::NPBUF < npg) mbar_arrive_expect_tx(&sm.p_full[st], C::PCOPY);
                 }
                 if (ok) {
                     umma_commit(&sm.o_done);
@@ -839,8 +910,8 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
                     if (!__all_sync(0xFFFFFFFFu, got2)) break;
                     ++od;
                     tc_fence_after();
-                    const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + META_ALPHA);
-                    const float a = warp < 3 ? al[32 * warp + lane] : 1.f;
+                    const float* al = reinterpret_cast<const float*>(sm.u.c1.recv[sm.epi_stage] + C::META_ALPHA);
+                    const float a = (MQ || warp < 3) ? al[32 * warp + lane] : 1.f;
                     if (__any_sync(0xFFFFFFFFu, a != 1.f)) {  // some head of this warp moved its reference
 #pragma unroll 1
                         for (int cb = 0; cb < LORA / 32; ++cb) {
@@ -880,7 +951,7 @@ __device__ __forceinline__ void decode_roles(Smem& sm, const CUtensorMap& tmap_p
         }
         __syncthreads();  // every role is done: the final write-out takes all warps
         if (*reinterpret_cast<volatile int32_t*>(&sm.fin_ready) == 4)
-            pv_write_out(sm, &tmap_olat, &tmap_part, single, p.nsplit, tbase, b, s);
+            pv_write_out<MQ>(sm, &tmap_olat, &tmap_part, single, p.nsplit, tbase, b, s, sg.hb);
     }
 
 }
@@ -900,7 +971,7 @@ __device__ __forceinline__ void early_loads(Smem& sm, const CUtensorMap& tmap_pa
         // producer t: third t of pages 0, 1, ... while they fall in the units q_abs leaves free
         const int t = (int)warp - W_PROD0;
         int i = 0;
-        for (; 3 * i + t < Q_UNIT0 && i < sg.npg && sg.lp0 + i < sg.n_lp - 1; ++i) {
+        for (; 3 * i + t < CD::Q_UNIT0 && i < sg.npg && sg.lp0 + i < sg.n_lp - 1; ++i) {
             const int u = 3 * i + t;  // the unit's first use
             *reinterpret_cast<volatile int32_t*>(&sm.unit_loaded[u]) = 1;
             mbar_arrive_expect_tx(&sm.full[u], THIRD);
@@ -923,6 +994,10 @@ __device__ __forceinline__ void early_loads(Smem& sm, const CUtensorMap& tmap_pa
 
 // ---- the split decode kernel ---------------------------------------------------------
 
+// MQ: the multi-query form of a prefill chunk.  Unit u is head block u % 3 of group u / 3 (up to four
+// consecutive token rows of one slot's chunk); the unit streams the slot's pages up to the longest
+// context among its rows, each row masking the tokens past its own, in a single split.
+template <bool MQ>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     k3mla_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_page,
                               const __grid_constant__ CUtensorMap tmap_page8,
@@ -931,27 +1006,58 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
                               const __grid_constant__ CUtensorMap tmap_part, const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemT<MQ>& sm =
+        *reinterpret_cast<SmemT<MQ>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t rank = cluster_ctarank();
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
 
     const int unit = blockIdx.x >> 1;
     SplitGeom sg;
-    sg.b = unit / p.nsplit;
-    sg.s = unit % p.nsplit;
-    const int ctx = ctx_effective(p.ctx_len, sg.b, p.max_ctx, p.max_pages, p.dev_err,
-                                  rank == 0 && threadIdx.x == 0 && sg.s == 0);
-    if (!split_geom(sg, ctx, p)) {  // empty split: both CTAs leave, nothing was shared
-        if (sg.s == 0 && rank == 1) {  // an empty context: its o_lat is zero (the workspace is written only
-            griddep_wait();            // after the kernel before has completed: it may still read it)
-            zero_olat(p.ws_olat, p.B, sg.b);
+    sg.hb = 0;
+    int mq_row[4] = {-1, -1, -1, -1}, mq_ntok[4] = {0, 0, 0, 0};
+    if constexpr (MQ) {
+        griddep_wait();  // the groups and row contexts come from the launch just before
+        const int4 gr = p.mq_groups[unit / 3];  // (slot, first token row, rows, -)
+        if (gr.z <= 0) return;                  // past the chunk's groups
+        sg.b = gr.x;
+        sg.s = 0;
+        sg.hb = unit % 3;
+        int ctx = 0;
+        for (int w = 0; w < 4 && w < gr.z; ++w) {
+            mq_row[w] = gr.y + w;
+            mq_ntok[w] = p.mq_ctx[gr.y + w];
+            ctx = max(ctx, mq_ntok[w]);
         }
-        return;
+        if (ctx <= 0) return;  // no row has a token: the launch before zeroed their o_lat
+        sg.single = true;
+        sg.start = 0;
+        sg.ntok = ctx;
+        sg.npg = (ctx + PAGE - 1) / PAGE;
+        sg.n_lp = sg.npg;
+        sg.lp0 = 0;
+        sg.oob_row = p.n_pages * p.n_layers * PAGE;
+    } else {
+        sg.b = unit / p.nsplit;
+        sg.s = unit % p.nsplit;
+        const int ctx = ctx_effective(p.ctx_len, sg.b, p.max_ctx, p.max_pages, p.dev_err,
+                                      rank == 0 && threadIdx.x == 0 && sg.s == 0);
+        if (!split_geom(sg, ctx, p)) {  // empty split: both CTAs leave, nothing was shared
+            if (sg.s == 0 && rank == 1) {  // an empty context: its o_lat is zero (the workspace is written
+                griddep_wait();            // only after the kernel before has completed: it may still read it)
+                zero_olat(p.ws_olat, p.B, sg.b);
+            }
+            return;
+        }
     }
 
     if (threadIdx.x == 0) {
         init_decode_barriers(sm, rank, sg.single, p.wait_ns);
+        if constexpr (MQ)
+            for (int w = 0; w < 4; ++w) {
+                sm.mq_row[w] = mq_row[w];
+                sm.mq_ntok[w] = mq_ntok[w];
+            }
         fence_mbarrier_init_cluster();
         if (rank == 0) tma_prefetch_desc(&tmap_q);
     }
@@ -971,10 +1077,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)
     // everything above overlaps the previous kernel in the stream (which must not write ctx_len, read
     // at the top to size the split); q_abs, the slab and the block table are read after it completed,
     // but for the early page loads of a layer-call
-    if (p.early) early_loads(sm, tmap_page, tmap_page8, p, sg, rank, warp, lane);
+    if constexpr (!MQ)
+        if (p.early) early_loads(sm, tmap_page, tmap_page8, p, sg, rank, warp, lane);
     griddep_wait();
     griddep_launch_dependents();
-    decode_roles(sm, tmap_page, tmap_page8, tmap_q, tmap_olat, tmap_part, p, sg, tbase, rank, warp, lane);
+    decode_roles<MQ>(sm, tmap_page, tmap_page8, tmap_q, tmap_olat, tmap_part, p, sg, tbase, rank, warp, lane);
 
     __syncwarp();
     tc_fence_before();
@@ -1012,13 +1119,13 @@ __global__ void __launch_bounds__(128, 1)
     bool ok = true;
     if (mode == 0) {
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&sm.q_land, QBYTES);
-            for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[3] + c * QCHUNK, &tmap_q, 0, 0, c, &sm.q_land);
+            mbar_arrive_expect_tx(&sm.q_land, CD::QBYTES);
+            for (int c = 0; c < 9; ++c) tma_load_3d(sm.u.c0.ring[3] + c * CD::QCHUNK, &tmap_q, 0, 0, c, &sm.q_land);
             mbar_arrive_expect_tx(&sm.full[0], SLOT0);
             for (int t = 0; t < 3; ++t) tma_load_3d(sm.u.c0.ring[0] + t * THIRD, &tmap_page, 0, 0, 3 * t, &sm.full[0]);
         }
         ok = __all_sync(0xFFFFFFFFu, wait_bar(&sm.q_land, 0, sm, nullptr));
-        if (ok) q_smem_to_tmem(tbase, sm.u.c0.ring[3]);
+        if (ok) q_smem_to_tmem<false>(tbase, sm.u.c0.ring[3]);
         tc_fence_before();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -1084,7 +1191,78 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
-static size_t smem_bytes() { return sizeof(Smem) + 1024; }
+// ---- multi-query decode of a prefill chunk: its groups of token rows -------------------
+
+// Upper bound of the groups of a chunk of R token rows over B slots: sum over slots of ceil(n_b / 4).
+static inline int mq_max_groups(int B, int R) { return (R + 3 * B) / 4 + 1; }
+
+// One CTA.  Token rows row_start[b] .. row_start[b+1]-1 (within [0, R)) belong to slot b, row j of
+// them at position pos0[b] + j: its context is pos0[b] + j + 1 tokens (clamped to cap, flagged when
+// it is larger).  Groups are up to four consecutive rows of one slot, slot by slot; the entries past
+// the last group are empty.  A row without tokens gets zero o_lat here (no unit writes it).
+__global__ void __launch_bounds__(1024) k3mla_mq_prep_kernel(const int32_t* __restrict__ pos0,
+                                                             const int32_t* __restrict__ row_start, int B, int R,
+                                                             int cap, int4* __restrict__ groups, int g_max,
+                                                             int32_t* __restrict__ rctx, uint16_t* __restrict__ olat,
+                                                             int32_t* dev_err)
+{
+    griddep_wait();
+    __shared__ int off[1024];
+    __shared__ int total;
+    const int tid = (int)threadIdx.x;
+    if (tid == 0) total = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < B; b0 += 1024) {
+        const int b = b0 + tid;
+        int lo = 0, n = 0;
+        if (b < B) {
+            lo = max(0, row_start[b]);
+            n = max(0, min(R, row_start[b + 1]) - lo);
+        }
+        off[tid] = (n + 3) / 4;
+        __syncthreads();
+        if (tid == 0) {  // exclusive prefix of the group counts, after those of the slots before
+            int acc = total;
+            for (int i = 0; i < 1024; ++i) {
+                const int c = off[i];
+                off[i] = acc;
+                acc += c;
+            }
+            total = acc;
+        }
+        __syncthreads();
+        for (int j = 0; 4 * j < n; ++j)
+            if (off[tid] + j < g_max) groups[off[tid] + j] = make_int4(b, lo + 4 * j, min(4, n - 4 * j), 0);
+        __syncthreads();
+    }
+    for (int g = total + tid; g < g_max; g += (int)blockDim.x) groups[g] = make_int4(0, 0, 0, 0);
+    for (int r = tid; r < R; r += (int)blockDim.x) {
+        int lo = 0, hi = B;  // the last slot b with row_start[b] <= r
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (row_start[mid] <= r) lo = mid;
+            else hi = mid;
+        }
+        int c = 0;
+        if (B > 0 && r >= row_start[lo] && r < row_start[lo + 1]) {
+            c = pos0[lo] + (r - row_start[lo]) + 1;
+            if (c > cap) {
+                if (dev_err) atomicOr(dev_err, (int)K3MLA_DEV_CTX);
+                c = cap;
+            }
+            c = max(c, 0);
+        }
+        rctx[r] = c;
+        if (c == 0)  // o_lat [96][R][512]: this row's 96 rows of 1 KB
+            for (int hh = 0; hh < H; ++hh) {
+                uint4* dst = reinterpret_cast<uint4*>(olat + ((size_t)hh * R + r) * LORA);
+                for (int k = 0; k < LORA / 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+    }
+    griddep_launch_dependents();
+}
+
+template <bool MQ> static size_t smem_bytes() { return sizeof(SmemT<MQ>) + 1024; }
 
 
 static int make_maps(const void* slab, uint64_t rows, const void* q, uint64_t q_rows, CUtensorMap* page,
@@ -1163,8 +1341,8 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
     int rc = make_maps(slab, (uint64_t)n_pages * n_layers * PAGE, q_abs, (uint64_t)B * H, &tm_page, &tm_page8, &tm_q);
     if (rc) return rc;
     static bool attr_done[64] = {};
-    const size_t smem = smem_bytes();
-    set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel), smem, attr_done);
+    const size_t smem = smem_bytes<false>();
+    set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel<false>), smem, attr_done);
 
     const WsLayout wl = ws_layout(B, ns);
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
@@ -1189,6 +1367,8 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
     dp.wait_ns = wait_ns;
     dp.withhold = withhold;
     dp.early = early;
+    dp.mq_groups = nullptr;
+    dp.mq_ctx = nullptr;
     // the PV CTAs' stores: o_lat [96][B][512] bf16 as (512 dims, B slots, 96 heads), and the f32 partials
     // [B][ns][96][512] as (512 dims, B ns 96 rows)
     CUtensorMap tm_olat, tm_part;
@@ -1209,7 +1389,7 @@ static int paged_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages
         tm_part = tm_olat;  // not used: no slot of this launch has several splits
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_pdl(k3mla_decode_split_kernel, dim3(2 * B * ns), dim3(THREADS), smem, st, "k3mla_decode_split_kernel",
+    rc = launch_pdl(k3mla_decode_split_kernel<false>, dim3(2 * B * ns), dim3(THREADS), smem, st, "k3mla_decode_split_kernel",
                     tm_page, tm_page8, tm_q, tm_olat, tm_part, dp);
     if (rc) return rc;
 
@@ -1256,6 +1436,116 @@ extern "C" int k3mla_diag_decode_timeout(const uint16_t* q_abs, const uint16_t* 
     return paged_decode(q_abs, slab, n_pages, n_layers, layer, block_table, max_pages_per_slot, ctx_len, w_kv_b,
                         scale_bf16, out, argmax_t, workspace, ws_bytes, B, max_ctx, split_tokens, dev_err, stream,
                         (uint64_t)wait_us * 1000ull, withhold_page + 1, 0);
+}
+
+// ---- multi-query decode of a prefill chunk ---------------------------------------------
+
+extern "C" size_t k3mla_chunk_decode_workspace_bytes(int B, int R, int max_ctx)
+{
+    if (B <= 0 || R <= 0 || max_ctx <= 0) return 0;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    return ws_layout(R, 1).total + up((size_t)mq_max_groups(B, R) * sizeof(int4)) + up((size_t)R * 4);
+}
+
+extern "C" int k3mla_chunk_decode(const uint16_t* q_abs, const uint16_t* slab, int n_pages, int n_layers, int layer,
+                                  const int32_t* block_table, int max_pages_per_slot, const int32_t* pos0,
+                                  const int32_t* row_start, int B, int R, const uint16_t* w_kv_b,
+                                  uint16_t scale_bf16, uint16_t* out, int32_t* argmax_t, void* workspace,
+                                  size_t ws_bytes, int max_ctx, int32_t* dev_err, void* stream)
+{
+    if (B <= 0 || R < 0 || n_pages <= 0 || n_layers <= 0 || layer < 0 || layer >= n_layers ||
+        max_pages_per_slot <= 0 || max_ctx <= 0) {
+        set_error("k3mla_chunk_decode: invalid sizes");
+        return K3MLA_E_INVALID;
+    }
+    if (R == 0) return K3MLA_OK;
+    if ((long long)n_pages * n_layers * PAGE + PAGE > 0x7FFFFFFFll || (long long)R * H > 0x7FFFFFFFll ||
+        6ll * mq_max_groups(B, R) > 0x7FFFFFFFll) {
+        set_error("k3mla_chunk_decode: sizes exceed the 2^31 TMA row or grid range");
+        return K3MLA_E_INVALID;
+    }
+    if (!q_abs || !slab || !block_table || !pos0 || !row_start || !w_kv_b || !out || !workspace ||
+        !aligned(q_abs, 16) || !aligned(slab, 16) || !aligned(w_kv_b, 16) || !aligned(out, 4) ||
+        !aligned(workspace, 256)) {
+        set_error("k3mla_chunk_decode: null or misaligned pointer");
+        return K3MLA_E_INVALID;
+    }
+    const size_t need = k3mla_chunk_decode_workspace_bytes(B, R, max_ctx);
+    if (ws_bytes < need) {
+        set_error("k3mla_chunk_decode: workspace %zu < %zu bytes", ws_bytes, need);
+        return K3MLA_E_WORKSPACE;
+    }
+    if (!device_ok()) return K3MLA_E_DEVICE;
+    const int G = mq_max_groups(B, R);
+    const int cap = (int)std::min<long long>(max_ctx, (long long)max_pages_per_slot * PAGE);
+    const int whole = (cap + TILE - 1) / TILE * TILE;  // one split holds any row's context
+    const WsLayout wl = ws_layout(R, 1);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    int4* groups = reinterpret_cast<int4*>(ws + wl.total);
+    int32_t* rctx = reinterpret_cast<int32_t*>(ws + wl.total + ((G * sizeof(int4) + 255) & ~size_t(255)));
+    uint16_t* olat = reinterpret_cast<uint16_t*>(ws + wl.olat);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = launch_pdl(k3mla_mq_prep_kernel, dim3(1), dim3(1024), 0, st, "k3mla_mq_prep_kernel", pos0, row_start, B,
+                        R, cap, groups, G, rctx, olat, dev_err);
+    if (rc) return rc;
+
+    CUtensorMap tm_page, tm_page8, tm_q, tm_olat;
+    rc = make_tmap_slab_3d(&tm_page, slab, (uint64_t)n_pages * n_layers * PAGE, ROW, 9, PAGE, 3);
+    if (rc) return rc;
+    rc = make_tmap_slab_3d(&tm_page8, slab, (uint64_t)n_pages * n_layers * PAGE, ROW, 9, HALF, 8);
+    if (rc) return rc;
+    rc = make_tmap_slab_3d(&tm_q, q_abs, (uint64_t)R * H, ROW, 9, 32, 1);  // 32 heads of one row a box
+    if (rc) return rc;
+    {   // o_lat [96][R][512] bf16 as (512 dims, R rows, 96 heads), box (64, 1, 32)
+        const uint64_t dims[3] = {LORA, (uint64_t)R, H};
+        const uint64_t strides[2] = {LORA * 2, (uint64_t)R * LORA * 2};
+        const uint32_t box[3] = {64, 1, 32};
+        rc = make_tmap_store(&tm_olat, false, 3, olat, dims, strides, box, true);
+        if (rc) return rc;
+    }
+    DecodeParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    dp.table = block_table;
+    dp.ctx_len = rctx;
+    dp.ws_olat = olat;
+    dp.ws_o = nullptr;
+    dp.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
+    dp.dev_err = dev_err;
+    dp.max_pages = max_pages_per_slot;
+    dp.n_pages = n_pages;
+    dp.n_layers = n_layers;
+    dp.layer = layer;
+    dp.B = R;
+    dp.max_ctx = cap;
+    dp.split_tokens = whole;
+    dp.nsplit = 1;
+    dp.scale2 = ((uint32_t)scale_bf16 << 16) | (uint32_t)scale_bf16;
+    dp.wait_ns = WAIT_NS;
+    dp.mq_groups = groups;
+    dp.mq_ctx = rctx;
+    static bool attr_done[64] = {};
+    const size_t smem = smem_bytes<true>();
+    set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel<true>), smem, attr_done);
+    rc = launch_pdl(k3mla_decode_split_kernel<true>, dim3(2 * 3 * G), dim3(THREADS), smem, st,
+                    "k3mla_decode_split_kernel<MQ>", tm_page, tm_page8, tm_q, tm_olat, tm_olat, dp);
+    if (rc) return rc;
+
+    MergeParams mp;
+    mp.ws_o = nullptr;
+    mp.ws_ml = dp.ws_ml;
+    mp.ws_olat = olat;
+    mp.ctx_len = rctx;
+    mp.w_kv_b = w_kv_b;
+    mp.out = out;
+    mp.argmax = argmax_t;
+    mp.dev_err = dev_err;
+    mp.B = R;
+    mp.max_ctx = cap;
+    mp.max_pages = max_pages_per_slot;
+    mp.split_tokens = whole;
+    mp.nsplit = 1;
+    mp.tile = 64;
+    return launch_merge_expand(mp, st);
 }
 
 // ---- one decode step of one layer ------------------------------------------------------
@@ -1407,7 +1697,7 @@ extern "C" int k3mla_diag_umma(int mode, const uint16_t* a, const uint16_t* b, f
     int rc = make_maps(b, PAGE, a, H, &tm_page, &tm_page8, &tm_q);
     if (rc) return rc;
     static bool attr_done[64] = {};
-    const size_t smem = smem_bytes();
+    const size_t smem = smem_bytes<false>();
     set_smem_attr(reinterpret_cast<const void*>(k3mla_diag_kernel), smem, attr_done);
     k3mla_diag_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tm_page, tm_page8, tm_q, mode, a, d);
     return check_launch("k3mla_diag_kernel");

@@ -31,6 +31,7 @@ EXPORTS = (
     "k3mla_decode_exact_workspace_bytes", "k3mla_pool_ensure_all", "k3mla_batch_planned_split_tokens",
     "k3mla_decode_layer_workspace_bytes", "k3mla_decode_layer", "k3mla_diag_decode_timeout",
     "k3mla_expanded_cache_bytes", "k3mla_expand_latent_cache", "k3mla_expanded_decode", "k3mla_diag_exact_exp",
+    "k3mla_chunk_decode_workspace_bytes", "k3mla_chunk_decode",
 )
 
 # Size of the library's built-in decode scratch (K3MLA_NOALLOC_SCRATCH_BYTES).
@@ -86,6 +87,8 @@ def load(build_if_needed: bool = True):
             "k3mla_copy_pages": ([P, I, P, I, I, P, P, I, P, P], I),
             "k3mla_append_latent_rows": ([P, I, I, I, P, I, P, P, P, I64, P, I64, I, I, P, P], I),
             "k3mla_chunk_views": ([P, I, I, P, P, I, P, P, P], I),
+            "k3mla_chunk_decode_workspace_bytes": ([I, I, I], SZ),
+            "k3mla_chunk_decode": ([P, P, I, I, I, P, I, P, P, I, I, P, ctypes.c_uint16, P, P, P, SZ, I, P, P], I),
             "k3mla_decode_exact_workspace_bytes": ([I, I], SZ),
             "k3mla_decode_layer_workspace_bytes": ([I, I], SZ),
             "k3mla_decode_layer": ([P, P, P, I, I, I, P, I, P, P, I64, P, I64, ctypes.c_uint16, P, P, P, SZ, I, I, P, P],
@@ -225,6 +228,33 @@ def chunk_views(block_table: torch.Tensor, pos0: torch.Tensor, row_start: torch.
         _dev(block_table, torch.int32, (B, M), "block_table"), B, M, _dev(pos0, torch.int32, (B,), "pos0"),
         _dev(row_start, torch.int32, (B + 1,), "row_start"), R, _dev(view_table, torch.int32, (R, M), "view_table"),
         _dev(view_ctx, torch.int32, (R,), "view_ctx"), _stream(stream)), "k3mla_chunk_views")
+
+
+def chunk_decode_workspace_bytes(B: int, R: int, max_ctx: int) -> int:
+    return int(load().k3mla_chunk_decode_workspace_bytes(B, R, max_ctx))
+
+
+def chunk_decode(q_abs: torch.Tensor, slab: torch.Tensor, layer: int, block_table: torch.Tensor,
+                 pos0: torch.Tensor, row_start: torch.Tensor, w_kv_b: torch.Tensor, scale_bf16: int,
+                 out: torch.Tensor, workspace: torch.Tensor, max_ctx: int, argmax: torch.Tensor | None = None,
+                 dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Multi-query decode of prefill chunks (k3mla_chunk_decode): q_abs [R, 96, 576] of the chunks'
+    token rows (slot b's rows row_start[b] .. row_start[b+1]-1, row j at position pos0[b] + j) ->
+    out [R, 96, 128], each row attending causally over its slot's cache."""
+    R = q_abs.shape[0]
+    B = pos0.shape[0]
+    n_pages, L = slab.shape[0], slab.shape[1]
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise K3mlaError("workspace must be a CUDA uint8 tensor")
+    lib = load()
+    _check(lib.k3mla_chunk_decode(
+        _dev(q_abs, torch.bfloat16, (R, H, ROW), "q_abs"), _dev(slab, torch.bfloat16, (n_pages, L, PAGE, ROW), "slab"),
+        n_pages, L, int(layer), _dev(block_table, torch.int32, None, "block_table"), block_table.shape[1],
+        _dev(pos0, torch.int32, (B,), "pos0"), _dev(row_start, torch.int32, (B + 1,), "row_start"), B, R,
+        _dev(w_kv_b, torch.bfloat16, (H * (NOPE + V), LORA), "w_kv_b"), ctypes.c_uint16(scale_bf16),
+        _dev(out, torch.bfloat16, (R, H, V), "out"), _opt(argmax, torch.int32, (R, H), "argmax"),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), int(max_ctx),
+        _opt(dev_err, torch.int32, (1,), "dev_err"), _stream(stream)), "k3mla_chunk_decode")
 
 
 def decode_exact_workspace_bytes(B: int, max_ctx: int) -> int:
