@@ -1223,7 +1223,7 @@ __global__ void __launch_bounds__(1024) k3mla_mq_prep_kernel(const int32_t* __re
         __syncthreads();
         if (tid == 0) {  // exclusive prefix of the group counts, after those of the slots before
             int acc = total;
-            for (int i = 0; i < 1024; ++i) {
+            for (int i = 0; i < 1024 && b0 + i < B; ++i) {
                 const int c = off[i];
                 off[i] = acc;
                 acc += c;
