@@ -214,18 +214,19 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
         }
         umma_commit(&d_full);
     }
-    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for the tile's NB slots and
-        // lands bf16 values in a [NB slots][512] tile over the (now idle) W_UK buffer; the CTA then
-        // writes each slot's 1 KB row of q_abs with 16-byte stores (measured faster here than one
-        // thread's bulk tensor stores of the same tile)
+    {   // epilogue: warp (quarter q, block mt) reads j = 128 mt + 32 q + lane for 32 of the tile's slots at
+        // a time and lands bf16 values in a [NB slots][512] tile over the (now idle) W_UK buffer; once
+        // those 32 slots are staged, the CTA writes their 1 KB rows of q_abs with 16-byte stores (measured
+        // faster here than one thread's bulk tensor stores of the same tile) while the next 32 are staged
         const int qq = warp & 3, mt = warp >> 2;
-        const bool got = ab_wait(&d_full, 0, nullptr);
+        const bool got = __all_sync(0xFFFFFFFFu, ab_wait(&d_full, 0, nullptr));
         uint16_t* tile = reinterpret_cast<uint16_t*>(sa);
-        if (__all_sync(0xFFFFFFFFu, got)) {
-            tc_fence_after();
-            const int j = 128 * mt + 32 * qq + lane;
+        if (got) tc_fence_after();
+        const int j = 128 * mt + 32 * qq + lane;
+        const int seg = threadIdx.x & 15;  // thread -> (slot 32 piece + tid / 16, 16-byte units 16k + seg)
 #pragma unroll
-            for (int piece = 0; piece < NB / 32; ++piece) {
+        for (int piece = 0; piece < NB / 32; ++piece) {
+            if (got) {
                 uint32_t acc[32];
                 tmem_ld32(tbase + ((uint32_t)(32 * qq) << 16) + (uint32_t)(NB * mt + 32 * piece), acc);
                 tmem_wait_ld();
@@ -233,18 +234,14 @@ __global__ void __launch_bounds__(AB_THREADS, 1)
                 for (int k = 0; k < 32; ++k)
                     tile[(32 * piece + k) * LORA + j] = (uint16_t)(pack2(__uint_as_float(acc[k]), 0.f) & 0xFFFFu);
             }
-        }
-        __syncthreads();
-        // thread -> (slot r, 16-byte units 8k + seg of its row)
-        const int seg = threadIdx.x & 7;
-#pragma unroll
-        for (int r = threadIdx.x >> 3; r < NB; r += AB_ROWS_PER_PASS) {
-            const int b = b0 + r;
-            if (b < B) {
+            __syncthreads();
+            static_assert(AB_THREADS == 16 * 32, "16 threads a slot row, 32 rows a piece");
+            const int r = 32 * piece + (threadIdx.x >> 4);
+            if (b0 + r < B) {
                 const uint4* srow = reinterpret_cast<const uint4*>(tile + r * LORA);
-                uint4* drow = reinterpret_cast<uint4*>(q_abs + ((size_t)b * H + h) * ROW);
+                uint4* drow = reinterpret_cast<uint4*>(q_abs + ((size_t)(b0 + r) * H + h) * ROW);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) drow[seg + 8 * k] = srow[seg + 8 * k];
+                for (int k = 0; k < 4; ++k) drow[seg + 16 * k] = srow[seg + 16 * k];
             }
         }
     }
