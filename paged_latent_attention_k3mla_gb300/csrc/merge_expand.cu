@@ -276,23 +276,30 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         }
     }
     {
-        // ---- epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15
+        // ---- epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15, and
+        // lands bf16 out in a [tile slots][128 v] tile over the (now idle) W_UV buffer; the CTA then writes
+        // each slot's 256-byte row of out with 16-byte stores
         const int q = warp & 3, cg = warp >> 2;
-        const bool got = mx_wait(&d_full, 0, p.dev_err);
-        if (__all_sync(0xFFFFFFFFu, got) && 16 * cg < p.tile) {
+        const bool got = __all_sync(0xFFFFFFFFu, mx_wait(&d_full, 0, p.dev_err));
+        uint16_t* tile = reinterpret_cast<uint16_t*>(sa);
+        if (got && 16 * cg < p.tile) {
             tc_fence_after();
             uint32_t acc16[16];
             tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * cg), acc16);
             tmem_wait_ld();
             const int v = 32 * q + lane;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int bb = b0 + 16 * cg + j;
-                if (bb < p.B)
-                    p.out[((size_t)bb * H + h) * VH + v] =
-                        (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc16[j]), 0.f) & 0xFFFFu);
-            }
+            for (int j = 0; j < 16; ++j)
+                tile[(16 * cg + j) * VH + v] = (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc16[j]), 0.f) & 0xFFFFu);
         }
+        __syncthreads();
+        if (got)
+            for (int u = (int)threadIdx.x; u < p.tile * (VH / 8); u += MX_THREADS) {
+                const int r = u / (VH / 8), k = u % (VH / 8), bb = b0 + r;
+                if (bb < p.B)
+                    reinterpret_cast<uint4*>(p.out + ((size_t)bb * H + h) * VH)[k] =
+                        reinterpret_cast<const uint4*>(tile + r * VH)[k];
+            }
     }
     tc_fence_before();
     __syncthreads();
