@@ -145,3 +145,31 @@ def test_argument_checks(gpu_lib):
         k3mla.chunk_decode(q_abs, wl.slab, 1, table, _dev(pos0), _dev(row_start), wl.w_kv_b[1], wl.scale_bits,
                            out, ws, 64)
     assert k3mla.chunk_decode_workspace_bytes(0, 4, 64) == 0
+
+
+def test_replay_from_a_cuda_graph_is_bitwise_the_eager_call(gpu_lib):
+    # the group builder, the multi-query split kernel and the merge capture like the rest of the library
+    wl, tbl, table, pos0, row_start, q, q_abs, R = _setup([0, 70, 200], [13, 4, 64], seed=695)
+    max_ctx = table.shape[1] * 64
+    eager, eager_am, err = _mq(wl, table, pos0, row_start, q_abs, R, max_ctx)
+    assert err == 0
+    ws = torch.empty(k3mla.chunk_decode_workspace_bytes(len(pos0), R, max_ctx), dtype=torch.uint8, device="cuda")
+    out = torch.full((R, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((R, H), -7, dtype=torch.int32, device="cuda")
+    p0, rs = _dev(pos0), _dev(row_start)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # the first call sets the kernels' attributes outside the capture
+        k3mla.chunk_decode(q_abs, wl.slab, 1, table, p0, rs, wl.w_kv_b[1], wl.scale_bits, out, ws, max_ctx,
+                           argmax=am, stream=s)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    am.fill_(-7)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        k3mla.chunk_decode(q_abs, wl.slab, 1, table, p0, rs, wl.w_kv_b[1], wl.scale_bits, out, ws, max_ctx,
+                           argmax=am, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(synth.bf16_bits(out), eager)
+    assert np.array_equal(am.cpu().numpy(), eager_am)
