@@ -308,6 +308,116 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 }
 
 
+
+// Every slot with at most one split and more than one 64-slot tile (a batch of token rows, say): one
+// CTA a head loads W_UV[h] once and takes the tiles in turn.  A tile's o_lat is TMA-loaded as soon as
+// the MMAs of the tile before have read the B buffer, while that tile's outputs are written: its
+// epilogue stages them beside W_UV (the last tile's over W_UV, which no MMA reads any more).
+constexpr int MX_O_BYTES = MX_SLOTS * VH * 2;  // a tile's bf16 outputs, staged for 16-byte stores
+
+__global__ void __launch_bounds__(MX_THREADS, 1)
+    k3mla_expand_tiles_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_o,
+                              const MergeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sb = sa + MX_A_BYTES;
+    uint16_t* so_next = reinterpret_cast<uint16_t*>(sb + MX_B_BYTES);
+    __shared__ uint64_t w_full, d_full, o_full;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int gave_up;  // a wait ran out: the remaining tiles are skipped
+    const int h = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = (p.B + MX_SLOTS - 1) / MX_SLOTS;
+
+    if (threadIdx.x == 0) {
+        gave_up = 0;
+        mbar_init(&w_full, 1);
+        mbar_init(&d_full, 1);
+        mbar_init(&o_full, 1);
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_o);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, MX_SLOTS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
+    if (threadIdx.x == 0) {  // W_UV[h], as in k3mla_merge_expand_kernel: a weight, loaded before the grid wait
+        mbar_arrive_expect_tx(&w_full, MX_A_BYTES);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            tma_load_3d_hint(sa + c * (VH * 128), &tmap_w, 0, h * WROWS_PER_HEAD + NOPE, c, &w_full,
+                             policy_evict_first());
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    auto load_tile = [&](int t) {  // o_lat rows h B + 64 t .. as the B operand (rows past the batch unused)
+        mbar_arrive_expect_tx(&o_full, MX_B_BYTES);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            tma_load_3d(sb + c * (MX_SLOTS * 128), &tmap_o, 0, h * p.B + t * MX_SLOTS, c, &o_full);
+    };
+    if (threadIdx.x == 0) load_tile(0);
+    for (int t = 0; t < ntiles; ++t) {
+        const int b0 = t * MX_SLOTS;
+        const bool last = t + 1 == ntiles;
+        const uint32_t par = (uint32_t)t & 1u;
+        if (p.argmax && threadIdx.x < MX_SLOTS && b0 + (int)threadIdx.x < p.B) {
+            const int b = b0 + (int)threadIdx.x;
+            const int ctx = mx_ctx_effective(p.ctx_len, b, p.max_ctx, p.max_pages);
+            p.argmax[(size_t)b * H + h] = ctx > 0 ? __float_as_int(p.ws_ml[((size_t)b * H + h) * 4 + 3]) : -1;
+        }
+        if (threadIdx.x == 0) {
+            const bool ok = mx_wait(&w_full, 0, p.dev_err) && mx_wait(&o_full, par, p.dev_err);
+            if (ok) {
+                tc_fence_after();
+                issue_expand(tbase, sa, sb, MX_SLOTS);
+            } else {
+                gave_up = 1;
+                const uint64_t t0 = globaltimer();  // let in-flight TMA copies land before the CTA exits
+                while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+            }
+            umma_commit(&d_full);
+            if (ok && !last && mx_wait(&d_full, par, p.dev_err)) load_tile(t + 1);  // the MMAs read sb
+        }
+        // epilogue: warp (quarter q, group cg) reads v rows 32q .. 32q+31, slots 16cg .. 16cg+15
+        uint16_t* so = last ? reinterpret_cast<uint16_t*>(sa) : so_next;
+        const int q = warp & 3, cg = warp >> 2;
+        const bool got = __all_sync(0xFFFFFFFFu, mx_wait(&d_full, par, p.dev_err));
+        if (got) {
+            tc_fence_after();
+            uint32_t acc16[16];
+            tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * cg), acc16);
+            tmem_wait_ld();
+            const int v = 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                so[(16 * cg + j) * VH + v] = (uint16_t)(mx_pack_bf16x2(__uint_as_float(acc16[j]), 0.f) & 0xFFFFu);
+        }
+        tc_fence_before();  // the TMEM loads before the next tile's MMAs
+        __syncthreads();
+        if (got)
+            for (int u = (int)threadIdx.x; u < MX_SLOTS * (VH / 8); u += MX_THREADS) {
+                const int r = u / (VH / 8), k = u % (VH / 8), bb = b0 + r;
+                if (bb < p.B)
+                    reinterpret_cast<uint4*>(p.out + ((size_t)bb * H + h) * VH)[k] =
+                        reinterpret_cast<const uint4*>(so + r * VH)[k];
+            }
+        __syncthreads();  // the staging buffer is free again; gave_up is seen by every thread
+        tc_fence_after();
+        if (*reinterpret_cast<volatile int*>(&gave_up)) break;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tbase, MX_SLOTS);
+}
+
 int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
 {
     static bool attr_set[64] = {};
@@ -327,6 +437,16 @@ int launch_merge_expand(const MergeParams& mp, cudaStream_t st)
     if (mp.nsplit == 1) {
         rc = make_tmap_slab_3d(&tmap_o, mp.ws_olat, (uint64_t)H * mp.B, LORA, 8, MX_SLOTS, 1);
         if (rc) return rc;
+    }
+    if (mp.nsplit == 1 && mp.B > MX_SLOTS) {  // several tiles of final o_lat: one CTA a head takes them all
+        static bool tiles_attr_set[64] = {};
+        const int smem_t = MX_A_BYTES + MX_B_BYTES + MX_O_BYTES + 1024;
+        if (dev < 0 || dev >= 64 || !tiles_attr_set[dev]) {
+            cudaFuncSetAttribute(k3mla_expand_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_t);
+            if (dev >= 0 && dev < 64) tiles_attr_set[dev] = true;
+        }
+        return launch_pdl(k3mla_expand_tiles_kernel, dim3(H), dim3(MX_THREADS), smem_t, st,
+                          "k3mla_expand_tiles_kernel", tmap_w, tmap_o, mp);
     }
     const dim3 grid(H, (mp.B + mp.tile - 1) / mp.tile);
     return launch_pdl(k3mla_merge_expand_kernel, grid, dim3(MX_THREADS), smem, st, "k3mla_merge_expand_kernel",
