@@ -251,6 +251,33 @@ def test_expanded_baseline_sizes_and_arguments():
     assert b"invalid sizes" in lib.k3mla_last_error()
 
 
+def test_chunk_decode_sizes_and_arguments():
+    # o_lat [96][R][512] bf16 and the rows' records (the decode workspace of one split), then the groups
+    # of rows (int4, at most (R + 3 B) / 4 + 1 of them) and the rows' contexts (int32), 256-aligned
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, R, max_ctx in ((1, 1, 64), (16, 1024, 4160), (3, 7, 300)):
+        g = (R + 3 * B) // 4 + 1
+        got = k3mla.chunk_decode_workspace_bytes(B, R, max_ctx)
+        one_split = r256(R * 96 * 512 * 2) + r256(R * 96 * 4 * 4)
+        assert got == one_split + r256(g * 16) + r256(R * 4), (B, R, got)
+    assert k3mla.chunk_decode_workspace_bytes(0, 4, 64) == 0
+    assert k3mla.chunk_decode_workspace_bytes(2, 0, 64) == 0
+    lib = k3mla.load()
+    # (q_abs, slab, n_pages, n_layers, layer, table, max_pages, pos0, row_start, B, R, w_kv_b, scale, out,
+    #  argmax, workspace, ws_bytes, max_ctx, dev_err, stream)
+    args = [None, None, 4, 1, 0, None, 4, None, None, 2, 0, None, 0x3D94, None, None, None, 0, 256, None, None]
+    assert lib.k3mla_chunk_decode(*args) == 0                   # R == 0: nothing to do
+    args[10] = 5
+    assert lib.k3mla_chunk_decode(*args) == -1
+    assert b"null or misaligned" in lib.k3mla_last_error()
+    args[9] = 0                                                 # no slots
+    assert lib.k3mla_chunk_decode(*args) == -1
+    assert b"invalid sizes" in lib.k3mla_last_error()
+    args[9], args[4] = 2, 1                                     # layer past the slab
+    assert lib.k3mla_chunk_decode(*args) == -1
+    assert b"invalid sizes" in lib.k3mla_last_error()
+
+
 def test_exact_exp_diagnostic_arguments():
     lib = k3mla.load()
     assert lib.k3mla_diag_exact_exp(None, None, None, 0, None) == 0     # nothing to do
