@@ -126,8 +126,9 @@ def test_rows_outside_every_slot_and_a_clamped_context(gpu_lib):
 
 
 def test_long_chunks_after_long_prefixes(gpu_lib):
-    # 300-token chunks after ~3,000-token prefixes: 75 groups a slot, units over several waves
-    prefix, chunk = [3000, 2881, 64], [300, 300, 130]
+    # 300-token chunks after ~3,000-token prefixes: 75 groups a slot, units over several waves; and a
+    # chunk after a 9,000-token prefix, whose rows' contexts (one split each) span 142 pages
+    prefix, chunk = [3000, 2881, 64, 9000], [300, 300, 130, 21]
     wl, tbl, table, pos0, row_start, q, q_abs, R = _setup(prefix, chunk, seed=680)
     max_ctx = table.shape[1] * 64
     out, am, err = _mq(wl, table, pos0, row_start, q_abs, R, max_ctx)
