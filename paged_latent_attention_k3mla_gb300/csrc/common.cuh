@@ -67,9 +67,9 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_
 int make_tmap_slab_3d(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems, uint32_t n_chunks,
                       uint32_t box_rows, uint32_t box_chunks);
 
-// Tensor map for bulk tensor stores: `rank` dims (innermost first), byte strides of dims 1..
-// (multiples of 16), the box, f32 or bf16 elements, with 128-byte swizzle (inner box extent 128
-// bytes) or none.
+// General tensor map (bulk tensor stores; also the multi-query q_abs loads): `rank` dims (innermost
+// first), byte strides of dims 1.. (multiples of 16), the box, f32 or bf16 elements, with 128-byte
+// swizzle (inner box extent 128 bytes) or none.
 int make_tmap_store(CUtensorMap* map, bool f32, uint32_t rank, const void* base, const uint64_t* dims,
                     const uint64_t* strides, const uint32_t* box, bool swizzle128);
 

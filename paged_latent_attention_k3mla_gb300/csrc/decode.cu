@@ -444,12 +444,19 @@ __device__ __noinline__ void pv_write_out(SmemT<MQ>& sm, const CUtensorMap* tm_o
             fence_proxy_async_cta();  // the boxes are read by bulk tensor stores (async proxy)
             named_bar(WO_BAR, C::WO_WARPS * 32);
             if (threadIdx.x == 0) {
-                if constexpr (MQ) {  // o_lat [96][R][512] as (512 dims, R rows, 96 heads), box (64, 1, 32)
-                    for (int w = 0; w < 4; ++w) {
-                        const int row = sm.mq_row[w];
-                        if (row < 0) continue;
-                        tma_store_3d(tm_olat, tile + k2 * BOX + 32 * w * 128, 64 * k2, row, 32 * hb);
-                        tma_store_3d(tm_olat, tile + (4 + k2) * BOX + 32 * w * 128, 256 + 64 * k2, row, 32 * hb);
+                if constexpr (MQ) {  // o_lat [96][R][512] as (512 dims, 96 heads, R rows): a full group's
+                    // four rows in one box (64, 32, 4), else each row in its own (the rows after a short
+                    // group belong to other units)
+                    if (sm.mq_row[3] >= 0) {
+                        tma_store_3d(tm_olat, tile + k2 * BOX, 64 * k2, 32 * hb, sm.mq_row[0]);
+                        tma_store_3d(tm_olat, tile + (4 + k2) * BOX, 256 + 64 * k2, 32 * hb, sm.mq_row[0]);
+                    } else {
+                        for (int w = 0; w < 4; ++w) {
+                            const int row = sm.mq_row[w];
+                            if (row < 0) continue;
+                            tma_store_3d(tm_part, tile + k2 * BOX + 32 * w * 128, 64 * k2, 32 * hb, row);
+                            tma_store_3d(tm_part, tile + (4 + k2) * BOX + 32 * w * 128, 256 + 64 * k2, 32 * hb, row);
+                        }
                     }
                 } else if (single) {  // o_lat [96][B][512] as (512 dims, B slots, 96 heads), box (64, 1, 96)
                     tma_store_3d(tm_olat, tile + k2 * (H * 128), 64 * k2, b, 0);
@@ -551,15 +558,12 @@ __device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& t
     const bool single = sg.single;
     const int32_t oob_row = sg.oob_row;
     if (rank == 0 && threadIdx.x == 0) {  // q_abs of the unit, staged in ring units Q_UNIT0.. until in TMEM
-        if constexpr (MQ) {  // 32 rows of each present token row per chunk, at row 32 w of the chunk
-            int nq = 0;
-            for (int w = 0; w < 4; ++w) nq += sm.mq_row[w] >= 0 ? 1 : 0;
-            mbar_arrive_expect_tx(&sm.q_land, 9 * nq * C::PSTAGE);
+        if constexpr (MQ) {  // per chunk one box: heads 32 hb .. of four consecutive token rows, row w of the
+            // group at row 32 w of the chunk (rows past the group are loaded too, or read as zeros past
+            // the last token row, and land in lanes nobody reads)
+            mbar_arrive_expect_tx(&sm.q_land, C::QBYTES);
             for (int c = 0; c < 9; ++c)
-                for (int w = 0; w < 4; ++w)
-                    if (sm.mq_row[w] >= 0)
-                        tma_load_3d(q_stage(sm) + c * C::QCHUNK + w * C::PSTAGE, &tmap_q, 0,
-                                    sm.mq_row[w] * H + 32 * sg.hb, c, &sm.q_land);
+                tma_load_4d(q_stage(sm) + c * C::QCHUNK, &tmap_q, 0, 32 * sg.hb, sm.mq_row[0], c, &sm.q_land);
         } else {
             mbar_arrive_expect_tx(&sm.q_land, C::QBYTES);
             for (int c = 0; c < 9; ++c) tma_load_3d(q_stage(sm) + c * C::QCHUNK, &tmap_q, 0, b * H, c, &sm.q_land);
@@ -1489,18 +1493,25 @@ extern "C" int k3mla_chunk_decode(const uint16_t* q_abs, const uint16_t* slab, i
                         R, cap, groups, G, rctx, olat, dev_err);
     if (rc) return rc;
 
-    CUtensorMap tm_page, tm_page8, tm_q, tm_olat;
+    CUtensorMap tm_page, tm_page8, tm_q, tm_olat, tm_orow;
     rc = make_tmap_slab_3d(&tm_page, slab, (uint64_t)n_pages * n_layers * PAGE, ROW, 9, PAGE, 3);
     if (rc) return rc;
     rc = make_tmap_slab_3d(&tm_page8, slab, (uint64_t)n_pages * n_layers * PAGE, ROW, 9, HALF, 8);
     if (rc) return rc;
-    rc = make_tmap_slab_3d(&tm_q, q_abs, (uint64_t)R * H, ROW, 9, 32, 1);  // 32 heads of one row a box
-    if (rc) return rc;
-    {   // o_lat [96][R][512] bf16 as (512 dims, R rows, 96 heads), box (64, 1, 32)
-        const uint64_t dims[3] = {LORA, (uint64_t)R, H};
-        const uint64_t strides[2] = {LORA * 2, (uint64_t)R * LORA * 2};
-        const uint32_t box[3] = {64, 1, 32};
-        rc = make_tmap_store(&tm_olat, false, 3, olat, dims, strides, box, true);
+    {   // q_abs [R][96][576] as (64 elements, 96 heads, R rows, 9 chunks): one box = a chunk of 32 heads
+        // of four consecutive token rows
+        const uint64_t dims[4] = {64, H, (uint64_t)R, 9};
+        const uint64_t strides[3] = {ROW * 2, (uint64_t)H * ROW * 2, 128};
+        const uint32_t box[4] = {64, 32, 4, 1};
+        rc = make_tmap_store(&tm_q, false, 4, q_abs, dims, strides, box, true);
+        if (rc) return rc;
+    }
+    {   // o_lat [96][R][512] bf16 as (512 dims, 96 heads, R rows): boxes of 32 heads x 4 rows, or x 1 row
+        const uint64_t dims[3] = {LORA, H, (uint64_t)R};
+        const uint64_t strides[2] = {(uint64_t)R * LORA * 2, LORA * 2};
+        const uint32_t box4[3] = {64, 32, 4}, box1[3] = {64, 32, 1};
+        rc = make_tmap_store(&tm_olat, false, 3, olat, dims, strides, box4, true);
+        if (!rc) rc = make_tmap_store(&tm_orow, false, 3, olat, dims, strides, box1, true);
         if (rc) return rc;
     }
     DecodeParams dp;
@@ -1527,7 +1538,7 @@ extern "C" int k3mla_chunk_decode(const uint16_t* q_abs, const uint16_t* slab, i
     const size_t smem = smem_bytes<true>();
     set_smem_attr(reinterpret_cast<const void*>(k3mla_decode_split_kernel<true>), smem, attr_done);
     rc = launch_pdl(k3mla_decode_split_kernel<true>, dim3(2 * 3 * G), dim3(THREADS), smem, st,
-                    "k3mla_decode_split_kernel<MQ>", tm_page, tm_page8, tm_q, tm_olat, tm_olat, dp);
+                    "k3mla_decode_split_kernel<MQ>", tm_page, tm_page8, tm_q, tm_olat, tm_orow, dp);
     if (rc) return rc;
 
     MergeParams mp;
