@@ -123,6 +123,13 @@ def test_rows_outside_every_slot_and_a_clamped_context(gpu_lib):
     vout2, vam2, verr2, _, _ = _views(wl, table, pos0, row_start, q_abs, R, max_ctx)
     assert verr2 == k3mla.DEV_CTX
     assert np.array_equal(out2, vout2) and np.array_equal(am2, vam2)
+    # packed rows that start after row 0: rows before row_start[0] belong to no slot either
+    shifted = row_start + 3
+    out3, am3, err3 = _mq(wl, table, pos0, shifted, q_abs, R, table.shape[1] * 64)
+    assert err3 == 0
+    assert np.all(out3[:3] == 0) and np.all(am3[:3] == -1)
+    vout3, vam3, _, _, _ = _views(wl, table, pos0, shifted, q_abs, R, table.shape[1] * 64)
+    assert np.array_equal(out3, vout3) and np.array_equal(am3, vam3)
 
 
 def test_long_chunks_after_long_prefixes(gpu_lib):
