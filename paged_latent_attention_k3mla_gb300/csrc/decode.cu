@@ -32,7 +32,9 @@
 //     contraction.
 //   * rank 1, the PV CTA, streams the same pages (chunks 0..7 as two 32 KB
 //     half-page boxes into a ring of five half-page slots, one producer each;
-//     these reads mostly hit L2 right after the score CTA's) and accumulates
+//     these reads mostly hit L2 right after the score CTA's; one of its warps
+//     prefetches pages into L2 ahead of the score CTA, whose DRAM ingest is
+//     bound by the 2.67 pages its ring holds in flight) and accumulates
 //     O[heads x 512 dims] += P . C in TMEM (M = 128 rows, the 96 heads first;
 //     two N = 256 halves; K = 64 tokens per page; B is the MN-major latent
 //     page), so that a thread reading its TMEM lane holds one head's O row.  Its
@@ -112,10 +114,13 @@ constexpr uint32_t Q_COL = 192;                // score CTA: Q, 288 columns (576
 constexpr float TAU = 16.0f;                   // max growth (natural log) before a rescale: p~ <= e^16,
                                                // l <= n e^16 stays far inside f32 for any context here
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
+constexpr int PF_PAGES = 7;                    // PV CTA: L2 prefetch distance, pages past the latest P (measured
+                                               // best of 4..9)
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 256, 0, 1);  // O half = P . C (B MN-major)
 // rank 0: warps 0-7 softmax, 8-10 producers, 11-13 MMA issuers; rank 1: warps 0-3
-// epilogue, 4-8 producers, 9 MMA issuer, 10-13 idle.  Warp 8 allocates TMEM in both.
+// epilogue, 4-8 producers, 9 MMA issuer, 10 L2 prefetch (decode), 11-13 idle.  Warp 8 allocates TMEM
+// in both.
 constexpr int THREADS = 448;
 constexpr int W_PROD0 = 8, W_MMA0 = 11, W_ALLOC = 8;
 // named barriers of the score CTA (0 is __syncthreads): the decision hand-off between the two
@@ -897,6 +902,16 @@ __device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& t
                 } else {
                     drain_inflight();
                     *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) = 1;
+                }
+            }
+        } else if (!MQ && warp == 10) {
+            if (lane == 0) {  // once page i's P has arrived, page i + PF_PAGES is prefetched into L2 for the
+                              // score CTA (a wait that sees a later phase only prefetches early)
+                for (int i = 0; i + PF_PAGES < npg; ++i) {
+                    if (!wait_bar(&sm.p_full[i % C::NPBUF], (uint32_t)((i / C::NPBUF) & 1), sm, p.dev_err, true)) break;
+                    const int32_t y = page_row(p, b, lp0 + i + PF_PAGES, n_lp, oob_row);
+                    if (y != oob_row)
+                        for (int t = 0; t < 3; ++t) tma_prefetch_3d(&tmap_page, 0, y, 3 * t);
                 }
             }
         } else if (warp < 4) {
