@@ -399,7 +399,7 @@ int k3mla_copy_pages(uint16_t* dst_slab, int dst_n_pages, const uint16_t* src_sl
                      int32_t* dev_err, void* stream);
 
 /* ---- paged decode with built-in scratch ---------------------------------------
- * The paper has no counterpart to this call.  It is k3mla_paged_decode without the
+ * The pegainfer PR #869 page has no counterpart to this call.  It is k3mla_paged_decode without the
  * `workspace` / `ws_bytes` pair, for callers that cannot allocate device memory at
  * the point where they decode: a serving process that reserves all device memory
  * for its own pool at start-up and forbids allocation while it serves, or a plugin
