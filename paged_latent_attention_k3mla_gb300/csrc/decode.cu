@@ -149,6 +149,7 @@ template <bool MQ> struct __align__(1024) SmemT {
     uint64_t o_done, epi_req, epi_done;
     uint64_t l_full;         // PV CTA: 1 / l of every row has arrived (single-split launches)
     int32_t fin_ready;       // PV CTA: epilogue warps that saw O complete (4: write it out)
+    int32_t p_seen;          // PV CTA: pages whose P has arrived (a count, read by the prefetch warp)
     float rl[C::ROWS];       // ... 1 / l by row, stored by the score CTA
     float xm[2][4][32];      // score CTA: reference max after a page, by page parity / quarter / lane
     float xa[2][4][32];      // ... and that page's rescale factor (1 when it kept the reference)
@@ -536,6 +537,7 @@ __device__ __forceinline__ void init_decode_barriers(SmemT<MQ>& sm, uint32_t ran
     mbar_init(&sm.l_full, 1);
     sm.abort_flag = 0;
     sm.fin_ready = 0;
+    sm.p_seen = 0;
     for (int i = 0; i < NHSLOT; ++i) sm.early_n[i] = 0;
     for (int i = 0; i < C::NUNIT; ++i) {
         sm.unit_loaded[i] = 0;
@@ -862,6 +864,7 @@ __device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& t
                         break;
                     }
                     fence_proxy_async_cta();  // the P tile arrived through st.async; the MMA reads it
+                    if constexpr (!MQ) *reinterpret_cast<volatile int32_t*>(&sm.p_seen) = i + 1;
                     const volatile uint32_t* rf =
                         reinterpret_cast<const volatile uint32_t*>(sm.u.c1.recv[st] + C::META_FLAGS);
                     const bool resc = (i > 0) && ((rf[0] | rf[1] | rf[2] | rf[3]) != 0u);
@@ -905,10 +908,13 @@ __device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& t
                 }
             }
         } else if (!MQ && warp == 10) {
-            if (lane == 0) {  // once page i's P has arrived, page i + PF_PAGES is prefetched into L2 for the
-                              // score CTA (a wait that sees a later phase only prefetches early)
+            if (lane == 0) {  // once the P of page i has arrived, page i + PF_PAGES is prefetched into L2 for
+                              // the score CTA.  The warp follows the PV issuer's count of pages (a barrier's
+                              // parity would repeat if it fell behind) and skips the pages it fell behind on.
                 for (int i = 0; i + PF_PAGES < npg; ++i) {
-                    if (!wait_bar(&sm.p_full[i % C::NPBUF], (uint32_t)((i / C::NPBUF) & 1), sm, p.dev_err, true)) break;
+                    if (!wait_count(&sm.p_seen, i + 1, sm, p.dev_err)) break;
+                    i = max(i, *reinterpret_cast<volatile int32_t*>(&sm.p_seen) - 1);
+                    if (i + PF_PAGES >= npg) break;
                     const int32_t y = page_row(p, b, lp0 + i + PF_PAGES, n_lp, oob_row);
                     if (y != oob_row)
                         for (int t = 0; t < 3; ++t) tma_prefetch_3d(&tmap_page, 0, y, 3 * t);
