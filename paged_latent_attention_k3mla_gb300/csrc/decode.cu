@@ -114,7 +114,7 @@ constexpr uint32_t Q_COL = 192;                // score CTA: Q, 288 columns (576
 constexpr float TAU = 16.0f;                   // max growth (natural log) before a rescale: p~ <= e^16,
                                                // l <= n e^16 stays far inside f32 for any context here
 constexpr uint64_t WAIT_NS = 1000000000ull;    // bounded waits: 1 s
-constexpr int PF_PAGES = 7;                    // PV CTA: L2 prefetch distance, pages past the latest P (measured
+constexpr int PF_PAGES = 8;                    // PV CTA: L2 prefetch distance, pages past the latest P (measured
                                                // best of 4..9)
 constexpr uint32_t IDESC_S = make_idesc_bf16(128, PAGE, 0, 0);  // S^T page = Q . C^T
 constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 256, 0, 1);  // O half = P . C (B MN-major)
