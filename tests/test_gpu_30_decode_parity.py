@@ -53,6 +53,25 @@ def test_default_split_with_single_and_multi_split_slots(gpu_lib):
     _parity(wl, 0, split=k3mla.SPLIT_AUTO, max_ctx=20000, name="auto_mixed")
 
 
+def test_prefetched_pages_with_holes_and_bad_ids(gpu_lib):
+    # the PV CTA prefetches into L2 the page eight past the latest page whose P has arrived: contexts
+    # around that distance (one split a slot of 8, 9, 10 and 64 pages), with -1 holes and a bad page id
+    # where the prefetches start and on a last page.  A prefetch never changes a result, and the bad id
+    # is flagged with the bit its load raises anyway
+    ctx = [8 * 64, 8 * 64 + 1, 9 * 64, 10 * 64 - 3, 4096, 4096]
+    wl = synth.make_custom(ctx, seed=310, device="cuda", max_pages=64)
+    wl.block_table[1, 8] = -1                       # the one page past a 9-page context's first eight
+    wl.block_table[3, 9] = -1
+    wl.block_table[4, 8] = wl.slab.shape[0] + 5     # out of range: read as zero and flagged
+    wl.block_table[5, 63] = -1                      # the last page of a full-length slot
+    g = gpu_layer(wl, 0, split=k3mla.SPLIT_AUTO, max_ctx=4096)
+    assert g["dev_err"] == k3mla.DEV_BAD_PAGE, g["dev_err"]
+    o = oracle_layer(wl, 0, probs_stride=4096)
+    ok, stats = compare(g, o, wl.ctx_len, name="prefetch_edges")
+    print("prefetch edges:", stats)
+    assert ok, stats
+
+
 def test_single_split_batch_over_one_slot_tile(gpu_lib):
     # one split per slot (split = max_ctx): the split kernel lands o_lat itself and the expansion
     # reads it in place; 67 slots cover two 64-slot tiles, two contexts are empty
