@@ -374,23 +374,28 @@ __device__ __forceinline__ void issue_score_third(uint32_t tbase, uint32_t d_col
 // 64 tokens each; rows 96..127 read whatever follows the buffer in this CTA's shared memory and only
 // land in TMEM lanes nobody reads); B = C, MN-major (dims contiguous).  Two N = 256 halves of the dims
 // x 4 K-steps of 16 tokens.
+// Half hh of the page (tokens 32 hh .. 32 hh + 31, held in one slot): 4 MMAs.
+__device__ __forceinline__ void issue_pv_half(uint32_t tbase, uint32_t half_addr, uint32_t pt_addr, int hh,
+                                              bool accumulate_first)
+{
+    const uint64_t a0 = make_sdesc(pt_addr, 16, 1024);
+    const uint64_t b0 = make_sdesc(half_addr, HCHUNK, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const uint64_t ad = a0 + (uint64_t)((uint32_t)((2 * hh + ks) * 32) >> 4);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const uint64_t bd = b0 + (uint64_t)((uint32_t)(4 * n * HCHUNK + ks * 2048) >> 4);
+            umma_ss(tbase + 256u * n, ad, bd, IDESC_PV, (accumulate_first || hh > 0 || ks > 0) ? 1u : 0u);
+        }
+    }
+}
+
 __device__ __forceinline__ void issue_pv_page(uint32_t tbase, uint32_t half0_addr, uint32_t half1_addr,
                                               uint32_t pt_addr, bool accumulate_first)
 {
-    const uint64_t a0 = make_sdesc(pt_addr, 16, 1024);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const uint64_t b0 = make_sdesc(hh ? half1_addr : half0_addr, HCHUNK, 1024);
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = a0 + (uint64_t)((uint32_t)((2 * hh + ks) * 32) >> 4);
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const uint64_t bd = b0 + (uint64_t)((uint32_t)(4 * n * HCHUNK + ks * 2048) >> 4);
-                umma_ss(tbase + 256u * n, ad, bd, IDESC_PV, (accumulate_first || hh > 0 || ks > 0) ? 1u : 0u);
-            }
-        }
-    }
+    issue_pv_half(tbase, half0_addr, pt_addr, 0, accumulate_first);
+    issue_pv_half(tbase, half1_addr, pt_addr, 1, accumulate_first);
 }
 
 // Byte offset in a P^T buffer of the 16-byte chunk with tokens 8j .. 8j+7 of head h.
@@ -891,9 +896,10 @@ __device__ __forceinline__ void decode_roles(SmemT<MQ>& sm, const CUtensorMap& t
                         ++epi_k;
                     }
                     tc_fence_after();
-                    issue_pv_page(tbase, smem_u32(sm.u.c1.ring[q0]), smem_u32(sm.u.c1.ring[q1]),
-                                  smem_u32(sm.u.c1.recv[st]), i > 0);
+                    // each half-page slot goes back to its producer once the four MMAs that read it are done
+                    issue_pv_half(tbase, smem_u32(sm.u.c1.ring[q0]), smem_u32(sm.u.c1.recv[st]), 0, i > 0);
                     umma_commit(&sm.empty[q0]);
+                    issue_pv_half(tbase, smem_u32(sm.u.c1.ring[q1]), smem_u32(sm.u.c1.recv[st]), 1, i > 0);
                     umma_commit(&sm.empty[q1]);
                     umma_commit_mc(&sm.p_empty[st], (uint16_t)0x1);
                     if (i + C::NPBUF < npg) mbar_arrive_expect_tx(&sm.p_full[st], C::PCOPY);
